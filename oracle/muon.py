@@ -1,0 +1,175 @@
+"""The Muon optimizer step, oracle version (test infrastructure).
+
+Follows the step as the pages describe it:
+
+* "Support Muon in BF16_Optimizer with FP32 gradient accumulation", PR
+  description: BF16 micro-batch gradients are accumulated in FP32; Muon runs
+  on the original (full) matrices after reduction; only each rank's owned
+  intersection of the update is copied back; momentum is FP32 and
+  partitioned like the master weights; alignment padding is excluded;
+  auxiliary (non-Muon) groups keep their own path.
+* "Run Muon once per optimizer step under ZeRO-3, not once per micro-batch",
+  "The change": at the step, after the overflow check and before the
+  gradient norm, Muon runs once on the accumulated gradient; the gradient
+  norm is taken over the Muon updates; a step the loss scaler discards
+  leaves the momentum untouched.  Review thread: per-head Muon splits a
+  tagged parameter (``muon_num_heads``) into head blocks; untagged
+  parameters stay whole.
+
+Readings where the pages are silent:
+
+* momentum m <- beta*m + g in float32 (beta*m rounded, then + g rounded);
+* gradient scale: each micro-batch adds scale*g, scale = 1/gas by default;
+* per-head: rows split into num_heads contiguous blocks of rows/num_heads,
+  each block normalised and orthogonalised on its own; num_heads <= 1 means
+  the whole matrix;
+* update u = NS(m) (no Nesterov term, no weight decay, no shape factor);
+* overflow: any non-finite accumulated gradient element of any parameter
+  (padding excluded) skips the step and nothing is written;
+* global norm = sqrt(sum over Muon params of ||u||^2 + sum over aux params
+  of ||g||^2); coef = min(1, clip / (norm + 1e-6)), clip <= 0 disables;
+* write-back: Muon params get accum = coef*u and master -= lr*coef*u;
+  aux params get accum = coef*g and their master is left alone (the
+  auxiliary optimizer is the caller's).
+"""
+import numpy as np
+
+from . import newton_schulz as ns
+
+CLIP_EPS = 1e-6
+
+
+def accumulate(accum, grad, scale, overwrite=False):
+    """One micro-batch: accum + scale*grad in float32 (the product is
+    rounded to float32 before the sum); overwrite gives scale*grad."""
+    sg = np.float32(scale) * np.asarray(grad, np.float32)
+    return sg if overwrite else np.asarray(accum, np.float32) + sg
+
+
+def momentum_update(m, g, beta):
+    """m <- beta*m + g in float32 (the product rounded, then the sum)."""
+    return np.float32(beta) * np.asarray(m, np.float32) + np.asarray(g, np.float32)
+
+
+def muon_update(g, m, beta, method="gram", steps=ns.DEFAULT_STEPS, num_heads=0,
+                mode="exact"):
+    """Momentum update then per-block Newton-Schulz of one Muon matrix.
+
+    Returns (new momentum (float32), update u in the matrix's shape)."""
+    m_new = momentum_update(m, g, beta)
+    rows = m_new.shape[0]
+    h = num_heads if num_heads and num_heads > 1 else 1
+    if rows % h:
+        raise ValueError("rows must be a multiple of num_heads")
+    br = rows // h
+    blocks = [ns.newton_schulz(m_new[i * br:(i + 1) * br], method, steps, mode)
+              for i in range(h)]
+    return m_new, np.vstack(blocks)
+
+
+def muon_step_full(mats, beta, lr, method="gram", steps=ns.DEFAULT_STEPS, clip=0.0,
+                   mode="exact"):
+    """One optimizer step on full matrices (no partition tables).
+
+    mats: list of dicts with keys g (accumulated gradient), m (momentum),
+    w (master), use_muon, num_heads.  Returns a dict with per-parameter
+    lists 'update', 'momentum', 'master' and scalars 'norm', 'coef',
+    'applied', 'ns_calls'."""
+    calls0 = ns.NS_CALLS[0]
+    if any(not np.all(np.isfinite(np.asarray(d["g"], np.float32))) for d in mats):
+        return {"applied": 0, "norm": 0.0, "coef": 0.0, "ns_calls": 0,
+                "update": [np.asarray(d["g"], np.float32) for d in mats],
+                "momentum": [np.asarray(d["m"], np.float32) for d in mats],
+                "master": [np.asarray(d["w"], np.float32) for d in mats]}
+    us, moms = [], []
+    for d in mats:
+        if d["use_muon"]:
+            m_new, u = muon_update(d["g"], d["m"], beta, method, steps,
+                                   d.get("num_heads", 0), mode)
+        else:
+            m_new, u = np.asarray(d["m"], np.float32), np.asarray(d["g"], np.float32)
+        moms.append(m_new)
+        us.append(u)
+    sq = 0.0
+    for u in us:
+        u64 = np.asarray(u, np.float64)
+        sq += float(np.sum(u64 * u64))
+    norm = float(np.sqrt(sq))
+    coef = min(1.0, clip / (norm + CLIP_EPS)) if clip > 0 else 1.0
+
+    updates, masters = [], []
+    for d, u in zip(mats, us):
+        w = np.asarray(d["w"], np.float32)
+        if mode == "exact":
+            v64 = coef * np.asarray(u, np.float64)
+            v = v64.astype(np.float32)
+            w_new = (w.astype(np.float64) - lr * v64).astype(np.float32) if d["use_muon"] else w
+        else:
+            v = np.float32(coef) * np.asarray(u, np.float32)
+            w_new = w - np.float32(lr) * v if d["use_muon"] else w
+        updates.append(v)
+        masters.append(w_new)
+    return {"applied": 1, "norm": norm, "coef": coef,
+            "ns_calls": ns.NS_CALLS[0] - calls0,
+            "update": updates, "momentum": moms, "master": masters}
+
+
+# ------------------------------------------------ flat, partitioned buffers
+
+def _owned_pieces(params, parts, k):
+    """(storage_begin, param_begin, length) for every partition intersecting
+    parameter k: the rank-owned intersections of one matrix."""
+    off = int(params["offset"][k])
+    n = int(params["rows"][k]) * int(params["cols"][k])
+    pieces = []
+    for q in parts:
+        lo = max(off, int(q["flat_begin"]))
+        hi = min(off + n, int(q["flat_end"]))
+        if lo < hi:
+            pieces.append((int(q["storage_offset"]) + lo - int(q["flat_begin"]), lo - off, hi - lo))
+    if sum(p[2] for p in pieces) != n:
+        raise ValueError(f"parameter {k} is not covered exactly once by the partitions")
+    return pieces
+
+
+def gather_matrix(buf, params, parts, k):
+    """Rebuild parameter k's full matrix from the partitioned buffer."""
+    rows, cols = int(params["rows"][k]), int(params["cols"][k])
+    out = np.empty(rows * cols, dtype=buf.dtype)
+    for s, p, n in _owned_pieces(params, parts, k):
+        out[p:p + n] = buf[s:s + n]
+    return out.reshape(rows, cols)
+
+
+def scatter_matrix(buf, params, parts, k, mat):
+    """Copy each partition's owned intersection of mat back into buf."""
+    flat = np.asarray(mat, dtype=buf.dtype).reshape(-1)
+    for s, p, n in _owned_pieces(params, parts, k):
+        buf[s:s + n] = flat[p:p + n]
+
+
+def muon_step_flat(accum, momentum, master, params, parts, beta, lr, method="gram",
+                   steps=ns.DEFAULT_STEPS, clip=0.0, mode="exact"):
+    """The step on flat, rank-partitioned storage buffers.
+
+    Reconstructs each parameter from its partitions, runs
+    :func:`muon_step_full`, then writes every partition's owned intersection
+    of the results back.  Elements no parameter covers (alignment padding,
+    gaps between partitions) are never read or written.  Returns new copies
+    of (accum, momentum, master) and the result dict."""
+    mats = []
+    for k in range(len(params)):
+        mats.append({"g": gather_matrix(accum, params, parts, k),
+                     "m": gather_matrix(momentum, params, parts, k),
+                     "w": gather_matrix(master, params, parts, k),
+                     "use_muon": bool(params["use_muon"][k]),
+                     "num_heads": int(params["num_heads"][k])})
+    res = muon_step_full(mats, beta, lr, method, steps, clip, mode)
+    acc2, mom2, mst2 = accum.copy(), momentum.copy(), master.copy()
+    if res["applied"]:
+        for k in range(len(params)):
+            scatter_matrix(acc2, params, parts, k, res["update"][k])
+            if mats[k]["use_muon"]:
+                scatter_matrix(mom2, params, parts, k, res["momentum"][k])
+                scatter_matrix(mst2, params, parts, k, res["master"][k])
+    return acc2, mom2, mst2, res
