@@ -25,8 +25,16 @@ Two arithmetic modes:
   X0 is rounded to bfloat16; each matrix product is accumulated in float64,
   rounded to float32, combined with its addend in float32 as
   ``alpha*acc + beta*E (+ gamma on the diagonal)`` and the result rounded to
-  bfloat16.  These are the rounding points of every product named above
-  (A, B, X for standard; R, P, Q, P R, R, Y for gram).
+  bfloat16.  standard: A, B and X are rounded this way every step.
+  gram: only the m x n products use BF16 operands -- R0 = X0 X0^T is kept in
+  float32 (its inputs are bfloat16), the m x m recurrence (P, Q, P R, R)
+  runs in float32 (float64 accumulation rounded to float32), and the final
+  Q is rounded to bfloat16 before Y = Q X0, whose result is rounded to
+  bfloat16.  Reason: R <- P R P squares the singular values, so a bfloat16
+  R cannot resolve singular values below about 2^-4 of the largest and the
+  recurrence amplifies its rounding by up to a^2 ~ 12 per step; the pages
+  give gram no precision, and FP32 for the small m x m recurrence is the
+  reading that keeps gram as accurate as the standard method.
 """
 import numpy as np
 
@@ -98,6 +106,19 @@ def _standard(X, steps, mode):
     return X
 
 
+def _gemm_f32(lhs, rhs, alpha, E=None, beta=0.0, gamma=0.0):
+    """float32(alpha*(lhs @ rhs) + beta*E + gamma*I): product accumulated in
+    float64, rounded to float32, epilogue in float32, result kept float32."""
+    acc = _f32(np.asarray(lhs, np.float64) @ np.asarray(rhs, np.float64))
+    out = np.float32(alpha) * acc
+    if E is not None:
+        out = out + np.float32(beta) * _f32(E)
+    if gamma != 0.0:
+        d = np.arange(min(out.shape))
+        out[d, d] = out[d, d] + np.float32(gamma)
+    return _f32(out)
+
+
 def _gram(X0, steps, mode):
     a, b, c = A_COEF, B_COEF, C_COEF
     m = X0.shape[0]
@@ -110,15 +131,15 @@ def _gram(X0, steps, mode):
             if k < steps - 1:
                 R = (P @ R) @ P
         return Q @ X0
-    R = _gemm_bf16(X0, X0.T, 1.0)
+    R = _gemm_f32(X0, X0.T, 1.0)
     Q = None
     for k in range(steps):
-        P = _gemm_bf16(R, R, c, R, b, gamma=a)
-        Q = P if k == 0 else _gemm_bf16(P, Q, 1.0)   # Q0 = I, so Q1 = P
+        P = _gemm_f32(R, R, c, R, b, gamma=a)
+        Q = P if k == 0 else _gemm_f32(P, Q, 1.0)   # Q0 = I, so Q1 = P
         if k < steps - 1:
-            T = _gemm_bf16(P, R, 1.0)
-            R = _gemm_bf16(T, P, 1.0)
-    return _gemm_bf16(Q, X0, 1.0)
+            T = _gemm_f32(P, R, 1.0)
+            R = _gemm_f32(T, P, 1.0)
+    return _gemm_bf16(round_bf16(Q), X0, 1.0)
 
 
 def iterate(X0, method="standard", steps=DEFAULT_STEPS, mode="exact"):
