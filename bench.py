@@ -1,0 +1,358 @@
+"""Benchmark of the Muon optimizer step on GB300.
+
+Default workload: the GPT-2-small parameter set (12 layers of Q, K (12
+heads), V, O 768x768, MLP up 3072x768 and down 768x3072; 84.9M elements,
+8 partitions, 128 alignment), four BF16 micro-batches accumulated in FP32,
+then one Muon step (5 standard Newton-Schulz steps, BF16 operands, clip
+0.05).  One timed step = 4 x accumulate + 1 x muon_step, all kernels of the
+library, inputs resident in HBM.  Every state buffer is 340 MB, larger than
+the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "Muon step time & NS TFLOP/s (% of GB300 bf16 dense peak) plus HBM GB/s, 1 GPU"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def peak_value(peaks, key):
+    for k in (key, key.replace("_gbs", "_GBps")):
+        if k in peaks and isinstance(peaks[k], (int, float)):
+            return float(peaks[k])
+    return FALLBACK[key]
+
+
+# ------------------------------------------------------------------ workloads
+
+def gpt2_workload(ns_method, mode):
+    lay = wl.gpt2_small_layout()
+    seed = wl.CONFIG_SEED["gpt2"]
+    sig = wl.loguniform_sigmas(lay, seed, 1e-4, 1e-1)
+    gas = 4
+    grads = [wl.bf16_storage_grad(lay, wl.gaussian_grads(lay, seed, mb, sig)) for mb in range(gas)]
+    m0 = wl.pack(lay, [0.1 * g for g in wl.gaussian_grads(lay, seed, 100, sig, bf16=False)])
+    w0 = wl.pack(lay, wl.gaussian_grads(lay, seed, 101, None, bf16=False))
+    desc = (f"gpt2-small muon step: 12 layers (q,k 12-head, v, o 768x768; up 3072x768; "
+            f"down 768x3072), 84.9M params, P=8, align 128, gas=4 bf16 grads, "
+            f"{ns_method} NS x5, {mode} operands, clip 0.05")
+    return lay, grads, m0, w0, gas, desc
+
+
+def ns_formula_flops(lay, method, steps=5):
+    """Algorithmic Newton-Schulz flops of one step: standard 5(4m^2n+2m^3),
+    gram 4m^2n + 34m^3 (5 steps), per head block."""
+    f = 0.0
+    for s in lay.specs:
+        if not s.use_muon:
+            continue
+        h = s.num_heads if s.num_heads > 1 else 1
+        r, c = s.rows // h, s.cols
+        m, n = min(r, c), max(r, c)
+        if method == "standard":
+            f += h * steps * (4.0 * m * m * n + 2.0 * m ** 3)
+        else:
+            f += h * (4.0 * m * m * n + (2 * steps + 2 * (steps - 1) + 4 * (steps - 1)) * m ** 3)
+    return f
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def cpu_oracle_sample(ns_method, mode, budget_s=20.0):
+    """Times the oracle on a bounded sample of the GPT-2-small step: the
+    whole step (accumulate x4, momentum, NS, norm, clip, write-back) on one
+    layer's six matrices (P=8); scaled to the full 12 layers by layer
+    count.  Returns (ms per full step estimate, sample description)."""
+    import oracle.muon as om
+    import oracle.bf16 as obf
+    lay = wl.gpt2_small_layout(layers=1)
+    seed = wl.CONFIG_SEED["gpt2"]
+    sig = wl.loguniform_sigmas(lay, seed, 1e-4, 1e-1)
+    grads = [obf.bits_to_f32(wl.bf16_storage_grad(lay, wl.gaussian_grads(lay, seed, mb, sig)))
+             for mb in range(4)]
+    m0 = wl.pack(lay, [0.1 * g for g in wl.gaussian_grads(lay, seed, 100, sig, bf16=False)])
+    w0 = wl.pack(lay, wl.gaussian_grads(lay, seed, 101, None, bf16=False))
+    omode = "bf16" if mode == "bf16" else "exact"
+    reps, t_tot = 0, 0.0
+    while True:
+        t0 = time.perf_counter()
+        acc = None
+        for mb in range(4):
+            acc = om.accumulate(acc, grads[mb], 0.25, overwrite=(mb == 0))
+        om.muon_step_flat(acc, m0, w0, lay.params, lay.parts, 0.95, 0.02, ns_method, 5, 0.05, omode)
+        t_tot += time.perf_counter() - t0
+        reps += 1
+        if t_tot > budget_s or reps >= 3:
+            break
+    ms_layer = 1000.0 * t_tot / reps
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    sample = (f"oracle ({omode} mode, numpy/BLAS fp64) on layer 0 of 12 (6 matrices, P=8), "
+              f"{reps} rep(s), full step = 12 x layer time")
+    return 12.0 * ms_layer, cores, sample
+
+
+# ------------------------------------------------------------------ GPU run
+
+def run_gpu(args, rank, world):
+    import torch
+    import newton_schulz_fp32_gb300 as nsg
+
+    dev = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(dev)
+    nsg.build()
+    lay, grads, m0, w0, gas, desc = gpt2_workload(args.ns_method, args.mode)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        acc = torch.zeros(lay.storage_size, dtype=torch.float32, device="cuda")
+        mom = torch.from_numpy(m0).cuda()
+        mst = torch.from_numpy(w0).cuda()
+        g_dev = [torch.from_numpy(g.view(np.int16)).cuda().view(torch.bfloat16) for g in grads]
+        g_host = [torch.from_numpy(g.view(np.int16)).view(torch.bfloat16).pin_memory() for g in grads]
+        res = torch.zeros(4, dtype=torch.int32, device="cuda")
+        res_host = torch.zeros(4, dtype=torch.int32).pin_memory()
+    torch.cuda.synchronize()
+    P, Q = lay.params, lay.parts
+
+    def step(grad_list):
+        for mb in range(gas):
+            nsg.accumulate(acc, grad_list[mb], 1.0 / gas, overwrite=(mb == 0), params=P, parts=Q,
+                           stream=stream)
+        nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, args.ns_method, 5, 0.05, args.mode, result=res,
+                 stream=stream)
+
+    # warm-up (plans are built on the first call)
+    for _ in range(args.warmup):
+        step(g_dev)
+    torch.cuda.synchronize()
+    r = nsg.read_result(res)
+    if r["applied"] != 1:
+        raise RuntimeError(f"warm-up step not applied: {r}")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident timed region
+    nsg.profile_read(reset=True)
+    nsg.profile_enable(True)
+    launches0 = nsg.get_stats()["kernel_launches_total"]
+    clocks = ClockSampler(dev)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(g_dev)
+    e1.record(stream)
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    clk = clocks.stop()
+    launches = nsg.get_stats()["kernel_launches_total"] - launches0
+    nsg.profile_enable(False)
+    phases = nsg.profile_read(reset=True)
+    if nsg.device_error() != 0:
+        raise RuntimeError("a kernel reported a device error during the timed region")
+
+    # ---- end to end: host grads -> device, the step, result -> host
+    h2d = sum(g.numel() * 2 for g in g_host)
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_wall = time.perf_counter()
+    e2.record(stream)
+    for _ in range(args.steps):
+        with torch.cuda.stream(stream):
+            for i in range(gas):
+                g_dev[i].copy_(g_host[i], non_blocking=True)
+        step(g_dev)
+        with torch.cuda.stream(stream):
+            res_host.copy_(res, non_blocking=True)
+        stream.synchronize()
+    e3.record(stream)
+    barrier()
+    wall_ms = 1000.0 * (time.perf_counter() - t_wall) / args.steps
+    e2e_ms = max(e2.elapsed_time(e3) / args.steps, wall_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    return lay, desc, ms, e2e_ms, h2d, phases, clk, launches
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ns-method", default="standard", choices=["standard", "gram"])
+    ap.add_argument("--mode", default="bf16", choices=["bf16", "fp32"])
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    peaks, peak_src = load_peaks()
+    lay1 = wl.gpt2_small_layout(layers=1)
+    ns_flops = ns_formula_flops(wl.gpt2_small_layout(), args.ns_method)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        ms_ref, cores, sample = cpu_oracle_sample(args.ns_method, args.mode, args.cpu_budget)
+        line = {"metric": METRIC, "value": ms_ref, "unit": "ms", "impl": "reference",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms_ref, "higher_is_better": False, "scaling": "weak",
+                "vs_baseline": None, "dtype": args.mode + "+fp32", "data": "synthetic",
+                "config": {"workload": "gpt2-small muon step (oracle on CPU, bounded sample)",
+                           "ns_method": args.ns_method, "operand_mode": args.mode},
+                "cpu_baseline": {"value": ms_ref, "unit": "ms", "cores": cores, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": ms_ref, "unit": "ms", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "ns_tflops": ns_flops / (ms_ref * 1e-3) / 1e12}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))))
+
+    lay, desc, ms, e2e_ms, h2d, phases, clk, launches = run_gpu(args, rank, world)
+
+    # roofline of the dominant phase
+    dom = max(phases, key=lambda k: phases[k]["ms"])
+    ph = phases[dom]
+    per_launch_ms = ph["ms"] / max(ph["launches"], 1)
+    if dom == "ns_gemm":
+        bound, unit = "tensor", "TFLOP/s"
+        achieved = (ph["flops"] / max(ph["launches"], 1)) / (per_launch_ms * 1e-3) / 1e12
+        peak = peak_value(peaks, "bf16_tflops") if args.mode == "bf16" else None
+    else:
+        bound, unit = "hbm", "GB/s"
+        achieved = (ph["bytes"] / max(ph["launches"], 1)) / (per_launch_ms * 1e-3) / 1e9
+        peak = peak_value(peaks, "hbm_gbs")
+    hbm_phases = [k for k in phases if k != "ns_gemm" and phases[k]["ms"] > 0]
+    hbm_bytes = sum(phases[k]["bytes"] for k in hbm_phases)
+    hbm_ms = sum(phases[k]["ms"] for k in hbm_phases)
+    ns_ms = phases["ns_gemm"]["ms"]
+    ns_tflops = phases["ns_gemm"]["flops"] / max(ns_ms * 1e-3, 1e-12) / 1e12
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        ms_ref, cores, sample = cpu_oracle_sample(args.ns_method, args.mode, args.cpu_budget)
+        cpu = {"value": ms_ref, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample}
+    line = {
+        "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": args.mode + "+fp32", "data": "synthetic",
+        "config": {"workload": desc, "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (each fp32 state buffer 340 MB), no flush",
+                   "ns_method": args.ns_method, "operand_mode": args.mode},
+        "ns_tflops": ns_tflops,
+        "ns_frac_of_peak": (ns_tflops / peak_value(peaks, "bf16_tflops")) if args.mode == "bf16" else None,
+        "ns_flops_per_step": ns_flops,
+        "hbm_gbs": hbm_bytes / max(hbm_ms * 1e-3, 1e-12) / 1e9,
+        "phases_ms_per_step": {k: phases[k]["ms"] / args.steps for k in phases},
+        "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src, "unit": unit,
+                     "frac": (achieved / peak) if peak else None, "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 16},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,215 @@
+/*
+ * muon.h -- C ABI of libmuon: the Muon optimizer step on one GB300 GPU.
+ *
+ * The step is the data-parallel hot path described by three DeepSpeed pull
+ * requests about Muon under ZeRO:
+ *   [BF16]  "Support Muon in BF16_Optimizer with FP32 gradient accumulation"
+ *   [ONCE]  "Run Muon once per optimizer step under ZeRO-3, not once per
+ *            micro-batch"
+ *   [OFFL]  "Fix Muon optimizer under ZeRO CPU offload and bound gather
+ *            buffers"
+ *
+ * Data model.  Every optimizer buffer (accumulated gradient, momentum, FP32
+ * master weights, and each micro-batch's BF16 gradient) is one flat array
+ * cut into partitions, one per emulated data-parallel rank ([BF16], PR
+ * description: flat, rank-partitioned buffers with alignment padding).
+ * Flat index i of partition p lives at storage element
+ *     storage_offset[p] + (i - flat_begin[p])
+ * of each buffer; the same mapping holds for all buffers.  A parameter is a
+ * rows x cols row-major matrix occupying flat indices
+ * [offset, offset + rows*cols).  Flat indices inside a partition that no
+ * parameter covers are padding: no call reads or writes them.
+ *
+ * Conventions for every call:
+ *   - Device pointers are CUDA device (or managed) addresses on the current
+ *     device; host pointers are ordinary host memory and are only read
+ *     during the call (tables are copied; the caller may free them after).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ *     GPU work is enqueued asynchronously on it; no call synchronises the
+ *     host except the first muon_step for a new table set (see below).
+ *   - Return value: MUON_OK (0) or a negative MUON_ERR_* code.  On error
+ *     nothing has been enqueued, and muon_last_error() describes it.
+ *   - The caller owns every buffer it passes.  The library owns a per-table
+ *     workspace (device memory) and plan, created on the first muon_step
+ *     with a given table set and freed by muon_release_workspace().
+ *     Creating a plan calls cudaMalloc and copies tables to the device, so
+ *     that first call synchronises and must not be stream-captured.
+ *   - Calls are not thread-safe with respect to each other.
+ */
+#ifndef MUON_H
+#define MUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MUON_API __attribute__((visibility("default")))
+#else
+#define MUON_API
+#endif
+
+#define MUON_OK 0
+#define MUON_ERR_INVALID (-1)     /* inconsistent tables or arguments */
+#define MUON_ERR_UNSUPPORTED (-2) /* valid request outside what is built */
+#define MUON_ERR_CUDA (-3)        /* a CUDA runtime/driver call failed */
+#define MUON_ERR_OOM (-4)         /* workspace allocation failed */
+
+/* One parameter.  use_muon = 0 marks an auxiliary (non-Muon) parameter:
+ * it is counted in the global norm and clipped, but not orthogonalised
+ * ([BF16], PR description: auxiliary Adam groups keep their own path).
+ * num_heads > 1 splits the rows into num_heads contiguous blocks that are
+ * normalised and orthogonalised independently (per-head Muon, [ONCE]
+ * review thread, muon_num_heads); rows % num_heads must be 0.
+ * 24 bytes, 8-byte aligned. */
+typedef struct muon_param {
+  int64_t offset;   /* flat index of element (0,0) */
+  int32_t rows;     /* >= 1 */
+  int32_t cols;     /* >= 1 */
+  int32_t num_heads;
+  int32_t use_muon; /* 1 = Muon matrix, 0 = auxiliary */
+} muon_param_t;
+
+/* One partition: flat indices [flat_begin, flat_end) stored at
+ * storage_offset.  Partitions must be sorted by flat_begin, must not
+ * overlap in flat space or in storage, and together must cover every
+ * parameter.  24 bytes. */
+typedef struct muon_partition {
+  int64_t flat_begin;
+  int64_t flat_end;
+  int64_t storage_offset;
+} muon_partition_t;
+
+typedef enum {
+  MUON_NS_STANDARD = 0, /* X <- aX + (bA + cA^2)X, A = XX^T            */
+  MUON_NS_GRAM = 1      /* same map through R = X0 X0^T, Y = Q X0       */
+} muon_ns_method_t;
+
+typedef enum {
+  MUON_OPERANDS_BF16 = 0, /* BF16 operands, FP32 accumulation (tensor cores) */
+  MUON_OPERANDS_FP32 = 1  /* FP32 operands and accumulation                   */
+} muon_operand_mode_t;
+
+typedef enum { MUON_DTYPE_BF16 = 0, MUON_DTYPE_FP32 = 1 } muon_dtype_t;
+
+/* Written on the device by muon_step (read it after synchronising). */
+typedef struct muon_result {
+  int32_t applied;   /* 1 = step applied, 0 = skipped (non-finite gradient) */
+  int32_t ns_calls;  /* Newton-Schulz problems run this step (0 if skipped) */
+  float global_norm; /* sqrt(sum ||u_muon||^2 + sum ||g_aux||^2)           */
+  float clip_coef;   /* min(1, clip / (global_norm + 1e-6)); 1 if clip <= 0 */
+} muon_result_t;
+
+/* Host-side counters. */
+typedef struct muon_stats {
+  int64_t steps;                  /* muon_step calls enqueued */
+  int64_t ns_calls_last_step;     /* NS problems enqueued by the last step */
+  int64_t muon_matrices;          /* Muon parameters in the last step */
+  int64_t kernel_launches_last_call; /* kernels the last call launched */
+  int64_t kernel_launches_total;  /* kernels launched since load */
+  size_t workspace_bytes;         /* device bytes held by all plans */
+} muon_stats_t;
+
+/* S1, FP32 gradient accumulation of one BF16 micro-batch ([BF16], PR
+ * description; [ONCE], "The change": partitions accumulate the raw
+ * gradient and Muon runs only at the step):
+ *     accum[s] = (overwrite ? 0 : accum[s]) + scale * float(grad[s])
+ * with scale*grad rounded to FP32 before the sum.  scale is normally
+ * 1/gradient_accumulation_steps.
+ *   accum : device float[storage size], in/out
+ *   grad  : device bfloat16 bit patterns (uint16) with accum's layout
+ *   n     : storage elements; used only when params == NULL, in which case
+ *           all n elements are processed (padding included)
+ *   params/nparams, parts/nparts : host tables; when given, only elements
+ *           some parameter covers are touched (padding is left alone)
+ * Errors: MUON_ERR_INVALID for bad tables or n < 0 with params == NULL. */
+MUON_API int muon_accumulate(float* accum, const uint16_t* grad, int64_t n, float scale,
+                    int overwrite, const muon_param_t* params, int nparams,
+                    const muon_partition_t* parts, int nparts, void* stream);
+
+/* S2-S4, the optimizer step, once per accumulation boundary ([ONCE], "The
+ * change"; [BF16], PR description):
+ *   1. overflow check: any non-finite accum element of any parameter
+ *      skips the step -- accum, momentum and master are left bit-identical
+ *      and d_result->applied = 0;
+ *   2. per Muon parameter (per head block): m <- beta*m + g (FP32, in
+ *      place), X0 = m / (||m||_F + 1e-7), transposed if rows > cols,
+ *      ns_steps Newton-Schulz steps (quintic 3.4445, -4.7750, 2.0315) by
+ *      ns_method in operand_mode precision, transposed back: u;
+ *   3. global norm over the Muon updates and the auxiliary gradients,
+ *      coef = min(1, clip / (norm + 1e-6)) (clip <= 0: coef = 1);
+ *   4. owned-slice write-back: Muon: accum = coef*u, master -= lr*coef*u;
+ *      auxiliary: accum = coef*g, master untouched.  Padding untouched.
+ *   accum, momentum, master : device float storage buffers, in/out
+ *   d_result : device muon_result_t, written at the end of the step
+ * Errors: MUON_ERR_INVALID (overlapping parameters, a parameter not covered
+ * by the partitions, unsorted or overlapping partitions, overlapping
+ * storage, rows/cols < 1, rows % num_heads != 0, NULL buffers),
+ * MUON_ERR_UNSUPPORTED (ns_steps < 1 or > 64, unknown method or mode),
+ * MUON_ERR_OOM, MUON_ERR_CUDA. */
+MUON_API int muon_step(float* accum, float* momentum, float* master,
+              const muon_param_t* params, int nparams,
+              const muon_partition_t* parts, int nparts, float beta, float lr,
+              int ns_method, int ns_steps, float clip, int operand_mode,
+              muon_result_t* d_result, void* stream);
+
+/* Newton-Schulz orthogonalisation of one rows x cols row-major matrix:
+ * normalise by the Frobenius norm (+1e-7), transpose if rows > cols,
+ * ns_steps quintic steps by ns_method, transpose back.
+ *   X, Y     : device arrays of io_dtype (muon_dtype_t), rows*cols each;
+ *              X is read only; Y may not alias X
+ *   operand_mode : arithmetic precision (muon_operand_mode_t)
+ * Uses a library workspace sized for the shape (kept until
+ * muon_release_workspace).  Errors as muon_step. */
+MUON_API int muon_newton_schulz(const void* X, void* Y, int rows, int cols, int io_dtype,
+                       int ns_method, int ns_steps, int operand_mode, void* stream);
+
+/* Host-side counters (no GPU work).  Returns MUON_OK. */
+MUON_API int muon_get_stats(muon_stats_t* out);
+
+/* Message for the last error on this thread ("" if none). */
+MUON_API const char* muon_last_error(void);
+
+/* Frees every plan and workspace (synchronises the device first). */
+MUON_API void muon_release_workspace(void);
+
+/* Synchronises the device and returns the first error code a kernel
+ * recorded since the last query (0 = none), clearing it.  The tensor-core
+ * kernels bound every wait; a wait that runs out records a positive code
+ * here instead of hanging (1 = TMA producer, 2 = MMA issuer, 3 = epilogue).
+ * A step whose products hit such an error also reports applied = -1. */
+MUON_API int muon_device_error(void);
+
+/* Phase timing with CUDA events on the launching stream, for benchmarks.
+ * muon_profile_enable(1) makes every later call record an event pair
+ * around each kernel launch; muon_profile_read() synchronises those events
+ * and returns, per phase, the launch count and total device milliseconds
+ * accumulated since the last reset, plus the algorithmic bytes moved or
+ * flops executed.  Phases are indexed by muon_phase_t. */
+typedef enum {
+  MUON_PHASE_ACCUMULATE = 0, /* S1 */
+  MUON_PHASE_REDUCE = 1,     /* S2 pass 1: overflow check + sums of squares */
+  MUON_PHASE_GATHER = 2,     /* S2 pass 2: momentum write + X0 */
+  MUON_PHASE_NS_GEMM = 3,    /* S3: the Newton-Schulz matrix products */
+  MUON_PHASE_NORM = 4,       /* S4a: update sums of squares, norm, clip */
+  MUON_PHASE_SCATTER = 5,    /* S4b: owned-slice write-back */
+  MUON_PHASE_COUNT = 6
+} muon_phase_t;
+
+typedef struct muon_phase_time {
+  int64_t launches;
+  double total_ms;
+  double algorithmic_bytes;
+  double algorithmic_flops;
+} muon_phase_time_t;
+
+MUON_API int muon_profile_enable(int on);
+MUON_API int muon_profile_read(muon_phase_time_t* out, int nphases, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MUON_H */

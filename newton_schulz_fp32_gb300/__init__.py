@@ -1,0 +1,205 @@
+"""Python binding of libmuon, the Muon optimizer step on one GB300 GPU.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libmuon.so`` (built in-tree by :func:`build`).  PyTorch tensors
+are accepted for device buffers and the current CUDA stream; plain integer
+device addresses work too.  There is no CPU fallback: if the library is
+missing or the call fails, a :class:`MuonError` is raised.
+
+Table formats match the C structs of ``include/muon.h``:
+``PARAM_DTYPE`` ``{int64 offset; int32 rows, cols, num_heads, use_muon}`` and
+``PART_DTYPE`` ``{int64 flat_begin, flat_end, storage_offset}``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmuon.so")
+
+PARAM_DTYPE = np.dtype([("offset", "<i8"), ("rows", "<i4"), ("cols", "<i4"),
+                        ("num_heads", "<i4"), ("use_muon", "<i4")])
+PART_DTYPE = np.dtype([("flat_begin", "<i8"), ("flat_end", "<i8"),
+                       ("storage_offset", "<i8")])
+
+MUON_OK, MUON_ERR_INVALID, MUON_ERR_UNSUPPORTED, MUON_ERR_CUDA, MUON_ERR_OOM = 0, -1, -2, -3, -4
+NS_METHODS = {"standard": 0, "gram": 1}
+OPERAND_MODES = {"bf16": 0, "fp32": 1}
+DTYPES = {"bf16": 0, "fp32": 1}
+PHASES = ["accumulate", "reduce", "gather", "ns_gemm", "norm", "scatter"]
+
+# Every symbol include/muon.h declares.
+EXPORTED = ["muon_accumulate", "muon_step", "muon_newton_schulz", "muon_get_stats",
+            "muon_last_error", "muon_release_workspace", "muon_device_error",
+            "muon_profile_enable", "muon_profile_read"]
+
+
+class MuonError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libmuon error {code}: {msg}")
+        self.code = code
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_int64), ("ns_calls_last_step", ctypes.c_int64),
+                ("muon_matrices", ctypes.c_int64), ("kernel_launches_last_call", ctypes.c_int64),
+                ("kernel_launches_total", ctypes.c_int64), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class PhaseTime(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int64), ("total_ms", ctypes.c_double),
+                ("algorithmic_bytes", ctypes.c_double), ("algorithmic_flops", ctypes.c_double)]
+
+
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False):
+    from . import builder as _b
+    return _b.build(force=force, verbose=verbose)
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MuonError(MUON_ERR_UNSUPPORTED,
+                            f"{LIB_PATH} is missing; build it with newton_schulz_fp32_gb300.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        L.muon_accumulate.argtypes = [P, P, I64, F, I, P, I, P, I, P]
+        L.muon_step.argtypes = [P, P, P, P, I, P, I, F, F, I, I, F, I, P, P]
+        L.muon_newton_schulz.argtypes = [P, P, I, I, I, I, I, I, P]
+        L.muon_get_stats.argtypes = [ctypes.POINTER(Stats)]
+        L.muon_last_error.restype = ctypes.c_char_p
+        L.muon_release_workspace.restype = None
+        L.muon_profile_enable.argtypes = [I]
+        L.muon_profile_read.argtypes = [ctypes.POINTER(PhaseTime), I, I]
+        for name in ("muon_accumulate", "muon_step", "muon_newton_schulz", "muon_get_stats",
+                     "muon_device_error", "muon_profile_enable", "muon_profile_read"):
+            getattr(L, name).restype = I
+        _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != MUON_OK:
+        raise MuonError(rc, lib().muon_last_error().decode())
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _table(arr, dtype):
+    if arr is None:
+        return None, 0
+    a = np.ascontiguousarray(arr)
+    if a.dtype != dtype:
+        a = np.ascontiguousarray(a.astype(dtype))
+    return a, len(a)
+
+
+def accumulate(accum, grad, scale: float, overwrite: bool = False, params=None, parts=None,
+               n: int | None = None, stream=None):
+    """accum += scale * bf16 grad (FP32), over parameter elements when tables
+    are given, else over all n (= accum.numel()) elements."""
+    p, np_ = _table(params, PARAM_DTYPE)
+    q, nq = _table(parts, PART_DTYPE)
+    if n is None:
+        n = accum.numel() if hasattr(accum, "numel") else -1
+    _check(lib().muon_accumulate(_ptr(accum), _ptr(grad), n, scale, int(overwrite),
+                                 p.ctypes.data if p is not None else None, np_,
+                                 q.ctypes.data if q is not None else None, nq, _stream(stream)))
+
+
+def step(accum, momentum, master, params, parts, beta: float, lr: float, ns_method="gram",
+         ns_steps: int = 5, clip: float = 0.0, operand_mode="bf16", result=None, stream=None):
+    """One Muon step (overflow check, momentum, Newton-Schulz, global norm
+    and clip, owned-slice write-back).  Returns the device result buffer
+    (torch int32[4]; decode with :func:`read_result`)."""
+    import torch
+    if result is None:
+        result = torch.zeros(4, dtype=torch.int32, device=accum.device)
+    p, np_ = _table(params, PARAM_DTYPE)
+    q, nq = _table(parts, PART_DTYPE)
+    method = NS_METHODS[ns_method] if isinstance(ns_method, str) else int(ns_method)
+    mode = OPERAND_MODES[operand_mode] if isinstance(operand_mode, str) else int(operand_mode)
+    _check(lib().muon_step(_ptr(accum), _ptr(momentum), _ptr(master),
+                           p.ctypes.data if np_ else None, np_,
+                           q.ctypes.data if nq else None, nq, beta, lr, method, ns_steps, clip,
+                           mode, _ptr(result), _stream(stream)))
+    return result
+
+
+def read_result(result) -> dict:
+    """Decode the 16-byte device result struct (synchronises on the copy)."""
+    r = result.cpu().numpy().astype(np.int32)
+    f = r.view(np.float32)
+    return {"applied": int(r[0]), "ns_calls": int(r[1]),
+            "global_norm": float(f[2]), "clip_coef": float(f[3])}
+
+
+def newton_schulz(X, Y=None, ns_method="gram", ns_steps: int = 5, operand_mode="bf16",
+                  stream=None):
+    """Orthogonalise one matrix X (bf16 or fp32, rows x cols) into Y."""
+    import torch
+    if X.dim() != 2:
+        raise ValueError("X must be 2-D")
+    if Y is None:
+        Y = torch.empty_like(X)
+    io = {torch.bfloat16: 0, torch.float32: 1}[X.dtype]
+    if Y.dtype != X.dtype or Y.shape != X.shape:
+        raise ValueError("Y must match X's shape and dtype")
+    method = NS_METHODS[ns_method] if isinstance(ns_method, str) else int(ns_method)
+    mode = OPERAND_MODES[operand_mode] if isinstance(operand_mode, str) else int(operand_mode)
+    _check(lib().muon_newton_schulz(_ptr(X), _ptr(Y), X.shape[0], X.shape[1], io, method,
+                                    ns_steps, mode, _stream(stream)))
+    return Y
+
+
+def get_stats() -> dict:
+    s = Stats()
+    _check(lib().muon_get_stats(ctypes.byref(s)))
+    return {k: getattr(s, k) for k, _ in Stats._fields_}
+
+
+def last_error() -> str:
+    return lib().muon_last_error().decode()
+
+
+def release_workspace():
+    lib().muon_release_workspace()
+
+
+def device_error() -> int:
+    return int(lib().muon_device_error())
+
+
+def profile_enable(on: bool = True):
+    _check(lib().muon_profile_enable(int(on)))
+
+
+def profile_read(reset: bool = False) -> dict:
+    arr = (PhaseTime * len(PHASES))()
+    _check(lib().muon_profile_read(arr, len(PHASES), int(reset)))
+    return {name: {"launches": arr[i].launches, "ms": arr[i].total_ms,
+                   "bytes": arr[i].algorithmic_bytes, "flops": arr[i].algorithmic_flops}
+            for i, name in enumerate(PHASES)}

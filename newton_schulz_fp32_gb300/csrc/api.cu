@@ -1,0 +1,940 @@
+// C ABI of libmuon: argument and table validation, the planner (tables ->
+// owners, segments, tiles, grouped GEMM work lists, workspace), the plan
+// cache, and the launch sequence of one Muon step.
+//
+// The tables are static for a training run, so everything derived from them
+// is computed once, copied to the device and reused ("layout is static,
+// computed once in init": "Support Muon in BF16_Optimizer with FP32 gradient
+// accumulation", review thread on the all_to_all_single split tables).
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "muon_internal.h"
+
+namespace muon {
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+#define MUON_CUDA_TRY(expr)                                                        \
+  do {                                                                             \
+    cudaError_t e_ = (expr);                                                       \
+    if (e_ != cudaSuccess)                                                         \
+      return fail(e_ == cudaErrorMemoryAllocation ? MUON_ERR_OOM : MUON_ERR_CUDA,  \
+                  std::string(#expr) + ": " + cudaGetErrorString(e_));             \
+  } while (0)
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// ------------------------------------------------------------------ device memory
+
+struct DevBuf {
+  void* p = nullptr;
+  size_t bytes = 0;
+  DevBuf() = default;
+  DevBuf(const DevBuf&) = delete;
+  DevBuf& operator=(const DevBuf&) = delete;
+  ~DevBuf() { reset(); }
+  void reset() {
+    if (p) cudaFree(p);
+    p = nullptr;
+    bytes = 0;
+  }
+  cudaError_t alloc(size_t n) {
+    reset();
+    if (n == 0) n = 16;
+    cudaError_t e = cudaMalloc(&p, n);
+    if (e == cudaSuccess) bytes = n;
+    else p = nullptr;
+    return e;
+  }
+  template <class T>
+  T* as() const { return static_cast<T*>(p); }
+};
+
+template <class T>
+cudaError_t upload(DevBuf& b, const std::vector<T>& v) {
+  cudaError_t e = b.alloc(v.size() * sizeof(T));
+  if (e != cudaSuccess || v.empty()) return e;
+  return cudaMemcpy(b.p, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice);
+}
+
+// ------------------------------------------------------------------ counters, profiling
+
+struct Counters {
+  int64_t steps = 0, ns_calls_last = 0, muon_mats_last = 0, launches_last = 0, launches_total = 0;
+};
+Counters g_cnt;
+std::mutex g_mu;
+
+struct PendingEvent {
+  int phase;
+  cudaEvent_t start, stop;
+  double bytes, flops;
+};
+bool g_profile = false;
+std::vector<PendingEvent> g_pending;
+std::vector<cudaEvent_t> g_event_pool;
+muon_phase_time_t g_phase[MUON_PHASE_COUNT];
+
+cudaEvent_t get_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Brackets one launch group with events (when profiling) and counts kernels.
+struct PhaseScope {
+  int phase, kernels;
+  double bytes, flops;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr, b = nullptr;
+  PhaseScope(int ph, cudaStream_t st, int nkern, double by, double fl)
+      : phase(ph), kernels(nkern), bytes(by), flops(fl), s(st) {
+    if (g_profile && nkern > 0) {
+      a = get_event();
+      b = get_event();
+      cudaEventRecord(a, s);
+    }
+  }
+  ~PhaseScope() {
+    g_cnt.launches_last += kernels;
+    g_cnt.launches_total += kernels;
+    if (a) {
+      cudaEventRecord(b, s);
+      g_pending.push_back({phase, a, b, bytes, flops});
+      g_phase[phase].launches += kernels;
+    }
+  }
+};
+
+// ------------------------------------------------------------------ TMA encode
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// bf16 2-D map: inner extent `inner`, `outer` rows of `ld` elements.
+bool encode_bf16_2d(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld,
+                    uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ layout (table plan)
+
+struct Layout {
+  std::vector<Owner> owners;
+  std::vector<Segment> segs;
+  std::vector<RTile> rtiles;
+  std::vector<ETile> gtiles;   // gather: Muon owners
+  std::vector<ETile> stiles;   // scatter: all owners
+  std::vector<YTile> ytiles;
+  std::vector<Run> runs;       // accumulate: every parameter element
+  int n_muon_params = 0;
+  int n_muon_owners = 0;
+  int64_t muon_elems = 0, aux_elems = 0;
+  int64_t x_elems = 0, sq_elems = 0;   // per workspace region
+};
+
+int validate_and_build(const muon_param_t* params, int nparams, const muon_partition_t* parts,
+                       int nparts, Layout& L) {
+  if (nparams < 0 || nparts < 0) return fail(MUON_ERR_INVALID, "negative table size");
+  if (nparams > 0 && !params) return fail(MUON_ERR_INVALID, "params is NULL");
+  if (nparts > 0 && !parts) return fail(MUON_ERR_INVALID, "parts is NULL");
+  if (nparams > 0 && nparts == 0) return fail(MUON_ERR_INVALID, "parameters but no partitions");
+  for (int i = 0; i < nparts; ++i) {
+    const muon_partition_t& q = parts[i];
+    if (q.flat_begin < 0 || q.flat_end < q.flat_begin || q.storage_offset < 0)
+      return fail(MUON_ERR_INVALID, "partition " + std::to_string(i) + " has a bad range");
+    if (i > 0 && parts[i - 1].flat_end > q.flat_begin)
+      return fail(MUON_ERR_INVALID,
+                  "partitions must be sorted by flat_begin and must not overlap (at " +
+                      std::to_string(i) + ")");
+  }
+  {  // storage ranges must not overlap
+    std::vector<std::pair<int64_t, int64_t>> st;
+    for (int i = 0; i < nparts; ++i)
+      if (parts[i].flat_end > parts[i].flat_begin)
+        st.push_back({parts[i].storage_offset,
+                      parts[i].storage_offset + parts[i].flat_end - parts[i].flat_begin});
+    std::sort(st.begin(), st.end());
+    for (size_t i = 1; i < st.size(); ++i)
+      if (st[i - 1].second > st[i].first)
+        return fail(MUON_ERR_INVALID, "partitions overlap in storage");
+  }
+  std::vector<std::pair<int64_t, int64_t>> pr;
+  for (int i = 0; i < nparams; ++i) {
+    const muon_param_t& p = params[i];
+    if (p.rows < 1 || p.cols < 1)
+      return fail(MUON_ERR_INVALID, "parameter " + std::to_string(i) + " has rows or cols < 1");
+    if (p.offset < 0) return fail(MUON_ERR_INVALID, "parameter " + std::to_string(i) + " offset < 0");
+    if (p.num_heads < 0)
+      return fail(MUON_ERR_INVALID, "parameter " + std::to_string(i) + " num_heads < 0");
+    if (p.use_muon && p.num_heads > 1 && p.rows % p.num_heads != 0)
+      return fail(MUON_ERR_INVALID,
+                  "parameter " + std::to_string(i) + ": rows not a multiple of num_heads");
+    pr.push_back({p.offset, p.offset + int64_t(p.rows) * p.cols});
+  }
+  std::sort(pr.begin(), pr.end());
+  for (size_t i = 1; i < pr.size(); ++i)
+    if (pr[i - 1].second > pr[i].first) return fail(MUON_ERR_INVALID, "parameters overlap");
+
+  auto first_part = [&](int64_t flat) {   // first partition with flat_end > flat
+    int lo = 0, hi = nparts;
+    while (lo < hi) {
+      int mid = (lo + hi) / 2;
+      if (parts[mid].flat_end > flat) hi = mid; else lo = mid + 1;
+    }
+    return lo;
+  };
+  // segments of [fb, fb + n) -> appended to L.segs; returns false if not covered
+  auto add_segments = [&](int64_t fb, int64_t n, Owner& o) {
+    o.seg_begin = static_cast<int32_t>(L.segs.size());
+    int64_t covered = 0, cursor = fb;
+    for (int j = first_part(fb); j < nparts && parts[j].flat_begin < fb + n; ++j) {
+      const int64_t lo = std::max(fb, parts[j].flat_begin);
+      const int64_t hi = std::min(fb + n, parts[j].flat_end);
+      if (lo >= hi) continue;
+      if (lo != cursor) return false;   // a hole between partitions
+      L.segs.push_back({lo - fb, parts[j].storage_offset + (lo - parts[j].flat_begin), hi - lo});
+      covered += hi - lo;
+      cursor = hi;
+    }
+    o.seg_count = static_cast<int32_t>(L.segs.size()) - o.seg_begin;
+    return covered == n;
+  };
+
+  for (int i = 0; i < nparams; ++i) {
+    const muon_param_t& p = params[i];
+    const int h = (p.use_muon && p.num_heads > 1) ? p.num_heads : 1;
+    const int br = p.rows / h;
+    if (p.use_muon) ++L.n_muon_params;
+    for (int b = 0; b < h; ++b) {
+      Owner o{};
+      o.flat_begin = p.offset + int64_t(b) * br * p.cols;
+      o.is_muon = p.use_muon ? 1 : 0;
+      o.rows = p.use_muon ? br : p.rows;
+      o.cols = p.cols;
+      o.numel = int64_t(o.rows) * o.cols;
+      o.transposed = (o.is_muon && o.rows > o.cols) ? 1 : 0;
+      o.m = std::min(o.rows, o.cols);
+      o.n = std::max(o.rows, o.cols);
+      if (!add_segments(o.flat_begin, o.numel, o))
+        return fail(MUON_ERR_INVALID,
+                    "parameter " + std::to_string(i) + " is not covered by the partitions");
+      if (o.is_muon) {
+        o.ldx = static_cast<int32_t>(round_up(o.n, 8));
+        o.ldm = static_cast<int32_t>(round_up(o.m, 8));
+        o.x_off = L.x_elems;
+        o.sq_off = L.sq_elems;
+        L.x_elems += round_up(int64_t(o.m) * o.ldx, 64);
+        L.sq_elems += round_up(int64_t(o.m) * o.ldm, 64);
+        L.muon_elems += o.numel;
+        ++L.n_muon_owners;
+      } else {
+        L.aux_elems += o.numel;
+      }
+      L.owners.push_back(o);
+    }
+  }
+
+  // tiles
+  for (int oi = 0; oi < static_cast<int>(L.owners.size()); ++oi) {
+    Owner& o = L.owners[oi];
+    o.rtile_begin = static_cast<int32_t>(L.rtiles.size());
+    for (int64_t r = 0; r < o.numel; r += kReduceTile)
+      L.rtiles.push_back({oi, static_cast<int32_t>(std::min<int64_t>(kReduceTile, o.numel - r)), r});
+    o.rtile_count = static_cast<int32_t>(L.rtiles.size()) - o.rtile_begin;
+    if (o.is_muon) {
+      if (!o.transposed) {
+        const int rows_per = std::max<int>(1, kRowTile / o.cols);
+        for (int r = 0; r < o.rows; r += rows_per) {
+          ETile t{};
+          t.owner = oi; t.kind = 0; t.r0 = r; t.nr = std::min(rows_per, o.rows - r);
+          L.gtiles.push_back(t);
+          L.stiles.push_back(t);
+        }
+      } else {
+        for (int r = 0; r < o.rows; r += kTT)
+          for (int c = 0; c < o.cols; c += kTT) {
+            ETile t{};
+            t.owner = oi; t.kind = 1; t.r0 = r; t.c0 = c;
+            L.gtiles.push_back(t);
+            L.stiles.push_back(t);
+          }
+      }
+      o.ytile_begin = static_cast<int32_t>(L.ytiles.size());
+      const int yrows = std::max<int>(1, kRowTile / o.n);
+      for (int r = 0; r < o.m; r += yrows)
+        L.ytiles.push_back({oi, r, std::min(yrows, o.m - r), 0});
+      o.ytile_count = static_cast<int32_t>(L.ytiles.size()) - o.ytile_begin;
+    } else {
+      for (int64_t r = 0; r < o.numel; r += kRowTile) {
+        ETile t{};
+        t.owner = oi; t.kind = 2; t.rel_begin = r;
+        t.len = std::min<int64_t>(kRowTile, o.numel - r);
+        L.stiles.push_back(t);
+      }
+    }
+    for (int s = 0; s < o.seg_count; ++s) {
+      const Segment& sg = L.segs[o.seg_begin + s];
+      for (int64_t r = 0; r < sg.len; r += 32768)
+        L.runs.push_back({sg.storage_begin + r, std::min<int64_t>(32768, sg.len - r)});
+    }
+  }
+  return MUON_OK;
+}
+
+// ------------------------------------------------------------------ NS plan
+
+enum Engine { ENGINE_TC = 0, ENGINE_SIMT = 1, ENGINE_CONVERT = 2 };
+
+// One launch of the NS iteration: a grouped GEMM over every block, or (for
+// ENGINE_CONVERT) the fp32 -> bf16 rounding of a whole workspace region.
+struct GemmPhase {
+  int engine = ENGINE_SIMT;
+  int ab_es = 4;   // A/B operand bytes for the CUDA-core engine
+  std::vector<GemmProblem> probs;
+  std::vector<GemmTile> tiles;
+  DevBuf d_probs, d_maps, d_tiles;
+  double flops = 0.0;   // algorithmic (full products)
+  const float* conv_src = nullptr;
+  void* conv_dst = nullptr;
+  int64_t conv_n = 0;
+};
+
+struct NsPlan {
+  int esize = 2;   // bytes of X0 / Y elements
+  bool use_tc = false;
+  int method = 0, steps = 5;
+  DevBuf ws;
+  void* x0 = nullptr;
+  void* y = nullptr;
+  std::vector<std::unique_ptr<GemmPhase>> phases;
+  double flops = 0.0;
+};
+
+// Adds one GEMM D = alpha A op(B) + beta E + gamma I (per block) to a phase.
+struct PhaseBuilder {
+  GemmPhase* ph;
+  void add(const GemmProblem& p) {
+    const bool tc = ph->engine == ENGINE_TC;
+    const int idx = static_cast<int>(ph->probs.size());
+    ph->probs.push_back(p);
+    const int bm = tc ? kTcBM : kSimtTile, bn = tc ? kTcBN : kSimtTile;
+    const int tm_n = (p.M + bm - 1) / bm, tn_n = (p.N + bn - 1) / bn;
+    for (int tm = 0; tm < tm_n; ++tm)
+      for (int tn = 0; tn < tn_n; ++tn) {
+        if (p.symmetric && tn * bn + bn - 1 < tm * bm) continue;   // strictly lower tile
+        ph->tiles.push_back({idx, tm, tn});
+      }
+    ph->flops += 2.0 * p.M * double(p.N) * p.K;
+  }
+};
+
+int finish_phase(GemmPhase& ph) {
+  if (ph.engine == ENGINE_CONVERT) return MUON_OK;
+  // heavy tiles first (K descending) for the static round-robin schedule
+  std::stable_sort(ph.tiles.begin(), ph.tiles.end(), [&](const GemmTile& a, const GemmTile& b) {
+    return ph.probs[a.problem].K > ph.probs[b.problem].K;
+  });
+  MUON_CUDA_TRY(upload(ph.d_probs, ph.probs));
+  MUON_CUDA_TRY(upload(ph.d_tiles, ph.tiles));
+  if (ph.engine == ENGINE_TC) {
+    std::vector<TcMaps> maps(ph.probs.size());
+    for (size_t i = 0; i < ph.probs.size(); ++i) {
+      const GemmProblem& p = ph.probs[i];
+      std::memset(&maps[i], 0, sizeof(TcMaps));
+      bool ok = encode_bf16_2d(&maps[i].a, p.A, p.K, p.M, p.lda, kTcBK, kTcBM);
+      if (p.b_kmajor) ok = ok && encode_bf16_2d(&maps[i].b, p.B, p.K, p.N, p.ldb, kTcBK, kTcBN);
+      else ok = ok && encode_bf16_2d(&maps[i].b, p.B, p.N, p.K, p.ldb, 64, kTcBK);
+      if (!ok) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    }
+    MUON_CUDA_TRY(upload(ph.d_maps, maps));
+  }
+  return MUON_OK;
+}
+
+// Work lists of the NS iteration over every Muon block (owner), laid out in
+// per-owner slices of the workspace regions (x_off for m x n, sq_off for
+// m x m).
+//
+// standard (both modes): per step A = X X^T (symmetric: upper tiles,
+//   mirrored), B = c A A + b A (symmetric), X' = B X + a X, ping-ponging X.
+//   The oracle's A and B are exactly symmetric too (bf16 products summed
+//   in float64 are exact), so mirroring changes no value.
+// gram: R0 = X0 X0^T (symmetric, fp32 result), then the m x m recurrence
+//   P = c R R + b R + a I, Q <- P Q, T = P R, R = T P, all in FP32 with B
+//   read MN-major (no symmetry assumed: in floating point R and P are not
+//   exactly symmetric); Q is rounded to bf16 (BF16 mode) and Y = Q X0.
+int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_elems,
+                  int method, int mode, int steps, NsPlan& P) {
+  const bool bf16 = mode == MUON_OPERANDS_BF16;
+  const char* env = std::getenv("MUON_GEMM");
+  const bool force_simt = env && std::strcmp(env, "simt") == 0;
+  P.esize = bf16 ? 2 : 4;
+  P.use_tc = bf16 && !force_simt && tc_available();
+  if (bf16 && !P.use_tc && !force_simt)
+    return fail(MUON_ERR_UNSUPPORTED, "BF16 operand mode needs an sm_103 (GB300) GPU");
+  const int big = P.use_tc ? ENGINE_TC : ENGINE_SIMT;   // engine of the bf16/fp32 X products
+  P.method = method;
+  P.steps = steps;
+  const size_t es = P.esize;
+  size_t bytes = es * size_t(2 * x_elems);
+  if (method == MUON_NS_STANDARD) bytes += es * size_t(2 * sq_elems);
+  else bytes += 4 * size_t(5 * sq_elems) + (bf16 ? 2 * size_t(sq_elems) : 0);
+  MUON_CUDA_TRY(P.ws.alloc(bytes + 256));
+  char* base = P.ws.as<char>();
+  char* X[2] = {base, base + es * x_elems};
+  char* sq_base = base + es * 2 * x_elems;
+  P.x0 = X[0];
+  const float a = kNsA, b = kNsB, c = kNsC;
+
+  auto mk = [&](char* A, int64_t lda, char* B, int64_t ldb, int bk, char* D, int64_t ldd, int d_es,
+                char* E, int64_t lde, int e_es, int M, int N, int K, int sym, float al, float be,
+                float ga) {
+    GemmProblem p{};
+    p.A = A; p.B = B; p.D = D; p.E = E;
+    p.lda = lda; p.ldb = ldb; p.ldd = ldd; p.lde = lde;
+    p.M = M; p.N = N; p.K = K;
+    p.b_kmajor = bk; p.symmetric = sym;
+    p.alpha = al; p.beta = be; p.gamma = ga;
+    p.d_es = d_es; p.e_es = e_es;
+    return p;
+  };
+  auto new_phase = [&](int engine, int ab_es) {
+    P.phases.emplace_back(new GemmPhase());
+    P.phases.back()->engine = engine;
+    P.phases.back()->ab_es = ab_es;
+    return PhaseBuilder{P.phases.back().get()};
+  };
+  auto xo = [&](char* r, const Owner& o) { return r + es * o.x_off; };
+  const int E_ = static_cast<int>(es);
+
+  if (method == MUON_NS_STANDARD) {
+    char* S[2] = {sq_base, sq_base + es * sq_elems};
+    auto so = [&](char* r, const Owner& o) { return r + es * o.sq_off; };
+    for (int st = 0; st < steps; ++st) {
+      char* src = X[st & 1];
+      char* dst = X[(st + 1) & 1];
+      PhaseBuilder g = new_phase(big, E_);   // A = X X^T
+      for (const Owner& o : owners)
+        if (o.is_muon)
+          g.add(mk(xo(src, o), o.ldx, xo(src, o), o.ldx, 1, so(S[0], o), o.ldm, E_, nullptr, 0, E_,
+                   o.m, o.m, o.n, 1, 1.f, 0.f, 0.f));
+      PhaseBuilder q = new_phase(big, E_);   // B = c A A + b A
+      for (const Owner& o : owners)
+        if (o.is_muon)
+          q.add(mk(so(S[0], o), o.ldm, so(S[0], o), o.ldm, 1, so(S[1], o), o.ldm, E_, so(S[0], o),
+                   o.ldm, E_, o.m, o.m, o.m, 1, c, b, 0.f));
+      PhaseBuilder u = new_phase(big, E_);   // X' = B X + a X
+      for (const Owner& o : owners)
+        if (o.is_muon)
+          u.add(mk(so(S[1], o), o.ldm, xo(src, o), o.ldx, 0, xo(dst, o), o.ldx, E_, xo(src, o), o.ldx,
+                   E_, o.m, o.n, o.m, 0, 1.f, a, 0.f));
+    }
+    P.y = X[steps & 1];
+  } else {
+    char* F[5];
+    for (int i = 0; i < 5; ++i) F[i] = sq_base + 4 * size_t(i) * sq_elems;
+    char *R = F[0], *Pm = F[1], *Qa = F[2], *Qb = F[3], *T = F[4];
+    char* Qbf = sq_base + 4 * size_t(5) * sq_elems;
+    auto s4 = [&](char* r, const Owner& o) { return r + 4 * o.sq_off; };
+    PhaseBuilder g0 = new_phase(big, E_);   // R = X0 X0^T, fp32 result
+    for (const Owner& o : owners)
+      if (o.is_muon)
+        g0.add(mk(xo(X[0], o), o.ldx, xo(X[0], o), o.ldx, 1, s4(R, o), o.ldm, 4, nullptr, 0, 4, o.m,
+                  o.m, o.n, 1, 1.f, 0.f, 0.f));
+    char* Qcur = Qa;
+    for (int k = 0; k < steps; ++k) {
+      char* Pk = (k == 0) ? Qa : Pm;   // Q1 = P0 (Q0 = I)
+      PhaseBuilder pp = new_phase(ENGINE_SIMT, 4);   // P = c R R + b R + a I
+      for (const Owner& o : owners)
+        if (o.is_muon)
+          pp.add(mk(s4(R, o), o.ldm, s4(R, o), o.ldm, 0, s4(Pk, o), o.ldm, 4, s4(R, o), o.ldm, 4, o.m,
+                    o.m, o.m, 0, c, b, a));
+      if (k > 0) {
+        char* Qn = (Qcur == Qa) ? Qb : Qa;
+        PhaseBuilder qq = new_phase(ENGINE_SIMT, 4);   // Q <- P Q
+        for (const Owner& o : owners)
+          if (o.is_muon)
+            qq.add(mk(s4(Pk, o), o.ldm, s4(Qcur, o), o.ldm, 0, s4(Qn, o), o.ldm, 4, nullptr, 0, 4,
+                      o.m, o.m, o.m, 0, 1.f, 0.f, 0.f));
+        Qcur = Qn;
+      }
+      if (k < steps - 1) {
+        PhaseBuilder tt = new_phase(ENGINE_SIMT, 4);   // T = P R
+        for (const Owner& o : owners)
+          if (o.is_muon)
+            tt.add(mk(s4(Pk, o), o.ldm, s4(R, o), o.ldm, 0, s4(T, o), o.ldm, 4, nullptr, 0, 4, o.m,
+                      o.m, o.m, 0, 1.f, 0.f, 0.f));
+        PhaseBuilder rr = new_phase(ENGINE_SIMT, 4);   // R = T P
+        for (const Owner& o : owners)
+          if (o.is_muon)
+            rr.add(mk(s4(T, o), o.ldm, s4(Pk, o), o.ldm, 0, s4(R, o), o.ldm, 4, nullptr, 0, 4, o.m,
+                      o.m, o.m, 0, 1.f, 0.f, 0.f));
+      }
+    }
+    char* Qy = Qcur;
+    if (bf16) {   // Q rounded to bf16 for the tensor-core product
+      P.phases.emplace_back(new GemmPhase());
+      GemmPhase& cv = *P.phases.back();
+      cv.engine = ENGINE_CONVERT;
+      cv.conv_src = reinterpret_cast<const float*>(Qcur);
+      cv.conv_dst = Qbf;
+      cv.conv_n = sq_elems;
+      Qy = Qbf;
+    }
+    PhaseBuilder yy = new_phase(big, E_);   // Y = Q X0
+    for (const Owner& o : owners)
+      if (o.is_muon)
+        yy.add(mk(Qy + es * o.sq_off, o.ldm, xo(X[0], o), o.ldx, 0, xo(X[1], o), o.ldx, E_, nullptr,
+                  0, E_, o.m, o.n, o.m, 0, 1.f, 0.f, 0.f));
+    P.y = X[1];
+  }
+  for (auto& ph : P.phases) {
+    int rc = finish_phase(*ph);
+    if (rc != MUON_OK) return rc;
+    P.flops += ph->flops;
+  }
+  return MUON_OK;
+}
+
+// ------------------------------------------------------------------ table plans
+
+struct TablePlan {
+  int device = -1;
+  uint64_t hash = 0;
+  std::vector<uint8_t> key;
+  Layout L;
+  DevBuf d_owners, d_segs, d_rtiles, d_gtiles, d_stiles, d_ytiles, d_runs;
+  DevBuf d_rsum, d_ysum, d_div, d_state, d_err;
+  std::map<std::tuple<int, int, int>, std::unique_ptr<NsPlan>> ns;
+};
+
+std::vector<std::unique_ptr<TablePlan>> g_plans;
+
+uint64_t fnv1a(const void* data, size_t n, uint64_t h = 1469598103934665603ull) {
+  const uint8_t* p = static_cast<const uint8_t*>(data);
+  for (size_t i = 0; i < n; ++i) {
+    h ^= p[i];
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+int get_table_plan(const muon_param_t* params, int nparams, const muon_partition_t* parts,
+                   int nparts, TablePlan** out) {
+  if (nparams < 0 || nparts < 0) return fail(MUON_ERR_INVALID, "negative table size");
+  if ((nparams > 0 && !params) || (nparts > 0 && !parts))
+    return fail(MUON_ERR_INVALID, "table pointer is NULL");
+  std::vector<uint8_t> key(sizeof(int) * 2 + sizeof(muon_param_t) * nparams +
+                           sizeof(muon_partition_t) * nparts);
+  std::memcpy(key.data(), &nparams, sizeof(int));
+  std::memcpy(key.data() + sizeof(int), &nparts, sizeof(int));
+  if (nparams) std::memcpy(key.data() + 2 * sizeof(int), params, sizeof(muon_param_t) * nparams);
+  if (nparts)
+    std::memcpy(key.data() + 2 * sizeof(int) + sizeof(muon_param_t) * nparams, parts,
+                sizeof(muon_partition_t) * nparts);
+  const uint64_t h = fnv1a(key.data(), key.size());
+  bool known = false;   // validated before (on some device)
+  for (auto& tp : g_plans) known = known || (tp->hash == h && tp->key == key);
+  std::unique_ptr<TablePlan> tp(new TablePlan());
+  if (!known) {
+    // validation needs no GPU: a bad table is reported before any CUDA call
+    int rc = validate_and_build(params, nparams, parts, nparts, tp->L);
+    if (rc != MUON_OK) return rc;
+  }
+  int dev = 0;
+  MUON_CUDA_TRY(cudaGetDevice(&dev));
+  for (auto& p : g_plans)
+    if (p->device == dev && p->hash == h && p->key == key) {
+      *out = p.get();
+      return MUON_OK;
+    }
+  if (known) {
+    int rc = validate_and_build(params, nparams, parts, nparts, tp->L);
+    if (rc != MUON_OK) return rc;
+  }
+  tp->device = dev;
+  tp->hash = h;
+  tp->key = std::move(key);
+  const Layout& L = tp->L;
+  MUON_CUDA_TRY(upload(tp->d_owners, L.owners));
+  MUON_CUDA_TRY(upload(tp->d_segs, L.segs));
+  MUON_CUDA_TRY(upload(tp->d_rtiles, L.rtiles));
+  MUON_CUDA_TRY(upload(tp->d_gtiles, L.gtiles));
+  MUON_CUDA_TRY(upload(tp->d_stiles, L.stiles));
+  MUON_CUDA_TRY(upload(tp->d_ytiles, L.ytiles));
+  MUON_CUDA_TRY(upload(tp->d_runs, L.runs));
+  MUON_CUDA_TRY(tp->d_rsum.alloc(sizeof(double) * (L.rtiles.size() + 1)));
+  MUON_CUDA_TRY(tp->d_ysum.alloc(sizeof(double) * (L.ytiles.size() + 1)));
+  MUON_CUDA_TRY(tp->d_div.alloc(sizeof(float) * (L.owners.size() + 1)));
+  MUON_CUDA_TRY(tp->d_state.alloc(sizeof(StepState)));
+  MUON_CUDA_TRY(tp->d_err.alloc(sizeof(int)));
+  MUON_CUDA_TRY(cudaMemset(tp->d_err.p, 0, sizeof(int)));
+  *out = tp.get();
+  g_plans.push_back(std::move(tp));
+  return MUON_OK;
+}
+
+int get_ns_plan(TablePlan& tp, int method, int mode, int steps, NsPlan** out) {
+  auto k = std::make_tuple(method, mode, steps);
+  auto it = tp.ns.find(k);
+  if (it != tp.ns.end()) {
+    *out = it->second.get();
+    return MUON_OK;
+  }
+  std::unique_ptr<NsPlan> P(new NsPlan());
+  int rc = build_ns_plan(tp.L.owners, tp.L.x_elems, tp.L.sq_elems, method, mode, steps, *P);
+  if (rc != MUON_OK) return rc;
+  *out = P.get();
+  tp.ns[k] = std::move(P);
+  return MUON_OK;
+}
+
+int check_method(int ns_method, int ns_steps, int mode) {
+  if (ns_method != MUON_NS_STANDARD && ns_method != MUON_NS_GRAM)
+    return fail(MUON_ERR_UNSUPPORTED, "unknown ns_method");
+  if (ns_steps < 1 || ns_steps > 64) return fail(MUON_ERR_UNSUPPORTED, "ns_steps must be in [1, 64]");
+  if (mode != MUON_OPERANDS_BF16 && mode != MUON_OPERANDS_FP32)
+    return fail(MUON_ERR_UNSUPPORTED, "unknown operand mode");
+  return MUON_OK;
+}
+
+int enqueue_gemms(NsPlan& P, const StepState* state, int* err, cudaStream_t s) {
+  for (auto& ph : P.phases) {
+    if (ph->engine == ENGINE_CONVERT) {
+      PhaseScope sc(MUON_PHASE_NS_GEMM, s, ph->conv_n > 0 ? 1 : 0, 6.0 * ph->conv_n, 0.0);
+      launch_convert_bf16(ph->conv_src, ph->conv_dst, ph->conv_n, state, s);
+      continue;
+    }
+    PhaseScope sc(MUON_PHASE_NS_GEMM, s, ph->tiles.empty() ? 0 : 1, 0.0, ph->flops);
+    if (ph->tiles.empty()) continue;
+    if (ph->engine == ENGINE_TC) {
+      if (launch_gemm_tc(ph->d_probs.as<GemmProblem>(), ph->d_maps.as<TcMaps>(),
+                         ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()), state, err,
+                         s) != 0)
+        return fail(MUON_ERR_CUDA, "tensor-core GEMM launch setup failed");
+    } else {
+      launch_gemm_simt(ph->d_probs.as<GemmProblem>(), ph->d_tiles.as<GemmTile>(),
+                       static_cast<int>(ph->tiles.size()), ph->ab_es, state, s);
+    }
+  }
+  return MUON_OK;
+}
+
+// ------------------------------------------------------------------ NS-only plans
+
+struct SinglePlan {
+  int device, rows, cols, method, mode, steps;
+  std::vector<Owner> owners;
+  int64_t x_elems, sq_elems;
+  int ntiles;
+  DevBuf tile_sum;
+  DevBuf err;
+  NsPlan ns;
+};
+std::vector<std::unique_ptr<SinglePlan>> g_single;
+
+}  // namespace
+}  // namespace muon
+
+// ==================================================================== C ABI
+
+using namespace muon;
+
+extern "C" int muon_accumulate(float* accum, const uint16_t* grad, int64_t n, float scale,
+                               int overwrite, const muon_param_t* params, int nparams,
+                               const muon_partition_t* parts, int nparts, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_err.clear();
+  g_cnt.launches_last = 0;
+  if (!accum || !grad) return fail(MUON_ERR_INVALID, "accum or grad is NULL");
+  if (reinterpret_cast<uintptr_t>(accum) % 16 || reinterpret_cast<uintptr_t>(grad) % 8)
+    return fail(MUON_ERR_INVALID, "accum must be 16-byte and grad 8-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (params == nullptr) {
+    if (n < 0) return fail(MUON_ERR_INVALID, "n < 0");
+    if (n == 0) return MUON_OK;
+    // dense: cached run list per n
+    static std::map<std::pair<int, int64_t>, std::unique_ptr<DevBuf>> dense;
+    int dev = 0;
+    MUON_CUDA_TRY(cudaGetDevice(&dev));
+    auto key = std::make_pair(dev, n);
+    auto it = dense.find(key);
+    if (it == dense.end()) {
+      std::vector<Run> runs;
+      for (int64_t r = 0; r < n; r += 32768) runs.push_back({r, std::min<int64_t>(32768, n - r)});
+      std::unique_ptr<DevBuf> b(new DevBuf());
+      MUON_CUDA_TRY(upload(*b, runs));
+      it = dense.emplace(key, std::move(b)).first;
+    }
+    const int nruns = static_cast<int>((n + 32767) / 32768);
+    PhaseScope sc(MUON_PHASE_ACCUMULATE, s, 1, double(n) * (overwrite ? 6 : 10), 0.0);
+    launch_accumulate(accum, grad, it->second->as<Run>(), nruns, scale, overwrite, s);
+  } else {
+    TablePlan* tp = nullptr;
+    int rc = get_table_plan(params, nparams, parts, nparts, &tp);
+    if (rc != MUON_OK) return rc;
+    const double el = double(tp->L.muon_elems + tp->L.aux_elems);
+    PhaseScope sc(MUON_PHASE_ACCUMULATE, s, tp->L.runs.empty() ? 0 : 1, el * (overwrite ? 6 : 10), 0.0);
+    launch_accumulate(accum, grad, tp->d_runs.as<Run>(), static_cast<int>(tp->L.runs.size()), scale,
+                      overwrite, s);
+  }
+  MUON_CUDA_TRY(cudaGetLastError());
+  return MUON_OK;
+}
+
+extern "C" int muon_step(float* accum, float* momentum, float* master, const muon_param_t* params,
+                         int nparams, const muon_partition_t* parts, int nparts, float beta,
+                         float lr, int ns_method, int ns_steps, float clip, int operand_mode,
+                         muon_result_t* d_result, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_err.clear();
+  g_cnt.launches_last = 0;
+  int rc = check_method(ns_method, ns_steps, operand_mode);
+  if (rc != MUON_OK) return rc;
+  if (!d_result) return fail(MUON_ERR_INVALID, "d_result is NULL");
+  if (nparams > 0 && (!accum || !momentum || !master))
+    return fail(MUON_ERR_INVALID, "accum, momentum or master is NULL");
+  if (!std::isfinite(beta) || !std::isfinite(lr) || !std::isfinite(clip))
+    return fail(MUON_ERR_INVALID, "beta, lr and clip must be finite");
+  TablePlan* tp = nullptr;
+  rc = get_table_plan(params, nparams, parts, nparts, &tp);
+  if (rc != MUON_OK) return rc;
+  NsPlan* P = nullptr;
+  rc = get_ns_plan(*tp, ns_method, operand_mode, ns_steps, &P);
+  if (rc != MUON_OK) return rc;
+  const Layout& L = tp->L;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  StreamLaunchArgs a{};
+  a.owners = tp->d_owners.as<Owner>();
+  a.segs = tp->d_segs.as<Segment>();
+  a.rtiles = tp->d_rtiles.as<RTile>();
+  a.ytiles = tp->d_ytiles.as<YTile>();
+  a.n_rtiles = static_cast<int>(L.rtiles.size());
+  a.n_ytiles = static_cast<int>(L.ytiles.size());
+  a.n_owners = static_cast<int>(L.owners.size());
+  a.accum = accum;
+  a.momentum = momentum;
+  a.master = master;
+  a.rtile_sum = tp->d_rsum.as<double>();
+  a.ytile_sum = tp->d_ysum.as<double>();
+  a.owner_div = tp->d_div.as<float>();
+  a.x0 = P->x0;
+  a.y = P->y;
+  a.esize = P->esize;
+  a.beta = beta;
+  a.lr = lr;
+  a.clip = clip;
+  a.state = tp->d_state.as<StepState>();
+  a.err_flag = tp->d_err.as<int>();
+  a.result = d_result;
+  a.ns_calls = L.n_muon_owners;
+
+  const double me = double(L.muon_elems), ae = double(L.aux_elems);
+  MUON_CUDA_TRY(cudaMemsetAsync(a.state, 0, sizeof(StepState), s));
+  {
+    PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 1 : 0) + 1, me * 8 + ae * 4, 0.0);
+    launch_reduce(a, s);
+    launch_owner_norm(a, s);
+  }
+  {
+    a.etiles = tp->d_gtiles.as<ETile>();
+    a.n_etiles = static_cast<int>(L.gtiles.size());
+    PhaseScope sc(MUON_PHASE_GATHER, s, a.n_etiles ? 1 : 0, me * (12 + P->esize), 0.0);
+    launch_gather(a, s);
+  }
+  rc = enqueue_gemms(*P, a.state, tp->d_err.as<int>(), s);
+  if (rc != MUON_OK) return rc;
+  {
+    PhaseScope sc(MUON_PHASE_NORM, s, (a.n_ytiles ? 1 : 0) + 1, me * P->esize, 0.0);
+    launch_update_sumsq(a, s);
+    launch_finalize(a, s);
+  }
+  {
+    a.etiles = tp->d_stiles.as<ETile>();
+    a.n_etiles = static_cast<int>(L.stiles.size());
+    PhaseScope sc(MUON_PHASE_SCATTER, s, a.n_etiles ? 1 : 0, me * (12 + P->esize) + ae * 8, 0.0);
+    launch_scatter(a, s);
+  }
+  MUON_CUDA_TRY(cudaGetLastError());
+  g_cnt.steps += 1;
+  g_cnt.ns_calls_last = L.n_muon_owners;
+  g_cnt.muon_mats_last = L.n_muon_params;
+  return MUON_OK;
+}
+
+extern "C" int muon_newton_schulz(const void* X, void* Y, int rows, int cols, int io_dtype,
+                                  int ns_method, int ns_steps, int operand_mode, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_err.clear();
+  g_cnt.launches_last = 0;
+  int rc = check_method(ns_method, ns_steps, operand_mode);
+  if (rc != MUON_OK) return rc;
+  if (!X || !Y) return fail(MUON_ERR_INVALID, "X or Y is NULL");
+  if (X == Y) return fail(MUON_ERR_INVALID, "Y may not alias X");
+  if (rows < 1 || cols < 1) return fail(MUON_ERR_INVALID, "rows and cols must be >= 1");
+  if (io_dtype != MUON_DTYPE_BF16 && io_dtype != MUON_DTYPE_FP32)
+    return fail(MUON_ERR_INVALID, "unknown io_dtype");
+  int dev = 0;
+  MUON_CUDA_TRY(cudaGetDevice(&dev));
+  SinglePlan* sp = nullptr;
+  for (auto& p : g_single)
+    if (p->device == dev && p->rows == rows && p->cols == cols && p->method == ns_method &&
+        p->mode == operand_mode && p->steps == ns_steps)
+      sp = p.get();
+  if (!sp) {
+    std::unique_ptr<SinglePlan> np(new SinglePlan());
+    np->device = dev; np->rows = rows; np->cols = cols;
+    np->method = ns_method; np->mode = operand_mode; np->steps = ns_steps;
+    Owner o{};
+    o.rows = rows; o.cols = cols; o.numel = int64_t(rows) * cols; o.is_muon = 1;
+    o.transposed = rows > cols; o.m = std::min(rows, cols); o.n = std::max(rows, cols);
+    o.ldx = static_cast<int32_t>(round_up(o.n, 8));
+    o.ldm = static_cast<int32_t>(round_up(o.m, 8));
+    np->owners.push_back(o);
+    np->x_elems = round_up(int64_t(o.m) * o.ldx, 64);
+    np->sq_elems = round_up(int64_t(o.m) * o.ldm, 64);
+    np->ntiles = static_cast<int>((o.numel + kReduceTile - 1) / kReduceTile);
+    MUON_CUDA_TRY(np->tile_sum.alloc(sizeof(double) * (np->ntiles + 1)));
+    MUON_CUDA_TRY(np->err.alloc(sizeof(int)));
+    MUON_CUDA_TRY(cudaMemset(np->err.p, 0, sizeof(int)));
+    rc = build_ns_plan(np->owners, np->x_elems, np->sq_elems, ns_method, operand_mode, ns_steps,
+                       np->ns);
+    if (rc != MUON_OK) return rc;
+    sp = np.get();
+    g_single.push_back(std::move(np));
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int io_es = io_dtype == MUON_DTYPE_BF16 ? 2 : 4;
+  const double numel = double(rows) * cols;
+  {
+    PhaseScope sc(MUON_PHASE_REDUCE, s, 2, numel * io_es, 0.0);
+    launch_ns_sumsq(X, io_es, int64_t(rows) * cols, sp->tile_sum.as<double>(), sp->ntiles, s);
+  }
+  {
+    PhaseScope sc(MUON_PHASE_GATHER, s, 1, numel * (io_es + sp->ns.esize), 0.0);
+    launch_ns_load(X, io_es, rows, cols, sp->tile_sum.as<double>(), sp->ntiles, sp->ns.x0,
+                   sp->ns.esize, sp->owners[0].ldx, s);
+  }
+  rc = enqueue_gemms(sp->ns, nullptr, sp->err.as<int>(), s);
+  if (rc != MUON_OK) return rc;
+  {
+    PhaseScope sc(MUON_PHASE_SCATTER, s, 1, numel * (io_es + sp->ns.esize), 0.0);
+    launch_ns_store(sp->ns.y, sp->ns.esize, sp->owners[0].ldx, Y, io_es, rows, cols, s);
+  }
+  MUON_CUDA_TRY(cudaGetLastError());
+  g_cnt.ns_calls_last = 1;
+  return MUON_OK;
+}
+
+extern "C" int muon_get_stats(muon_stats_t* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!out) return fail(MUON_ERR_INVALID, "out is NULL");
+  out->steps = g_cnt.steps;
+  out->ns_calls_last_step = g_cnt.ns_calls_last;
+  out->muon_matrices = g_cnt.muon_mats_last;
+  out->kernel_launches_last_call = g_cnt.launches_last;
+  out->kernel_launches_total = g_cnt.launches_total;
+  size_t ws = 0;
+  for (auto& tp : g_plans)
+    for (auto& kv : tp->ns) ws += kv.second->ws.bytes;
+  for (auto& sp : g_single) ws += sp->ns.ws.bytes;
+  out->workspace_bytes = ws;
+  return MUON_OK;
+}
+
+extern "C" const char* muon_last_error(void) { return g_err.c_str(); }
+
+extern "C" void muon_release_workspace(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  cudaDeviceSynchronize();
+  g_plans.clear();
+  g_single.clear();
+}
+
+extern "C" int muon_device_error(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (cudaDeviceSynchronize() != cudaSuccess) return fail(MUON_ERR_CUDA, "device synchronize failed");
+  int worst = 0;
+  auto check = [&](DevBuf& b) {
+    int v = 0;
+    if (b.p && cudaMemcpy(&v, b.p, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess && v) {
+      worst = v;
+      cudaMemset(b.p, 0, sizeof(int));
+    }
+  };
+  for (auto& tp : g_plans) check(tp->d_err);
+  for (auto& sp : g_single) check(sp->err);
+  return worst;
+}
+
+extern "C" int muon_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_profile = on != 0;
+  return MUON_OK;
+}
+
+extern "C" int muon_profile_read(muon_phase_time_t* out, int nphases, int reset) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& pe : g_pending) {
+    if (cudaEventSynchronize(pe.stop) != cudaSuccess) return fail(MUON_ERR_CUDA, "event sync failed");
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, pe.start, pe.stop);
+    g_phase[pe.phase].total_ms += ms;
+    g_phase[pe.phase].algorithmic_bytes += pe.bytes;
+    g_phase[pe.phase].algorithmic_flops += pe.flops;
+    g_event_pool.push_back(pe.start);
+    g_event_pool.push_back(pe.stop);
+  }
+  g_pending.clear();
+  if (out)
+    for (int i = 0; i < nphases && i < MUON_PHASE_COUNT; ++i) out[i] = g_phase[i];
+  if (reset) std::memset(g_phase, 0, sizeof(g_phase));
+  return MUON_OK;
+}

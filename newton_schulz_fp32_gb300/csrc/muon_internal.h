@@ -1,0 +1,192 @@
+// Internal data structures of libmuon, shared by the host planner and the
+// CUDA kernels.  Plain structs only; everything here is copied to the device
+// once per plan ("static tables computed once": the split tables of
+// "Support Muon in BF16_Optimizer with FP32 gradient accumulation", review
+// thread on all_to_all_single).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/muon.h"
+
+namespace muon {
+
+// Fixed constants of the method (readings documented in the header).
+constexpr float kNsA = 3.4445f;
+constexpr float kNsB = -4.7750f;
+constexpr float kNsC = 2.0315f;
+constexpr double kNormEps = 1e-7;   // X0 = m / (||m||_F + kNormEps)
+constexpr double kClipEps = 1e-6;   // coef = min(1, clip / (norm + kClipEps))
+
+// Work granularity of the streaming kernels.
+constexpr int kReduceTile = 16384;  // elements per pass-1 tile (sum order fixed by it)
+constexpr int kRowTile = 16384;     // target elements per row-aligned 1-D tile
+constexpr int kTT = 64;             // 2-D transpose tile edge
+constexpr int kStreamThreads = 256;
+
+// A contiguous run shared by flat space and storage: the intersection of one
+// owner (head block or auxiliary parameter) with one partition.
+struct Segment {
+  int64_t rel_begin;      // first element, relative to the owner's start
+  int64_t storage_begin;  // storage index of that element
+  int64_t len;
+};
+
+// One unit of the step: a Muon head block (an NS problem) or an auxiliary
+// parameter.  Rows/cols are the block's own shape as it lies in the flat
+// buffer (row-major); m x n is the canonical NS orientation (m <= n).
+struct Owner {
+  int64_t flat_begin;
+  int64_t numel;
+  int32_t rows, cols;
+  int32_t m, n;
+  int32_t transposed;   // rows > cols: X0 = block^T
+  int32_t is_muon;
+  int32_t seg_begin, seg_count;
+  int32_t rtile_begin, rtile_count;   // pass-1 tiles of this owner
+  int32_t ytile_begin, ytile_count;   // update sum-of-squares tiles
+  int32_t ldx;          // leading dimension of the m x n workspace matrices
+  int32_t ldm;          // leading dimension of the m x m workspace matrices
+  int64_t x_off;        // element offset of this owner in each m x n region
+  int64_t sq_off;       // element offset of this owner in each m x m region
+};
+
+// Pass-1 tile: owner elements [rel_begin, rel_begin + len).
+struct RTile {
+  int32_t owner;
+  int32_t len;
+  int64_t rel_begin;
+};
+
+// Tile of the gather (pass 2) and scatter kernels.
+//   kind 0: rows [r0, r0 + nr) of a non-transposed Muon owner
+//   kind 1: 64 x 64 tile at (r0, c0) of a transposed Muon owner
+//   kind 2: elements [rel_begin, rel_begin + len) of an auxiliary owner
+struct ETile {
+  int32_t owner;
+  int32_t kind;
+  int32_t r0, nr;
+  int32_t c0, pad;
+  int64_t rel_begin;
+  int64_t len;
+};
+
+// Tile of the update sum of squares: rows [r0, r0 + nr) of an owner's
+// canonical m x n result.
+struct YTile {
+  int32_t owner;
+  int32_t r0, nr;
+  int32_t pad;
+};
+
+// Accumulate work: storage run [begin, begin + len).
+struct Run {
+  int64_t begin;
+  int64_t len;
+};
+
+// Device-side state of one step, reset at its start.
+struct StepState {
+  int32_t overflow;
+  int32_t applied;
+  float coef;
+  float norm;
+  double sumsq;
+};
+
+// One matrix product of the NS iteration:
+//   D = alpha * A op(B) + beta * E + gamma * I
+// A is M x K row-major (lda); B is N x K row-major when b_kmajor (ldb),
+// else K x N row-major; D and E are M x N row-major.  When symmetric, only
+// tiles touching the upper triangle are computed and each upper element is
+// mirrored, so D is exactly symmetric.  A and B share one element type per
+// launch (bf16 or fp32); D and E carry their own (d_es, e_es: 2 or 4 bytes).
+struct GemmProblem {
+  const void* A;
+  const void* B;
+  void* D;
+  const void* E;
+  int64_t lda, ldb, ldd, lde;
+  int32_t M, N, K;
+  int32_t b_kmajor;
+  int32_t symmetric;
+  float alpha, beta, gamma;
+  int32_t d_es, e_es;
+  int32_t pad;
+};
+
+struct GemmTile {
+  int32_t problem;
+  int32_t tm, tn;
+};
+
+// TMA descriptors of one problem for the tensor-core path.
+struct TcMaps {   // CUtensorMap carries its own 64-byte alignment
+  CUtensorMap a;
+  CUtensorMap b;
+};
+
+// ---------------------------------------------------------------- launches
+// (defined in the .cu files; all enqueue on `stream`)
+
+struct StreamLaunchArgs {
+  const Owner* owners;
+  const Segment* segs;
+  const RTile* rtiles;
+  const ETile* etiles;
+  const YTile* ytiles;
+  int n_rtiles, n_etiles, n_ytiles, n_owners;
+  float* accum;
+  float* momentum;
+  float* master;
+  double* rtile_sum;
+  double* ytile_sum;
+  float* owner_div;
+  void* x0;          // X0 region (m x n per owner)
+  const void* y;     // final NS result region
+  int esize;         // bytes per workspace element (2 = bf16, 4 = fp32)
+  float beta, lr, clip;
+  StepState* state;
+  const int* err_flag;   // set by a tensor-core kernel whose wait ran out
+  muon_result_t* result;
+  int ns_calls;
+};
+
+void launch_accumulate(float* accum, const uint16_t* grad, const Run* runs, int nruns,
+                       float scale, int overwrite, cudaStream_t s);
+void launch_reduce(const StreamLaunchArgs& a, cudaStream_t s);
+void launch_owner_norm(const StreamLaunchArgs& a, cudaStream_t s);
+void launch_gather(const StreamLaunchArgs& a, cudaStream_t s);
+void launch_update_sumsq(const StreamLaunchArgs& a, cudaStream_t s);
+void launch_finalize(const StreamLaunchArgs& a, cudaStream_t s);
+void launch_scatter(const StreamLaunchArgs& a, cudaStream_t s);
+
+// NS-only entry: one matrix, io dtype bf16 or fp32.
+void launch_ns_sumsq(const void* X, int io_esize, int64_t numel, double* tile_sum,
+                     int ntiles, cudaStream_t s);
+void launch_ns_load(const void* X, int io_esize, int rows, int cols, const double* tile_sum,
+                    int ntiles, void* X0, int esize, int ldx, cudaStream_t s);
+void launch_ns_store(const void* Yws, int esize, int ldx, void* Y, int io_esize, int rows,
+                     int cols, cudaStream_t s);
+
+// Matrix products.  ab_es selects bf16 (2) or fp32 (4) A/B operands.
+void launch_gemm_simt(const GemmProblem* probs, const GemmTile* tiles, int ntiles, int ab_es,
+                      const StepState* state, cudaStream_t s);
+// dst[i] = bf16(src[i]) for i < n
+void launch_convert_bf16(const float* src, void* dst, int64_t n, const StepState* state,
+                         cudaStream_t s);
+constexpr int kSimtTile = 128;
+
+// Tensor-core (tcgen05) path, BF16 operands.
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 256;
+constexpr int kTcBK = 64;
+bool tc_available();
+int launch_gemm_tc(const GemmProblem* probs, const TcMaps* maps, const GemmTile* tiles,
+                   int ntiles, const StepState* state, int* err_flag, cudaStream_t s);
+
+}  // namespace muon

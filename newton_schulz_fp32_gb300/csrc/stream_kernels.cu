@@ -1,0 +1,492 @@
+// Streaming (HBM-bound) kernels of the Muon step:
+//   S1  accumulate              accum += scale * bf16 grad
+//   S2  reduce (pass 1)         overflow check + per-tile sums of squares of
+//                               m' = beta*m + g (Muon) or g (auxiliary)
+//       owner_norm              per-block divisor ||m'||_F + 1e-7
+//       gather (pass 2)         momentum <- m', X0 = m' / divisor in the
+//                               canonical (rows <= cols) orientation
+//   S4  update_sumsq            per-tile sums of squares of the NS result
+//       finalize                global norm, clip coefficient, result struct
+//       scatter                 owned-slice write-back of coef*u (Muon) and
+//                               coef*g (auxiliary), master -= lr*coef*u
+// Step order and semantics follow "Run Muon once per optimizer step under
+// ZeRO-3, not once per micro-batch" ("The change": overflow check, then
+// Muon, then the gradient norm over the Muon updates, then clipping) and
+// "Support Muon in BF16_Optimizer with FP32 gradient accumulation" (PR
+// description: FP32 accumulation, full-matrix Muon, owned intersections,
+// padding excluded).
+//
+// Every reduction has a fixed shape that depends only on an owner's element
+// index, never on where partition boundaries fall, so results are bitwise
+// independent of the partition table.
+#include <cuda_bf16.h>
+
+#include "muon_internal.h"
+
+namespace muon {
+
+namespace {
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ float load_ws(const void* base, int esize, int64_t i) {
+  if (esize == 2) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
+  return reinterpret_cast<const float*>(base)[i];
+}
+
+__device__ __forceinline__ void store_ws(void* base, int esize, int64_t i, float v) {
+  if (esize == 2)
+    reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<float*>(base)[i] = v;
+}
+
+// Last segment whose rel_begin <= rel.
+__device__ __forceinline__ int find_seg(const Segment* s, int n, int64_t rel) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (s[mid].rel_begin <= rel) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Fixed-shape block reduction of one double per thread; result valid in
+// thread 0.
+template <int NT>
+__device__ __forceinline__ double block_sum(double v) {
+  __shared__ double red[NT / 32];
+  #pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  double r = 0.0;
+  if (w == 0) {
+    r = (l < NT / 32) ? red[l] : 0.0;
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  }
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ float momentum_of(float beta, float m, float g) {
+  return __fadd_rn(__fmul_rn(beta, m), g);
+}
+
+// ------------------------------------------------------------------ S1
+
+__device__ __forceinline__ float acc_one(float a, float g, float scale, int overwrite) {
+  const float sg = __fmul_rn(scale, g);
+  return overwrite ? sg : __fadd_rn(a, sg);
+}
+
+__global__ void __launch_bounds__(kStreamThreads)
+k_accumulate(float* __restrict__ accum, const uint16_t* __restrict__ grad,
+             const Run* __restrict__ runs, float scale, int overwrite) {
+  const Run r = runs[blockIdx.x];
+  const int64_t b = r.begin, e = r.begin + r.len;
+  int64_t vb = (b + 3) & ~int64_t(3);
+  if (vb > e) vb = e;
+  const int64_t ve = vb + ((e - vb) & ~int64_t(3));
+  for (int64_t i = b + threadIdx.x; i < vb; i += blockDim.x)
+    accum[i] = acc_one(accum[i], bf16_bits_to_float(grad[i]), scale, overwrite);
+  constexpr int U = 4;
+  const int64_t step = int64_t(4) * blockDim.x;
+  int64_t i = vb + int64_t(4) * threadIdx.x;
+  for (; i + (U - 1) * step < ve; i += U * step) {
+    float4 a[U];
+    uint2 g[U];
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+      g[u] = *reinterpret_cast<const uint2*>(grad + i + u * step);
+      if (!overwrite) a[u] = *reinterpret_cast<const float4*>(accum + i + u * step);
+      else a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float4 o;
+      o.x = acc_one(a[u].x, __uint_as_float(g[u].x << 16), scale, overwrite);
+      o.y = acc_one(a[u].y, __uint_as_float(g[u].x & 0xffff0000u), scale, overwrite);
+      o.z = acc_one(a[u].z, __uint_as_float(g[u].y << 16), scale, overwrite);
+      o.w = acc_one(a[u].w, __uint_as_float(g[u].y & 0xffff0000u), scale, overwrite);
+      *reinterpret_cast<float4*>(accum + i + u * step) = o;
+    }
+  }
+  for (; i < ve; i += step) {
+    const float4 a = overwrite ? make_float4(0.f, 0.f, 0.f, 0.f)
+                               : *reinterpret_cast<const float4*>(accum + i);
+    const uint2 g = *reinterpret_cast<const uint2*>(grad + i);
+    float4 o;
+    o.x = acc_one(a.x, __uint_as_float(g.x << 16), scale, overwrite);
+    o.y = acc_one(a.y, __uint_as_float(g.x & 0xffff0000u), scale, overwrite);
+    o.z = acc_one(a.z, __uint_as_float(g.y << 16), scale, overwrite);
+    o.w = acc_one(a.w, __uint_as_float(g.y & 0xffff0000u), scale, overwrite);
+    *reinterpret_cast<float4*>(accum + i) = o;
+  }
+  for (int64_t j = ve + threadIdx.x; j < e; j += blockDim.x)
+    accum[j] = acc_one(accum[j], bf16_bits_to_float(grad[j]), scale, overwrite);
+}
+
+// ------------------------------------------------------------------ S2 pass 1
+
+// Thread t of the tile handles elements tile_begin + t + k*NT in increasing
+// order, whatever segments they fall in: the sum order depends only on the
+// owner-relative index.
+__global__ void __launch_bounds__(kStreamThreads)
+k_reduce(StreamLaunchArgs a) {
+  constexpr int NT = kStreamThreads;
+  const RTile t = a.rtiles[blockIdx.x];
+  const Owner o = a.owners[t.owner];
+  const Segment* segs = a.segs + o.seg_begin;
+  const int64_t tb = t.rel_begin, te = t.rel_begin + t.len;
+  float acc = 0.f;
+  bool bad = false;
+  int si = find_seg(segs, o.seg_count, tb);
+  for (; si < o.seg_count && segs[si].rel_begin < te; ++si) {
+    const Segment sg = segs[si];
+    const int64_t lo = sg.rel_begin > tb ? sg.rel_begin : tb;
+    const int64_t hi = (sg.rel_begin + sg.len) < te ? (sg.rel_begin + sg.len) : te;
+    // first element >= lo with (rel - tb) % NT == threadIdx.x
+    const int64_t off = (lo - tb) % NT;
+    int64_t rel = lo + ((threadIdx.x - off + NT) % NT);
+    const int64_t base = sg.storage_begin - sg.rel_begin;
+    if (o.is_muon) {
+      #pragma unroll 4
+      for (; rel < hi; rel += NT) {
+        const float g = a.accum[base + rel];
+        const float m = a.momentum[base + rel];
+        bad |= !isfinite(g);
+        const float v = momentum_of(a.beta, m, g);
+        acc = __fmaf_rn(v, v, acc);
+      }
+    } else {
+      #pragma unroll 4
+      for (; rel < hi; rel += NT) {
+        const float g = a.accum[base + rel];
+        bad |= !isfinite(g);
+        acc = __fmaf_rn(g, g, acc);
+      }
+    }
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(&a.state->overflow, 1);
+  const double s = block_sum<NT>(static_cast<double>(acc));
+  if (threadIdx.x == 0) a.rtile_sum[blockIdx.x] = s;
+}
+
+__global__ void k_owner_norm(StreamLaunchArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.n_owners) return;
+  const Owner o = a.owners[i];
+  if (!o.is_muon) return;
+  double s = 0.0;
+  for (int k = 0; k < o.rtile_count; ++k) s += a.rtile_sum[o.rtile_begin + k];
+  a.owner_div[i] = static_cast<float>(sqrt(s) + kNormEps);
+}
+
+// ------------------------------------------------------------------ S2 pass 2
+
+// Calls f(rel, storage_index) for the elements [lo, hi) of one owner row,
+// lane-strided across a warp, resolving partition segments.
+template <class F>
+__device__ __forceinline__ void for_row(const Segment* segs, int nseg, int64_t lo, int64_t hi,
+                                        int lane, F&& f) {
+  int si = find_seg(segs, nseg, lo);
+  for (; si < nseg && segs[si].rel_begin < hi; ++si) {
+    const Segment sg = segs[si];
+    const int64_t plo = sg.rel_begin > lo ? sg.rel_begin : lo;
+    const int64_t phi = (sg.rel_begin + sg.len) < hi ? (sg.rel_begin + sg.len) : hi;
+    const int64_t base = sg.storage_begin - sg.rel_begin;
+    for (int64_t rel = plo + lane; rel < phi; rel += 32) f(rel, base + rel);
+  }
+}
+
+__global__ void __launch_bounds__(kStreamThreads)
+k_gather(StreamLaunchArgs a) {
+  if (a.state->overflow) return;
+  __shared__ float tile[kTT][kTT + 1];
+  const ETile t = a.etiles[blockIdx.x];
+  const Owner o = a.owners[t.owner];
+  const Segment* segs = a.segs + o.seg_begin;
+  const float d = a.owner_div[t.owner];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  char* x0 = static_cast<char*>(a.x0) + o.x_off * a.esize;
+  if (t.kind == 0) {
+    for (int r = t.r0 + warp; r < t.r0 + t.nr; r += nw) {
+      const int64_t rb = int64_t(r) * o.cols;
+      for_row(segs, o.seg_count, rb, rb + o.cols, lane, [&](int64_t rel, int64_t st) {
+        const float mv = momentum_of(a.beta, a.momentum[st], a.accum[st]);
+        a.momentum[st] = mv;
+        store_ws(x0, a.esize, int64_t(r) * o.ldx + (rel - rb), __fdiv_rn(mv, d));
+      });
+    }
+  } else {
+    // transposed block: rows x cols with rows > cols; X0 = block^T (cols x rows)
+    const int r_end = min(t.r0 + kTT, o.rows), c_end = min(t.c0 + kTT, o.cols);
+    for (int rr = warp; rr < kTT; rr += nw) {
+      const int r = t.r0 + rr;
+      if (r >= r_end) break;
+      const int64_t rb = int64_t(r) * o.cols;
+      for_row(segs, o.seg_count, rb + t.c0, rb + c_end, lane, [&](int64_t rel, int64_t st) {
+        const float mv = momentum_of(a.beta, a.momentum[st], a.accum[st]);
+        a.momentum[st] = mv;
+        tile[rr][rel - rb - t.c0] = __fdiv_rn(mv, d);
+      });
+    }
+    __syncthreads();
+    for (int cc = warp; cc < kTT; cc += nw) {
+      const int c = t.c0 + cc;
+      if (c >= c_end) break;
+      for (int rr = lane; rr < kTT && t.r0 + rr < r_end; rr += 32)
+        store_ws(x0, a.esize, int64_t(c) * o.ldx + t.r0 + rr, tile[rr][cc]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ S4a
+
+__global__ void __launch_bounds__(kStreamThreads)
+k_update_sumsq(StreamLaunchArgs a) {
+  if (a.state->overflow) return;
+  const YTile t = a.ytiles[blockIdx.x];
+  const Owner o = a.owners[t.owner];
+  const char* y = static_cast<const char*>(a.y) + o.x_off * a.esize;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float acc = 0.f;
+  for (int r = t.r0 + warp; r < t.r0 + t.nr; r += kStreamThreads / 32)
+    for (int c = lane; c < o.n; c += 32) {
+      const float v = load_ws(y, a.esize, int64_t(r) * o.ldx + c);
+      acc = __fmaf_rn(v, v, acc);
+    }
+  const double s = block_sum<kStreamThreads>(static_cast<double>(acc));
+  if (threadIdx.x == 0) a.ytile_sum[blockIdx.x] = s;
+}
+
+constexpr int kFinThreads = 1024;
+
+__global__ void __launch_bounds__(kFinThreads)
+k_finalize(StreamLaunchArgs a) {
+  if (a.state->overflow) {
+    if (threadIdx.x == 0) {
+      a.state->applied = 0;
+      a.state->coef = 0.f;
+      muon_result_t r{0, 0, 0.f, 0.f};
+      *a.result = r;
+    }
+    return;
+  }
+  double s = 0.0;
+  for (int i = threadIdx.x; i < a.n_ytiles; i += kFinThreads) s += a.ytile_sum[i];
+  for (int i = threadIdx.x; i < a.n_rtiles; i += kFinThreads)
+    if (!a.owners[a.rtiles[i].owner].is_muon) s += a.rtile_sum[i];
+  const double tot = block_sum<kFinThreads>(s);
+  if (threadIdx.x == 0) {
+    const double norm = sqrt(tot);
+    double coef = 1.0;
+    if (a.clip > 0.f) {
+      coef = static_cast<double>(a.clip) / (norm + kClipEps);
+      if (coef > 1.0) coef = 1.0;
+    }
+    const int applied = (a.err_flag != nullptr && *a.err_flag != 0) ? -1 : 1;
+    a.state->applied = applied;
+    a.state->coef = static_cast<float>(coef);
+    a.state->norm = static_cast<float>(norm);
+    a.state->sumsq = tot;
+    muon_result_t r{applied, a.ns_calls, static_cast<float>(norm), static_cast<float>(coef)};
+    *a.result = r;
+  }
+}
+
+// ------------------------------------------------------------------ S4b
+
+__global__ void __launch_bounds__(kStreamThreads)
+k_scatter(StreamLaunchArgs a) {
+  if (a.state->overflow) return;
+  __shared__ float tile[kTT][kTT + 1];
+  const float coef = a.state->coef, lr = a.lr;
+  const ETile t = a.etiles[blockIdx.x];
+  const Owner o = a.owners[t.owner];
+  const Segment* segs = a.segs + o.seg_begin;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  if (t.kind == 2) {
+    // auxiliary parameter: accum = coef * g, master untouched
+    const int64_t te = t.rel_begin + t.len;
+    int si = find_seg(segs, o.seg_count, t.rel_begin);
+    for (; si < o.seg_count && segs[si].rel_begin < te; ++si) {
+      const Segment sg = segs[si];
+      const int64_t lo = sg.rel_begin > t.rel_begin ? sg.rel_begin : t.rel_begin;
+      const int64_t hi = (sg.rel_begin + sg.len) < te ? (sg.rel_begin + sg.len) : te;
+      const int64_t base = sg.storage_begin - sg.rel_begin;
+      for (int64_t rel = lo + threadIdx.x; rel < hi; rel += blockDim.x)
+        a.accum[base + rel] = __fmul_rn(coef, a.accum[base + rel]);
+    }
+    return;
+  }
+  const char* y = static_cast<const char*>(a.y) + o.x_off * a.esize;
+  if (t.kind == 0) {
+    for (int r = t.r0 + warp; r < t.r0 + t.nr; r += nw) {
+      const int64_t rb = int64_t(r) * o.cols;
+      for_row(segs, o.seg_count, rb, rb + o.cols, lane, [&](int64_t rel, int64_t st) {
+        const float v = __fmul_rn(coef, load_ws(y, a.esize, int64_t(r) * o.ldx + (rel - rb)));
+        a.accum[st] = v;
+        a.master[st] = __fsub_rn(a.master[st], __fmul_rn(lr, v));
+      });
+    }
+  } else {
+    const int r_end = min(t.r0 + kTT, o.rows), c_end = min(t.c0 + kTT, o.cols);
+    // Y is cols x rows here: Y row c holds block column c
+    for (int cc = warp; cc < kTT; cc += nw) {
+      const int c = t.c0 + cc;
+      if (c >= c_end) break;
+      for (int rr = lane; rr < kTT && t.r0 + rr < r_end; rr += 32)
+        tile[rr][cc] = load_ws(y, a.esize, int64_t(c) * o.ldx + t.r0 + rr);
+    }
+    __syncthreads();
+    for (int rr = warp; rr < kTT; rr += nw) {
+      const int r = t.r0 + rr;
+      if (r >= r_end) break;
+      const int64_t rb = int64_t(r) * o.cols;
+      for_row(segs, o.seg_count, rb + t.c0, rb + c_end, lane, [&](int64_t rel, int64_t st) {
+        const float v = __fmul_rn(coef, tile[rr][rel - rb - t.c0]);
+        a.accum[st] = v;
+        a.master[st] = __fsub_rn(a.master[st], __fmul_rn(lr, v));
+      });
+    }
+  }
+}
+
+// ------------------------------------------------------------------ NS-only entry
+
+__global__ void __launch_bounds__(kStreamThreads)
+k_ns_sumsq(const void* X, int io_esize, int64_t numel, double* tile_sum) {
+  const int64_t tb = int64_t(blockIdx.x) * kReduceTile;
+  const int64_t te = min(tb + kReduceTile, numel);
+  float acc = 0.f;
+  #pragma unroll 4
+  for (int64_t i = tb + threadIdx.x; i < te; i += kStreamThreads) {
+    const float v = load_ws(X, io_esize, i);
+    acc = __fmaf_rn(v, v, acc);
+  }
+  const double s = block_sum<kStreamThreads>(static_cast<double>(acc));
+  if (threadIdx.x == 0) tile_sum[blockIdx.x] = s;
+}
+
+__global__ void __launch_bounds__(kFinThreads)
+k_ns_norm(double* tile_sum, int ntiles) {
+  double s = 0.0;
+  for (int i = threadIdx.x; i < ntiles; i += kFinThreads) s += tile_sum[i];
+  const double tot = block_sum<kFinThreads>(s);
+  // the divisor is stored as a float in slot ntiles
+  if (threadIdx.x == 0)
+    reinterpret_cast<float*>(tile_sum + ntiles)[0] = static_cast<float>(sqrt(tot) + kNormEps);
+}
+
+// X (rows x cols, io dtype) -> X0 (m x n canonical, workspace dtype) = X / d
+__global__ void __launch_bounds__(kStreamThreads)
+k_ns_load(const void* X, int io_esize, int rows, int cols, const double* tile_sum, int ntiles,
+          void* X0, int esize, int ldx) {
+  __shared__ float tile[kTT][kTT + 1];
+  const float d = reinterpret_cast<const float*>(tile_sum + ntiles)[0];
+  const int r0 = blockIdx.y * kTT, c0 = blockIdx.x * kTT;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool tr = rows > cols;
+  for (int rr = warp; rr < kTT; rr += 8) {
+    const int r = r0 + rr;
+    if (r >= rows) break;
+    for (int cc = lane; cc < kTT && c0 + cc < cols; cc += 32) {
+      const float v = __fdiv_rn(load_ws(X, io_esize, int64_t(r) * cols + c0 + cc), d);
+      if (tr) tile[rr][cc] = v;
+      else store_ws(X0, esize, int64_t(r) * ldx + c0 + cc, v);
+    }
+  }
+  if (!tr) return;
+  __syncthreads();
+  for (int cc = warp; cc < kTT; cc += 8) {
+    const int c = c0 + cc;
+    if (c >= cols) break;
+    for (int rr = lane; rr < kTT && r0 + rr < rows; rr += 32)
+      store_ws(X0, esize, int64_t(c) * ldx + r0 + rr, tile[rr][cc]);
+  }
+}
+
+// Y workspace (m x n canonical) -> Y (rows x cols, io dtype)
+__global__ void __launch_bounds__(kStreamThreads)
+k_ns_store(const void* Yws, int esize, int ldx, void* Y, int io_esize, int rows, int cols) {
+  __shared__ float tile[kTT][kTT + 1];
+  const int r0 = blockIdx.y * kTT, c0 = blockIdx.x * kTT;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool tr = rows > cols;
+  if (!tr) {
+    for (int rr = warp; rr < kTT; rr += 8) {
+      const int r = r0 + rr;
+      if (r >= rows) break;
+      for (int cc = lane; cc < kTT && c0 + cc < cols; cc += 32)
+        store_ws(Y, io_esize, int64_t(r) * cols + c0 + cc,
+                 load_ws(Yws, esize, int64_t(r) * ldx + c0 + cc));
+    }
+    return;
+  }
+  for (int cc = warp; cc < kTT; cc += 8) {
+    const int c = c0 + cc;
+    if (c >= cols) break;
+    for (int rr = lane; rr < kTT && r0 + rr < rows; rr += 32)
+      tile[rr][cc] = load_ws(Yws, esize, int64_t(c) * ldx + r0 + rr);
+  }
+  __syncthreads();
+  for (int rr = warp; rr < kTT; rr += 8) {
+    const int r = r0 + rr;
+    if (r >= rows) break;
+    for (int cc = lane; cc < kTT && c0 + cc < cols; cc += 32)
+      store_ws(Y, io_esize, int64_t(r) * cols + c0 + cc, tile[rr][cc]);
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+
+void launch_accumulate(float* accum, const uint16_t* grad, const Run* runs, int nruns,
+                       float scale, int overwrite, cudaStream_t s) {
+  if (nruns > 0) k_accumulate<<<nruns, kStreamThreads, 0, s>>>(accum, grad, runs, scale, overwrite);
+}
+void launch_reduce(const StreamLaunchArgs& a, cudaStream_t s) {
+  if (a.n_rtiles > 0) k_reduce<<<a.n_rtiles, kStreamThreads, 0, s>>>(a);
+}
+void launch_owner_norm(const StreamLaunchArgs& a, cudaStream_t s) {
+  if (a.n_owners > 0) k_owner_norm<<<(a.n_owners + 127) / 128, 128, 0, s>>>(a);
+}
+void launch_gather(const StreamLaunchArgs& a, cudaStream_t s) {
+  if (a.n_etiles > 0) k_gather<<<a.n_etiles, kStreamThreads, 0, s>>>(a);
+}
+void launch_update_sumsq(const StreamLaunchArgs& a, cudaStream_t s) {
+  if (a.n_ytiles > 0) k_update_sumsq<<<a.n_ytiles, kStreamThreads, 0, s>>>(a);
+}
+void launch_finalize(const StreamLaunchArgs& a, cudaStream_t s) {
+  k_finalize<<<1, kFinThreads, 0, s>>>(a);
+}
+void launch_scatter(const StreamLaunchArgs& a, cudaStream_t s) {
+  if (a.n_etiles > 0) k_scatter<<<a.n_etiles, kStreamThreads, 0, s>>>(a);
+}
+
+void launch_ns_sumsq(const void* X, int io_esize, int64_t numel, double* tile_sum, int ntiles,
+                     cudaStream_t s) {
+  k_ns_sumsq<<<ntiles, kStreamThreads, 0, s>>>(X, io_esize, numel, tile_sum);
+  k_ns_norm<<<1, kFinThreads, 0, s>>>(tile_sum, ntiles);
+}
+void launch_ns_load(const void* X, int io_esize, int rows, int cols, const double* tile_sum,
+                    int ntiles, void* X0, int esize, int ldx, cudaStream_t s) {
+  dim3 g((cols + kTT - 1) / kTT, (rows + kTT - 1) / kTT);
+  k_ns_load<<<g, kStreamThreads, 0, s>>>(X, io_esize, rows, cols, tile_sum, ntiles, X0, esize, ldx);
+}
+void launch_ns_store(const void* Yws, int esize, int ldx, void* Y, int io_esize, int rows,
+                     int cols, cudaStream_t s) {
+  dim3 g((cols + kTT - 1) / kTT, (rows + kTT - 1) / kTT);
+  k_ns_store<<<g, kStreamThreads, 0, s>>>(Yws, esize, ldx, Y, io_esize, rows, cols);
+}
+
+}  // namespace muon

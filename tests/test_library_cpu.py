@@ -1,0 +1,99 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports
+every symbol the header declares, and rejects bad tables and arguments on
+the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import newton_schulz_fp32_gb300 as nsg
+import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 1 << 20   # a non-NULL, aligned address that is never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nsg.build()
+    return nsg.lib()
+
+
+def header_symbols():
+    with open(os.path.join(ROOT, "include", "muon.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"MUON_API\s+[\w\s\*]+?\b(muon_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = header_symbols()
+    assert len(syms) >= 9
+    assert sorted(nsg.EXPORTED) == syms
+    for s in syms:
+        assert hasattr(lib, s), s
+
+
+def test_struct_sizes_match_header():
+    assert nsg.PARAM_DTYPE.itemsize == 24 and nsg.PART_DTYPE.itemsize == 24
+    assert nsg.PARAM_DTYPE == wl.PARAM_DTYPE and nsg.PART_DTYPE == wl.PART_DTYPE
+    assert ctypes.sizeof(nsg.Stats) == 48 and ctypes.sizeof(nsg.PhaseTime) == 32
+
+
+def _step(lib, params, parts, **kw):
+    args = dict(beta=0.95, lr=0.02, method=0, steps=5, clip=0.0, mode=0)
+    args.update(kw)
+    p = np.ascontiguousarray(params, dtype=nsg.PARAM_DTYPE)
+    q = np.ascontiguousarray(parts, dtype=nsg.PART_DTYPE)
+    return lib.muon_step(FAKE, FAKE, FAKE, p.ctypes.data if len(p) else None, len(p),
+                         q.ctypes.data if len(q) else None, len(q), args["beta"], args["lr"],
+                         args["method"], args["steps"], args["clip"], args["mode"], FAKE, None)
+
+
+def test_invalid_tables_rejected_on_host(lib):
+    lay = wl.tiny_layout()
+    P, Q = lay.params.copy(), lay.parts.copy()
+    cases = []
+    bad = P.copy(); bad["offset"][1] = 100                       # overlaps the first matrix
+    cases.append((bad, Q, "overlap"))
+    bad = P.copy(); bad["offset"][0] = lay.flat_size - 5         # runs past the partitions
+    cases.append((bad, Q, "covered"))
+    bad = P.copy(); bad["rows"][0] = 0
+    cases.append((bad, Q, "rows or cols"))
+    bad = P.copy(); bad["num_heads"][0] = 4                      # 17 % 4 != 0
+    cases.append((bad, Q, "num_heads"))
+    badq = Q.copy(); badq[[0, 1]] = badq[[1, 0]]                 # unsorted
+    cases.append((P, badq, "sorted"))
+    badq = Q.copy(); badq["storage_offset"][1] = 50              # storage overlap
+    cases.append((P, badq, "storage"))
+    badq = Q.copy(); badq["flat_end"][0] = 100                   # hole inside the first matrix
+    cases.append((P, badq, "covered"))
+    for params, parts, word in cases:
+        rc = _step(lib, params, parts)
+        assert rc == nsg.MUON_ERR_INVALID, (word, rc)
+        assert word in lib.muon_last_error().decode(), lib.muon_last_error()
+
+
+def test_unsupported_arguments(lib):
+    lay = wl.tiny_layout()
+    assert _step(lib, lay.params, lay.parts, steps=0) == nsg.MUON_ERR_UNSUPPORTED
+    assert _step(lib, lay.params, lay.parts, method=7) == nsg.MUON_ERR_UNSUPPORTED
+    assert _step(lib, lay.params, lay.parts, mode=3) == nsg.MUON_ERR_UNSUPPORTED
+    assert _step(lib, lay.params, lay.parts, lr=float("nan")) == nsg.MUON_ERR_INVALID
+
+
+def test_valid_tables_without_gpu_fail_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    lay = wl.gpt2_small_layout(layers=1)
+    assert _step(lib, lay.params, lay.parts) == nsg.MUON_ERR_CUDA
+    assert lib.muon_last_error().decode() != ""
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(nsg, "_lib", None)
+    monkeypatch.setattr(nsg, "LIB_PATH", "/nonexistent/libmuon.so")
+    with pytest.raises(nsg.MuonError):
+        nsg.lib()
