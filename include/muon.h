@@ -167,6 +167,33 @@ MUON_API int muon_step(float* accum, float* momentum, float* master,
 MUON_API int muon_newton_schulz(const void* X, void* Y, int rows, int cols, int io_dtype,
                        int ns_method, int ns_steps, int operand_mode, void* stream);
 
+/* Newton-Schulz of one matrix, exactly as muon_newton_schulz (same
+ * arguments, kernels and results), for callers that cannot allocate device
+ * memory: code that runs while a stream is being captured into a CUDA
+ * graph, processes whose device memory belongs to an allocator that must
+ * not be bypassed, runtimes that forbid allocation after start-up.  It
+ * calls no cudaMalloc/cudaFree and no allocating library routine; all of
+ * its scratch (norm partials, the X and m x m work matrices, GEMM and TMA
+ * descriptors) sits in one fixed 16 MiB __device__ array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  The pages have no counterpart of this entry point.
+ *   Limits: rows * cols <= MUON_NOALLOC_MAX_ELEMS, min(rows, cols) <=
+ *   MUON_NOALLOC_MAX_MIN_DIM, max(rows, cols) <= MUON_NOALLOC_MAX_DIM;
+ *   larger matrices return MUON_ERR_UNSUPPORTED (see muon_last_error()).
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *   that first call before any stream capture.
+ *   All calls share the one array and leave their contents in it: two
+ *   calls whose work overlaps on the GPU (different streams or host
+ *   threads) race and corrupt each other's results.
+ *   The descriptors are copied from host memory on `stream` each call. */
+#define MUON_NOALLOC_MAX_ELEMS 1048576
+#define MUON_NOALLOC_MAX_MIN_DIM 512
+#define MUON_NOALLOC_MAX_DIM 16384
+MUON_API int muon_newton_schulz_noalloc(const void* X, void* Y, int rows, int cols,
+                                        int io_dtype, int ns_method, int ns_steps,
+                                        int operand_mode, void* stream);
+
 /* Host-side counters (no GPU work).  Returns MUON_OK. */
 MUON_API int muon_get_stats(muon_stats_t* out);
 

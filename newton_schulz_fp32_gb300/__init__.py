@@ -34,7 +34,7 @@ PHASES = ["accumulate", "reduce", "gather", "ns_gemm", "norm", "scatter"]
 # Every symbol include/muon.h declares.
 EXPORTED = ["muon_accumulate", "muon_step", "muon_newton_schulz", "muon_get_stats",
             "muon_last_error", "muon_release_workspace", "muon_device_error",
-            "muon_profile_enable", "muon_profile_read"]
+            "muon_profile_enable", "muon_profile_read", "muon_newton_schulz_noalloc"]
 
 
 class MuonError(RuntimeError):
@@ -74,12 +74,14 @@ def lib():
         L.muon_accumulate.argtypes = [P, P, I64, F, I, P, I, P, I, P]
         L.muon_step.argtypes = [P, P, P, P, I, P, I, F, F, I, I, F, I, P, P]
         L.muon_newton_schulz.argtypes = [P, P, I, I, I, I, I, I, P]
+        L.muon_newton_schulz_noalloc.argtypes = [P, P, I, I, I, I, I, I, P]
         L.muon_get_stats.argtypes = [ctypes.POINTER(Stats)]
         L.muon_last_error.restype = ctypes.c_char_p
         L.muon_release_workspace.restype = None
         L.muon_profile_enable.argtypes = [I]
         L.muon_profile_read.argtypes = [ctypes.POINTER(PhaseTime), I, I]
-        for name in ("muon_accumulate", "muon_step", "muon_newton_schulz", "muon_get_stats",
+        for name in ("muon_accumulate", "muon_step", "muon_newton_schulz",
+                     "muon_newton_schulz_noalloc", "muon_get_stats",
                      "muon_device_error", "muon_profile_enable", "muon_profile_read"):
             getattr(L, name).restype = I
         _lib = L

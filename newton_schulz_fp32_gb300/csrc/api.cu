@@ -680,6 +680,12 @@ struct SinglePlan {
 std::vector<std::unique_ptr<SinglePlan>> g_single;
 
 }  // namespace
+
+void set_last_error(const char* msg) {
+  if (msg) g_err = msg;
+  else g_err.clear();
+}
+
 }  // namespace muon
 
 // ==================================================================== C ABI

@@ -181,6 +181,9 @@ void launch_convert_bf16(const float* src, void* dst, int64_t n, const StepState
                          cudaStream_t s);
 constexpr int kSimtTile = 128;
 
+// Sets (msg != nullptr) or clears the text muon_last_error() returns.
+void set_last_error(const char* msg);
+
 // Tensor-core (tcgen05) path, BF16 operands.
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
