@@ -263,6 +263,99 @@ def run_gpu(args, rank, world):
     return lay, desc, ms, e2e_ms, h2d, phases, clk, launches
 
 
+def timed(torch, nsg, fn, steps, warmup, stream):
+    """Warm-up, then CUDA-event time of `steps` calls on `stream`, with the
+    library's per-phase profile over the timed calls."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    nsg.profile_read(reset=True)
+    nsg.profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    nsg.profile_enable(False)
+    phases = nsg.profile_read(reset=True)
+    if nsg.device_error() != 0:
+        raise RuntimeError("a kernel reported a device error")
+    return e0.elapsed_time(e1) / steps, phases
+
+
+def run_sweep(args, peaks, peak_src):
+    """Newton-Schulz of single matrices (X ~ bf16 N(0,1)), one JSON line per
+    shape: time per NS call and formula TFLOP/s, 5(4m^2n + 2m^3) for
+    standard, 4m^2n + 34m^3 for gram."""
+    import torch
+    import newton_schulz_fp32_gb300 as nsg
+    nsg.build()
+    stream = torch.cuda.Stream()
+    shapes = [tuple(int(v) for v in s.split("x")) for s in args.shapes.split(",")] if args.shapes \
+        else wl.SWEEP_SHAPES
+    gen = torch.Generator(device="cuda").manual_seed(wl.CONFIG_SEED["sweep"])
+    for (r, c) in shapes:
+        with torch.cuda.stream(stream):
+            X = torch.randn((r, c), generator=gen, device="cuda", dtype=torch.float32)
+            X = X.to(torch.bfloat16) if args.mode == "bf16" else X
+            Y = torch.empty_like(X)
+        torch.cuda.synchronize()
+        m, n = min(r, c), max(r, c)
+        flops = 5 * (4.0 * m * m * n + 2.0 * m ** 3) if args.ns_method == "standard" \
+            else 4.0 * m * m * n + 34.0 * m ** 3
+        ms, ph = timed(torch, nsg, lambda: nsg.newton_schulz(X, Y, args.ns_method, 5, args.mode,
+                                                             stream=stream),
+                       args.steps, args.warmup, stream)
+        g = ph["ns_gemm"]
+        tf = flops / (ms * 1e-3) / 1e12
+        peak = peak_value(peaks, "bf16_tflops") if args.mode == "bf16" else None
+        print(json.dumps({"metric": "NS time per matrix", "value": ms, "unit": "ms",
+                          "config": {"workload": f"ns sweep {r}x{c}", "ns_method": args.ns_method,
+                                     "operand_mode": args.mode},
+                          "ns_tflops": tf, "frac_of_peak": (tf / peak) if peak else None,
+                          "peak_source": peak_src,
+                          "gemm_ms": g["ms"] / args.steps, "gemm_launches": g["launches"] / args.steps,
+                          "gemm_tflops_on_gemm_time": g["flops"] / max(g["ms"] * 1e-3, 1e-12) / 1e12}))
+        del X, Y
+        nsg.release_workspace()
+        torch.cuda.empty_cache()
+
+
+def run_ragged(args, peaks, peak_src):
+    """8192 small matrices (rows {32..256} x cols {128..1024}, half tall),
+    fp32 gradients written into accum, one gram Muon step."""
+    import torch
+    import newton_schulz_fp32_gb300 as nsg
+    nsg.build()
+    seed = wl.CONFIG_SEED["ragged"]
+    lay = wl.ragged_layout(8192, seed=seed)
+    rng = wl.rng_for(seed, 1)
+    scales = 10.0 ** rng.uniform(-5, 0, len(lay.specs))
+    mats = [(wl.rng_for(seed, 2, i).standard_normal((s.rows, s.cols), dtype=np.float32)
+             * np.float32(scales[i])) for i, s in enumerate(lay.specs)]
+    stream = torch.cuda.Stream()
+    g0 = torch.from_numpy(wl.pack(lay, mats)).cuda()
+    acc = g0.clone()
+    mom = torch.zeros_like(acc)
+    mst = torch.zeros_like(acc)
+    res = torch.zeros(4, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+
+    def step():
+        with torch.cuda.stream(stream):
+            acc.copy_(g0)
+        nsg.step(acc, mom, mst, lay.params, lay.parts, 0.95, 0.02, "gram", 5, 0.0, args.mode,
+                 result=res, stream=stream)
+    ms, ph = timed(torch, nsg, step, args.steps, args.warmup, stream)
+    flops = ns_formula_flops(lay, "gram")
+    print(json.dumps({"metric": "Muon step time", "value": ms, "unit": "ms",
+                      "config": {"workload": "ragged 8192 matrices, gram NS x5", "operand_mode": args.mode,
+                                 "elements": lay.n_muon_elements},
+                      "ns_tflops_gram_flops": flops / (ph["ns_gemm"]["ms"] / args.steps * 1e-3) / 1e12,
+                      "phases_ms_per_step": {k: ph[k]["ms"] / args.steps for k in ph}}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -273,8 +366,15 @@ def main():
     ap.add_argument("--mode", default="bf16", choices=["bf16", "fp32"])
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="gpt2", choices=["gpt2", "sweep", "ragged"],
+                    help="gpt2 is the benchmark line; sweep and ragged print extra lines")
+    ap.add_argument("--shapes", default="", help="sweep shapes, e.g. 4096x4096,4096x16384")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.workload != "gpt2" and args.impl == "ours":
+        peaks, peak_src = load_peaks()
+        (run_sweep if args.workload == "sweep" else run_ragged)(args, peaks, peak_src)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

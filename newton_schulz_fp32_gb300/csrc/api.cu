@@ -126,42 +126,6 @@ struct PhaseScope {
   }
 };
 
-// ------------------------------------------------------------------ TMA encode
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// bf16 2-D map: inner extent `inner`, `outer` rows of `ld` elements.
-bool encode_bf16_2d(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld,
-                    uint32_t box_inner, uint32_t box_outer) {
-  EncodeTiledFn fn = get_encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // ------------------------------------------------------------------ layout (table plan)
 
 struct Layout {
@@ -384,14 +348,9 @@ int finish_phase(GemmPhase& ph) {
   MUON_CUDA_TRY(upload(ph.d_tiles, ph.tiles));
   if (ph.engine == ENGINE_TC) {
     std::vector<TcMaps> maps(ph.probs.size());
-    for (size_t i = 0; i < ph.probs.size(); ++i) {
-      const GemmProblem& p = ph.probs[i];
-      std::memset(&maps[i], 0, sizeof(TcMaps));
-      bool ok = encode_bf16_2d(&maps[i].a, p.A, p.K, p.M, p.lda, kTcBK, kTcBM);
-      if (p.b_kmajor) ok = ok && encode_bf16_2d(&maps[i].b, p.B, p.K, p.N, p.ldb, kTcBK, kTcBN);
-      else ok = ok && encode_bf16_2d(&maps[i].b, p.B, p.N, p.K, p.ldb, 64, kTcBK);
-      if (!ok) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    }
+    for (size_t i = 0; i < ph.probs.size(); ++i)
+      if (!tc_encode_maps(ph.probs[i], &maps[i]))
+        return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     MUON_CUDA_TRY(upload(ph.d_maps, maps));
   }
   return MUON_OK;

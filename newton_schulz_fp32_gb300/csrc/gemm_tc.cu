@@ -25,6 +25,8 @@
 // error code, stops issuing work, frees its tensor memory and exits.
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "muon_internal.h"
 
 namespace muon {
@@ -37,7 +39,16 @@ constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;                // 2 accumulators x 256 fp32 columns
 constexpr int NTHREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+// Epilogue staging per epilogue warp: two 32 x 32 bf16 addend chunks (TMA
+// loads, 64-byte swizzle) and one 32 x 32 output chunk (TMA store; bf16 with
+// 64-byte or fp32 with 128-byte swizzle).  Every buffer is 1 KB aligned.
+constexpr int EPI_E_BYTES = 32 * 32 * 2;                                 // 2 KB
+constexpr int EPI_D_BYTES = 32 * 32 * 4;                                 // 4 KB
+constexpr int EPI_WARP_BYTES = 2 * EPI_E_BYTES + EPI_D_BYTES;            // 8 KB
+constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 4 + 8;   // full, empty, tfull x2, tempty x2, E x2 per epilogue warp
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 enum : int { ERR_TIMEOUT_PRODUCER = 1, ERR_TIMEOUT_MMA = 2, ERR_TIMEOUT_EPILOGUE = 3 };
@@ -100,6 +111,33 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Byte offsets inside a swizzled 32 x 32 chunk: 64-byte rows with the
+// 64-byte swizzle (16-byte granule index XOR bits 7-8 of the offset) for
+// bf16, 128-byte rows with the 128-byte swizzle (XOR bits 7-9) for fp32.
+__device__ __forceinline__ uint32_t sw64(int row, int granule) {
+  return uint32_t(row) * 64u + (uint32_t(granule ^ ((row >> 1) & 3)) << 4);
+}
+__device__ __forceinline__ uint32_t sw128(int row, int granule) {
+  return uint32_t(row) * 128u + (uint32_t(granule ^ (row & 7)) << 4);
 }
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
@@ -170,6 +208,105 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Epilogue of one 32 x 32 output chunk held by one warp (lane = row):
+//   x = alpha * acc + beta * E + gamma * [row == col]
+// E arrives by TMA in `ebuf` (64-byte swizzle, conflict-free row reads).
+// The result is staged in `dbuf` in the swizzled layout and written by one
+// TMA store (which also clips rows >= M and columns >= N).  Symmetric
+// products: a diagonal chunk is symmetrised in `dbuf` (lower = mirror of the
+// rounded upper) before the store; a chunk above the diagonal is also
+// written transposed to the mirror position with direct stores (lanes hold
+// consecutive rows, so each store instruction covers 64 or 128 contiguous
+// bytes).
+__device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, const TcMaps* mp, const float* v,
+                                               int gm0, int gn0, int lane, bool diag,
+                                               const uint8_t* ebuf, uint8_t* dbuf, uint32_t dbuf_s) {
+  const int gm = gm0 + lane;
+  float x[32];
+  #pragma unroll
+  for (int j = 0; j < 32; ++j) x[j] = __fmul_rn(p.alpha, v[j]);
+  if (p.E != nullptr) {
+    #pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint4 w = *reinterpret_cast<const uint4*>(ebuf + sw64(lane, g));
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 f = __bfloat1622float2(h[u]);
+        x[g * 8 + 2 * u] = __fadd_rn(x[g * 8 + 2 * u], __fmul_rn(p.beta, f.x));
+        x[g * 8 + 2 * u + 1] = __fadd_rn(x[g * 8 + 2 * u + 1], __fmul_rn(p.beta, f.y));
+      }
+    }
+  }
+  if (p.gamma != 0.f) {
+    #pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (gm == gn0 + j) x[j] = __fadd_rn(x[j], p.gamma);
+  }
+  const bool f32 = p.d_es == 4;
+  // the previous chunk's TMA store must have finished reading dbuf
+  if (lane == 0) tma_store_wait_read();
+  __syncwarp();
+  if (f32) {
+    #pragma unroll
+    for (int g = 0; g < 8; ++g)
+      *reinterpret_cast<float4*>(dbuf + sw128(lane, g)) =
+          make_float4(x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
+  } else {
+    #pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      __nv_bfloat162 h[4];
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) h[u] = __floats2bfloat162_rn(x[8 * g + 2 * u], x[8 * g + 2 * u + 1]);
+      *reinterpret_cast<uint4*>(dbuf + sw64(lane, g)) = *reinterpret_cast<const uint4*>(h);
+    }
+  }
+  __syncwarp();
+  if (diag) {
+    // element (r, c) of the chunk: granule c / 8 (bf16) or c / 4 (fp32)
+    float low[32];
+    #pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      low[c] = 0.f;
+      if (c < lane) {
+        if (f32)
+          low[c] = *reinterpret_cast<const float*>(dbuf + sw128(c, lane >> 2) + (lane & 3) * 4);
+        else
+          low[c] = __bfloat162float(
+              *reinterpret_cast<const __nv_bfloat16*>(dbuf + sw64(c, lane >> 3) + (lane & 7) * 2));
+      }
+    }
+    __syncwarp();
+    #pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      if (c < lane) {
+        if (f32)
+          *reinterpret_cast<float*>(dbuf + sw128(lane, c >> 2) + (c & 3) * 4) = low[c];
+        else
+          *reinterpret_cast<__nv_bfloat16*>(dbuf + sw64(lane, c >> 3) + (c & 7) * 2) =
+              __float2bfloat16_rn(low[c]);
+      }
+    }
+    __syncwarp();
+  }
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) tma_store_2d(&mp->d, gn0, gm0, dbuf_s);
+  if (p.symmetric && !diag && gm < p.M) {
+    if (f32) {
+      float* D = reinterpret_cast<float*>(p.D);
+      #pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (gn0 + j < p.N) D[int64_t(gn0 + j) * p.ldd + gm] = x[j];
+    } else {
+      __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(p.D);
+      #pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (gn0 + j < p.N) D[int64_t(gn0 + j) * p.ldd + gm] = __float2bfloat16_rn(x[j]);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps,
           const GemmTile* __restrict__ tiles, int ntiles, const StepState* state,
@@ -179,15 +316,17 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;          // 1024-aligned stage ring
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t bar_base = base + STAGES * STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES);
+  uint8_t* epi_base = base_ptr + STAGES * STAGE_BYTES;    // per-warp epilogue staging
+  const uint32_t bar_base = base + STAGES * STAGE_BYTES + EPI_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES + EPI_BYTES);
   // barrier layout: full[STAGES], empty[STAGES], tfull[2], tempty[2]
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
   auto tfull_bar = [&](int i) { return bar_base + 8u * (2 * STAGES + i); };
   auto tempty_bar = [&](int i) { return bar_base + 8u * (2 * STAGES + 2 + i); };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  auto e_bar = [&](int w, int b) { return bar_base + 8u * (2 * STAGES + 4 + 2 * w + b); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -200,6 +339,8 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
       mbar_init(tfull_bar(i), 1);
       mbar_init(tempty_bar(i), 4);      // one arrival per epilogue warp
     }
+    for (int w = 0; w < 4; ++w)
+      for (int b = 0; b < 2; ++b) mbar_init(e_bar(w, b), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -294,102 +435,67 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // TMEM lane quarter of this warp
-    const int row_in_tile = q * 32 + lane;
+    const int ew = warp - 2;                      // epilogue warp 0..3
+    uint8_t* ebuf0 = epi_base + ew * EPI_WARP_BYTES;      // two addend buffers, then the output
+    uint8_t* dbuf = ebuf0 + 2 * EPI_E_BYTES;
+    const uint32_t ebuf0_s = smem_u32(ebuf0);
+    const uint32_t dbuf_s = smem_u32(dbuf);
+    uint32_t eph = 0u;   // bit b: parity of addend buffer b
     int acc = 0;
     uint32_t acc_ph = 0;
-    for (int ti = blockIdx.x; ti < ntiles && !*abort_flag; ti += gridDim.x) {
+    bool ok = true;
+    for (int ti = blockIdx.x; ti < ntiles && ok && !*abort_flag; ti += gridDim.x) {
       const GemmTile t = tiles[ti];
       const GemmProblem p = probs[t.problem];
-      if (!mbar_wait(tfull_bar(acc), acc_ph, abort_flag, err_flag, ERR_TIMEOUT_EPILOGUE)) break;
+      const TcMaps* mp = maps + t.problem;
+      const int gm0 = t.tm * BM + q * 32;          // first row of this warp's 32-row slab
+      // chunks this warp writes: inside the matrix, and for symmetric
+      // products not strictly below the diagonal (32-aligned both ways)
+      uint32_t todo = 0;
+      if (gm0 < p.M)
+        for (int c = 0; c < BN / 32; ++c) {
+          const int gn0 = t.tn * BN + c * 32;
+          if (gn0 < p.N && !(p.symmetric && gn0 < gm0)) todo |= 1u << c;
+        }
+      const bool has_e = p.E != nullptr;
+      int eb = 0;
+      if (has_e && todo && lane == 0) {   // prefetch the first addend chunk
+        const int c0 = __ffs(todo) - 1;
+        mbar_expect_tx(e_bar(ew, eb), EPI_E_BYTES);
+        tma_load_2d(ebuf0_s + eb * EPI_E_BYTES, &mp->e, t.tn * BN + c0 * 32, gm0, e_bar(ew, eb));
+      }
+      if (!mbar_wait(tfull_bar(acc), acc_ph, abort_flag, err_flag, ERR_TIMEOUT_EPILOGUE)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      const int gm = t.tm * BM + row_in_tile;
-      const bool row_ok = gm < p.M;
-      __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(p.D);
-      const __nv_bfloat16* E = reinterpret_cast<const __nv_bfloat16*>(p.E);
-      for (int c = 0; c < BN / 32; ++c) {
+      uint32_t rest = todo;
+      while (rest) {
+        const int c = __ffs(rest) - 1;
+        rest &= rest - 1;
         const int gn0 = t.tn * BN + c * 32;
-        if (gn0 >= p.N) break;                     // warp-uniform
+        if (has_e) {
+          if (rest && lane == 0) {   // prefetch the next addend chunk
+            const int cn = __ffs(rest) - 1;
+            mbar_expect_tx(e_bar(ew, eb ^ 1), EPI_E_BYTES);
+            tma_load_2d(ebuf0_s + (eb ^ 1) * EPI_E_BYTES, &mp->e, t.tn * BN + cn * 32, gm0,
+                        e_bar(ew, eb ^ 1));
+          }
+          if (!mbar_wait(e_bar(ew, eb), (eph >> eb) & 1u, abort_flag, err_flag,
+                         ERR_TIMEOUT_EPILOGUE)) {
+            ok = false;
+            break;
+          }
+          eph ^= 1u << eb;
+        }
         float v[32];
         tmem_ld32(tmem_base + static_cast<uint32_t>(acc * BN + c * 32) +
                       (static_cast<uint32_t>(q * 32) << 16),
                   v);
-        if (!row_ok) continue;
-        if (p.symmetric && gn0 + 31 < gm) continue;  // strictly below the diagonal
-        const bool full = gn0 + 32 <= p.N;
-        float e[32];
-        if (E != nullptr) {
-          const __nv_bfloat16* er = E + int64_t(gm) * p.lde + gn0;
-          if (full) {
-            #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              const uint4 w = *reinterpret_cast<const uint4*>(er + j);
-              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
-              #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float2 f = __bfloat1622float2(h[u]);
-                e[j + 2 * u] = f.x;
-                e[j + 2 * u + 1] = f.y;
-              }
-            }
-          } else {
-            #pragma unroll
-            for (int j = 0; j < 32; ++j) e[j] = (gn0 + j < p.N) ? __bfloat162float(er[j]) : 0.f;
-          }
-        }
-        float x[32];
-        #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float t = __fmul_rn(p.alpha, v[j]);
-          if (E != nullptr) t = __fadd_rn(t, __fmul_rn(p.beta, e[j]));
-          if (p.gamma != 0.f && gm == gn0 + j) t = __fadd_rn(t, p.gamma);
-          x[j] = t;
-        }
-        if (p.d_es == 4) {
-          // fp32 output (the Gram matrix of the gram method)
-          float* Df = reinterpret_cast<float*>(p.D);
-          float* dr = Df + int64_t(gm) * p.ldd + gn0;
-          if (!p.symmetric) {
-            if (full) {
-              #pragma unroll
-              for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(dr + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
-            } else {
-              for (int j = 0; j < 32; ++j)
-                if (gn0 + j < p.N) dr[j] = x[j];
-            }
-          } else {
-            #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int gn = gn0 + j;
-              if (gn >= p.N || gn < gm) continue;
-              dr[j] = x[j];
-              if (gn > gm) Df[int64_t(gn) * p.ldd + gm] = x[j];
-            }
-          }
-          continue;
-        }
-        __nv_bfloat16 o[32];
-        #pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = __float2bfloat16_rn(x[j]);
-        __nv_bfloat16* dr = D + int64_t(gm) * p.ldd + gn0;
-        if (!p.symmetric) {
-          if (full) {
-            #pragma unroll
-            for (int j = 0; j < 32; j += 8)
-              *reinterpret_cast<uint4*>(dr + j) = *reinterpret_cast<const uint4*>(&o[j]);
-          } else {
-            for (int j = 0; j < 32; ++j)
-              if (gn0 + j < p.N) dr[j] = o[j];
-          }
-        } else {
-          #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int gn = gn0 + j;
-            if (gn >= p.N || gn < gm) continue;
-            dr[j] = o[j];
-            if (gn > gm) D[int64_t(gn) * p.ldd + gm] = o[j];
-          }
-        }
+        epilogue_chunk(p, mp, v, gm0, gn0, lane, p.symmetric && gn0 == gm0,
+                       ebuf0 + eb * EPI_E_BYTES, dbuf, dbuf_s);
+        __syncwarp();
+        eb ^= 1;
       }
       tc_fence_before();
       __syncwarp();
@@ -397,6 +503,8 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
       acc ^= 1;
       if (acc == 0) acc_ph ^= 1u;
     }
+    if (lane == 0) tma_store_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -411,7 +519,57 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
 
 int g_num_sms = 0;
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D map over a row-major matrix: `inner` elements per row, `outer` rows,
+// row stride `ld` elements.
+bool encode_2d(CUtensorMap* m, const void* base, int es, int64_t inner, int64_t outer, int64_t ld,
+               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * es)};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
+
+bool tc_encode_maps(const GemmProblem& p, TcMaps* out) {
+  std::memset(out, 0, sizeof(TcMaps));
+  bool ok = encode_2d(&out->a, p.A, 2, p.K, p.M, p.lda, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (p.b_kmajor)
+    ok = ok && encode_2d(&out->b, p.B, 2, p.K, p.N, p.ldb, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    ok = ok && encode_2d(&out->b, p.B, 2, p.N, p.K, p.ldb, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (p.E != nullptr)
+    ok = ok && p.e_es == 2 &&
+         encode_2d(&out->e, p.E, 2, p.N, p.M, p.lde, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && encode_2d(&out->d, p.D, p.d_es, p.N, p.M, p.ldd, 32, 32,
+                       p.d_es == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+  return ok;
+}
 
 bool tc_available() {
   int dev = 0;

@@ -126,8 +126,10 @@ struct GemmTile {
 
 // TMA descriptors of one problem for the tensor-core path.
 struct TcMaps {   // CUtensorMap carries its own 64-byte alignment
-  CUtensorMap a;
-  CUtensorMap b;
+  CUtensorMap a;   // A tiles: 128 rows x 64 K, 128-byte swizzle
+  CUtensorMap b;   // B tiles: 256 x 64 (K-major) or 64 x 64 boxes (MN-major)
+  CUtensorMap e;   // addend chunks 32 x 32 bf16, 64-byte swizzle (if E)
+  CUtensorMap d;   // output chunks 32 x 32 (bf16 64-byte / fp32 128-byte swizzle)
 };
 
 // ---------------------------------------------------------------- launches
@@ -189,6 +191,8 @@ constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
 constexpr int kTcBK = 64;
 bool tc_available();
+// Encodes the TMA descriptors of one problem; false if the driver refuses.
+bool tc_encode_maps(const GemmProblem& p, TcMaps* out);
 int launch_gemm_tc(const GemmProblem* probs, const TcMaps* maps, const GemmTile* tiles,
                    int ntiles, const StepState* state, int* err_flag, cudaStream_t s);
 

@@ -47,39 +47,6 @@ int nofail(int code, const char* msg) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 int64_t rup(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn encode_fn() {
-  static EncodeFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(p);
-  }
-  return fn;
-}
-
-bool encode(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld,
-            uint32_t bi, uint32_t bo) {
-  EncodeFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
-  cuuint64_t strides[1] = {cuuint64_t(ld * 2)};
-  cuuint32_t box[2] = {bi, bo};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 enum { ENG_TC = 0, ENG_SIMT = 1, ENG_CONVERT = 2 };
 
 // One launch of the iteration (one problem: the single matrix).
@@ -266,13 +233,8 @@ extern "C" int muon_newton_schulz_noalloc(const void* X, void* Y, int rows, int 
   for (int i = 0; i < nops; ++i) {
     h_probs[i] = g_ops[i].prob;
     std::memset(&g_maps[i], 0, sizeof(TcMaps));
-    if (g_ops[i].engine == ENG_TC) {
-      const GemmProblem& p = g_ops[i].prob;
-      bool e = encode(&g_maps[i].a, p.A, p.K, p.M, p.lda, kTcBK, kTcBM);
-      if (p.b_kmajor) e = e && encode(&g_maps[i].b, p.B, p.K, p.N, p.ldb, kTcBK, kTcBN);
-      else e = e && encode(&g_maps[i].b, p.B, p.N, p.K, p.ldb, 64, kTcBK);
-      if (!e) return nofail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    }
+    if (g_ops[i].engine == ENG_TC && !tc_encode_maps(g_ops[i].prob, &g_maps[i]))
+      return nofail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   }
   for (int l = 0; l < nlists; ++l)
     std::memcpy(h_tiles + l * kMaxTilesPerList, g_lists[l].tiles, sizeof(GemmTile) * g_lists[l].count);
