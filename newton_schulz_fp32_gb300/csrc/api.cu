@@ -244,6 +244,38 @@ int validate_and_build(const muon_param_t* params, int nparams, const muon_parti
     }
   }
 
+  // A tile qualifies for the kernels' 16-byte path when it lies in one
+  // segment with 16-byte aligned storage (see ETile).
+  auto mark_fast = [&](ETile& t, const Owner& o) {
+    int64_t a, b;
+    bool shape_ok;
+    if (t.kind == 0) {
+      a = int64_t(t.r0) * o.cols;
+      b = int64_t(t.r0 + t.nr) * o.cols;
+      shape_ok = o.cols % 4 == 0 && o.ldx == o.cols;
+    } else if (t.kind == 1) {
+      const int re = std::min(t.r0 + kTT, o.rows);
+      a = int64_t(t.r0) * o.cols + t.c0;
+      b = int64_t(re - 1) * o.cols + t.c0 + kTT;
+      shape_ok = o.cols % 4 == 0 && t.c0 + kTT <= o.cols;
+    } else {
+      a = t.rel_begin;
+      b = t.rel_begin + t.len;
+      shape_ok = t.rel_begin % 4 == 0 && t.len % 4 == 0;
+    }
+    if (!shape_ok) return;
+    for (int k = o.seg_begin; k < o.seg_begin + o.seg_count; ++k) {
+      const Segment& sg = L.segs[k];
+      if (a < sg.rel_begin || a >= sg.rel_begin + sg.len) continue;
+      const int64_t delta = sg.storage_begin - sg.rel_begin;
+      if (b <= sg.rel_begin + sg.len && ((delta + a) & 3) == 0) {
+        t.fast = 1;
+        t.sdelta = delta;
+      }
+      return;
+    }
+  };
+
   // tiles
   for (int oi = 0; oi < static_cast<int>(L.owners.size()); ++oi) {
     Owner& o = L.owners[oi];
@@ -257,6 +289,7 @@ int validate_and_build(const muon_param_t* params, int nparams, const muon_parti
         for (int r = 0; r < o.rows; r += rows_per) {
           ETile t{};
           t.owner = oi; t.kind = 0; t.r0 = r; t.nr = std::min(rows_per, o.rows - r);
+          mark_fast(t, o);
           L.gtiles.push_back(t);
           L.stiles.push_back(t);
         }
@@ -265,6 +298,7 @@ int validate_and_build(const muon_param_t* params, int nparams, const muon_parti
           for (int c = 0; c < o.cols; c += kTT) {
             ETile t{};
             t.owner = oi; t.kind = 1; t.r0 = r; t.c0 = c;
+            mark_fast(t, o);
             L.gtiles.push_back(t);
             L.stiles.push_back(t);
           }
@@ -279,6 +313,7 @@ int validate_and_build(const muon_param_t* params, int nparams, const muon_parti
         ETile t{};
         t.owner = oi; t.kind = 2; t.rel_begin = r;
         t.len = std::min<int64_t>(kRowTile, o.numel - r);
+        mark_fast(t, o);
         L.stiles.push_back(t);
       }
     }

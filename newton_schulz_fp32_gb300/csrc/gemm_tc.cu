@@ -38,15 +38,16 @@ constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;                // 2 accumulators x 256 fp32 columns
-constexpr int NTHREADS = 192;
-// Epilogue staging per epilogue warp: two 32 x 32 bf16 addend chunks (TMA
-// loads, 64-byte swizzle) and one 32 x 32 output chunk (TMA store; bf16 with
-// 64-byte or fp32 with 128-byte swizzle).  Every buffer is 1 KB aligned.
+constexpr int EPI_WARPS = 8;                  // two per TMEM lane quarter, 4 chunks each
+constexpr int NTHREADS = 64 + 32 * EPI_WARPS;
+// Epilogue staging per epilogue warp: one 32 x 32 bf16 addend chunk (TMA
+// load, 64-byte swizzle) and one output box of 64-byte rows (TMA store,
+// 64-byte swizzle: 32 bf16 or 16 fp32 columns).  Buffers are 1 KB aligned.
 constexpr int EPI_E_BYTES = 32 * 32 * 2;                                 // 2 KB
-constexpr int EPI_D_BYTES = 32 * 32 * 4;                                 // 4 KB
-constexpr int EPI_WARP_BYTES = 2 * EPI_E_BYTES + EPI_D_BYTES;            // 8 KB
-constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 4 + 8;   // full, empty, tfull x2, tempty x2, E x2 per epilogue warp
+constexpr int EPI_D_BYTES = 32 * 64;                                     // 2 KB
+constexpr int EPI_WARP_BYTES = EPI_E_BYTES + EPI_D_BYTES;                // 4 KB
+constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS;   // full, empty, tfull x2, tempty x2, E per epilogue warp
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
@@ -130,14 +131,10 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Byte offsets inside a swizzled 32 x 32 chunk: 64-byte rows with the
-// 64-byte swizzle (16-byte granule index XOR bits 7-8 of the offset) for
-// bf16, 128-byte rows with the 128-byte swizzle (XOR bits 7-9) for fp32.
+// Byte offset of 16-byte granule `granule` of row `row` in a box of 64-byte
+// rows under the 64-byte swizzle (granule index XOR bits 7-8 of the offset).
 __device__ __forceinline__ uint32_t sw64(int row, int granule) {
   return uint32_t(row) * 64u + (uint32_t(granule ^ ((row >> 1) & 3)) << 4);
-}
-__device__ __forceinline__ uint32_t sw128(int row, int granule) {
-  return uint32_t(row) * 128u + (uint32_t(granule ^ (row & 7)) << 4);
 }
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
@@ -208,91 +205,66 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Epilogue of one 32 x 32 output chunk held by one warp (lane = row):
-//   x = alpha * acc + beta * E + gamma * [row == col]
-// E arrives by TMA in `ebuf` (64-byte swizzle, conflict-free row reads).
-// The result is staged in `dbuf` in the swizzled layout and written by one
-// TMA store (which also clips rows >= M and columns >= N).  Symmetric
-// products: a diagonal chunk is symmetrised in `dbuf` (lower = mirror of the
-// rounded upper) before the store; a chunk above the diagonal is also
-// written transposed to the mirror position with direct stores (lanes hold
-// consecutive rows, so each store instruction covers 64 or 128 contiguous
-// bytes).
-__device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, const TcMaps* mp, const float* v,
-                                               int gm0, int gn0, int lane, bool diag,
-                                               const uint8_t* ebuf, uint8_t* dbuf, uint32_t dbuf_s) {
+// Writes one 32 x 32 output chunk held by one warp (lane = row, x = the
+// finished fp32 values).  Off the diagonal the chunk is staged in `dbuf` in
+// the 64-byte-swizzled layout and written by TMA stores (which clip rows >= M
+// and columns >= N): one box for bf16, two 16-column boxes for fp32.  A
+// chunk above the diagonal of a symmetric product is also written transposed
+// to its mirror position with direct stores (lanes hold consecutive rows, so
+// each store instruction covers 64 or 128 contiguous bytes).  A chunk on the
+// diagonal is written directly: its upper triangle (with the diagonal) by
+// rows and its strictly upper part again as the mirror, so the lower
+// triangle is an exact copy of the upper.
+__device__ __forceinline__ void store_chunk(const GemmProblem& p, const TcMaps* mp, const float* x,
+                                            int gm0, int gn0, int lane, bool diag, uint8_t* dbuf,
+                                            uint32_t dbuf_s) {
   const int gm = gm0 + lane;
-  float x[32];
-  #pragma unroll
-  for (int j = 0; j < 32; ++j) x[j] = __fmul_rn(p.alpha, v[j]);
-  if (p.E != nullptr) {
-    #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      const uint4 w = *reinterpret_cast<const uint4*>(ebuf + sw64(lane, g));
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
-      #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float2 f = __bfloat1622float2(h[u]);
-        x[g * 8 + 2 * u] = __fadd_rn(x[g * 8 + 2 * u], __fmul_rn(p.beta, f.x));
-        x[g * 8 + 2 * u + 1] = __fadd_rn(x[g * 8 + 2 * u + 1], __fmul_rn(p.beta, f.y));
-      }
-    }
-  }
-  if (p.gamma != 0.f) {
-    #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (gm == gn0 + j) x[j] = __fadd_rn(x[j], p.gamma);
-  }
   const bool f32 = p.d_es == 4;
-  // the previous chunk's TMA store must have finished reading dbuf
-  if (lane == 0) tma_store_wait_read();
-  __syncwarp();
-  if (f32) {
+  if (diag) {
+    if (gm >= p.M) return;
     #pragma unroll
-    for (int g = 0; g < 8; ++g)
-      *reinterpret_cast<float4*>(dbuf + sw128(lane, g)) =
-          make_float4(x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
-  } else {
+    for (int j = 0; j < 32; ++j) {
+      const int gn = gn0 + j;
+      if (gn >= p.N || j < lane) continue;
+      if (f32) {
+        float* D = reinterpret_cast<float*>(p.D);
+        D[int64_t(gm) * p.ldd + gn] = x[j];
+        if (j > lane) D[int64_t(gn) * p.ldd + gm] = x[j];
+      } else {
+        __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(p.D);
+        const __nv_bfloat16 o = __float2bfloat16_rn(x[j]);
+        D[int64_t(gm) * p.ldd + gn] = o;
+        if (j > lane) D[int64_t(gn) * p.ldd + gm] = o;
+      }
+    }
+    return;
+  }
+  #pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const bool live = (h == 0) || (f32 && gn0 + 16 < p.N);   // warp-uniform
+    if (!live) continue;
+    if (lane == 0) tma_store_wait_read();   // the previous store has read dbuf
+    __syncwarp();
     #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      __nv_bfloat162 h[4];
-      #pragma unroll
-      for (int u = 0; u < 4; ++u) h[u] = __floats2bfloat162_rn(x[8 * g + 2 * u], x[8 * g + 2 * u + 1]);
-      *reinterpret_cast<uint4*>(dbuf + sw64(lane, g)) = *reinterpret_cast<const uint4*>(h);
-    }
-  }
-  __syncwarp();
-  if (diag) {
-    // element (r, c) of the chunk: granule c / 8 (bf16) or c / 4 (fp32)
-    float low[32];
-    #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      low[c] = 0.f;
-      if (c < lane) {
-        if (f32)
-          low[c] = *reinterpret_cast<const float*>(dbuf + sw128(c, lane >> 2) + (lane & 3) * 4);
-        else
-          low[c] = __bfloat162float(
-              *reinterpret_cast<const __nv_bfloat16*>(dbuf + sw64(c, lane >> 3) + (lane & 7) * 2));
+      uint4 w;
+      if (f32) {
+        const float* xs = x + 16 * h + 4 * g;
+        w = make_uint4(__float_as_uint(xs[0]), __float_as_uint(xs[1]), __float_as_uint(xs[2]),
+                       __float_as_uint(xs[3]));
+      } else {
+        __nv_bfloat162 hh[4];
+        #pragma unroll
+        for (int u = 0; u < 4; ++u) hh[u] = __floats2bfloat162_rn(x[8 * g + 2 * u], x[8 * g + 2 * u + 1]);
+        w = *reinterpret_cast<const uint4*>(hh);
       }
+      *reinterpret_cast<uint4*>(dbuf + sw64(lane, g)) = w;
     }
+    fence_async_smem();
     __syncwarp();
-    #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      if (c < lane) {
-        if (f32)
-          *reinterpret_cast<float*>(dbuf + sw128(lane, c >> 2) + (c & 3) * 4) = low[c];
-        else
-          *reinterpret_cast<__nv_bfloat16*>(dbuf + sw64(lane, c >> 3) + (c & 7) * 2) =
-              __float2bfloat16_rn(low[c]);
-      }
-    }
-    __syncwarp();
+    if (lane == 0) tma_store_2d(&mp->d, gn0 + 16 * h, gm0, dbuf_s);
   }
-  fence_async_smem();
-  __syncwarp();
-  if (lane == 0) tma_store_2d(&mp->d, gn0, gm0, dbuf_s);
-  if (p.symmetric && !diag && gm < p.M) {
+  if (p.symmetric && gm < p.M) {
     if (f32) {
       float* D = reinterpret_cast<float*>(p.D);
       #pragma unroll
@@ -324,7 +296,7 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
   auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
   auto tfull_bar = [&](int i) { return bar_base + 8u * (2 * STAGES + i); };
   auto tempty_bar = [&](int i) { return bar_base + 8u * (2 * STAGES + 2 + i); };
-  auto e_bar = [&](int w, int b) { return bar_base + 8u * (2 * STAGES + 4 + 2 * w + b); };
+  auto e_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + 4 + w); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS + 1);
 
@@ -337,10 +309,9 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull_bar(i), 1);
-      mbar_init(tempty_bar(i), 4);      // one arrival per epilogue warp
+      mbar_init(tempty_bar(i), EPI_WARPS);   // one arrival per epilogue warp
     }
-    for (int w = 0; w < 4; ++w)
-      for (int b = 0; b < 2; ++b) mbar_init(e_bar(w, b), 1);
+    for (int w = 0; w < EPI_WARPS; ++w) mbar_init(e_bar(w), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -434,35 +405,34 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                       // TMEM lane quarter of this warp
-    const int ew = warp - 2;                      // epilogue warp 0..3
-    uint8_t* ebuf0 = epi_base + ew * EPI_WARP_BYTES;      // two addend buffers, then the output
-    uint8_t* dbuf = ebuf0 + 2 * EPI_E_BYTES;
-    const uint32_t ebuf0_s = smem_u32(ebuf0);
+    const int q = warp & 3;                       // TMEM lane quarter this warp may read
+    const int ew = warp - 2;                      // epilogue warp 0..7
+    const int c_lo = (ew >> 2) * 4;               // its chunks: columns [32 c_lo, 32 c_lo + 128)
+    uint8_t* ebuf = epi_base + ew * EPI_WARP_BYTES;
+    uint8_t* dbuf = ebuf + EPI_E_BYTES;
+    const uint32_t ebuf_s = smem_u32(ebuf);
     const uint32_t dbuf_s = smem_u32(dbuf);
-    uint32_t eph = 0u;   // bit b: parity of addend buffer b
+    uint32_t eph = 0u;
     int acc = 0;
     uint32_t acc_ph = 0;
     bool ok = true;
     for (int ti = blockIdx.x; ti < ntiles && ok && !*abort_flag; ti += gridDim.x) {
       const GemmTile t = tiles[ti];
-      const GemmProblem p = probs[t.problem];
+      const GemmProblem& p = probs[t.problem];     // read through L1, not held in registers
       const TcMaps* mp = maps + t.problem;
       const int gm0 = t.tm * BM + q * 32;          // first row of this warp's 32-row slab
       // chunks this warp writes: inside the matrix, and for symmetric
       // products not strictly below the diagonal (32-aligned both ways)
       uint32_t todo = 0;
       if (gm0 < p.M)
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = c_lo; c < c_lo + 4; ++c) {
           const int gn0 = t.tn * BN + c * 32;
           if (gn0 < p.N && !(p.symmetric && gn0 < gm0)) todo |= 1u << c;
         }
       const bool has_e = p.E != nullptr;
-      int eb = 0;
       if (has_e && todo && lane == 0) {   // prefetch the first addend chunk
-        const int c0 = __ffs(todo) - 1;
-        mbar_expect_tx(e_bar(ew, eb), EPI_E_BYTES);
-        tma_load_2d(ebuf0_s + eb * EPI_E_BYTES, &mp->e, t.tn * BN + c0 * 32, gm0, e_bar(ew, eb));
+        mbar_expect_tx(e_bar(ew), EPI_E_BYTES);
+        tma_load_2d(ebuf_s, &mp->e, t.tn * BN + (__ffs(todo) - 1) * 32, gm0, e_bar(ew));
       }
       if (!mbar_wait(tfull_bar(acc), acc_ph, abort_flag, err_flag, ERR_TIMEOUT_EPILOGUE)) {
         ok = false;
@@ -474,28 +444,42 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
         const int c = __ffs(rest) - 1;
         rest &= rest - 1;
         const int gn0 = t.tn * BN + c * 32;
+        float x[32];
+        tmem_ld32(tmem_base + static_cast<uint32_t>(acc * BN + c * 32) +
+                      (static_cast<uint32_t>(q * 32) << 16),
+                  x);
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = __fmul_rn(p.alpha, x[j]);
         if (has_e) {
-          if (rest && lane == 0) {   // prefetch the next addend chunk
-            const int cn = __ffs(rest) - 1;
-            mbar_expect_tx(e_bar(ew, eb ^ 1), EPI_E_BYTES);
-            tma_load_2d(ebuf0_s + (eb ^ 1) * EPI_E_BYTES, &mp->e, t.tn * BN + cn * 32, gm0,
-                        e_bar(ew, eb ^ 1));
-          }
-          if (!mbar_wait(e_bar(ew, eb), (eph >> eb) & 1u, abort_flag, err_flag,
-                         ERR_TIMEOUT_EPILOGUE)) {
+          if (!mbar_wait(e_bar(ew), eph, abort_flag, err_flag, ERR_TIMEOUT_EPILOGUE)) {
             ok = false;
             break;
           }
-          eph ^= 1u << eb;
+          eph ^= 1u;
+          #pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint4 w = *reinterpret_cast<const uint4*>(ebuf + sw64(lane, g));
+            const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&w);
+            #pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float2 f = __bfloat1622float2(hh[u]);
+              x[g * 8 + 2 * u] = __fadd_rn(x[g * 8 + 2 * u], __fmul_rn(p.beta, f.x));
+              x[g * 8 + 2 * u + 1] = __fadd_rn(x[g * 8 + 2 * u + 1], __fmul_rn(p.beta, f.y));
+            }
+          }
+          __syncwarp();   // every lane has read the addend: the buffer may be refilled
+          if (rest && lane == 0) {
+            mbar_expect_tx(e_bar(ew), EPI_E_BYTES);
+            tma_load_2d(ebuf_s, &mp->e, t.tn * BN + (__ffs(rest) - 1) * 32, gm0, e_bar(ew));
+          }
         }
-        float v[32];
-        tmem_ld32(tmem_base + static_cast<uint32_t>(acc * BN + c * 32) +
-                      (static_cast<uint32_t>(q * 32) << 16),
-                  v);
-        epilogue_chunk(p, mp, v, gm0, gn0, lane, p.symmetric && gn0 == gm0,
-                       ebuf0 + eb * EPI_E_BYTES, dbuf, dbuf_s);
+        if (p.gamma != 0.f) {
+          #pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (gm0 + lane == gn0 + j) x[j] = __fadd_rn(x[j], p.gamma);
+        }
+        store_chunk(p, mp, x, gm0, gn0, lane, p.symmetric && gn0 == gm0, dbuf, dbuf_s);
         __syncwarp();
-        eb ^= 1;
       }
       tc_fence_before();
       __syncwarp();
@@ -566,8 +550,8 @@ bool tc_encode_maps(const GemmProblem& p, TcMaps* out) {
   if (p.E != nullptr)
     ok = ok && p.e_es == 2 &&
          encode_2d(&out->e, p.E, 2, p.N, p.M, p.lde, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-  ok = ok && encode_2d(&out->d, p.D, p.d_es, p.N, p.M, p.ldd, 32, 32,
-                       p.d_es == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_2d(&out->d, p.D, p.d_es, p.N, p.M, p.ldd, p.d_es == 2 ? 32 : 16, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B);
   return ok;
 }
 

@@ -66,13 +66,17 @@ struct RTile {
 //   kind 0: rows [r0, r0 + nr) of a non-transposed Muon owner
 //   kind 1: 64 x 64 tile at (r0, c0) of a transposed Muon owner
 //   kind 2: elements [rel_begin, rel_begin + len) of an auxiliary owner
+// fast = 1 when the whole tile lies in one segment, its storage is 16-byte
+// aligned and its rows are whole multiples of 4 elements: then storage index
+// = sdelta + owner-relative index and the kernels use 16-byte accesses.
 struct ETile {
   int32_t owner;
   int32_t kind;
   int32_t r0, nr;
-  int32_t c0, pad;
+  int32_t c0, fast;
   int64_t rel_begin;
   int64_t len;
+  int64_t sdelta;
 };
 
 // Tile of the update sum of squares: rows [r0, r0 + nr) of an owner's
@@ -129,7 +133,7 @@ struct TcMaps {   // CUtensorMap carries its own 64-byte alignment
   CUtensorMap a;   // A tiles: 128 rows x 64 K, 128-byte swizzle
   CUtensorMap b;   // B tiles: 256 x 64 (K-major) or 64 x 64 boxes (MN-major)
   CUtensorMap e;   // addend chunks 32 x 32 bf16, 64-byte swizzle (if E)
-  CUtensorMap d;   // output chunks 32 x 32 (bf16 64-byte / fp32 128-byte swizzle)
+  CUtensorMap d;   // output boxes: 32 rows of 64 bytes (32 bf16 or 16 fp32), 64-byte swizzle
 };
 
 // ---------------------------------------------------------------- launches

@@ -204,6 +204,223 @@ __device__ __forceinline__ void for_row(const Segment* segs, int nseg, int64_t l
   }
 }
 
+// ---- 16-byte fast paths (tile in one segment, aligned; see ETile::fast).
+// All loads of a batch are issued before any store, so a thread keeps
+// several 16-byte requests in flight.
+
+__device__ __forceinline__ void store4_ws(void* base, int esize, int64_t i, float4 v) {
+  if (esize == 2) {
+    __nv_bfloat162 h[2] = {__floats2bfloat162_rn(v.x, v.y), __floats2bfloat162_rn(v.z, v.w)};
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(base) + i) =
+        *reinterpret_cast<const uint2*>(h);
+  } else {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + i) = v;
+  }
+}
+
+__device__ __forceinline__ float4 load4_ws(const void* base, int esize, int64_t i) {
+  if (esize == 2) {
+    const uint2 w = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(base) + i);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + i);
+}
+
+// rows of a non-transposed block: owner elements [e0, e1), X0 index = rel
+__device__ __forceinline__ void gather_fast_rows(const StreamLaunchArgs& a, const ETile& t,
+                                                 const Owner& o, float d, char* x0) {
+  constexpr int U = 4;
+  const int64_t e0 = int64_t(t.r0) * o.cols, e1 = int64_t(t.r0 + t.nr) * o.cols;
+  const float* __restrict__ G = a.accum + t.sdelta;
+  float* __restrict__ M = a.momentum + t.sdelta;
+  const int64_t stride = int64_t(4) * kStreamThreads;
+  for (int64_t i0 = e0 + 4 * threadIdx.x; i0 < e1; i0 += stride * U) {
+    float4 g[U], m[U];
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < e1) {
+        g[u] = *reinterpret_cast<const float4*>(G + i);
+        m[u] = *reinterpret_cast<const float4*>(M + i);
+      }
+    }
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < e1) {
+        float4 mv;
+        mv.x = momentum_of(a.beta, m[u].x, g[u].x);
+        mv.y = momentum_of(a.beta, m[u].y, g[u].y);
+        mv.z = momentum_of(a.beta, m[u].z, g[u].z);
+        mv.w = momentum_of(a.beta, m[u].w, g[u].w);
+        *reinterpret_cast<float4*>(M + i) = mv;
+        store4_ws(x0, a.esize, i,
+                  make_float4(__fdiv_rn(mv.x, d), __fdiv_rn(mv.y, d), __fdiv_rn(mv.z, d),
+                              __fdiv_rn(mv.w, d)));
+      }
+    }
+  }
+}
+
+// 64 x 64 tile of a transposed block: read rows, write X0 = tile^T
+__device__ __forceinline__ void gather_fast_tr(const StreamLaunchArgs& a, const ETile& t,
+                                               const Owner& o, float d, char* x0,
+                                               float (*tile)[kTT + 1]) {
+  const int r_end = min(t.r0 + kTT, o.rows);
+  const int rq = threadIdx.x >> 4, cq = (threadIdx.x & 15) * 4;   // 16 rows x 16 float4 per pass
+  float4 g[4], m[4];
+  #pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = t.r0 + rq + 16 * k;
+    if (r < r_end) {
+      const int64_t i = t.sdelta + int64_t(r) * o.cols + t.c0 + cq;
+      g[k] = *reinterpret_cast<const float4*>(a.accum + i);
+      m[k] = *reinterpret_cast<const float4*>(a.momentum + i);
+    }
+  }
+  #pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = t.r0 + rq + 16 * k;
+    if (r < r_end) {
+      const int64_t i = t.sdelta + int64_t(r) * o.cols + t.c0 + cq;
+      float4 mv;
+      mv.x = momentum_of(a.beta, m[k].x, g[k].x);
+      mv.y = momentum_of(a.beta, m[k].y, g[k].y);
+      mv.z = momentum_of(a.beta, m[k].z, g[k].z);
+      mv.w = momentum_of(a.beta, m[k].w, g[k].w);
+      *reinterpret_cast<float4*>(a.momentum + i) = mv;
+      float* tr = tile[rq + 16 * k];
+      tr[cq] = __fdiv_rn(mv.x, d);
+      tr[cq + 1] = __fdiv_rn(mv.y, d);
+      tr[cq + 2] = __fdiv_rn(mv.z, d);
+      tr[cq + 3] = __fdiv_rn(mv.w, d);
+    }
+  }
+  __syncthreads();
+  // X0 rows c0..c0+63 (block columns), 8 elements per thread, 32 rows per pass
+  const int xr = threadIdx.x >> 3, rs = (threadIdx.x & 7) * 8;
+  #pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int cc = xr + 32 * pass;
+    const int64_t xi = int64_t(t.c0 + cc) * o.ldx + t.r0 + rs;
+    if (t.r0 + rs + 8 <= r_end) {
+      float v[8];
+      #pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = tile[rs + k][cc];
+      store4_ws(x0, a.esize, xi, make_float4(v[0], v[1], v[2], v[3]));
+      store4_ws(x0, a.esize, xi + 4, make_float4(v[4], v[5], v[6], v[7]));
+    } else {
+      for (int k = 0; k < 8 && t.r0 + rs + k < r_end; ++k) store_ws(x0, a.esize, xi + k, tile[rs + k][cc]);
+    }
+  }
+}
+
+__device__ __forceinline__ void scatter_fast_rows(const StreamLaunchArgs& a, const ETile& t,
+                                                  const Owner& o, float coef, const char* y) {
+  constexpr int U = 4;
+  const int64_t e0 = int64_t(t.r0) * o.cols, e1 = int64_t(t.r0 + t.nr) * o.cols;
+  float* __restrict__ A = a.accum + t.sdelta;
+  float* __restrict__ W = a.master + t.sdelta;
+  const int64_t stride = int64_t(4) * kStreamThreads;
+  for (int64_t i0 = e0 + 4 * threadIdx.x; i0 < e1; i0 += stride * U) {
+    float4 u4[U], w[U];
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < e1) {
+        u4[u] = load4_ws(y, a.esize, i);
+        w[u] = *reinterpret_cast<const float4*>(W + i);
+      }
+    }
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < e1) {
+        const float4 v = make_float4(__fmul_rn(coef, u4[u].x), __fmul_rn(coef, u4[u].y),
+                                     __fmul_rn(coef, u4[u].z), __fmul_rn(coef, u4[u].w));
+        *reinterpret_cast<float4*>(A + i) = v;
+        *reinterpret_cast<float4*>(W + i) =
+            make_float4(__fsub_rn(w[u].x, __fmul_rn(a.lr, v.x)), __fsub_rn(w[u].y, __fmul_rn(a.lr, v.y)),
+                        __fsub_rn(w[u].z, __fmul_rn(a.lr, v.z)), __fsub_rn(w[u].w, __fmul_rn(a.lr, v.w)));
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void scatter_fast_tr(const StreamLaunchArgs& a, const ETile& t,
+                                                const Owner& o, float coef, const char* y,
+                                                float (*tile)[kTT + 1]) {
+  const int r_end = min(t.r0 + kTT, o.rows);
+  // Y rows c0..c0+63 hold block columns; 8 elements per thread, 32 rows per pass
+  const int yr = threadIdx.x >> 3, rs = (threadIdx.x & 7) * 8;
+  float4 lo[2], hi[2];
+  #pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int64_t yi = int64_t(t.c0 + yr + 32 * pass) * o.ldx + t.r0 + rs;
+    if (t.r0 + rs + 8 <= r_end) {
+      lo[pass] = load4_ws(y, a.esize, yi);
+      hi[pass] = load4_ws(y, a.esize, yi + 4);
+    } else {
+      float v[8];
+      for (int k = 0; k < 8; ++k) v[k] = (t.r0 + rs + k < r_end) ? load_ws(y, a.esize, yi + k) : 0.f;
+      lo[pass] = make_float4(v[0], v[1], v[2], v[3]);
+      hi[pass] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  }
+  #pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int cc = yr + 32 * pass;
+    tile[rs + 0][cc] = lo[pass].x; tile[rs + 1][cc] = lo[pass].y;
+    tile[rs + 2][cc] = lo[pass].z; tile[rs + 3][cc] = lo[pass].w;
+    tile[rs + 4][cc] = hi[pass].x; tile[rs + 5][cc] = hi[pass].y;
+    tile[rs + 6][cc] = hi[pass].z; tile[rs + 7][cc] = hi[pass].w;
+  }
+  __syncthreads();
+  const int rq = threadIdx.x >> 4, cq = (threadIdx.x & 15) * 4;
+  float4 w[4];
+  #pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = t.r0 + rq + 16 * k;
+    if (r < r_end)
+      w[k] = *reinterpret_cast<const float4*>(a.master + t.sdelta + int64_t(r) * o.cols + t.c0 + cq);
+  }
+  #pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = t.r0 + rq + 16 * k;
+    if (r < r_end) {
+      const int64_t i = t.sdelta + int64_t(r) * o.cols + t.c0 + cq;
+      const float* tr = tile[rq + 16 * k];
+      const float4 v = make_float4(__fmul_rn(coef, tr[cq]), __fmul_rn(coef, tr[cq + 1]),
+                                   __fmul_rn(coef, tr[cq + 2]), __fmul_rn(coef, tr[cq + 3]));
+      *reinterpret_cast<float4*>(a.accum + i) = v;
+      *reinterpret_cast<float4*>(a.master + i) =
+          make_float4(__fsub_rn(w[k].x, __fmul_rn(a.lr, v.x)), __fsub_rn(w[k].y, __fmul_rn(a.lr, v.y)),
+                      __fsub_rn(w[k].z, __fmul_rn(a.lr, v.z)), __fsub_rn(w[k].w, __fmul_rn(a.lr, v.w)));
+    }
+  }
+}
+
+__device__ __forceinline__ void scatter_fast_aux(const StreamLaunchArgs& a, const ETile& t, float coef) {
+  constexpr int U = 4;
+  float* __restrict__ A = a.accum + t.sdelta;
+  const int64_t e0 = t.rel_begin, e1 = t.rel_begin + t.len;
+  const int64_t stride = int64_t(4) * kStreamThreads;
+  for (int64_t i0 = e0 + 4 * threadIdx.x; i0 < e1; i0 += stride * U) {
+    float4 g[U];
+    #pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u * stride < e1) g[u] = *reinterpret_cast<const float4*>(A + i0 + u * stride);
+    #pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u * stride < e1)
+        *reinterpret_cast<float4*>(A + i0 + u * stride) =
+            make_float4(__fmul_rn(coef, g[u].x), __fmul_rn(coef, g[u].y), __fmul_rn(coef, g[u].z),
+                        __fmul_rn(coef, g[u].w));
+  }
+}
+
 __global__ void __launch_bounds__(kStreamThreads)
 k_gather(StreamLaunchArgs a) {
   if (a.state->overflow) return;
@@ -215,6 +432,11 @@ k_gather(StreamLaunchArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   char* x0 = static_cast<char*>(a.x0) + o.x_off * a.esize;
+  if (t.fast) {
+    if (t.kind == 0) gather_fast_rows(a, t, o, d, x0);
+    else gather_fast_tr(a, t, o, d, x0, tile);
+    return;
+  }
   if (t.kind == 0) {
     for (int r = t.r0 + warp; r < t.r0 + t.nr; r += nw) {
       const int64_t rb = int64_t(r) * o.cols;
@@ -313,6 +535,13 @@ k_scatter(StreamLaunchArgs a) {
   const Segment* segs = a.segs + o.seg_begin;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
+  if (t.fast) {
+    const char* yb = static_cast<const char*>(a.y) + o.x_off * a.esize;
+    if (t.kind == 0) scatter_fast_rows(a, t, o, coef, yb);
+    else if (t.kind == 1) scatter_fast_tr(a, t, o, coef, yb, tile);
+    else scatter_fast_aux(a, t, coef);
+    return;
+  }
   if (t.kind == 2) {
     // auxiliary parameter: accum = coef * g, master untouched
     const int64_t te = t.rel_begin + t.len;
