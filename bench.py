@@ -356,6 +356,49 @@ def run_ragged(args, peaks, peak_src):
                       "phases_ms_per_step": {k: ph[k]["ms"] / args.steps for k in ph}}))
 
 
+def run_llama(args, peaks, peak_src):
+    """Llama-3-8B-shaped parameter set (32 layers x {q, o 4096^2; k, v
+    1024x4096; gate, up 14336x4096; down 4096x14336}, 6.98G elements, 64
+    partitions, align 128): 2 bf16 micro-batches (even-indexed matrices
+    low-rank rank 8 + 1e-3 noise) accumulated in fp32, one standard Muon
+    step.  All state resident in HBM (~84 GB fp32 + 28 GB grads)."""
+    import torch
+    import newton_schulz_fp32_gb300 as nsg
+    nsg.build()
+    lay = wl.llama3_8b_layout()
+    seed = wl.CONFIG_SEED["llama"]
+    n = lay.storage_size
+    stream = torch.cuda.Stream()
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    acc = torch.zeros(n, dtype=torch.float32, device="cuda")
+    mom = torch.zeros(n, dtype=torch.float32, device="cuda")
+    mst = torch.randn(n, dtype=torch.float32, device="cuda", generator=gen)
+    grads = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    for mb in range(2):
+        wl.llama_grad_into(lay, seed, mb, grads[mb])
+    res = torch.zeros(4, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    P, Q = lay.params, lay.parts
+
+    def step():
+        for mb in range(2):
+            nsg.accumulate(acc, grads[mb], 0.5, overwrite=(mb == 0), params=P, parts=Q, stream=stream)
+        nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, "standard", 5, 0.0, args.mode, result=res,
+                 stream=stream)
+    ms, ph = timed(torch, nsg, step, args.steps, args.warmup, stream)
+    flops = ns_formula_flops(lay, "standard")
+    g = ph["ns_gemm"]
+    hbm = [k for k in ph if k != "ns_gemm" and ph[k]["ms"] > 0]
+    print(json.dumps({"metric": "Muon step time", "value": ms, "unit": "ms",
+                      "config": {"workload": "llama3-8b muon step, 6.98G params, P=64, gas=2, "
+                                             "standard NS x5", "operand_mode": args.mode},
+                      "ns_tflops": flops / (g["ms"] / args.steps * 1e-3) / 1e12,
+                      "ns_flops_per_step": flops,
+                      "hbm_gbs": sum(ph[k]["bytes"] for k in hbm) / (sum(ph[k]["ms"] for k in hbm) * 1e-3) / 1e9,
+                      "phases_ms_per_step": {k: ph[k]["ms"] / args.steps for k in ph},
+                      "result": nsg.read_result(res)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -366,14 +409,15 @@ def main():
     ap.add_argument("--mode", default="bf16", choices=["bf16", "fp32"])
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="gpt2", choices=["gpt2", "sweep", "ragged"],
+    ap.add_argument("--workload", default="gpt2", choices=["gpt2", "sweep", "ragged", "llama"],
                     help="gpt2 is the benchmark line; sweep and ragged print extra lines")
     ap.add_argument("--shapes", default="", help="sweep shapes, e.g. 4096x4096,4096x16384")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.workload != "gpt2" and args.impl == "ours":
         peaks, peak_src = load_peaks()
-        (run_sweep if args.workload == "sweep" else run_ragged)(args, peaks, peak_src)
+        {"sweep": run_sweep, "ragged": run_ragged, "llama": run_llama}[args.workload](
+            args, peaks, peak_src)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

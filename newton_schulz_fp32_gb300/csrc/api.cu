@@ -281,7 +281,23 @@ int validate_and_build(const muon_param_t* params, int nparams, const muon_parti
     Owner& o = L.owners[oi];
     o.rtile_begin = static_cast<int32_t>(L.rtiles.size());
     for (int64_t r = 0; r < o.numel; r += kReduceTile)
-      L.rtiles.push_back({oi, static_cast<int32_t>(std::min<int64_t>(kReduceTile, o.numel - r)), r});
+    {
+      RTile rt{};
+      rt.owner = oi;
+      rt.len = static_cast<int32_t>(std::min<int64_t>(kReduceTile, o.numel - r));
+      rt.rel_begin = r;
+      for (int k = o.seg_begin; k < o.seg_begin + o.seg_count; ++k) {
+        const Segment& sg = L.segs[k];
+        if (r < sg.rel_begin || r >= sg.rel_begin + sg.len) continue;
+        const int64_t delta = sg.storage_begin - sg.rel_begin;
+        if (r + rt.len <= sg.rel_begin + sg.len && rt.len % 4 == 0 && ((delta + r) & 3) == 0) {
+          rt.fast = 1;
+          rt.sdelta = delta;
+        }
+        break;
+      }
+      L.rtiles.push_back(rt);
+    }
     o.rtile_count = static_cast<int32_t>(L.rtiles.size()) - o.rtile_begin;
     if (o.is_muon) {
       if (!o.transposed) {

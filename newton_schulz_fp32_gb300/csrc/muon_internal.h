@@ -55,11 +55,16 @@ struct Owner {
   int64_t sq_off;       // element offset of this owner in each m x m region
 };
 
-// Pass-1 tile: owner elements [rel_begin, rel_begin + len).
+// Pass-1 tile: owner elements [rel_begin, rel_begin + len).  Thread t sums
+// the elements of 4-element groups t, t + 256, ... in order, so the sum
+// order depends only on the owner-relative index.  fast = 1: the tile lies
+// in one segment, len % 4 == 0 and storage (sdelta + rel) is 16-byte aligned.
 struct RTile {
   int32_t owner;
   int32_t len;
   int64_t rel_begin;
+  int32_t fast, pad;
+  int64_t sdelta;
 };
 
 // Tile of the gather (pass 2) and scatter kernels.

@@ -133,42 +133,62 @@ k_accumulate(float* __restrict__ accum, const uint16_t* __restrict__ grad,
 
 // ------------------------------------------------------------------ S2 pass 1
 
-// Thread t of the tile handles elements tile_begin + t + k*NT in increasing
-// order, whatever segments they fall in: the sum order depends only on the
-// owner-relative index.
+// Thread t of the tile sums the 4-element groups t, t + NT, t + 2 NT, ...
+// (elements in order within a group), whatever segments they fall in: the
+// sum order depends only on the owner-relative index.  Tiles inside one
+// aligned segment read float4s; others resolve each element's segment.
+__device__ __forceinline__ void reduce_one(float g, float m, bool muon, float beta, float& acc,
+                                           bool& bad) {
+  bad |= !isfinite(g);
+  const float v = muon ? momentum_of(beta, m, g) : g;
+  acc = __fmaf_rn(v, v, acc);
+}
+
 __global__ void __launch_bounds__(kStreamThreads)
 k_reduce(StreamLaunchArgs a) {
   constexpr int NT = kStreamThreads;
   const RTile t = a.rtiles[blockIdx.x];
   const Owner o = a.owners[t.owner];
-  const Segment* segs = a.segs + o.seg_begin;
+  const bool muon = o.is_muon != 0;
   const int64_t tb = t.rel_begin, te = t.rel_begin + t.len;
+  const int ngroups = (t.len + 3) / 4;
   float acc = 0.f;
   bool bad = false;
-  int si = find_seg(segs, o.seg_count, tb);
-  for (; si < o.seg_count && segs[si].rel_begin < te; ++si) {
-    const Segment sg = segs[si];
-    const int64_t lo = sg.rel_begin > tb ? sg.rel_begin : tb;
-    const int64_t hi = (sg.rel_begin + sg.len) < te ? (sg.rel_begin + sg.len) : te;
-    // first element >= lo with (rel - tb) % NT == threadIdx.x
-    const int64_t off = (lo - tb) % NT;
-    int64_t rel = lo + ((threadIdx.x - off + NT) % NT);
-    const int64_t base = sg.storage_begin - sg.rel_begin;
-    if (o.is_muon) {
-      #pragma unroll 4
-      for (; rel < hi; rel += NT) {
-        const float g = a.accum[base + rel];
-        const float m = a.momentum[base + rel];
-        bad |= !isfinite(g);
-        const float v = momentum_of(a.beta, m, g);
-        acc = __fmaf_rn(v, v, acc);
+  if (t.fast) {
+    const float* G = a.accum + t.sdelta + tb;
+    const float* M = a.momentum + t.sdelta + tb;
+    constexpr int U = 4;
+    for (int g0 = threadIdx.x; g0 < ngroups; g0 += NT * U) {
+      float4 gv[U], mv[U];
+      #pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int g = g0 + u * NT;
+        if (g < ngroups) {
+          gv[u] = *reinterpret_cast<const float4*>(G + 4 * g);
+          mv[u] = muon ? *reinterpret_cast<const float4*>(M + 4 * g) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
-    } else {
-      #pragma unroll 4
-      for (; rel < hi; rel += NT) {
-        const float g = a.accum[base + rel];
-        bad |= !isfinite(g);
-        acc = __fmaf_rn(g, g, acc);
+      #pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (g0 + u * NT < ngroups) {
+          reduce_one(gv[u].x, mv[u].x, muon, a.beta, acc, bad);
+          reduce_one(gv[u].y, mv[u].y, muon, a.beta, acc, bad);
+          reduce_one(gv[u].z, mv[u].z, muon, a.beta, acc, bad);
+          reduce_one(gv[u].w, mv[u].w, muon, a.beta, acc, bad);
+        }
+      }
+    }
+  } else {
+    const Segment* segs = a.segs + o.seg_begin;
+    int si = -1;
+    for (int g = threadIdx.x; g < ngroups; g += NT) {
+      for (int j = 0; j < 4; ++j) {
+        const int64_t rel = tb + 4 * int64_t(g) + j;
+        if (rel >= te) break;
+        if (si < 0) si = find_seg(segs, o.seg_count, rel);
+        while (rel >= segs[si].rel_begin + segs[si].len) ++si;
+        const int64_t st = segs[si].storage_begin + (rel - segs[si].rel_begin);
+        reduce_one(a.accum[st], muon ? a.momentum[st] : 0.f, muon, a.beta, acc, bad);
       }
     }
   }
@@ -478,12 +498,32 @@ k_update_sumsq(StreamLaunchArgs a) {
   const Owner o = a.owners[t.owner];
   const char* y = static_cast<const char*>(a.y) + o.x_off * a.esize;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per = 16 / a.esize;                     // elements per 16-byte load
+  const int nv = (o.n / per) * per;                 // vectorised part of each row
   float acc = 0.f;
-  for (int r = t.r0 + warp; r < t.r0 + t.nr; r += kStreamThreads / 32)
-    for (int c = lane; c < o.n; c += 32) {
-      const float v = load_ws(y, a.esize, int64_t(r) * o.ldx + c);
+  for (int r = t.r0 + warp; r < t.r0 + t.nr; r += kStreamThreads / 32) {
+    const int64_t rb = int64_t(r) * o.ldx;
+    for (int c = lane * per; c < nv; c += 32 * per) {
+      const uint4 w = *reinterpret_cast<const uint4*>(y + (rb + c) * a.esize);
+      if (a.esize == 2) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+        #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __bfloat1622float2(h[k]);
+          acc = __fmaf_rn(f.x, f.x, acc);
+          acc = __fmaf_rn(f.y, f.y, acc);
+        }
+      } else {
+        const float* f = reinterpret_cast<const float*>(&w);
+        #pragma unroll
+        for (int k = 0; k < 4; ++k) acc = __fmaf_rn(f[k], f[k], acc);
+      }
+    }
+    for (int c = nv + lane; c < o.n; c += 32) {
+      const float v = load_ws(y, a.esize, rb + c);
       acc = __fmaf_rn(v, v, acc);
     }
+  }
   const double s = block_sum<kStreamThreads>(static_cast<double>(acc));
   if (threadIdx.x == 0) a.ytile_sum[blockIdx.x] = s;
 }

@@ -296,3 +296,66 @@ def test_ragged_small_matrices_gram(torch):
     for k in wl.rng_for(seed, 3).choice(len(lay.specs), 64, replace=False):
         _, u_or = om.muon_update(mats[k], z[k], BETA, "gram", 5, 0, "bf16")
         assert_close_update(u_un[k], u_or, "bf16", lay.specs[k].name)
+
+
+def test_llama3_8b_config_sampled(torch):
+    """Llama-3-8B shapes at full size (6.98G elements, P=64, gas=2, standard
+    NS): every block's update in the quintic band (checked on the device);
+    sampled Gaussian matrices against the BF16 oracle; a sampled low-rank
+    matrix by the declared rule (top-8 subspace within 1e-2, sigma_max
+    within the band) and, in FP32 mode, against the exact oracle at
+    atol 1e-4 / rtol 1e-3."""
+    lay = wl.llama3_8b_layout()
+    seed = wl.CONFIG_SEED["llama"]
+    n = lay.storage_size
+    acc = torch.zeros(n, dtype=torch.float32, device="cuda")
+    mom = torch.zeros(n, dtype=torch.float32, device="cuda")
+    mst = torch.zeros(n, dtype=torch.float32, device="cuda")
+    grad = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    sample = [1, 7 * 31 + 1, 7 * 31 + 2]          # k of layer 0, k and v of layer 31
+    g_host = {k: [] for k in sample}
+    for mb in range(2):
+        wl.llama_grad_into(lay, seed, mb, grad)
+        for k in sample:
+            off, s = int(lay.params["offset"][k]), lay.specs[k]
+            g_host[k].append(grad[off:off + s.numel].float().cpu().numpy().reshape(s.rows, s.cols))
+        nsg.accumulate(acc, grad, 0.5, overwrite=(mb == 0), params=lay.params, parts=lay.parts)
+    del grad
+    res = nsg.read_result(nsg.step(acc, mom, mst, lay.params, lay.parts, BETA, LR, "standard", 5,
+                                   0.0, "bf16"))
+    assert res["applied"] == 1 and res["ns_calls"] == 224 and res["clip_coef"] == 1.0
+    # band check of every block on the device: Gaussian blocks have all m
+    # singular values in the band; rank-8-plus-1e-3-noise blocks have 8 in
+    # the band and noise directions (normalised ~1e-5, amplified ~a^5 ~ 485)
+    # that add well under 1 to the sum of squares
+    for k, spec in enumerate(lay.specs):
+        off = int(lay.params["offset"][k])
+        u = acc[off:off + spec.numel].double()
+        sq = float((u * u).sum())
+        r = min(spec.rows, spec.cols) if k % 2 == 1 else 8
+        extra = 0.0 if k % 2 == 1 else 1.0
+        assert r * BAND_LO ** 2 * 0.98 <= sq <= r * BAND_HI ** 2 * 1.02 + extra, (spec.name, sq / r)
+    for k in sample:
+        spec = lay.specs[k]
+        off = int(lay.params["offset"][k])
+        g = om.accumulate(om.accumulate(None, g_host[k][0], 0.5, True), g_host[k][1], 0.5)
+        m_gpu = mom[off:off + spec.numel].cpu().numpy().reshape(spec.rows, spec.cols)
+        assert np.array_equal(bits(m_gpu), bits(om.momentum_update(np.zeros_like(g), g, BETA)))
+        u_gpu = acc[off:off + spec.numel].cpu().numpy().reshape(spec.rows, spec.cols)
+        u_or = ons.newton_schulz(m_gpu, "standard", 5, "bf16")
+        if k % 2 == 1:            # Gaussian
+            assert_close_update(u_gpu, u_or, "bf16", spec.name)
+        else:                     # low-rank + noise: declared rule in BF16 mode
+            U = np.linalg.svd(m_gpu.astype(np.float64), full_matrices=False)[0][:, :8]
+            proj = lambda x: U @ (U.T @ np.asarray(x, np.float64))
+            assert relf(proj(u_gpu), proj(u_or)) <= 1e-2, spec.name
+            assert np.linalg.norm(u_gpu.astype(np.float64), 2) <= BAND_HI * (1 + 1e-2)
+            # and at the strict tolerance in FP32 mode
+            y32 = nsg.newton_schulz(torch.from_numpy(m_gpu).cuda(), ns_method="standard",
+                                    operand_mode="fp32").cpu().numpy()
+            assert_close_update(y32, ons.newton_schulz(m_gpu, "standard", 5, "exact"), "fp32",
+                                spec.name + " fp32")
+    del acc, mom, mst
+    nsg.release_workspace()
+    torch.cuda.empty_cache()
+    assert nsg.device_error() == 0

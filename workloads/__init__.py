@@ -285,6 +285,32 @@ def bf16_storage_grad(layout: Layout, mats, padding_value: float = 0.0) -> np.nd
     return to_bf16_bits(pack(layout, mats, np.float32, fill=padding_value))
 
 
+def llama_grad_into(layout: Layout, seed: int, micro_batch: int, out, params=None):
+    """Fills a device bfloat16 storage tensor (identity storage) with one
+    micro-batch of Llama-shaped gradients, generated on the device with
+    torch's seeded generator: even-indexed parameters are low-rank plus
+    noise (U V^T with U, V N(0,1) of rank 8, plus 1e-3 N(0,1)), odd-indexed
+    ones N(0,1).  `params` restricts generation to those parameter indices
+    (the rest of `out` is left alone).  Input generation only."""
+    import torch
+    dev = out.device
+    for i, (spec, prow) in enumerate(zip(layout.specs, layout.params)):
+        if params is not None and i not in params:
+            continue
+        g = torch.Generator(device=dev).manual_seed(int(seed) * 1_000_003 + i * 7919 + micro_batch)
+        r, c = spec.rows, spec.cols
+        if i % 2 == 0:
+            U = torch.randn((r, 8), generator=g, device=dev)
+            V = torch.randn((8, c), generator=g, device=dev)
+            m = U @ V
+            m.add_(torch.randn((r, c), generator=g, device=dev), alpha=1e-3)
+        else:
+            m = torch.randn((r, c), generator=g, device=dev)
+        off = int(prow["offset"])
+        out[off:off + r * c].copy_(m.reshape(-1).to(torch.bfloat16))
+        del m
+
+
 NAN_SENTINEL_BITS = np.uint32(0x7FC0DEAD)   # a quiet NaN with a payload
 
 
