@@ -344,7 +344,7 @@ int validate_and_build(const muon_param_t* params, int nparams, const muon_parti
 
 // ------------------------------------------------------------------ NS plan
 
-enum Engine { ENGINE_TC = 0, ENGINE_SIMT = 1, ENGINE_CONVERT = 2 };
+enum Engine { ENGINE_TC = 0, ENGINE_SIMT = 1, ENGINE_CONVERT = 2, ENGINE_X3 = 3 };
 
 // One launch of the NS iteration: a grouped GEMM over every block, or (for
 // ENGINE_CONVERT) the fp32 -> bf16 rounding of a whole workspace region.
@@ -361,7 +361,8 @@ struct GemmPhase {
 };
 
 struct NsPlan {
-  int esize = 2;   // bytes of X0 / Y elements
+  int esize = 2;       // X0 / Y element format: 2 bf16, 4 fp32, 6 split-3
+  int64_t x_ps = 0;    // split-3: elements between the planes of an X region
   bool use_tc = false;
   int method = 0, steps = 5;
   DevBuf ws;
@@ -375,10 +376,11 @@ struct NsPlan {
 struct PhaseBuilder {
   GemmPhase* ph;
   void add(const GemmProblem& p) {
-    const bool tc = ph->engine == ENGINE_TC;
+    int bm = kSimtTile, bn = kSimtTile;
+    if (ph->engine == ENGINE_TC) { bm = kTcBM; bn = kTcBN; }
+    if (ph->engine == ENGINE_X3) { bm = kX3BM; bn = kX3BN; }
     const int idx = static_cast<int>(ph->probs.size());
     ph->probs.push_back(p);
-    const int bm = tc ? kTcBM : kSimtTile, bn = tc ? kTcBN : kSimtTile;
     const int tm_n = (p.M + bm - 1) / bm, tn_n = (p.N + bn - 1) / bn;
     for (int tm = 0; tm < tm_n; ++tm)
       for (int tn = 0; tn < tn_n; ++tn) {
@@ -397,61 +399,91 @@ int finish_phase(GemmPhase& ph) {
   });
   MUON_CUDA_TRY(upload(ph.d_probs, ph.probs));
   MUON_CUDA_TRY(upload(ph.d_tiles, ph.tiles));
-  if (ph.engine == ENGINE_TC) {
+  if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3) {
     std::vector<TcMaps> maps(ph.probs.size());
-    for (size_t i = 0; i < ph.probs.size(); ++i)
-      if (!tc_encode_maps(ph.probs[i], &maps[i]))
-        return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    for (size_t i = 0; i < ph.probs.size(); ++i) {
+      const bool ok = ph.engine == ENGINE_TC ? tc_encode_maps(ph.probs[i], &maps[i])
+                                             : x3_encode_maps(ph.probs[i], &maps[i]);
+      if (!ok) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    }
     MUON_CUDA_TRY(upload(ph.d_maps, maps));
   }
   return MUON_OK;
 }
 
+// A matrix in a workspace region: element format (2 bf16, 4 fp32, 6
+// split-3), plane stride, leading dimension.
+struct WsMat {
+  char* p;
+  int es;
+  int64_t ps;
+  int64_t ld;
+};
+
 // Work lists of the NS iteration over every Muon block (owner), laid out in
 // per-owner slices of the workspace regions (x_off for m x n, sq_off for
 // m x m).
 //
-// standard (both modes): per step A = X X^T (symmetric: upper tiles,
-//   mirrored), B = c A A + b A (symmetric), X' = B X + a X, ping-ponging X.
-//   The oracle's A and B are exactly symmetric too (bf16 products summed
-//   in float64 are exact), so mirroring changes no value.
-// gram: R0 = X0 X0^T (symmetric, fp32 result), then the m x m recurrence
-//   P = c R R + b R + a I, Q <- P Q, T = P R, R = T P, all in FP32 with B
-//   read MN-major (no symmetry assumed: in floating point R and P are not
-//   exactly symmetric); Q is rounded to bf16 (BF16 mode) and Y = Q X0.
+// standard: per step A = X X^T (symmetric: upper tiles, mirrored),
+//   B = c A A + b A (symmetric), X' = B X + a X, ping-ponging X.  The
+//   oracle's A and B are exactly symmetric too (bf16 products summed in
+//   float64 are exact), so mirroring changes no value.
+// gram: R0 = X0 X0^T (symmetric), then the m x m recurrence
+//   P = c R R + b R + a I, Q <- P Q, T = P R, R = T P in FP32 with B read
+//   MN-major (no symmetry assumed: in floating point R and P are not
+//   exactly symmetric); then Y = bf16(Q) X0 (BF16 mode) or Q X0 (FP32 mode).
+// Engines: BF16 operands on the tensor cores (ENGINE_TC); FP32 operands on
+// the tensor cores through split-3 planes (ENGINE_X3); with MUON_GEMM=simt
+// everything runs on the CUDA-core kernel with plain bf16 / fp32 storage.
 int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_elems,
                   int method, int mode, int steps, NsPlan& P) {
   const bool bf16 = mode == MUON_OPERANDS_BF16;
   const char* env = std::getenv("MUON_GEMM");
   const bool force_simt = env && std::strcmp(env, "simt") == 0;
-  P.esize = bf16 ? 2 : 4;
-  P.use_tc = bf16 && !force_simt && tc_available();
+  P.use_tc = !force_simt && tc_available();
   if (bf16 && !P.use_tc && !force_simt)
     return fail(MUON_ERR_UNSUPPORTED, "BF16 operand mode needs an sm_103 (GB300) GPU");
-  const int big = P.use_tc ? ENGINE_TC : ENGINE_SIMT;   // engine of the bf16/fp32 X products
+  const bool tc = P.use_tc;
+  const int xe = bf16 ? 2 : (tc ? 6 : 4);          // X regions
+  const int fe = tc ? 6 : 4;                       // gram's m x m regions
+  const int se = method == MUON_NS_STANDARD ? xe : fe;
+  auto bytes_of = [](int es) { return size_t(es == 6 ? 6 : es); };
+  auto eb = [](int es) { return int64_t(es == 6 ? 2 : es); };
+  P.esize = xe;
+  P.x_ps = xe == 6 ? x_elems : 0;
   P.method = method;
   P.steps = steps;
-  const size_t es = P.esize;
-  size_t bytes = es * size_t(2 * x_elems);
-  if (method == MUON_NS_STANDARD) bytes += es * size_t(2 * sq_elems);
-  else bytes += 4 * size_t(5 * sq_elems) + (bf16 ? 2 * size_t(sq_elems) : 0);
+  const int nsq = method == MUON_NS_STANDARD ? 2 : 5;
+  const bool need_qbf = method == MUON_NS_GRAM && bf16 && !tc;
+  size_t bytes = 2 * bytes_of(xe) * size_t(x_elems) + nsq * bytes_of(se) * size_t(sq_elems);
+  if (need_qbf) bytes += 2 * size_t(sq_elems);
   MUON_CUDA_TRY(P.ws.alloc(bytes + 256));
   char* base = P.ws.as<char>();
-  char* X[2] = {base, base + es * x_elems};
-  char* sq_base = base + es * 2 * x_elems;
+  char* X[2] = {base, base + bytes_of(xe) * x_elems};
+  char* sq_base = base + 2 * bytes_of(xe) * x_elems;
+  char* S[5];
+  for (int i = 0; i < nsq; ++i) S[i] = sq_base + i * bytes_of(se) * size_t(sq_elems);
+  char* Qbf = sq_base + nsq * bytes_of(se) * size_t(sq_elems);
   P.x0 = X[0];
   const float a = kNsA, b = kNsB, c = kNsC;
 
-  auto mk = [&](char* A, int64_t lda, char* B, int64_t ldb, int bk, char* D, int64_t ldd, int d_es,
-                char* E, int64_t lde, int e_es, int M, int N, int K, int sym, float al, float be,
-                float ga) {
+  auto xm = [&](char* r, const Owner& o) {
+    return WsMat{r + eb(xe) * o.x_off, xe, xe == 6 ? x_elems : 0, o.ldx};
+  };
+  auto sm = [&](char* r, const Owner& o, int es) {
+    return WsMat{r + eb(es) * o.sq_off, es, es == 6 ? sq_elems : 0, o.ldm};
+  };
+  const WsMat none{nullptr, 2, 0, 0};
+  auto mk = [&](WsMat A, WsMat B, int bk, WsMat D, WsMat E, int M, int N, int K, int sym, float al,
+                float be, float ga) {
     GemmProblem p{};
-    p.A = A; p.B = B; p.D = D; p.E = E;
-    p.lda = lda; p.ldb = ldb; p.ldd = ldd; p.lde = lde;
+    p.A = A.p; p.B = B.p; p.D = D.p; p.E = E.p;
+    p.lda = A.ld; p.ldb = B.ld; p.ldd = D.ld; p.lde = E.ld;
+    p.a_ps = A.ps; p.b_ps = B.ps; p.d_ps = D.ps; p.e_ps = E.ps;
     p.M = M; p.N = N; p.K = K;
     p.b_kmajor = bk; p.symmetric = sym;
     p.alpha = al; p.beta = be; p.gamma = ga;
-    p.d_es = d_es; p.e_es = e_es;
+    p.d_es = D.es; p.e_es = E.p ? E.es : D.es;
     return p;
   };
   auto new_phase = [&](int engine, int ab_es) {
@@ -460,88 +492,99 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_
     P.phases.back()->ab_es = ab_es;
     return PhaseBuilder{P.phases.back().get()};
   };
-  auto xo = [&](char* r, const Owner& o) { return r + es * o.x_off; };
-  const int E_ = static_cast<int>(es);
+  // engine for products whose operands have format es
+  auto engine_for = [&](int es) { return !tc ? ENGINE_SIMT : (es == 2 ? ENGINE_TC : ENGINE_X3); };
 
   if (method == MUON_NS_STANDARD) {
-    char* S[2] = {sq_base, sq_base + es * sq_elems};
-    auto so = [&](char* r, const Owner& o) { return r + es * o.sq_off; };
+    const int eng = engine_for(xe);
     for (int st = 0; st < steps; ++st) {
       char* src = X[st & 1];
       char* dst = X[(st + 1) & 1];
-      PhaseBuilder g = new_phase(big, E_);   // A = X X^T
+      PhaseBuilder g = new_phase(eng, xe);   // A = X X^T
       for (const Owner& o : owners)
         if (o.is_muon)
-          g.add(mk(xo(src, o), o.ldx, xo(src, o), o.ldx, 1, so(S[0], o), o.ldm, E_, nullptr, 0, E_,
-                   o.m, o.m, o.n, 1, 1.f, 0.f, 0.f));
-      PhaseBuilder q = new_phase(big, E_);   // B = c A A + b A
+          g.add(mk(xm(src, o), xm(src, o), 1, sm(S[0], o, se), none, o.m, o.m, o.n, 1, 1.f, 0.f, 0.f));
+      PhaseBuilder q = new_phase(eng, xe);   // B = c A A + b A
       for (const Owner& o : owners)
         if (o.is_muon)
-          q.add(mk(so(S[0], o), o.ldm, so(S[0], o), o.ldm, 1, so(S[1], o), o.ldm, E_, so(S[0], o),
-                   o.ldm, E_, o.m, o.m, o.m, 1, c, b, 0.f));
-      PhaseBuilder u = new_phase(big, E_);   // X' = B X + a X
+          q.add(mk(sm(S[0], o, se), sm(S[0], o, se), 1, sm(S[1], o, se), sm(S[0], o, se), o.m, o.m,
+                   o.m, 1, c, b, 0.f));
+      PhaseBuilder u = new_phase(eng, xe);   // X' = B X + a X
       for (const Owner& o : owners)
         if (o.is_muon)
-          u.add(mk(so(S[1], o), o.ldm, xo(src, o), o.ldx, 0, xo(dst, o), o.ldx, E_, xo(src, o), o.ldx,
-                   E_, o.m, o.n, o.m, 0, 1.f, a, 0.f));
+          u.add(mk(sm(S[1], o, se), xm(src, o), 0, xm(dst, o), xm(src, o), o.m, o.n, o.m, 0, 1.f, a,
+                   0.f));
     }
     P.y = X[steps & 1];
   } else {
-    char* F[5];
-    for (int i = 0; i < 5; ++i) F[i] = sq_base + 4 * size_t(i) * sq_elems;
-    char *R = F[0], *Pm = F[1], *Qa = F[2], *Qb = F[3], *T = F[4];
-    char* Qbf = sq_base + 4 * size_t(5) * sq_elems;
-    auto s4 = [&](char* r, const Owner& o) { return r + 4 * o.sq_off; };
-    PhaseBuilder g0 = new_phase(big, E_);   // R = X0 X0^T, fp32 result
+    char *R = S[0], *Pm = S[1], *Qa = S[2], *Qb = S[3], *T = S[4];
+    const int rec = tc ? ENGINE_X3 : ENGINE_SIMT;
+    PhaseBuilder g0 = new_phase(engine_for(xe), xe);   // R = X0 X0^T
     for (const Owner& o : owners)
       if (o.is_muon)
-        g0.add(mk(xo(X[0], o), o.ldx, xo(X[0], o), o.ldx, 1, s4(R, o), o.ldm, 4, nullptr, 0, 4, o.m,
-                  o.m, o.n, 1, 1.f, 0.f, 0.f));
+        g0.add(mk(xm(X[0], o), xm(X[0], o), 1, sm(R, o, fe), none, o.m, o.m, o.n, 1, 1.f, 0.f, 0.f));
     char* Qcur = Qa;
     for (int k = 0; k < steps; ++k) {
       char* Pk = (k == 0) ? Qa : Pm;   // Q1 = P0 (Q0 = I)
-      PhaseBuilder pp = new_phase(ENGINE_SIMT, 4);   // P = c R R + b R + a I
+      PhaseBuilder pp = new_phase(rec, fe);   // P = c R R + b R + a I
       for (const Owner& o : owners)
         if (o.is_muon)
-          pp.add(mk(s4(R, o), o.ldm, s4(R, o), o.ldm, 0, s4(Pk, o), o.ldm, 4, s4(R, o), o.ldm, 4, o.m,
-                    o.m, o.m, 0, c, b, a));
+          pp.add(mk(sm(R, o, fe), sm(R, o, fe), 0, sm(Pk, o, fe), sm(R, o, fe), o.m, o.m, o.m, 0, c, b,
+                    a));
       if (k > 0) {
         char* Qn = (Qcur == Qa) ? Qb : Qa;
-        PhaseBuilder qq = new_phase(ENGINE_SIMT, 4);   // Q <- P Q
+        PhaseBuilder qq = new_phase(rec, fe);   // Q <- P Q
         for (const Owner& o : owners)
           if (o.is_muon)
-            qq.add(mk(s4(Pk, o), o.ldm, s4(Qcur, o), o.ldm, 0, s4(Qn, o), o.ldm, 4, nullptr, 0, 4,
-                      o.m, o.m, o.m, 0, 1.f, 0.f, 0.f));
+            qq.add(mk(sm(Pk, o, fe), sm(Qcur, o, fe), 0, sm(Qn, o, fe), none, o.m, o.m, o.m, 0, 1.f,
+                      0.f, 0.f));
         Qcur = Qn;
       }
       if (k < steps - 1) {
-        PhaseBuilder tt = new_phase(ENGINE_SIMT, 4);   // T = P R
+        PhaseBuilder tt = new_phase(rec, fe);   // T = P R
         for (const Owner& o : owners)
           if (o.is_muon)
-            tt.add(mk(s4(Pk, o), o.ldm, s4(R, o), o.ldm, 0, s4(T, o), o.ldm, 4, nullptr, 0, 4, o.m,
-                      o.m, o.m, 0, 1.f, 0.f, 0.f));
-        PhaseBuilder rr = new_phase(ENGINE_SIMT, 4);   // R = T P
+            tt.add(mk(sm(Pk, o, fe), sm(R, o, fe), 0, sm(T, o, fe), none, o.m, o.m, o.m, 0, 1.f, 0.f,
+                      0.f));
+        PhaseBuilder rr = new_phase(rec, fe);   // R = T P
         for (const Owner& o : owners)
           if (o.is_muon)
-            rr.add(mk(s4(T, o), o.ldm, s4(Pk, o), o.ldm, 0, s4(R, o), o.ldm, 4, nullptr, 0, 4, o.m,
-                      o.m, o.m, 0, 1.f, 0.f, 0.f));
+            rr.add(mk(sm(T, o, fe), sm(Pk, o, fe), 0, sm(R, o, fe), none, o.m, o.m, o.m, 0, 1.f, 0.f,
+                      0.f));
       }
     }
-    char* Qy = Qcur;
-    if (bf16) {   // Q rounded to bf16 for the tensor-core product
+    PhaseBuilder* yy = nullptr;
+    if (bf16 && tc) {
+      // bf16(Q) is exactly the hi plane of the split-3 Q
+      PhaseBuilder ph = new_phase(ENGINE_TC, 2);
+      for (const Owner& o : owners)
+        if (o.is_muon) {
+          WsMat q = sm(Qcur, o, fe);
+          q.es = 2;
+          q.ps = 0;
+          ph.add(mk(q, xm(X[0], o), 0, xm(X[1], o), none, o.m, o.n, o.m, 0, 1.f, 0.f, 0.f));
+        }
+      yy = nullptr;
+    } else if (need_qbf) {   // CUDA-core path: round Q to bf16, then Y = Q X0
       P.phases.emplace_back(new GemmPhase());
       GemmPhase& cv = *P.phases.back();
       cv.engine = ENGINE_CONVERT;
       cv.conv_src = reinterpret_cast<const float*>(Qcur);
       cv.conv_dst = Qbf;
       cv.conv_n = sq_elems;
-      Qy = Qbf;
+      PhaseBuilder ph = new_phase(ENGINE_SIMT, 2);
+      for (const Owner& o : owners)
+        if (o.is_muon)
+          ph.add(mk(WsMat{Qbf + 2 * o.sq_off, 2, 0, o.ldm}, xm(X[0], o), 0, xm(X[1], o), none, o.m,
+                    o.n, o.m, 0, 1.f, 0.f, 0.f));
+    } else {   // FP32 mode: Y = Q X0 in FP32 (split-3 or fp32)
+      PhaseBuilder ph = new_phase(engine_for(xe), xe);
+      for (const Owner& o : owners)
+        if (o.is_muon)
+          ph.add(mk(sm(Qcur, o, fe), xm(X[0], o), 0, xm(X[1], o), none, o.m, o.n, o.m, 0, 1.f, 0.f,
+                    0.f));
     }
-    PhaseBuilder yy = new_phase(big, E_);   // Y = Q X0
-    for (const Owner& o : owners)
-      if (o.is_muon)
-        yy.add(mk(Qy + es * o.sq_off, o.ldm, xo(X[0], o), o.ldx, 0, xo(X[1], o), o.ldx, E_, nullptr,
-                  0, E_, o.m, o.n, o.m, 0, 1.f, 0.f, 0.f));
+    (void)yy;
     P.y = X[1];
   }
   for (auto& ph : P.phases) {
@@ -668,6 +711,11 @@ int enqueue_gemms(NsPlan& P, const StepState* state, int* err, cudaStream_t s) {
                          ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()), state, err,
                          s) != 0)
         return fail(MUON_ERR_CUDA, "tensor-core GEMM launch setup failed");
+    } else if (ph->engine == ENGINE_X3) {
+      if (launch_gemm_x3(ph->d_probs.as<GemmProblem>(), ph->d_maps.as<TcMaps>(),
+                         ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()), state, err,
+                         s) != 0)
+        return fail(MUON_ERR_CUDA, "split-3 tensor-core GEMM launch setup failed");
     } else {
       launch_gemm_simt(ph->d_probs.as<GemmProblem>(), ph->d_tiles.as<GemmTile>(),
                        static_cast<int>(ph->tiles.size()), ph->ab_es, state, s);
@@ -784,6 +832,7 @@ extern "C" int muon_step(float* accum, float* momentum, float* master, const muo
   a.x0 = P->x0;
   a.y = P->y;
   a.esize = P->esize;
+  a.x_ps = P->x_ps;
   a.beta = beta;
   a.lr = lr;
   a.clip = clip;
@@ -876,13 +925,13 @@ extern "C" int muon_newton_schulz(const void* X, void* Y, int rows, int cols, in
   {
     PhaseScope sc(MUON_PHASE_GATHER, s, 1, numel * (io_es + sp->ns.esize), 0.0);
     launch_ns_load(X, io_es, rows, cols, sp->tile_sum.as<double>(), sp->ntiles, sp->ns.x0,
-                   sp->ns.esize, sp->owners[0].ldx, s);
+                   sp->ns.esize, sp->owners[0].ldx, sp->ns.x_ps, s);
   }
   rc = enqueue_gemms(sp->ns, nullptr, sp->err.as<int>(), s);
   if (rc != MUON_OK) return rc;
   {
     PhaseScope sc(MUON_PHASE_SCATTER, s, 1, numel * (io_es + sp->ns.esize), 0.0);
-    launch_ns_store(sp->ns.y, sp->ns.esize, sp->owners[0].ldx, Y, io_es, rows, cols, s);
+    launch_ns_store(sp->ns.y, sp->ns.esize, sp->owners[0].ldx, sp->ns.x_ps, Y, io_es, rows, cols, s);
   }
   MUON_CUDA_TRY(cudaGetLastError());
   g_cnt.ns_calls_last = 1;

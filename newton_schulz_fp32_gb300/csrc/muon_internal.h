@@ -124,8 +124,10 @@ struct GemmProblem {
   int32_t b_kmajor;
   int32_t symmetric;
   float alpha, beta, gamma;
-  int32_t d_es, e_es;
+  int32_t d_es, e_es;   // 2 bf16, 4 fp32, 6 split-3 (three bf16 planes)
   int32_t pad;
+  // split-3 operands: element distance between the hi, mid and lo planes
+  int64_t a_ps, b_ps, d_ps, e_ps;
 };
 
 struct GemmTile {
@@ -159,7 +161,8 @@ struct StreamLaunchArgs {
   float* owner_div;
   void* x0;          // X0 region (m x n per owner)
   const void* y;     // final NS result region
-  int esize;         // bytes per workspace element (2 = bf16, 4 = fp32)
+  int esize;         // workspace element format: 2 bf16, 4 fp32, 6 split-3 planes
+  int64_t x_ps;      // split-3: elements between the planes of the X0 / Y regions
   float beta, lr, clip;
   StepState* state;
   const int* err_flag;   // set by a tensor-core kernel whose wait ran out
@@ -180,9 +183,9 @@ void launch_scatter(const StreamLaunchArgs& a, cudaStream_t s);
 void launch_ns_sumsq(const void* X, int io_esize, int64_t numel, double* tile_sum,
                      int ntiles, cudaStream_t s);
 void launch_ns_load(const void* X, int io_esize, int rows, int cols, const double* tile_sum,
-                    int ntiles, void* X0, int esize, int ldx, cudaStream_t s);
-void launch_ns_store(const void* Yws, int esize, int ldx, void* Y, int io_esize, int rows,
-                     int cols, cudaStream_t s);
+                    int ntiles, void* X0, int esize, int ldx, int64_t ps, cudaStream_t s);
+void launch_ns_store(const void* Yws, int esize, int ldx, int64_t ps, void* Y, int io_esize,
+                     int rows, int cols, cudaStream_t s);
 
 // Matrix products.  ab_es selects bf16 (2) or fp32 (4) A/B operands.
 void launch_gemm_simt(const GemmProblem* probs, const GemmTile* tiles, int ntiles, int ab_es,
@@ -191,6 +194,13 @@ void launch_gemm_simt(const GemmProblem* probs, const GemmTile* tiles, int ntile
 void launch_convert_bf16(const float* src, void* dst, int64_t n, const StepState* state,
                          cudaStream_t s);
 constexpr int kSimtTile = 128;
+
+// FP32-accurate products on the BF16 tensor cores from split-3 operands
+// (three exact bf16 planes per FP32 matrix; gemm_tc3.cu).
+bool x3_encode_maps(const GemmProblem& p, TcMaps* out);
+int launch_gemm_x3(const GemmProblem* probs, const TcMaps* maps, const GemmTile* tiles, int ntiles,
+                   const StepState* state, int* err_flag, cudaStream_t s);
+constexpr int kX3BM = 128, kX3BN = 128;
 
 // Sets (msg != nullptr) or clears the text muon_last_error() returns.
 void set_last_error(const char* msg);

@@ -249,7 +249,7 @@ extern "C" int muon_newton_schulz_noalloc(const void* X, void* Y, int rows, int 
 
   // ---- launches
   launch_ns_sumsq(X, io_es, numel, tile_sum, ntiles, s);
-  launch_ns_load(X, io_es, rows, cols, tile_sum, ntiles, X0, es, ldx, s);
+  launch_ns_load(X, io_es, rows, cols, tile_sum, ntiles, X0, es, ldx, 0, s);
   for (int i = 0; i < nops; ++i) {
     const Op& o = g_ops[i];
     if (o.engine == ENG_CONVERT) {
@@ -265,7 +265,7 @@ extern "C" int muon_newton_schulz_noalloc(const void* X, void* Y, int rows, int 
       launch_gemm_simt(d_probs + i, tl, nt, o.ab_es, nullptr, s);
     }
   }
-  launch_ns_store(Yws, es, ldx, Y, io_es, rows, cols, s);
+  launch_ns_store(Yws, es, ldx, 0, Y, io_es, rows, cols, s);
   if (cudaGetLastError() != cudaSuccess) return nofail(MUON_ERR_CUDA, "kernel launch failed");
   return MUON_OK;
 }

@@ -21,7 +21,7 @@
 // independent of the partition table.
 #include <cuda_bf16.h>
 
-#include "muon_internal.h"
+#include "tc_common.cuh"
 
 namespace muon {
 
@@ -31,16 +31,29 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-__device__ __forceinline__ float load_ws(const void* base, int esize, int64_t i) {
+// Workspace elements: esize 2 = bf16, 4 = fp32, 6 = split-3 (three bf16
+// planes `ps` elements apart whose sum is the fp32 value exactly).
+__device__ __forceinline__ int ebytes(int esize) { return esize == 6 ? 2 : esize; }
+
+__device__ __forceinline__ float load_ws(const void* base, int esize, int64_t i, int64_t ps = 0) {
   if (esize == 2) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
+  if (esize == 6) {
+    const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(base);
+    return __fadd_rn(__fadd_rn(__bfloat162float(b[i]), __bfloat162float(b[i + ps])),
+                     __bfloat162float(b[i + 2 * ps]));
+  }
   return reinterpret_cast<const float*>(base)[i];
 }
 
-__device__ __forceinline__ void store_ws(void* base, int esize, int64_t i, float v) {
-  if (esize == 2)
+__device__ __forceinline__ void store_ws(void* base, int esize, int64_t i, float v, int64_t ps = 0) {
+  if (esize == 2) {
     reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
-  else
+  } else if (esize == 6) {
+    __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(base);
+    tc::split3(v, b[i], b[i + ps], b[i + 2 * ps]);
+  } else {
     reinterpret_cast<float*>(base)[i] = v;
+  }
 }
 
 // Last segment whose rel_begin <= rel.
@@ -228,22 +241,46 @@ __device__ __forceinline__ void for_row(const Segment* segs, int nseg, int64_t l
 // All loads of a batch are issued before any store, so a thread keeps
 // several 16-byte requests in flight.
 
-__device__ __forceinline__ void store4_ws(void* base, int esize, int64_t i, float4 v) {
+__device__ __forceinline__ uint2 pack4_bf16(float a, float b, float c, float d) {
+  __nv_bfloat162 h[2] = {__floats2bfloat162_rn(a, b), __floats2bfloat162_rn(c, d)};
+  return *reinterpret_cast<const uint2*>(h);
+}
+
+__device__ __forceinline__ float4 unpack4_bf16(uint2 w) {
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ void store4_ws(void* base, int esize, int64_t i, float4 v, int64_t ps = 0) {
   if (esize == 2) {
-    __nv_bfloat162 h[2] = {__floats2bfloat162_rn(v.x, v.y), __floats2bfloat162_rn(v.z, v.w)};
-    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(base) + i) =
-        *reinterpret_cast<const uint2*>(h);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(base) + i) = pack4_bf16(v.x, v.y, v.z, v.w);
+  } else if (esize == 6) {
+    __nv_bfloat16 h[4][3];
+    const float f[4] = {v.x, v.y, v.z, v.w};
+    #pragma unroll
+    for (int k = 0; k < 4; ++k) tc::split3(f[k], h[k][0], h[k][1], h[k][2]);
+    __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(base) + i;
+    #pragma unroll
+    for (int pl = 0; pl < 3; ++pl) {
+      __nv_bfloat16 q[4] = {h[0][pl], h[1][pl], h[2][pl], h[3][pl]};
+      *reinterpret_cast<uint2*>(b + pl * ps) = *reinterpret_cast<const uint2*>(q);
+    }
   } else {
     *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + i) = v;
   }
 }
 
-__device__ __forceinline__ float4 load4_ws(const void* base, int esize, int64_t i) {
-  if (esize == 2) {
-    const uint2 w = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(base) + i);
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
-    return make_float4(a.x, a.y, b.x, b.y);
+__device__ __forceinline__ float4 load4_ws(const void* base, int esize, int64_t i, int64_t ps = 0) {
+  if (esize == 2)
+    return unpack4_bf16(*reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(base) + i));
+  if (esize == 6) {
+    const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(base) + i;
+    const float4 h = unpack4_bf16(*reinterpret_cast<const uint2*>(b));
+    const float4 m = unpack4_bf16(*reinterpret_cast<const uint2*>(b + ps));
+    const float4 l = unpack4_bf16(*reinterpret_cast<const uint2*>(b + 2 * ps));
+    return make_float4(__fadd_rn(__fadd_rn(h.x, m.x), l.x), __fadd_rn(__fadd_rn(h.y, m.y), l.y),
+                       __fadd_rn(__fadd_rn(h.z, m.z), l.z), __fadd_rn(__fadd_rn(h.w, m.w), l.w));
   }
   return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + i);
 }
@@ -278,7 +315,8 @@ __device__ __forceinline__ void gather_fast_rows(const StreamLaunchArgs& a, cons
         *reinterpret_cast<float4*>(M + i) = mv;
         store4_ws(x0, a.esize, i,
                   make_float4(__fdiv_rn(mv.x, d), __fdiv_rn(mv.y, d), __fdiv_rn(mv.z, d),
-                              __fdiv_rn(mv.w, d)));
+                              __fdiv_rn(mv.w, d)),
+                  a.x_ps);
       }
     }
   }
@@ -329,10 +367,11 @@ __device__ __forceinline__ void gather_fast_tr(const StreamLaunchArgs& a, const 
       float v[8];
       #pragma unroll
       for (int k = 0; k < 8; ++k) v[k] = tile[rs + k][cc];
-      store4_ws(x0, a.esize, xi, make_float4(v[0], v[1], v[2], v[3]));
-      store4_ws(x0, a.esize, xi + 4, make_float4(v[4], v[5], v[6], v[7]));
+      store4_ws(x0, a.esize, xi, make_float4(v[0], v[1], v[2], v[3]), a.x_ps);
+      store4_ws(x0, a.esize, xi + 4, make_float4(v[4], v[5], v[6], v[7]), a.x_ps);
     } else {
-      for (int k = 0; k < 8 && t.r0 + rs + k < r_end; ++k) store_ws(x0, a.esize, xi + k, tile[rs + k][cc]);
+      for (int k = 0; k < 8 && t.r0 + rs + k < r_end; ++k)
+        store_ws(x0, a.esize, xi + k, tile[rs + k][cc], a.x_ps);
     }
   }
 }
@@ -350,7 +389,7 @@ __device__ __forceinline__ void scatter_fast_rows(const StreamLaunchArgs& a, con
     for (int u = 0; u < U; ++u) {
       const int64_t i = i0 + u * stride;
       if (i < e1) {
-        u4[u] = load4_ws(y, a.esize, i);
+        u4[u] = load4_ws(y, a.esize, i, a.x_ps);
         w[u] = *reinterpret_cast<const float4*>(W + i);
       }
     }
@@ -380,11 +419,12 @@ __device__ __forceinline__ void scatter_fast_tr(const StreamLaunchArgs& a, const
   for (int pass = 0; pass < 2; ++pass) {
     const int64_t yi = int64_t(t.c0 + yr + 32 * pass) * o.ldx + t.r0 + rs;
     if (t.r0 + rs + 8 <= r_end) {
-      lo[pass] = load4_ws(y, a.esize, yi);
-      hi[pass] = load4_ws(y, a.esize, yi + 4);
+      lo[pass] = load4_ws(y, a.esize, yi, a.x_ps);
+      hi[pass] = load4_ws(y, a.esize, yi + 4, a.x_ps);
     } else {
       float v[8];
-      for (int k = 0; k < 8; ++k) v[k] = (t.r0 + rs + k < r_end) ? load_ws(y, a.esize, yi + k) : 0.f;
+      for (int k = 0; k < 8; ++k)
+        v[k] = (t.r0 + rs + k < r_end) ? load_ws(y, a.esize, yi + k, a.x_ps) : 0.f;
       lo[pass] = make_float4(v[0], v[1], v[2], v[3]);
       hi[pass] = make_float4(v[4], v[5], v[6], v[7]);
     }
@@ -451,7 +491,7 @@ k_gather(StreamLaunchArgs a) {
   const float d = a.owner_div[t.owner];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
-  char* x0 = static_cast<char*>(a.x0) + o.x_off * a.esize;
+  char* x0 = static_cast<char*>(a.x0) + o.x_off * ebytes(a.esize);
   if (t.fast) {
     if (t.kind == 0) gather_fast_rows(a, t, o, d, x0);
     else gather_fast_tr(a, t, o, d, x0, tile);
@@ -463,7 +503,7 @@ k_gather(StreamLaunchArgs a) {
       for_row(segs, o.seg_count, rb, rb + o.cols, lane, [&](int64_t rel, int64_t st) {
         const float mv = momentum_of(a.beta, a.momentum[st], a.accum[st]);
         a.momentum[st] = mv;
-        store_ws(x0, a.esize, int64_t(r) * o.ldx + (rel - rb), __fdiv_rn(mv, d));
+        store_ws(x0, a.esize, int64_t(r) * o.ldx + (rel - rb), __fdiv_rn(mv, d), a.x_ps);
       });
     }
   } else {
@@ -484,7 +524,7 @@ k_gather(StreamLaunchArgs a) {
       const int c = t.c0 + cc;
       if (c >= c_end) break;
       for (int rr = lane; rr < kTT && t.r0 + rr < r_end; rr += 32)
-        store_ws(x0, a.esize, int64_t(c) * o.ldx + t.r0 + rr, tile[rr][cc]);
+        store_ws(x0, a.esize, int64_t(c) * o.ldx + t.r0 + rr, tile[rr][cc], a.x_ps);
     }
   }
 }
@@ -496,31 +536,40 @@ k_update_sumsq(StreamLaunchArgs a) {
   if (a.state->overflow) return;
   const YTile t = a.ytiles[blockIdx.x];
   const Owner o = a.owners[t.owner];
-  const char* y = static_cast<const char*>(a.y) + o.x_off * a.esize;
+  const char* y = static_cast<const char*>(a.y) + o.x_off * ebytes(a.esize);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int per = 16 / a.esize;                     // elements per 16-byte load
+  const int per = a.esize == 4 ? 4 : 8;             // elements per 16-byte load (per plane)
   const int nv = (o.n / per) * per;                 // vectorised part of each row
   float acc = 0.f;
   for (int r = t.r0 + warp; r < t.r0 + t.nr; r += kStreamThreads / 32) {
     const int64_t rb = int64_t(r) * o.ldx;
     for (int c = lane * per; c < nv; c += 32 * per) {
-      const uint4 w = *reinterpret_cast<const uint4*>(y + (rb + c) * a.esize);
-      if (a.esize == 2) {
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
-        #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = __bfloat1622float2(h[k]);
-          acc = __fmaf_rn(f.x, f.x, acc);
-          acc = __fmaf_rn(f.y, f.y, acc);
-        }
-      } else {
+      if (a.esize == 4) {
+        const uint4 w = *reinterpret_cast<const uint4*>(y + (rb + c) * 4);
         const float* f = reinterpret_cast<const float*>(&w);
         #pragma unroll
         for (int k = 0; k < 4; ++k) acc = __fmaf_rn(f[k], f[k], acc);
+      } else {
+        float f[8];
+        const uint4 w = *reinterpret_cast<const uint4*>(y + (rb + c) * 2);
+        const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&w);
+        #pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] = __bfloat162float(h[k]);
+        if (a.esize == 6) {
+          const uint4 wm = *reinterpret_cast<const uint4*>(y + (rb + c + a.x_ps) * 2);
+          const uint4 wl = *reinterpret_cast<const uint4*>(y + (rb + c + 2 * a.x_ps) * 2);
+          const __nv_bfloat16* hm = reinterpret_cast<const __nv_bfloat16*>(&wm);
+          const __nv_bfloat16* hl = reinterpret_cast<const __nv_bfloat16*>(&wl);
+          #pragma unroll
+          for (int k = 0; k < 8; ++k)
+            f[k] = __fadd_rn(__fadd_rn(f[k], __bfloat162float(hm[k])), __bfloat162float(hl[k]));
+        }
+        #pragma unroll
+        for (int k = 0; k < 8; ++k) acc = __fmaf_rn(f[k], f[k], acc);
       }
     }
     for (int c = nv + lane; c < o.n; c += 32) {
-      const float v = load_ws(y, a.esize, rb + c);
+      const float v = load_ws(y, a.esize, rb + c, a.x_ps);
       acc = __fmaf_rn(v, v, acc);
     }
   }
@@ -576,7 +625,7 @@ k_scatter(StreamLaunchArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   if (t.fast) {
-    const char* yb = static_cast<const char*>(a.y) + o.x_off * a.esize;
+    const char* yb = static_cast<const char*>(a.y) + o.x_off * ebytes(a.esize);
     if (t.kind == 0) scatter_fast_rows(a, t, o, coef, yb);
     else if (t.kind == 1) scatter_fast_tr(a, t, o, coef, yb, tile);
     else scatter_fast_aux(a, t, coef);
@@ -596,12 +645,12 @@ k_scatter(StreamLaunchArgs a) {
     }
     return;
   }
-  const char* y = static_cast<const char*>(a.y) + o.x_off * a.esize;
+  const char* y = static_cast<const char*>(a.y) + o.x_off * ebytes(a.esize);
   if (t.kind == 0) {
     for (int r = t.r0 + warp; r < t.r0 + t.nr; r += nw) {
       const int64_t rb = int64_t(r) * o.cols;
       for_row(segs, o.seg_count, rb, rb + o.cols, lane, [&](int64_t rel, int64_t st) {
-        const float v = __fmul_rn(coef, load_ws(y, a.esize, int64_t(r) * o.ldx + (rel - rb)));
+        const float v = __fmul_rn(coef, load_ws(y, a.esize, int64_t(r) * o.ldx + (rel - rb), a.x_ps));
         a.accum[st] = v;
         a.master[st] = __fsub_rn(a.master[st], __fmul_rn(lr, v));
       });
@@ -613,7 +662,7 @@ k_scatter(StreamLaunchArgs a) {
       const int c = t.c0 + cc;
       if (c >= c_end) break;
       for (int rr = lane; rr < kTT && t.r0 + rr < r_end; rr += 32)
-        tile[rr][cc] = load_ws(y, a.esize, int64_t(c) * o.ldx + t.r0 + rr);
+        tile[rr][cc] = load_ws(y, a.esize, int64_t(c) * o.ldx + t.r0 + rr, a.x_ps);
     }
     __syncthreads();
     for (int rr = warp; rr < kTT; rr += nw) {
@@ -658,7 +707,7 @@ k_ns_norm(double* tile_sum, int ntiles) {
 // X (rows x cols, io dtype) -> X0 (m x n canonical, workspace dtype) = X / d
 __global__ void __launch_bounds__(kStreamThreads)
 k_ns_load(const void* X, int io_esize, int rows, int cols, const double* tile_sum, int ntiles,
-          void* X0, int esize, int ldx) {
+          void* X0, int esize, int ldx, int64_t ps) {
   __shared__ float tile[kTT][kTT + 1];
   const float d = reinterpret_cast<const float*>(tile_sum + ntiles)[0];
   const int r0 = blockIdx.y * kTT, c0 = blockIdx.x * kTT;
@@ -670,7 +719,7 @@ k_ns_load(const void* X, int io_esize, int rows, int cols, const double* tile_su
     for (int cc = lane; cc < kTT && c0 + cc < cols; cc += 32) {
       const float v = __fdiv_rn(load_ws(X, io_esize, int64_t(r) * cols + c0 + cc), d);
       if (tr) tile[rr][cc] = v;
-      else store_ws(X0, esize, int64_t(r) * ldx + c0 + cc, v);
+      else store_ws(X0, esize, int64_t(r) * ldx + c0 + cc, v, ps);
     }
   }
   if (!tr) return;
@@ -679,13 +728,14 @@ k_ns_load(const void* X, int io_esize, int rows, int cols, const double* tile_su
     const int c = c0 + cc;
     if (c >= cols) break;
     for (int rr = lane; rr < kTT && r0 + rr < rows; rr += 32)
-      store_ws(X0, esize, int64_t(c) * ldx + r0 + rr, tile[rr][cc]);
+      store_ws(X0, esize, int64_t(c) * ldx + r0 + rr, tile[rr][cc], ps);
   }
 }
 
 // Y workspace (m x n canonical) -> Y (rows x cols, io dtype)
 __global__ void __launch_bounds__(kStreamThreads)
-k_ns_store(const void* Yws, int esize, int ldx, void* Y, int io_esize, int rows, int cols) {
+k_ns_store(const void* Yws, int esize, int ldx, int64_t ps, void* Y, int io_esize, int rows,
+           int cols) {
   __shared__ float tile[kTT][kTT + 1];
   const int r0 = blockIdx.y * kTT, c0 = blockIdx.x * kTT;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -696,7 +746,7 @@ k_ns_store(const void* Yws, int esize, int ldx, void* Y, int io_esize, int rows,
       if (r >= rows) break;
       for (int cc = lane; cc < kTT && c0 + cc < cols; cc += 32)
         store_ws(Y, io_esize, int64_t(r) * cols + c0 + cc,
-                 load_ws(Yws, esize, int64_t(r) * ldx + c0 + cc));
+                 load_ws(Yws, esize, int64_t(r) * ldx + c0 + cc, ps));
     }
     return;
   }
@@ -704,7 +754,7 @@ k_ns_store(const void* Yws, int esize, int ldx, void* Y, int io_esize, int rows,
     const int c = c0 + cc;
     if (c >= cols) break;
     for (int rr = lane; rr < kTT && r0 + rr < rows; rr += 32)
-      tile[rr][cc] = load_ws(Yws, esize, int64_t(c) * ldx + r0 + rr);
+      tile[rr][cc] = load_ws(Yws, esize, int64_t(c) * ldx + r0 + rr, ps);
   }
   __syncthreads();
   for (int rr = warp; rr < kTT; rr += 8) {
@@ -748,14 +798,15 @@ void launch_ns_sumsq(const void* X, int io_esize, int64_t numel, double* tile_su
   k_ns_norm<<<1, kFinThreads, 0, s>>>(tile_sum, ntiles);
 }
 void launch_ns_load(const void* X, int io_esize, int rows, int cols, const double* tile_sum,
-                    int ntiles, void* X0, int esize, int ldx, cudaStream_t s) {
+                    int ntiles, void* X0, int esize, int ldx, int64_t ps, cudaStream_t s) {
   dim3 g((cols + kTT - 1) / kTT, (rows + kTT - 1) / kTT);
-  k_ns_load<<<g, kStreamThreads, 0, s>>>(X, io_esize, rows, cols, tile_sum, ntiles, X0, esize, ldx);
+  k_ns_load<<<g, kStreamThreads, 0, s>>>(X, io_esize, rows, cols, tile_sum, ntiles, X0, esize, ldx,
+                                         ps);
 }
-void launch_ns_store(const void* Yws, int esize, int ldx, void* Y, int io_esize, int rows,
-                     int cols, cudaStream_t s) {
+void launch_ns_store(const void* Yws, int esize, int ldx, int64_t ps, void* Y, int io_esize,
+                     int rows, int cols, cudaStream_t s) {
   dim3 g((cols + kTT - 1) / kTT, (rows + kTT - 1) / kTT);
-  k_ns_store<<<g, kStreamThreads, 0, s>>>(Yws, esize, ldx, Y, io_esize, rows, cols);
+  k_ns_store<<<g, kStreamThreads, 0, s>>>(Yws, esize, ldx, ps, Y, io_esize, rows, cols);
 }
 
 }  // namespace muon

@@ -212,23 +212,33 @@ def test_newton_schulz_entry(torch, shape, method, mode):
     assert_close_update(Y.float().cpu().numpy(), want, mode, f"{shape} {method} {mode}")
 
 
-def test_tensor_core_path_matches_cuda_core_path(torch):
-    """The tcgen05 products against the CUDA-core products (both BF16
-    operands, FP32 accumulation) on one matrix: both within bf16 noise."""
-    G = wl.to_bf16_values(wl.rng_for(52).standard_normal((640, 1100)).astype(np.float32))
-    X = to_dev(G, torch, torch.bfloat16)
+@pytest.mark.parametrize("method", ["standard", "gram"])
+@pytest.mark.parametrize("mode", ["bf16", "fp32"])
+def test_tensor_core_path_matches_cuda_core_path(torch, method, mode):
+    """The tensor-core products (BF16 operands, or FP32 through split-3
+    planes) against the CUDA-core products on one matrix, both by the
+    mode's rule, and both against the oracle."""
+    G = wl.rng_for(52).standard_normal((640, 1100)).astype(np.float32)
+    if mode == "bf16":
+        G = wl.to_bf16_values(G)
+        X = to_dev(G, torch, torch.bfloat16)
+    else:
+        X = to_dev(G, torch)
     outs = []
     for path in (None, "simt"):
         nsg.release_workspace()
         if path:
             os.environ["MUON_GEMM"] = path
         try:
-            outs.append(nsg.newton_schulz(X, ns_method="standard", operand_mode="bf16")
+            outs.append(nsg.newton_schulz(X, ns_method=method, operand_mode=mode)
                         .float().cpu().numpy())
         finally:
             os.environ.pop("MUON_GEMM", None)
             nsg.release_workspace()
-    assert relf(outs[0], outs[1]) < 1e-2
+    assert_close_update(outs[0], outs[1], mode, f"tensor vs cuda cores {method} {mode}")
+    want = ons.newton_schulz(G, method, 5, ORACLE_MODE[mode])
+    for o in outs:
+        assert_close_update(o, want, mode, f"{method} {mode} vs oracle")
 
 
 def test_gpt2_small_config(torch):
