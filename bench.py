@@ -29,6 +29,25 @@ import workloads as wl  # noqa: E402
 METRIC = "Muon step time & NS TFLOP/s (% of GB300 bf16 dense peak) plus HBM GB/s, 1 GPU"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# DRAM bytes per launch of the bf16 tensor-core GEMM in this workload, from
+# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum averaged over
+# the 15 launches of one step; command in profiles/gpt2_step_launches.md),
+# valid only for the kernel sources it was taken on (hash below).
+GEMM_TRAFFIC = {"bytes_per_launch": 205.12e6, "sources_sha256_16": "0cfc9f09745dbc35",
+                "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc.cu",
+                          "newton_schulz_fp32_gb300/csrc/tc_common.cuh"]}
+
+
+def gemm_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_TRAFFIC["files"]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != GEMM_TRAFFIC["sources_sha256_16"]:
+        return None   # the kernel changed since the counters were taken
+    return GEMM_TRAFFIC["bytes_per_launch"]
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -489,7 +508,10 @@ def main():
         "phases_ms_per_step": {k: phases[k]["ms"] / args.steps for k in phases},
         "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_source": peak_src, "unit": unit,
-                     "frac": (achieved / peak) if peak else None, "traffic": None},
+                     "frac": (achieved / peak) if peak else None,
+                     "traffic": gemm_traffic() if dom == "ns_gemm" and args.mode == "bf16"
+                     and args.ns_method == "standard" else None,
+                     "traffic_unit": "bytes per launch (DRAM read + write, ncu)"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 16},
         "gpu_launches": launches,
