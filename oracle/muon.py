@@ -67,51 +67,124 @@ def muon_update(g, m, beta, method="gram", steps=ns.DEFAULT_STEPS, num_heads=0,
     return m_new, np.vstack(blocks)
 
 
+def scale_grad(g, grad_scale):
+    """g * grad_scale in float32 (a loss scale is undone by passing its
+    reciprocal); grad_scale == 1 leaves the gradient as it is."""
+    g = np.asarray(g, np.float32)
+    return g if grad_scale == 1.0 else np.float32(grad_scale) * g
+
+
+def adam_update(g, exp_avg, exp_avg_sq, w, lr, beta1, beta2, eps, step):
+    """Textbook Adam (Kingma & Ba, 2015) for the auxiliary groups, in float32
+    and in this operation order: exp_avg = b1*m + (1-b1)*g;
+    exp_avg_sq = b2*v + ((1-b2)*g)*g; denom = sqrt(v)/sqrt(1-b2^t) + eps;
+    w = w + (-(lr/(1-b1^t))) * (exp_avg/denom).  The pages keep the
+    auxiliary groups on their own Adam path ("Support Muon in BF16_Optimizer
+    with FP32 gradient accumulation", PR description); fusing it is this
+    library's option."""
+    f = np.float32
+    g = np.asarray(g, f)
+    m = f(beta1) * np.asarray(exp_avg, f) + f(1.0 - beta1) * g
+    v = f(beta2) * np.asarray(exp_avg_sq, f) + (f(1.0 - beta2) * g) * g
+    bc1 = 1.0 - beta1 ** step
+    bc2 = 1.0 - beta2 ** step
+    denom = np.sqrt(v) / f(np.sqrt(bc2)) + f(eps)
+    w_new = np.asarray(w, f) + f(-(lr / bc1)) * (m / denom)
+    return m, v, w_new
+
+
 def muon_step_full(mats, beta, lr, method="gram", steps=ns.DEFAULT_STEPS, clip=0.0,
-                   mode="exact"):
+                   mode="exact", clip_mode="update", grad_scale=1.0, adam=None):
     """One optimizer step on full matrices (no partition tables).
 
     mats: list of dicts with keys g (accumulated gradient), m (momentum),
-    w (master), use_muon, num_heads.  Returns a dict with per-parameter
-    lists 'update', 'momentum', 'master' and scalars 'norm', 'coef',
-    'applied', 'ns_calls'."""
+    w (master), use_muon, num_heads, and for auxiliary parameters when
+    `adam` is given exp_avg / exp_avg_sq.  Returns a dict with per-parameter
+    lists 'update', 'momentum', 'master' (and 'exp_avg', 'exp_avg_sq') and
+    scalars 'norm', 'coef', 'applied', 'ns_calls'.
+
+    clip_mode "update" (default): the global norm is taken over the Muon
+    updates and the auxiliary gradients, then every update is scaled ("Run
+    Muon once per optimizer step under ZeRO-3 ...", "The change").
+    clip_mode "grad": the global norm is taken over the gradients and the
+    gradients are clipped before Muon runs ("Support Muon in BF16_Optimizer
+    with FP32 gradient accumulation", PR description: Muon updates are
+    computed after gradient reduction and global clipping).
+    grad_scale multiplies the accumulated gradient first, so a loss scale is
+    undone before any norm is taken ("Fix Muon optimizer under ZeRO CPU
+    offload and bound gather buffers", loss-scaling commit: the clipping
+    norm must not see the loss scale).
+    adam: dict(lr, beta1, beta2, eps, step) applies adam_update to the
+    auxiliary parameters with their clipped gradient."""
     calls0 = ns.NS_CALLS[0]
-    if any(not np.all(np.isfinite(np.asarray(d["g"], np.float32))) for d in mats):
-        return {"applied": 0, "norm": 0.0, "coef": 0.0, "ns_calls": 0,
-                "update": [np.asarray(d["g"], np.float32) for d in mats],
-                "momentum": [np.asarray(d["m"], np.float32) for d in mats],
-                "master": [np.asarray(d["w"], np.float32) for d in mats]}
+    gs = [scale_grad(d["g"], grad_scale) for d in mats]
+    if any(not np.all(np.isfinite(g)) for g in gs):
+        out = {"applied": 0, "norm": 0.0, "coef": 0.0, "ns_calls": 0,
+               "update": [np.asarray(d["g"], np.float32) for d in mats],
+               "momentum": [np.asarray(d["m"], np.float32) for d in mats],
+               "master": [np.asarray(d["w"], np.float32) for d in mats]}
+        if adam is not None:
+            out["exp_avg"] = [d.get("exp_avg") for d in mats]
+            out["exp_avg_sq"] = [d.get("exp_avg_sq") for d in mats]
+        return out
+
+    def coef_of(sq):
+        norm = float(np.sqrt(sq))
+        return norm, (min(1.0, clip / (norm + CLIP_EPS)) if clip > 0 else 1.0)
+
+    def sumsq(arrs):
+        sq = 0.0
+        for x in arrs:
+            x64 = np.asarray(x, np.float64)
+            sq += float(np.sum(x64 * x64))
+        return sq
+
+    pre = clip_mode == "grad"
+    if clip_mode not in ("update", "grad"):
+        raise ValueError(clip_mode)
+    if pre:
+        norm, coef = coef_of(sumsq(gs))
+        gin = [g if coef == 1.0 else np.float32(coef) * g for g in gs]
+    else:
+        gin = gs
     us, moms = [], []
-    for d in mats:
+    for d, g in zip(mats, gin):
         if d["use_muon"]:
-            m_new, u = muon_update(d["g"], d["m"], beta, method, steps,
-                                   d.get("num_heads", 0), mode)
+            m_new, u = muon_update(g, d["m"], beta, method, steps, d.get("num_heads", 0), mode)
         else:
-            m_new, u = np.asarray(d["m"], np.float32), np.asarray(d["g"], np.float32)
+            m_new, u = np.asarray(d["m"], np.float32), g
         moms.append(m_new)
         us.append(u)
-    sq = 0.0
-    for u in us:
-        u64 = np.asarray(u, np.float64)
-        sq += float(np.sum(u64 * u64))
-    norm = float(np.sqrt(sq))
-    coef = min(1.0, clip / (norm + CLIP_EPS)) if clip > 0 else 1.0
+    if not pre:
+        norm, coef = coef_of(sumsq(us))
+    post = 1.0 if pre else coef
 
-    updates, masters = [], []
+    updates, masters, ea, eas = [], [], [], []
     for d, u in zip(mats, us):
         w = np.asarray(d["w"], np.float32)
-        if mode == "exact":
-            v64 = coef * np.asarray(u, np.float64)
+        if mode == "exact" and d["use_muon"]:
+            v64 = post * np.asarray(u, np.float64)
             v = v64.astype(np.float32)
-            w_new = (w.astype(np.float64) - lr * v64).astype(np.float32) if d["use_muon"] else w
+            w_new = (w.astype(np.float64) - lr * v64).astype(np.float32)
         else:
-            v = np.float32(coef) * np.asarray(u, np.float32)
+            v = np.asarray(u, np.float32) if post == 1.0 else np.float32(post) * np.asarray(u, np.float32)
             w_new = w - np.float32(lr) * v if d["use_muon"] else w
+        if adam is not None and not d["use_muon"]:
+            m1, v2, w_new = adam_update(v, d["exp_avg"], d["exp_avg_sq"], w, **adam)
+            ea.append(m1)
+            eas.append(v2)
+        else:
+            ea.append(d.get("exp_avg"))
+            eas.append(d.get("exp_avg_sq"))
         updates.append(v)
         masters.append(w_new)
-    return {"applied": 1, "norm": norm, "coef": coef,
-            "ns_calls": ns.NS_CALLS[0] - calls0,
-            "update": updates, "momentum": moms, "master": masters}
+    out = {"applied": 1, "norm": norm, "coef": coef,
+           "ns_calls": ns.NS_CALLS[0] - calls0,
+           "update": updates, "momentum": moms, "master": masters}
+    if adam is not None:
+        out["exp_avg"] = ea
+        out["exp_avg_sq"] = eas
+    return out
 
 
 # ------------------------------------------------ flat, partitioned buffers
@@ -149,27 +222,39 @@ def scatter_matrix(buf, params, parts, k, mat):
 
 
 def muon_step_flat(accum, momentum, master, params, parts, beta, lr, method="gram",
-                   steps=ns.DEFAULT_STEPS, clip=0.0, mode="exact"):
+                   steps=ns.DEFAULT_STEPS, clip=0.0, mode="exact", clip_mode="update",
+                   grad_scale=1.0, adam=None, exp_avg=None, exp_avg_sq=None):
     """The step on flat, rank-partitioned storage buffers.
 
     Reconstructs each parameter from its partitions, runs
     :func:`muon_step_full`, then writes every partition's owned intersection
     of the results back.  Elements no parameter covers (alignment padding,
     gaps between partitions) are never read or written.  Returns new copies
-    of (accum, momentum, master) and the result dict."""
+    of (accum, momentum, master) and the result dict; with `adam`, the
+    updated exp_avg / exp_avg_sq storage buffers are in the result dict."""
     mats = []
     for k in range(len(params)):
-        mats.append({"g": gather_matrix(accum, params, parts, k),
-                     "m": gather_matrix(momentum, params, parts, k),
-                     "w": gather_matrix(master, params, parts, k),
-                     "use_muon": bool(params["use_muon"][k]),
-                     "num_heads": int(params["num_heads"][k])})
-    res = muon_step_full(mats, beta, lr, method, steps, clip, mode)
+        d = {"g": gather_matrix(accum, params, parts, k),
+             "m": gather_matrix(momentum, params, parts, k),
+             "w": gather_matrix(master, params, parts, k),
+             "use_muon": bool(params["use_muon"][k]),
+             "num_heads": int(params["num_heads"][k])}
+        if adam is not None and not d["use_muon"]:
+            d["exp_avg"] = gather_matrix(exp_avg, params, parts, k)
+            d["exp_avg_sq"] = gather_matrix(exp_avg_sq, params, parts, k)
+        mats.append(d)
+    res = muon_step_full(mats, beta, lr, method, steps, clip, mode, clip_mode, grad_scale, adam)
     acc2, mom2, mst2 = accum.copy(), momentum.copy(), master.copy()
+    if adam is not None:
+        res["exp_avg_buf"], res["exp_avg_sq_buf"] = exp_avg.copy(), exp_avg_sq.copy()
     if res["applied"]:
         for k in range(len(params)):
             scatter_matrix(acc2, params, parts, k, res["update"][k])
             if mats[k]["use_muon"]:
                 scatter_matrix(mom2, params, parts, k, res["momentum"][k])
                 scatter_matrix(mst2, params, parts, k, res["master"][k])
+            elif adam is not None:
+                scatter_matrix(mst2, params, parts, k, res["master"][k])
+                scatter_matrix(res["exp_avg_buf"], params, parts, k, res["exp_avg"][k])
+                scatter_matrix(res["exp_avg_sq_buf"], params, parts, k, res["exp_avg_sq"][k])
     return acc2, mom2, mst2, res
