@@ -156,6 +156,55 @@ MUON_API int muon_step(float* accum, float* momentum, float* master,
               int ns_method, int ns_steps, float clip, int operand_mode,
               muon_result_t* d_result, void* stream);
 
+/* Options of muon_step_ex.  Zero-initialise, set struct_size, then set
+ * what differs from the defaults (the defaults reproduce muon_step).
+ *   clip_mode  MUON_CLIP_UPDATE (default): the global norm is taken over the
+ *              Muon updates and the auxiliary gradients and scales every
+ *              update ([ONCE], "The change").  MUON_CLIP_GRAD: the norm is
+ *              taken over all gradients and the gradients are clipped
+ *              before the momentum and Newton-Schulz ([BF16], PR
+ *              description: Muon runs after reduction and global clipping);
+ *              result.global_norm is then the gradient norm.
+ *   grad_scale multiplies accum before anything else (0 means 1): pass
+ *              1/S to undo a loss scale S, so neither the overflow check
+ *              nor the clip norm sees it ([OFFL], loss-scaling commit).
+ *   aux_adam   1: auxiliary parameters also get an Adam step on their
+ *              clipped gradient, in place on master, exp_avg and exp_avg_sq
+ *              (device float buffers with accum's layout; only auxiliary
+ *              elements are touched): m = b1 m + (1-b1) g,
+ *              v = b2 v + (1-b2) g g, w += -(lr/(1-b1^t)) m /
+ *              (sqrt(v)/sqrt(1-b2^t) + eps) (Kingma & Ba); t = adam_step
+ *              >= 1.  ([BF16], PR description: auxiliary Adam groups keep
+ *              their own update path; fusing it is optional.)
+ *   workspace_budget  bytes; 0 = unbounded.  Otherwise the Newton-Schulz
+ *              blocks run in waves whose workspace fits the budget (a
+ *              block larger than the budget runs alone), the unclipped
+ *              update is parked in accum, and a final pass applies the clip
+ *              coefficient.  Results are identical to the unbounded step. */
+typedef enum { MUON_CLIP_UPDATE = 0, MUON_CLIP_GRAD = 1 } muon_clip_mode_t;
+
+typedef struct muon_step_options {
+  int32_t struct_size;   /* sizeof(muon_step_options_t) */
+  int32_t clip_mode;     /* muon_clip_mode_t */
+  float grad_scale;      /* 0 or 1 = no scaling */
+  int32_t aux_adam;      /* 0 / 1 */
+  float adam_lr, adam_beta1, adam_beta2, adam_eps;
+  int64_t adam_step;     /* >= 1 when aux_adam */
+  float* exp_avg;        /* device, when aux_adam */
+  float* exp_avg_sq;     /* device, when aux_adam */
+  uint64_t workspace_budget;
+} muon_step_options_t;
+
+/* muon_step with options (NULL = defaults).  Errors as muon_step, plus
+ * MUON_ERR_INVALID for a bad struct_size, a non-finite or negative
+ * grad_scale, aux_adam without state buffers or with adam_step < 1. */
+MUON_API int muon_step_ex(float* accum, float* momentum, float* master,
+                          const muon_param_t* params, int nparams,
+                          const muon_partition_t* parts, int nparts, float beta,
+                          float lr, int ns_method, int ns_steps, float clip,
+                          int operand_mode, const muon_step_options_t* opts,
+                          muon_result_t* d_result, void* stream);
+
 /* Newton-Schulz orthogonalisation of one rows x cols row-major matrix:
  * normalise by the Frobenius norm (+1e-7), transpose if rows > cols,
  * ns_steps quintic steps by ns_method, transpose back.

@@ -34,7 +34,9 @@ PHASES = ["accumulate", "reduce", "gather", "ns_gemm", "norm", "scatter"]
 # Every symbol include/muon.h declares.
 EXPORTED = ["muon_accumulate", "muon_step", "muon_newton_schulz", "muon_get_stats",
             "muon_last_error", "muon_release_workspace", "muon_device_error",
-            "muon_profile_enable", "muon_profile_read", "muon_newton_schulz_noalloc"]
+            "muon_profile_enable", "muon_profile_read", "muon_newton_schulz_noalloc",
+            "muon_step_ex"]
+CLIP_MODES = {"update": 0, "grad": 1}
 
 
 class MuonError(RuntimeError):
@@ -47,6 +49,16 @@ class Stats(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_int64), ("ns_calls_last_step", ctypes.c_int64),
                 ("muon_matrices", ctypes.c_int64), ("kernel_launches_last_call", ctypes.c_int64),
                 ("kernel_launches_total", ctypes.c_int64), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class StepOptions(ctypes.Structure):
+    """muon_step_options_t."""
+    _fields_ = [("struct_size", ctypes.c_int32), ("clip_mode", ctypes.c_int32),
+                ("grad_scale", ctypes.c_float), ("aux_adam", ctypes.c_int32),
+                ("adam_lr", ctypes.c_float), ("adam_beta1", ctypes.c_float),
+                ("adam_beta2", ctypes.c_float), ("adam_eps", ctypes.c_float),
+                ("adam_step", ctypes.c_int64), ("exp_avg", ctypes.c_void_p),
+                ("exp_avg_sq", ctypes.c_void_p), ("workspace_budget", ctypes.c_uint64)]
 
 
 class PhaseTime(ctypes.Structure):
@@ -73,6 +85,8 @@ def lib():
         P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
         L.muon_accumulate.argtypes = [P, P, I64, F, I, P, I, P, I, P]
         L.muon_step.argtypes = [P, P, P, P, I, P, I, F, F, I, I, F, I, P, P]
+        L.muon_step_ex.argtypes = [P, P, P, P, I, P, I, F, F, I, I, F, I,
+                                   ctypes.POINTER(StepOptions), P, P]
         L.muon_newton_schulz.argtypes = [P, P, I, I, I, I, I, I, P]
         L.muon_newton_schulz_noalloc.argtypes = [P, P, I, I, I, I, I, I, P]
         L.muon_get_stats.argtypes = [ctypes.POINTER(Stats)]
@@ -80,7 +94,7 @@ def lib():
         L.muon_release_workspace.restype = None
         L.muon_profile_enable.argtypes = [I]
         L.muon_profile_read.argtypes = [ctypes.POINTER(PhaseTime), I, I]
-        for name in ("muon_accumulate", "muon_step", "muon_newton_schulz",
+        for name in ("muon_accumulate", "muon_step", "muon_step_ex", "muon_newton_schulz",
                      "muon_newton_schulz_noalloc", "muon_get_stats",
                      "muon_device_error", "muon_profile_enable", "muon_profile_read"):
             getattr(L, name).restype = I
@@ -132,11 +146,31 @@ def accumulate(accum, grad, scale: float, overwrite: bool = False, params=None, 
                                  q.ctypes.data if q is not None else None, nq, _stream(stream)))
 
 
+def step_options(clip_mode="update", grad_scale: float = 1.0, adam: dict | None = None,
+                 workspace_budget: int = 0) -> StepOptions:
+    """A muon_step_options_t.  adam: dict(lr, beta1, beta2, eps, step,
+    exp_avg, exp_avg_sq) with device float buffers in accum's layout."""
+    o = StepOptions()
+    o.struct_size = ctypes.sizeof(StepOptions)
+    o.clip_mode = CLIP_MODES[clip_mode] if isinstance(clip_mode, str) else int(clip_mode)
+    o.grad_scale = grad_scale
+    o.workspace_budget = int(workspace_budget)
+    if adam is not None:
+        o.aux_adam = 1
+        o.adam_lr, o.adam_beta1 = adam["lr"], adam["beta1"]
+        o.adam_beta2, o.adam_eps = adam["beta2"], adam["eps"]
+        o.adam_step = int(adam["step"])
+        o.exp_avg, o.exp_avg_sq = _ptr(adam["exp_avg"]), _ptr(adam["exp_avg_sq"])
+    return o
+
+
 def step(accum, momentum, master, params, parts, beta: float, lr: float, ns_method="gram",
-         ns_steps: int = 5, clip: float = 0.0, operand_mode="bf16", result=None, stream=None):
+         ns_steps: int = 5, clip: float = 0.0, operand_mode="bf16", result=None, stream=None,
+         options: StepOptions | None = None):
     """One Muon step (overflow check, momentum, Newton-Schulz, global norm
-    and clip, owned-slice write-back).  Returns the device result buffer
-    (torch int32[4]; decode with :func:`read_result`)."""
+    and clip, owned-slice write-back): muon_step, or muon_step_ex when
+    `options` (see :func:`step_options`) is given.  Returns the device
+    result buffer (torch int32[4]; decode with :func:`read_result`)."""
     import torch
     if result is None:
         result = torch.zeros(4, dtype=torch.int32, device=accum.device)
@@ -144,11 +178,23 @@ def step(accum, momentum, master, params, parts, beta: float, lr: float, ns_meth
     q, nq = _table(parts, PART_DTYPE)
     method = NS_METHODS[ns_method] if isinstance(ns_method, str) else int(ns_method)
     mode = OPERAND_MODES[operand_mode] if isinstance(operand_mode, str) else int(operand_mode)
-    _check(lib().muon_step(_ptr(accum), _ptr(momentum), _ptr(master),
-                           p.ctypes.data if np_ else None, np_,
-                           q.ctypes.data if nq else None, nq, beta, lr, method, ns_steps, clip,
-                           mode, _ptr(result), _stream(stream)))
+    args = (_ptr(accum), _ptr(momentum), _ptr(master), p.ctypes.data if np_ else None, np_,
+            q.ctypes.data if nq else None, nq, beta, lr, method, ns_steps, clip, mode)
+    if options is None:
+        _check(lib().muon_step(*args, _ptr(result), _stream(stream)))
+    else:
+        _check(lib().muon_step_ex(*args, ctypes.byref(options), _ptr(result), _stream(stream)))
     return result
+
+
+def step_ex(accum, momentum, master, params, parts, beta: float, lr: float, ns_method="gram",
+            ns_steps: int = 5, clip: float = 0.0, operand_mode="bf16", clip_mode="update",
+            grad_scale: float = 1.0, adam: dict | None = None, workspace_budget: int = 0,
+            result=None, stream=None):
+    """muon_step_ex with its options as keyword arguments."""
+    return step(accum, momentum, master, params, parts, beta, lr, ns_method, ns_steps, clip,
+                operand_mode, result, stream,
+                step_options(clip_mode, grad_scale, adam, workspace_budget))
 
 
 def read_result(result) -> dict:

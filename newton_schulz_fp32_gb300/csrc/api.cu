@@ -8,6 +8,7 @@
 // accumulation", review thread on the all_to_all_single split tables).
 #include <algorithm>
 #include <cmath>
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <map>
@@ -792,11 +793,63 @@ extern "C" int muon_accumulate(float* accum, const uint16_t* grad, int64_t n, fl
   return MUON_OK;
 }
 
-extern "C" int muon_step(float* accum, float* momentum, float* master, const muon_param_t* params,
-                         int nparams, const muon_partition_t* parts, int nparts, float beta,
-                         float lr, int ns_method, int ns_steps, float clip, int operand_mode,
-                         muon_result_t* d_result, void* stream) {
-  std::lock_guard<std::mutex> lk(g_mu);
+namespace {
+
+bool misaligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 != 0; }
+
+// Validates the options and fills the option fields of the launch
+// arguments; NULL options give muon_step's behaviour.
+int apply_options(const muon_step_options_t* opts, StreamLaunchArgs& a) {
+  a.grad_scale = 1.f;
+  a.clip_mode = MUON_CLIP_UPDATE;
+  a.reduce_mode = 0;
+  a.adam = 0;
+  a.park = 0;
+  if (!opts) return MUON_OK;
+  if (opts->struct_size != static_cast<int32_t>(sizeof(muon_step_options_t)))
+    return fail(MUON_ERR_INVALID, "opts->struct_size must be sizeof(muon_step_options_t)");
+  if (opts->clip_mode != MUON_CLIP_UPDATE && opts->clip_mode != MUON_CLIP_GRAD)
+    return fail(MUON_ERR_INVALID, "unknown clip_mode");
+  if (!std::isfinite(opts->grad_scale) || opts->grad_scale < 0.f)
+    return fail(MUON_ERR_INVALID, "grad_scale must be finite and >= 0");
+  if (opts->workspace_budget != 0)
+    return fail(MUON_ERR_UNSUPPORTED, "workspace_budget is not supported yet");
+  a.clip_mode = opts->clip_mode;
+  a.grad_scale = opts->grad_scale == 0.f ? 1.f : opts->grad_scale;
+  if (opts->aux_adam != 0 && opts->aux_adam != 1) return fail(MUON_ERR_INVALID, "aux_adam must be 0 or 1");
+  if (opts->aux_adam) {
+    if (!opts->exp_avg || !opts->exp_avg_sq)
+      return fail(MUON_ERR_INVALID, "aux_adam needs exp_avg and exp_avg_sq");
+    if (misaligned16(opts->exp_avg) || misaligned16(opts->exp_avg_sq))
+      return fail(MUON_ERR_INVALID, "exp_avg and exp_avg_sq must be 16-byte aligned");
+    if (opts->adam_step < 1) return fail(MUON_ERR_INVALID, "adam_step must be >= 1");
+    const float b1 = opts->adam_beta1, b2 = opts->adam_beta2;
+    if (!std::isfinite(opts->adam_lr) || !std::isfinite(opts->adam_eps) || opts->adam_eps < 0.f ||
+        !(b1 >= 0.f && b1 < 1.f) || !(b2 >= 0.f && b2 < 1.f))
+      return fail(MUON_ERR_INVALID, "adam_lr, adam_eps >= 0 finite and betas in [0, 1) required");
+    // Kingma & Ba: bias corrections 1 - beta^t, formed in double and rounded
+    // once to the FP32 constants the kernel multiplies by
+    const double t = static_cast<double>(opts->adam_step);
+    const double bc1 = 1.0 - std::pow(static_cast<double>(b1), t);
+    const double bc2 = 1.0 - std::pow(static_cast<double>(b2), t);
+    a.adam = 1;
+    a.adam_b1 = b1;
+    a.adam_b2 = b2;
+    a.adam_omb1 = static_cast<float>(1.0 - static_cast<double>(b1));
+    a.adam_omb2 = static_cast<float>(1.0 - static_cast<double>(b2));
+    a.adam_eps = opts->adam_eps;
+    a.adam_sqrt_bc2 = static_cast<float>(std::sqrt(bc2));
+    a.adam_neg_step = static_cast<float>(-(static_cast<double>(opts->adam_lr) / bc1));
+    a.exp_avg = opts->exp_avg;
+    a.exp_avg_sq = opts->exp_avg_sq;
+  }
+  return MUON_OK;
+}
+
+int step_impl(float* accum, float* momentum, float* master, const muon_param_t* params,
+              int nparams, const muon_partition_t* parts, int nparts, float beta, float lr,
+              int ns_method, int ns_steps, float clip, int operand_mode,
+              const muon_step_options_t* opts, muon_result_t* d_result, void* stream) {
   g_err.clear();
   g_cnt.launches_last = 0;
   int rc = check_method(ns_method, ns_steps, operand_mode);
@@ -804,8 +857,13 @@ extern "C" int muon_step(float* accum, float* momentum, float* master, const muo
   if (!d_result) return fail(MUON_ERR_INVALID, "d_result is NULL");
   if (nparams > 0 && (!accum || !momentum || !master))
     return fail(MUON_ERR_INVALID, "accum, momentum or master is NULL");
+  if (misaligned16(accum) || misaligned16(momentum) || misaligned16(master))
+    return fail(MUON_ERR_INVALID, "accum, momentum and master must be 16-byte aligned");
   if (!std::isfinite(beta) || !std::isfinite(lr) || !std::isfinite(clip))
     return fail(MUON_ERR_INVALID, "beta, lr and clip must be finite");
+  StreamLaunchArgs a{};
+  rc = apply_options(opts, a);
+  if (rc != MUON_OK) return rc;
   TablePlan* tp = nullptr;
   rc = get_table_plan(params, nparams, parts, nparts, &tp);
   if (rc != MUON_OK) return rc;
@@ -815,7 +873,6 @@ extern "C" int muon_step(float* accum, float* momentum, float* master, const muo
   const Layout& L = tp->L;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  StreamLaunchArgs a{};
   a.owners = tp->d_owners.as<Owner>();
   a.segs = tp->d_segs.as<Segment>();
   a.rtiles = tp->d_rtiles.as<RTile>();
@@ -840,11 +897,23 @@ extern "C" int muon_step(float* accum, float* momentum, float* master, const muo
   a.err_flag = tp->d_err.as<int>();
   a.result = d_result;
   a.ns_calls = L.n_muon_owners;
+  const bool pre = a.clip_mode == MUON_CLIP_GRAD;
 
   const double me = double(L.muon_elems), ae = double(L.aux_elems);
   MUON_CUDA_TRY(cudaMemsetAsync(a.state, 0, sizeof(StepState), s));
-  {
+  if (!pre) {
     PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 1 : 0) + 1, me * 8 + ae * 4, 0.0);
+    a.reduce_mode = 0;
+    launch_reduce(a, s);
+    launch_owner_norm(a, s);
+  } else {
+    // gradient norm over every parameter, clip coefficient, then the
+    // per-block momentum norms of the clipped gradients
+    PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 2 : 0) + 2, me * 12 + ae * 4, 0.0);
+    a.reduce_mode = 1;
+    launch_reduce(a, s);
+    launch_finalize_pre(a, s);
+    a.reduce_mode = 2;
     launch_reduce(a, s);
     launch_owner_norm(a, s);
   }
@@ -857,14 +926,15 @@ extern "C" int muon_step(float* accum, float* momentum, float* master, const muo
   rc = enqueue_gemms(*P, a.state, tp->d_err.as<int>(), s);
   if (rc != MUON_OK) return rc;
   {
-    PhaseScope sc(MUON_PHASE_NORM, s, (a.n_ytiles ? 1 : 0) + 1, me * P->esize, 0.0);
-    launch_update_sumsq(a, s);
+    PhaseScope sc(MUON_PHASE_NORM, s, (a.n_ytiles && !pre ? 1 : 0) + 1, pre ? 0.0 : me * P->esize, 0.0);
+    if (!pre) launch_update_sumsq(a, s);
     launch_finalize(a, s);
   }
   {
     a.etiles = tp->d_stiles.as<ETile>();
     a.n_etiles = static_cast<int>(L.stiles.size());
-    PhaseScope sc(MUON_PHASE_SCATTER, s, a.n_etiles ? 1 : 0, me * (12 + P->esize) + ae * 8, 0.0);
+    PhaseScope sc(MUON_PHASE_SCATTER, s, a.n_etiles ? 1 : 0,
+                  me * (12 + P->esize) + ae * (a.adam ? 32 : 8), 0.0);
     launch_scatter(a, s);
   }
   MUON_CUDA_TRY(cudaGetLastError());
@@ -872,6 +942,28 @@ extern "C" int muon_step(float* accum, float* momentum, float* master, const muo
   g_cnt.ns_calls_last = L.n_muon_owners;
   g_cnt.muon_mats_last = L.n_muon_params;
   return MUON_OK;
+}
+
+}  // namespace
+
+extern "C" int muon_step(float* accum, float* momentum, float* master, const muon_param_t* params,
+                         int nparams, const muon_partition_t* parts, int nparts, float beta,
+                         float lr, int ns_method, int ns_steps, float clip, int operand_mode,
+                         muon_result_t* d_result, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return step_impl(accum, momentum, master, params, nparams, parts, nparts, beta, lr, ns_method,
+                   ns_steps, clip, operand_mode, nullptr, d_result, stream);
+}
+
+extern "C" int muon_step_ex(float* accum, float* momentum, float* master,
+                            const muon_param_t* params, int nparams,
+                            const muon_partition_t* parts, int nparts, float beta, float lr,
+                            int ns_method, int ns_steps, float clip, int operand_mode,
+                            const muon_step_options_t* opts, muon_result_t* d_result,
+                            void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return step_impl(accum, momentum, master, params, nparams, parts, nparts, beta, lr, ns_method,
+                   ns_steps, clip, operand_mode, opts, d_result, stream);
 }
 
 extern "C" int muon_newton_schulz(const void* X, void* Y, int rows, int cols, int io_dtype,

@@ -168,6 +168,15 @@ struct StreamLaunchArgs {
   const int* err_flag;   // set by a tensor-core kernel whose wait ran out
   muon_result_t* result;
   int ns_calls;
+  // step options (muon_step_ex)
+  float grad_scale;      // g = accum * grad_scale
+  int clip_mode;         // 0: clip the updates; 1: clip the gradients first
+  int reduce_mode;       // k_reduce: 0 update-mode sums, 1 gradient norm, 2 momentum after pre-clip
+  int adam;              // auxiliary Adam on/off
+  float adam_b1, adam_omb1, adam_b2, adam_omb2, adam_eps, adam_sqrt_bc2, adam_neg_step;
+  float* exp_avg;
+  float* exp_avg_sq;
+  int park;              // bounded workspace: scatter writes the unclipped update to accum only
 };
 
 void launch_accumulate(float* accum, const uint16_t* grad, const Run* runs, int nruns,
@@ -177,6 +186,7 @@ void launch_owner_norm(const StreamLaunchArgs& a, cudaStream_t s);
 void launch_gather(const StreamLaunchArgs& a, cudaStream_t s);
 void launch_update_sumsq(const StreamLaunchArgs& a, cudaStream_t s);
 void launch_finalize(const StreamLaunchArgs& a, cudaStream_t s);
+void launch_finalize_pre(const StreamLaunchArgs& a, cudaStream_t s);
 void launch_scatter(const StreamLaunchArgs& a, cudaStream_t s);
 
 // NS-only entry: one matrix, io dtype bf16 or fp32.

@@ -90,6 +90,50 @@ __device__ __forceinline__ float momentum_of(float beta, float m, float g) {
   return __fadd_rn(__fmul_rn(beta, m), g);
 }
 
+// The gradient the step uses: accum * grad_scale (a loss scale undone).
+__device__ __forceinline__ float grad_in(const StreamLaunchArgs& a, float g) {
+  return a.grad_scale == 1.f ? g : __fmul_rn(a.grad_scale, g);
+}
+
+// The gradient fed to the momentum: grad_in, times the clip coefficient
+// when gradients are clipped before Muon (cpre = 1 otherwise).
+__device__ __forceinline__ float grad_m(const StreamLaunchArgs& a, float cpre, float g) {
+  const float gs = grad_in(a, g);
+  return a.clip_mode == 1 ? __fmul_rn(cpre, gs) : gs;
+}
+
+// Adam on one auxiliary element (clipped gradient g), in the oracle's
+// operation order: m, v and w in, updated m, v and w out.
+__device__ __forceinline__ void adam_el(const StreamLaunchArgs& a, float g, float& m, float& v, float& w) {
+  m = __fadd_rn(__fmul_rn(a.adam_b1, m), __fmul_rn(a.adam_omb1, g));
+  v = __fadd_rn(__fmul_rn(a.adam_b2, v), __fmul_rn(__fmul_rn(a.adam_omb2, g), g));
+  const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), a.adam_sqrt_bc2), a.adam_eps);
+  w = __fadd_rn(w, __fmul_rn(a.adam_neg_step, __fdiv_rn(m, denom)));
+}
+
+__device__ __forceinline__ void adam_one(const StreamLaunchArgs& a, int64_t st, float g) {
+  float m = a.exp_avg[st], v = a.exp_avg_sq[st], w = a.master[st];
+  adam_el(a, g, m, v, w);
+  a.exp_avg[st] = m;
+  a.exp_avg_sq[st] = v;
+  a.master[st] = w;
+}
+
+// Adam on four consecutive auxiliary elements starting at a 16-byte aligned
+// storage index.
+__device__ __forceinline__ void adam_four(const StreamLaunchArgs& a, int64_t st, float4 g) {
+  float4 m = *reinterpret_cast<const float4*>(a.exp_avg + st);
+  float4 v = *reinterpret_cast<const float4*>(a.exp_avg_sq + st);
+  float4 w = *reinterpret_cast<const float4*>(a.master + st);
+  adam_el(a, g.x, m.x, v.x, w.x);
+  adam_el(a, g.y, m.y, v.y, w.y);
+  adam_el(a, g.z, m.z, v.z, w.z);
+  adam_el(a, g.w, m.w, v.w, w.w);
+  *reinterpret_cast<float4*>(a.exp_avg + st) = m;
+  *reinterpret_cast<float4*>(a.exp_avg_sq + st) = v;
+  *reinterpret_cast<float4*>(a.master + st) = w;
+}
+
 // ------------------------------------------------------------------ S1
 
 __device__ __forceinline__ float acc_one(float a, float g, float scale, int overwrite) {
@@ -150,19 +194,32 @@ k_accumulate(float* __restrict__ accum, const uint16_t* __restrict__ grad,
 // (elements in order within a group), whatever segments they fall in: the
 // sum order depends only on the owner-relative index.  Tiles inside one
 // aligned segment read float4s; others resolve each element's segment.
-__device__ __forceinline__ void reduce_one(float g, float m, bool muon, float beta, float& acc,
-                                           bool& bad) {
-  bad |= !isfinite(g);
-  const float v = muon ? momentum_of(beta, m, g) : g;
+// One element of pass 1: the sum of squares of what the mode needs and the
+// overflow check on the gradient the step uses.
+__device__ __forceinline__ void reduce_one(const StreamLaunchArgs& a, float graw, float m, bool use_m,
+                                           float c, float& acc, bool& bad) {
+  const float gs = grad_in(a, graw);
+  bad |= !isfinite(gs);
+  const float ge = c == 1.f ? gs : __fmul_rn(c, gs);
+  const float v = use_m ? momentum_of(a.beta, m, ge) : ge;
   acc = __fmaf_rn(v, v, acc);
 }
 
+// Thread t of the tile sums the 4-element groups t, t + NT, t + 2 NT, ...
+// (elements in order within a group), whatever segments they fall in: the
+// sum order depends only on the owner-relative index.  Tiles inside one
+// aligned segment read float4s; others resolve each element's segment.
+// reduce_mode 0: Muon tiles sum (beta m + g)^2, auxiliary tiles g^2;
+//             1: every tile sums g^2 (the gradient norm, clip-before-Muon);
+//             2: Muon tiles sum (beta m + coef g)^2 after the gradient clip.
 __global__ void __launch_bounds__(kStreamThreads)
 k_reduce(StreamLaunchArgs a) {
   constexpr int NT = kStreamThreads;
   const RTile t = a.rtiles[blockIdx.x];
   const Owner o = a.owners[t.owner];
-  const bool muon = o.is_muon != 0;
+  if (a.reduce_mode == 2 && (!o.is_muon || a.state->overflow)) return;
+  const bool use_m = a.reduce_mode == 1 ? false : (o.is_muon != 0);
+  const float c = a.reduce_mode == 2 ? a.state->coef : 1.f;
   const int64_t tb = t.rel_begin, te = t.rel_begin + t.len;
   const int ngroups = (t.len + 3) / 4;
   float acc = 0.f;
@@ -178,16 +235,16 @@ k_reduce(StreamLaunchArgs a) {
         const int g = g0 + u * NT;
         if (g < ngroups) {
           gv[u] = *reinterpret_cast<const float4*>(G + 4 * g);
-          mv[u] = muon ? *reinterpret_cast<const float4*>(M + 4 * g) : make_float4(0.f, 0.f, 0.f, 0.f);
+          mv[u] = use_m ? *reinterpret_cast<const float4*>(M + 4 * g) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
       #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (g0 + u * NT < ngroups) {
-          reduce_one(gv[u].x, mv[u].x, muon, a.beta, acc, bad);
-          reduce_one(gv[u].y, mv[u].y, muon, a.beta, acc, bad);
-          reduce_one(gv[u].z, mv[u].z, muon, a.beta, acc, bad);
-          reduce_one(gv[u].w, mv[u].w, muon, a.beta, acc, bad);
+          reduce_one(a, gv[u].x, mv[u].x, use_m, c, acc, bad);
+          reduce_one(a, gv[u].y, mv[u].y, use_m, c, acc, bad);
+          reduce_one(a, gv[u].z, mv[u].z, use_m, c, acc, bad);
+          reduce_one(a, gv[u].w, mv[u].w, use_m, c, acc, bad);
         }
       }
     }
@@ -201,11 +258,11 @@ k_reduce(StreamLaunchArgs a) {
         if (si < 0) si = find_seg(segs, o.seg_count, rel);
         while (rel >= segs[si].rel_begin + segs[si].len) ++si;
         const int64_t st = segs[si].storage_begin + (rel - segs[si].rel_begin);
-        reduce_one(a.accum[st], muon ? a.momentum[st] : 0.f, muon, a.beta, acc, bad);
+        reduce_one(a, a.accum[st], use_m ? a.momentum[st] : 0.f, use_m, c, acc, bad);
       }
     }
   }
-  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(&a.state->overflow, 1);
+  if (__syncthreads_or(bad) && threadIdx.x == 0 && a.reduce_mode != 2) atomicOr(&a.state->overflow, 1);
   const double s = block_sum<NT>(static_cast<double>(acc));
   if (threadIdx.x == 0) a.rtile_sum[blockIdx.x] = s;
 }
@@ -287,7 +344,7 @@ __device__ __forceinline__ float4 load4_ws(const void* base, int esize, int64_t 
 
 // rows of a non-transposed block: owner elements [e0, e1), X0 index = rel
 __device__ __forceinline__ void gather_fast_rows(const StreamLaunchArgs& a, const ETile& t,
-                                                 const Owner& o, float d, char* x0) {
+                                                 const Owner& o, float d, float cpre, char* x0) {
   constexpr int U = 4;
   const int64_t e0 = int64_t(t.r0) * o.cols, e1 = int64_t(t.r0 + t.nr) * o.cols;
   const float* __restrict__ G = a.accum + t.sdelta;
@@ -308,10 +365,10 @@ __device__ __forceinline__ void gather_fast_rows(const StreamLaunchArgs& a, cons
       const int64_t i = i0 + u * stride;
       if (i < e1) {
         float4 mv;
-        mv.x = momentum_of(a.beta, m[u].x, g[u].x);
-        mv.y = momentum_of(a.beta, m[u].y, g[u].y);
-        mv.z = momentum_of(a.beta, m[u].z, g[u].z);
-        mv.w = momentum_of(a.beta, m[u].w, g[u].w);
+        mv.x = momentum_of(a.beta, m[u].x, grad_m(a, cpre, g[u].x));
+        mv.y = momentum_of(a.beta, m[u].y, grad_m(a, cpre, g[u].y));
+        mv.z = momentum_of(a.beta, m[u].z, grad_m(a, cpre, g[u].z));
+        mv.w = momentum_of(a.beta, m[u].w, grad_m(a, cpre, g[u].w));
         *reinterpret_cast<float4*>(M + i) = mv;
         store4_ws(x0, a.esize, i,
                   make_float4(__fdiv_rn(mv.x, d), __fdiv_rn(mv.y, d), __fdiv_rn(mv.z, d),
@@ -324,7 +381,7 @@ __device__ __forceinline__ void gather_fast_rows(const StreamLaunchArgs& a, cons
 
 // 64 x 64 tile of a transposed block: read rows, write X0 = tile^T
 __device__ __forceinline__ void gather_fast_tr(const StreamLaunchArgs& a, const ETile& t,
-                                               const Owner& o, float d, char* x0,
+                                               const Owner& o, float d, float cpre, char* x0,
                                                float (*tile)[kTT + 1]) {
   const int r_end = min(t.r0 + kTT, o.rows);
   const int rq = threadIdx.x >> 4, cq = (threadIdx.x & 15) * 4;   // 16 rows x 16 float4 per pass
@@ -344,10 +401,10 @@ __device__ __forceinline__ void gather_fast_tr(const StreamLaunchArgs& a, const 
     if (r < r_end) {
       const int64_t i = t.sdelta + int64_t(r) * o.cols + t.c0 + cq;
       float4 mv;
-      mv.x = momentum_of(a.beta, m[k].x, g[k].x);
-      mv.y = momentum_of(a.beta, m[k].y, g[k].y);
-      mv.z = momentum_of(a.beta, m[k].z, g[k].z);
-      mv.w = momentum_of(a.beta, m[k].w, g[k].w);
+      mv.x = momentum_of(a.beta, m[k].x, grad_m(a, cpre, g[k].x));
+      mv.y = momentum_of(a.beta, m[k].y, grad_m(a, cpre, g[k].y));
+      mv.z = momentum_of(a.beta, m[k].z, grad_m(a, cpre, g[k].z));
+      mv.w = momentum_of(a.beta, m[k].w, grad_m(a, cpre, g[k].w));
       *reinterpret_cast<float4*>(a.momentum + i) = mv;
       float* tr = tile[rq + 16 * k];
       tr[cq] = __fdiv_rn(mv.x, d);
@@ -462,6 +519,8 @@ __device__ __forceinline__ void scatter_fast_tr(const StreamLaunchArgs& a, const
   }
 }
 
+// auxiliary elements [rel_begin, rel_begin + len): accum = coef * g, plus
+// Adam on the master when enabled
 __device__ __forceinline__ void scatter_fast_aux(const StreamLaunchArgs& a, const ETile& t, float coef) {
   constexpr int U = 4;
   float* __restrict__ A = a.accum + t.sdelta;
@@ -473,11 +532,15 @@ __device__ __forceinline__ void scatter_fast_aux(const StreamLaunchArgs& a, cons
     for (int u = 0; u < U; ++u)
       if (i0 + u * stride < e1) g[u] = *reinterpret_cast<const float4*>(A + i0 + u * stride);
     #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (i0 + u * stride < e1)
-        *reinterpret_cast<float4*>(A + i0 + u * stride) =
-            make_float4(__fmul_rn(coef, g[u].x), __fmul_rn(coef, g[u].y), __fmul_rn(coef, g[u].z),
-                        __fmul_rn(coef, g[u].w));
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < e1) {
+        const float4 v = make_float4(__fmul_rn(coef, grad_in(a, g[u].x)), __fmul_rn(coef, grad_in(a, g[u].y)),
+                                     __fmul_rn(coef, grad_in(a, g[u].z)), __fmul_rn(coef, grad_in(a, g[u].w)));
+        *reinterpret_cast<float4*>(A + i) = v;
+        if (a.adam) adam_four(a, t.sdelta + i, v);
+      }
+    }
   }
 }
 
@@ -492,16 +555,17 @@ k_gather(StreamLaunchArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   char* x0 = static_cast<char*>(a.x0) + o.x_off * ebytes(a.esize);
+  const float cpre = a.clip_mode == 1 ? a.state->coef : 1.f;
   if (t.fast) {
-    if (t.kind == 0) gather_fast_rows(a, t, o, d, x0);
-    else gather_fast_tr(a, t, o, d, x0, tile);
+    if (t.kind == 0) gather_fast_rows(a, t, o, d, cpre, x0);
+    else gather_fast_tr(a, t, o, d, cpre, x0, tile);
     return;
   }
   if (t.kind == 0) {
     for (int r = t.r0 + warp; r < t.r0 + t.nr; r += nw) {
       const int64_t rb = int64_t(r) * o.cols;
       for_row(segs, o.seg_count, rb, rb + o.cols, lane, [&](int64_t rel, int64_t st) {
-        const float mv = momentum_of(a.beta, a.momentum[st], a.accum[st]);
+        const float mv = momentum_of(a.beta, a.momentum[st], grad_m(a, cpre, a.accum[st]));
         a.momentum[st] = mv;
         store_ws(x0, a.esize, int64_t(r) * o.ldx + (rel - rb), __fdiv_rn(mv, d), a.x_ps);
       });
@@ -514,7 +578,7 @@ k_gather(StreamLaunchArgs a) {
       if (r >= r_end) break;
       const int64_t rb = int64_t(r) * o.cols;
       for_row(segs, o.seg_count, rb + t.c0, rb + c_end, lane, [&](int64_t rel, int64_t st) {
-        const float mv = momentum_of(a.beta, a.momentum[st], a.accum[st]);
+        const float mv = momentum_of(a.beta, a.momentum[st], grad_m(a, cpre, a.accum[st]));
         a.momentum[st] = mv;
         tile[rr][rel - rb - t.c0] = __fdiv_rn(mv, d);
       });
@@ -579,6 +643,31 @@ k_update_sumsq(StreamLaunchArgs a) {
 
 constexpr int kFinThreads = 1024;
 
+// norm = sqrt(tot), coef = min(1, clip / (norm + 1e-6)) (1 when clip <= 0),
+// both kept in the step state.
+__device__ __forceinline__ void set_clip(const StreamLaunchArgs& a, double tot) {
+  const double norm = sqrt(tot);
+  double coef = 1.0;
+  if (a.clip > 0.f) {
+    coef = static_cast<double>(a.clip) / (norm + kClipEps);
+    if (coef > 1.0) coef = 1.0;
+  }
+  a.state->coef = static_cast<float>(coef);
+  a.state->norm = static_cast<float>(norm);
+  a.state->sumsq = tot;
+}
+
+// Clip before Muon: the global norm over every parameter's gradient, from
+// the tile sums of reduce mode 1, in a fixed order.
+__global__ void __launch_bounds__(kFinThreads)
+k_finalize_pre(StreamLaunchArgs a) {
+  if (a.state->overflow) return;
+  double s = 0.0;
+  for (int i = threadIdx.x; i < a.n_rtiles; i += kFinThreads) s += a.rtile_sum[i];
+  const double tot = block_sum<kFinThreads>(s);
+  if (threadIdx.x == 0) set_clip(a, tot);
+}
+
 __global__ void __launch_bounds__(kFinThreads)
 k_finalize(StreamLaunchArgs a) {
   if (a.state->overflow) {
@@ -590,24 +679,18 @@ k_finalize(StreamLaunchArgs a) {
     }
     return;
   }
-  double s = 0.0;
-  for (int i = threadIdx.x; i < a.n_ytiles; i += kFinThreads) s += a.ytile_sum[i];
-  for (int i = threadIdx.x; i < a.n_rtiles; i += kFinThreads)
-    if (!a.owners[a.rtiles[i].owner].is_muon) s += a.rtile_sum[i];
-  const double tot = block_sum<kFinThreads>(s);
+  const int applied = (a.err_flag != nullptr && *a.err_flag != 0) ? -1 : 1;
+  if (a.clip_mode == 0) {
+    double s = 0.0;
+    for (int i = threadIdx.x; i < a.n_ytiles; i += kFinThreads) s += a.ytile_sum[i];
+    for (int i = threadIdx.x; i < a.n_rtiles; i += kFinThreads)
+      if (!a.owners[a.rtiles[i].owner].is_muon) s += a.rtile_sum[i];
+    const double tot = block_sum<kFinThreads>(s);
+    if (threadIdx.x == 0) set_clip(a, tot);
+  }
   if (threadIdx.x == 0) {
-    const double norm = sqrt(tot);
-    double coef = 1.0;
-    if (a.clip > 0.f) {
-      coef = static_cast<double>(a.clip) / (norm + kClipEps);
-      if (coef > 1.0) coef = 1.0;
-    }
-    const int applied = (a.err_flag != nullptr && *a.err_flag != 0) ? -1 : 1;
     a.state->applied = applied;
-    a.state->coef = static_cast<float>(coef);
-    a.state->norm = static_cast<float>(norm);
-    a.state->sumsq = tot;
-    muon_result_t r{applied, a.ns_calls, static_cast<float>(norm), static_cast<float>(coef)};
+    muon_result_t r{applied, a.ns_calls, a.state->norm, a.state->coef};
     *a.result = r;
   }
 }
@@ -618,7 +701,10 @@ __global__ void __launch_bounds__(kStreamThreads)
 k_scatter(StreamLaunchArgs a) {
   if (a.state->overflow) return;
   __shared__ float tile[kTT][kTT + 1];
+  // clip before Muon: the update is written unscaled (the gradient already
+  // carried the coefficient); auxiliary gradients take coef either way
   const float coef = a.state->coef, lr = a.lr;
+  const float post = a.clip_mode == 1 ? 1.f : coef;
   const ETile t = a.etiles[blockIdx.x];
   const Owner o = a.owners[t.owner];
   const Segment* segs = a.segs + o.seg_begin;
@@ -626,13 +712,13 @@ k_scatter(StreamLaunchArgs a) {
   const int nw = blockDim.x >> 5;
   if (t.fast) {
     const char* yb = static_cast<const char*>(a.y) + o.x_off * ebytes(a.esize);
-    if (t.kind == 0) scatter_fast_rows(a, t, o, coef, yb);
-    else if (t.kind == 1) scatter_fast_tr(a, t, o, coef, yb, tile);
+    if (t.kind == 0) scatter_fast_rows(a, t, o, post, yb);
+    else if (t.kind == 1) scatter_fast_tr(a, t, o, post, yb, tile);
     else scatter_fast_aux(a, t, coef);
     return;
   }
   if (t.kind == 2) {
-    // auxiliary parameter: accum = coef * g, master untouched
+    // auxiliary parameter: accum = coef * g; master untouched unless Adam
     const int64_t te = t.rel_begin + t.len;
     int si = find_seg(segs, o.seg_count, t.rel_begin);
     for (; si < o.seg_count && segs[si].rel_begin < te; ++si) {
@@ -640,8 +726,11 @@ k_scatter(StreamLaunchArgs a) {
       const int64_t lo = sg.rel_begin > t.rel_begin ? sg.rel_begin : t.rel_begin;
       const int64_t hi = (sg.rel_begin + sg.len) < te ? (sg.rel_begin + sg.len) : te;
       const int64_t base = sg.storage_begin - sg.rel_begin;
-      for (int64_t rel = lo + threadIdx.x; rel < hi; rel += blockDim.x)
-        a.accum[base + rel] = __fmul_rn(coef, a.accum[base + rel]);
+      for (int64_t rel = lo + threadIdx.x; rel < hi; rel += blockDim.x) {
+        const float v = __fmul_rn(coef, grad_in(a, a.accum[base + rel]));
+        a.accum[base + rel] = v;
+        if (a.adam) adam_one(a, base + rel, v);
+      }
     }
     return;
   }
@@ -650,7 +739,7 @@ k_scatter(StreamLaunchArgs a) {
     for (int r = t.r0 + warp; r < t.r0 + t.nr; r += nw) {
       const int64_t rb = int64_t(r) * o.cols;
       for_row(segs, o.seg_count, rb, rb + o.cols, lane, [&](int64_t rel, int64_t st) {
-        const float v = __fmul_rn(coef, load_ws(y, a.esize, int64_t(r) * o.ldx + (rel - rb), a.x_ps));
+        const float v = __fmul_rn(post, load_ws(y, a.esize, int64_t(r) * o.ldx + (rel - rb), a.x_ps));
         a.accum[st] = v;
         a.master[st] = __fsub_rn(a.master[st], __fmul_rn(lr, v));
       });
@@ -670,7 +759,7 @@ k_scatter(StreamLaunchArgs a) {
       if (r >= r_end) break;
       const int64_t rb = int64_t(r) * o.cols;
       for_row(segs, o.seg_count, rb + t.c0, rb + c_end, lane, [&](int64_t rel, int64_t st) {
-        const float v = __fmul_rn(coef, tile[rr][rel - rb - t.c0]);
+        const float v = __fmul_rn(post, tile[rr][rel - rb - t.c0]);
         a.accum[st] = v;
         a.master[st] = __fsub_rn(a.master[st], __fmul_rn(lr, v));
       });
@@ -787,6 +876,9 @@ void launch_update_sumsq(const StreamLaunchArgs& a, cudaStream_t s) {
 }
 void launch_finalize(const StreamLaunchArgs& a, cudaStream_t s) {
   k_finalize<<<1, kFinThreads, 0, s>>>(a);
+}
+void launch_finalize_pre(const StreamLaunchArgs& a, cudaStream_t s) {
+  k_finalize_pre<<<1, kFinThreads, 0, s>>>(a);
 }
 void launch_scatter(const StreamLaunchArgs& a, cudaStream_t s) {
   if (a.n_etiles > 0) k_scatter<<<a.n_etiles, kStreamThreads, 0, s>>>(a);

@@ -97,3 +97,50 @@ def test_python_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(nsg, "LIB_PATH", "/nonexistent/libmuon.so")
     with pytest.raises(nsg.MuonError):
         nsg.lib()
+
+
+def _step_ex(lib, opts, ptrs=(FAKE, FAKE, FAKE)):
+    lay = wl.tiny_layout()
+    p = np.ascontiguousarray(lay.params, dtype=nsg.PARAM_DTYPE)
+    q = np.ascontiguousarray(lay.parts, dtype=nsg.PART_DTYPE)
+    return lib.muon_step_ex(*ptrs, p.ctypes.data, len(p), q.ctypes.data, len(q), 0.95, 0.02, 1, 5,
+                            0.0, 0, ctypes.byref(opts) if opts is not None else None, FAKE, None)
+
+
+def test_step_options_struct_layout():
+    assert ctypes.sizeof(nsg.StepOptions) == 64
+    assert nsg.StepOptions.adam_step.offset == 32 and nsg.StepOptions.workspace_budget.offset == 56
+
+
+def test_step_options_rejected_on_host(lib):
+    adam = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, step=1, exp_avg=FAKE, exp_avg_sq=FAKE)
+    cases = []
+    o = nsg.step_options(); o.struct_size = 8
+    cases.append((o, "struct_size"))
+    cases.append((nsg.step_options(clip_mode=5), "clip_mode"))
+    cases.append((nsg.step_options(grad_scale=-1.0), "grad_scale"))
+    cases.append((nsg.step_options(grad_scale=float("inf")), "grad_scale"))
+    cases.append((nsg.step_options(adam=dict(adam, exp_avg=None)), "exp_avg"))
+    cases.append((nsg.step_options(adam=dict(adam, exp_avg_sq=FAKE + 4)), "aligned"))
+    cases.append((nsg.step_options(adam=dict(adam, step=0)), "adam_step"))
+    cases.append((nsg.step_options(adam=dict(adam, beta2=1.0)), "betas"))
+    cases.append((nsg.step_options(adam=dict(adam, eps=-1.0)), "adam_eps"))
+    for opts, word in cases:
+        rc = _step_ex(lib, opts)
+        assert rc == nsg.MUON_ERR_INVALID, (word, rc)
+        assert word in lib.muon_last_error().decode(), lib.muon_last_error()
+
+
+def test_step_buffers_must_be_16_byte_aligned(lib):
+    for ptrs in ((FAKE + 4, FAKE, FAKE), (FAKE, FAKE + 8, FAKE), (FAKE, FAKE, FAKE + 12)):
+        assert _step_ex(lib, None, ptrs) == nsg.MUON_ERR_INVALID
+        assert "16-byte" in lib.muon_last_error().decode()
+
+
+def test_valid_options_without_gpu_fail_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    adam = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, step=3, exp_avg=FAKE, exp_avg_sq=FAKE)
+    for opts in (None, nsg.step_options(), nsg.step_options("grad", 2.0 ** -10, adam)):
+        assert _step_ex(lib, opts) == nsg.MUON_ERR_CUDA
