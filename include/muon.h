@@ -180,7 +180,9 @@ MUON_API int muon_step(float* accum, float* momentum, float* master,
  *              blocks run in waves whose workspace fits the budget (a
  *              block larger than the budget runs alone), the unclipped
  *              update is parked in accum, and a final pass applies the clip
- *              coefficient.  Results are identical to the unbounded step. */
+ *              coefficient (with MUON_CLIP_GRAD the coefficient is known
+ *              before the waves and updates are written directly).  Results
+ *              are bit-identical to the unbounded step. */
 typedef enum { MUON_CLIP_UPDATE = 0, MUON_CLIP_GRAD = 1 } muon_clip_mode_t;
 
 typedef struct muon_step_options {

@@ -361,6 +361,14 @@ struct GemmPhase {
   int64_t conv_n = 0;
 };
 
+// Tile ranges of one wave of a bounded-workspace plan (owner order).
+struct WaveRange {
+  int g0, g1;   // gather tiles
+  int s0, s1;   // scatter tiles
+  int y0, y1;   // update tiles
+  double elems; // Muon elements of the wave
+};
+
 struct NsPlan {
   int esize = 2;       // X0 / Y element format: 2 bf16, 4 fp32, 6 split-3
   int64_t x_ps = 0;    // split-3: elements between the planes of an X region
@@ -371,6 +379,12 @@ struct NsPlan {
   void* y = nullptr;
   std::vector<std::unique_ptr<GemmPhase>> phases;
   double flops = 0.0;
+  // Bounded workspace: the Muon owners run in waves that share `ws`; each
+  // wave is a plan of its own over owners whose x_off / sq_off are relative
+  // to the wave (the owner table with those offsets is d_owners).
+  std::vector<std::unique_ptr<NsPlan>> waves;
+  std::vector<WaveRange> ranges;
+  DevBuf d_owners;
 };
 
 // Adds one GEMM D = alpha A op(B) + beta E + gamma I (per block) to a phase.
@@ -436,30 +450,60 @@ struct WsMat {
 // Engines: BF16 operands on the tensor cores (ENGINE_TC); FP32 operands on
 // the tensor cores through split-3 planes (ENGINE_X3); with MUON_GEMM=simt
 // everything runs on the CUDA-core kernel with plain bf16 / fp32 storage.
-int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_elems,
-                  int method, int mode, int steps, NsPlan& P) {
+// Element formats and region counts of a plan: X regions (m x n) in xe,
+// the m x m regions in se, nsq of them, and a bf16 copy of Q for the
+// CUDA-core gram path.
+struct NsFormats {
+  bool tc = false;
+  int xe = 2, fe = 4, se = 2, nsq = 2;
+  bool need_qbf = false;
+  static size_t bytes_of(int es) { return size_t(es == 6 ? 6 : es); }
+  size_t ws_bytes(int64_t x_elems, int64_t sq_elems) const {
+    size_t b = 2 * bytes_of(xe) * size_t(x_elems) + nsq * bytes_of(se) * size_t(sq_elems);
+    if (need_qbf) b += 2 * size_t(sq_elems);
+    return b;
+  }
+};
+
+int ns_formats(int method, int mode, NsFormats& f) {
   const bool bf16 = mode == MUON_OPERANDS_BF16;
   const char* env = std::getenv("MUON_GEMM");
   const bool force_simt = env && std::strcmp(env, "simt") == 0;
-  P.use_tc = !force_simt && tc_available();
-  if (bf16 && !P.use_tc && !force_simt)
+  f.tc = !force_simt && tc_available();
+  if (bf16 && !f.tc && !force_simt)
     return fail(MUON_ERR_UNSUPPORTED, "BF16 operand mode needs an sm_103 (GB300) GPU");
-  const bool tc = P.use_tc;
-  const int xe = bf16 ? 2 : (tc ? 6 : 4);          // X regions
-  const int fe = tc ? 6 : 4;                       // gram's m x m regions
-  const int se = method == MUON_NS_STANDARD ? xe : fe;
-  auto bytes_of = [](int es) { return size_t(es == 6 ? 6 : es); };
+  f.xe = bf16 ? 2 : (f.tc ? 6 : 4);
+  f.fe = f.tc ? 6 : 4;
+  f.se = method == MUON_NS_STANDARD ? f.xe : f.fe;
+  f.nsq = method == MUON_NS_STANDARD ? 2 : 5;
+  f.need_qbf = method == MUON_NS_GRAM && bf16 && !f.tc;
+  return MUON_OK;
+}
+
+// Builds the GEMM phases of `owners` (their x_off / sq_off index regions of
+// x_elems / sq_elems elements).  The workspace is allocated unless `ext`
+// (at least ws_bytes(x_elems, sq_elems) bytes) is given.
+int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_elems,
+                  int method, int mode, int steps, NsPlan& P, char* ext = nullptr) {
+  const bool bf16 = mode == MUON_OPERANDS_BF16;
+  NsFormats F;
+  int rc0 = ns_formats(method, mode, F);
+  if (rc0 != MUON_OK) return rc0;
+  P.use_tc = F.tc;
+  const bool tc = F.tc;
+  const int xe = F.xe, fe = F.fe, se = F.se, nsq = F.nsq;
+  const bool need_qbf = F.need_qbf;
+  auto bytes_of = NsFormats::bytes_of;
   auto eb = [](int es) { return int64_t(es == 6 ? 2 : es); };
   P.esize = xe;
   P.x_ps = xe == 6 ? x_elems : 0;
   P.method = method;
   P.steps = steps;
-  const int nsq = method == MUON_NS_STANDARD ? 2 : 5;
-  const bool need_qbf = method == MUON_NS_GRAM && bf16 && !tc;
-  size_t bytes = 2 * bytes_of(xe) * size_t(x_elems) + nsq * bytes_of(se) * size_t(sq_elems);
-  if (need_qbf) bytes += 2 * size_t(sq_elems);
-  MUON_CUDA_TRY(P.ws.alloc(bytes + 256));
-  char* base = P.ws.as<char>();
+  char* base = ext;
+  if (!base) {
+    MUON_CUDA_TRY(P.ws.alloc(F.ws_bytes(x_elems, sq_elems) + 256));
+    base = P.ws.as<char>();
+  }
   char* X[2] = {base, base + bytes_of(xe) * x_elems};
   char* sq_base = base + 2 * bytes_of(xe) * x_elems;
   char* S[5];
@@ -605,7 +649,7 @@ struct TablePlan {
   Layout L;
   DevBuf d_owners, d_segs, d_rtiles, d_gtiles, d_stiles, d_ytiles, d_runs;
   DevBuf d_rsum, d_ysum, d_div, d_state, d_err;
-  std::map<std::tuple<int, int, int>, std::unique_ptr<NsPlan>> ns;
+  std::map<std::tuple<int, int, int, uint64_t>, std::unique_ptr<NsPlan>> ns;
 };
 
 std::vector<std::unique_ptr<TablePlan>> g_plans;
@@ -674,15 +718,82 @@ int get_table_plan(const muon_param_t* params, int nparams, const muon_partition
   return MUON_OK;
 }
 
-int get_ns_plan(TablePlan& tp, int method, int mode, int steps, NsPlan** out) {
-  auto k = std::make_tuple(method, mode, steps);
+// Splits the Muon owners, in order, into waves whose workspace fits
+// `budget` bytes (an owner larger than the budget is a wave of its own) and
+// builds one plan per wave over a shared workspace.
+int build_wave_plan(const Layout& L, int method, int mode, int steps, uint64_t budget, NsPlan& P) {
+  NsFormats F;
+  int rc = ns_formats(method, mode, F);
+  if (rc != MUON_OK) return rc;
+  // The shared workspace holds the largest wave's m x n regions and the
+  // largest wave's m x m regions, which may come from different waves, so
+  // an owner joins the current wave only while those running maxima still
+  // fit the budget.
+  std::vector<Owner> owners = L.owners;
+  std::vector<std::vector<int>> waves;
+  int64_t cx = 0, csq = 0, mx = 0, msq = 0;
+  for (int i = 0; i < static_cast<int>(owners.size()); ++i) {
+    Owner& o = owners[i];
+    if (!o.is_muon) continue;
+    const int64_t ox = round_up(int64_t(o.m) * o.ldx, 64), osq = round_up(int64_t(o.m) * o.ldm, 64);
+    if (waves.empty() ||
+        F.ws_bytes(std::max(mx, cx + ox), std::max(msq, csq + osq)) > budget) {
+      waves.emplace_back();
+      cx = csq = 0;
+    }
+    o.x_off = cx;
+    o.sq_off = csq;
+    cx += ox;
+    csq += osq;
+    mx = std::max(mx, cx);
+    msq = std::max(msq, csq);
+    waves.back().push_back(i);
+  }
+  MUON_CUDA_TRY(P.ws.alloc(F.ws_bytes(mx, msq) + 256));
+  MUON_CUDA_TRY(upload(P.d_owners, owners));
+  P.esize = F.xe;
+  P.x_ps = F.xe == 6 ? mx : 0;
+  P.use_tc = F.tc;
+  P.method = method;
+  P.steps = steps;
+  // first tile of each owner in the gather / scatter / update tile lists
+  auto first_of = [&](auto const& tiles, int owner) {
+    int lo = 0, hi = static_cast<int>(tiles.size());
+    while (lo < hi) {
+      const int mid = (lo + hi) / 2;
+      if (tiles[mid].owner < owner) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+  };
+  for (size_t w = 0; w < waves.size(); ++w) {
+    std::vector<Owner> wo;
+    for (int i : waves[w]) wo.push_back(owners[i]);
+    std::unique_ptr<NsPlan> sub(new NsPlan());
+    rc = build_ns_plan(wo, mx, msq, method, mode, steps, *sub, P.ws.as<char>());
+    if (rc != MUON_OK) return rc;
+    P.flops += sub->flops;
+    P.x0 = sub->x0;
+    P.y = sub->y;
+    const int ob = waves[w].front(), oe = waves[w].back() + 1;
+    double el = 0.0;
+    for (int i : waves[w]) el += double(owners[i].numel);
+    P.ranges.push_back({first_of(L.gtiles, ob), first_of(L.gtiles, oe), first_of(L.stiles, ob),
+                        first_of(L.stiles, oe), first_of(L.ytiles, ob), first_of(L.ytiles, oe), el});
+    P.waves.push_back(std::move(sub));
+  }
+  return MUON_OK;
+}
+
+int get_ns_plan(TablePlan& tp, int method, int mode, int steps, uint64_t budget, NsPlan** out) {
+  auto k = std::make_tuple(method, mode, steps, budget);
   auto it = tp.ns.find(k);
   if (it != tp.ns.end()) {
     *out = it->second.get();
     return MUON_OK;
   }
   std::unique_ptr<NsPlan> P(new NsPlan());
-  int rc = build_ns_plan(tp.L.owners, tp.L.x_elems, tp.L.sq_elems, method, mode, steps, *P);
+  int rc = budget ? build_wave_plan(tp.L, method, mode, steps, budget, *P)
+                  : build_ns_plan(tp.L.owners, tp.L.x_elems, tp.L.sq_elems, method, mode, steps, *P);
   if (rc != MUON_OK) return rc;
   *out = P.get();
   tp.ns[k] = std::move(P);
@@ -812,8 +923,6 @@ int apply_options(const muon_step_options_t* opts, StreamLaunchArgs& a) {
     return fail(MUON_ERR_INVALID, "unknown clip_mode");
   if (!std::isfinite(opts->grad_scale) || opts->grad_scale < 0.f)
     return fail(MUON_ERR_INVALID, "grad_scale must be finite and >= 0");
-  if (opts->workspace_budget != 0)
-    return fail(MUON_ERR_UNSUPPORTED, "workspace_budget is not supported yet");
   a.clip_mode = opts->clip_mode;
   a.grad_scale = opts->grad_scale == 0.f ? 1.f : opts->grad_scale;
   if (opts->aux_adam != 0 && opts->aux_adam != 1) return fail(MUON_ERR_INVALID, "aux_adam must be 0 or 1");
@@ -868,12 +977,14 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
   rc = get_table_plan(params, nparams, parts, nparts, &tp);
   if (rc != MUON_OK) return rc;
   NsPlan* P = nullptr;
-  rc = get_ns_plan(*tp, ns_method, operand_mode, ns_steps, &P);
+  const uint64_t budget = opts ? opts->workspace_budget : 0;
+  rc = get_ns_plan(*tp, ns_method, operand_mode, ns_steps, budget, &P);
   if (rc != MUON_OK) return rc;
   const Layout& L = tp->L;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool waves = budget != 0;
 
-  a.owners = tp->d_owners.as<Owner>();
+  a.owners = waves ? P->d_owners.as<Owner>() : tp->d_owners.as<Owner>();
   a.segs = tp->d_segs.as<Segment>();
   a.rtiles = tp->d_rtiles.as<RTile>();
   a.ytiles = tp->d_ytiles.as<YTile>();
@@ -917,25 +1028,71 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
     launch_reduce(a, s);
     launch_owner_norm(a, s);
   }
-  {
-    a.etiles = tp->d_gtiles.as<ETile>();
-    a.n_etiles = static_cast<int>(L.gtiles.size());
-    PhaseScope sc(MUON_PHASE_GATHER, s, a.n_etiles ? 1 : 0, me * (12 + P->esize), 0.0);
-    launch_gather(a, s);
-  }
-  rc = enqueue_gemms(*P, a.state, tp->d_err.as<int>(), s);
-  if (rc != MUON_OK) return rc;
-  {
-    PhaseScope sc(MUON_PHASE_NORM, s, (a.n_ytiles && !pre ? 1 : 0) + 1, pre ? 0.0 : me * P->esize, 0.0);
-    if (!pre) launch_update_sumsq(a, s);
-    launch_finalize(a, s);
-  }
-  {
-    a.etiles = tp->d_stiles.as<ETile>();
-    a.n_etiles = static_cast<int>(L.stiles.size());
-    PhaseScope sc(MUON_PHASE_SCATTER, s, a.n_etiles ? 1 : 0,
-                  me * (12 + P->esize) + ae * (a.adam ? 32 : 8), 0.0);
-    launch_scatter(a, s);
+  if (!waves) {
+    {
+      a.etiles = tp->d_gtiles.as<ETile>();
+      a.n_etiles = static_cast<int>(L.gtiles.size());
+      PhaseScope sc(MUON_PHASE_GATHER, s, a.n_etiles ? 1 : 0, me * (12 + P->esize), 0.0);
+      launch_gather(a, s);
+    }
+    rc = enqueue_gemms(*P, a.state, tp->d_err.as<int>(), s);
+    if (rc != MUON_OK) return rc;
+    {
+      PhaseScope sc(MUON_PHASE_NORM, s, (a.n_ytiles && !pre ? 1 : 0) + 1, pre ? 0.0 : me * P->esize,
+                    0.0);
+      if (!pre) launch_update_sumsq(a, s);
+      launch_finalize(a, s);
+    }
+    {
+      a.etiles = tp->d_stiles.as<ETile>();
+      a.n_etiles = static_cast<int>(L.stiles.size());
+      PhaseScope sc(MUON_PHASE_SCATTER, s, a.n_etiles ? 1 : 0,
+                    me * (12 + P->esize) + ae * (a.adam ? 32 : 8), 0.0);
+      launch_scatter(a, s);
+    }
+  } else {
+    // bounded workspace: per wave gather, NS, update sums and the Muon
+    // write-back (unscaled and parked in accum when the coefficient comes
+    // from the updates); then the coefficient and a final pass
+    for (size_t w = 0; w < P->waves.size(); ++w) {
+      const WaveRange& R = P->ranges[w];
+      StreamLaunchArgs b = a;
+      {
+        b.etiles = tp->d_gtiles.as<ETile>() + R.g0;
+        b.n_etiles = R.g1 - R.g0;
+        PhaseScope sc(MUON_PHASE_GATHER, s, b.n_etiles ? 1 : 0, R.elems * (12 + P->esize), 0.0);
+        launch_gather(b, s);
+      }
+      rc = enqueue_gemms(*P->waves[w], a.state, tp->d_err.as<int>(), s);
+      if (rc != MUON_OK) return rc;
+      if (!pre) {
+        b.ytiles = tp->d_ytiles.as<YTile>() + R.y0;
+        b.ytile_sum = tp->d_ysum.as<double>() + R.y0;
+        b.n_ytiles = R.y1 - R.y0;
+        PhaseScope sc(MUON_PHASE_NORM, s, b.n_ytiles ? 1 : 0, R.elems * P->esize, 0.0);
+        launch_update_sumsq(b, s);
+      }
+      {
+        b.park = 1;
+        b.etiles = tp->d_stiles.as<ETile>() + R.s0;
+        b.n_etiles = R.s1 - R.s0;
+        PhaseScope sc(MUON_PHASE_SCATTER, s, b.n_etiles ? 1 : 0,
+                      R.elems * (pre ? 12 + P->esize : 4 + P->esize), 0.0);
+        launch_scatter(b, s);
+      }
+    }
+    {
+      PhaseScope sc(MUON_PHASE_NORM, s, 1, 0.0, 0.0);
+      launch_finalize(a, s);
+    }
+    {
+      a.park = 2;
+      a.etiles = tp->d_stiles.as<ETile>();
+      a.n_etiles = static_cast<int>(L.stiles.size());
+      PhaseScope sc(MUON_PHASE_SCATTER, s, a.n_etiles ? 1 : 0,
+                    (pre ? 0.0 : me * 16) + ae * (a.adam ? 32 : 8), 0.0);
+      launch_scatter(a, s);
+    }
   }
   MUON_CUDA_TRY(cudaGetLastError());
   g_cnt.steps += 1;

@@ -434,7 +434,7 @@ __device__ __forceinline__ void gather_fast_tr(const StreamLaunchArgs& a, const 
 }
 
 __device__ __forceinline__ void scatter_fast_rows(const StreamLaunchArgs& a, const ETile& t,
-                                                  const Owner& o, float coef, const char* y) {
+                                                  const Owner& o, float coef, bool wm, const char* y) {
   constexpr int U = 4;
   const int64_t e0 = int64_t(t.r0) * o.cols, e1 = int64_t(t.r0 + t.nr) * o.cols;
   float* __restrict__ A = a.accum + t.sdelta;
@@ -447,7 +447,7 @@ __device__ __forceinline__ void scatter_fast_rows(const StreamLaunchArgs& a, con
       const int64_t i = i0 + u * stride;
       if (i < e1) {
         u4[u] = load4_ws(y, a.esize, i, a.x_ps);
-        w[u] = *reinterpret_cast<const float4*>(W + i);
+        if (wm) w[u] = *reinterpret_cast<const float4*>(W + i);
       }
     }
     #pragma unroll
@@ -457,16 +457,17 @@ __device__ __forceinline__ void scatter_fast_rows(const StreamLaunchArgs& a, con
         const float4 v = make_float4(__fmul_rn(coef, u4[u].x), __fmul_rn(coef, u4[u].y),
                                      __fmul_rn(coef, u4[u].z), __fmul_rn(coef, u4[u].w));
         *reinterpret_cast<float4*>(A + i) = v;
-        *reinterpret_cast<float4*>(W + i) =
-            make_float4(__fsub_rn(w[u].x, __fmul_rn(a.lr, v.x)), __fsub_rn(w[u].y, __fmul_rn(a.lr, v.y)),
-                        __fsub_rn(w[u].z, __fmul_rn(a.lr, v.z)), __fsub_rn(w[u].w, __fmul_rn(a.lr, v.w)));
+        if (wm)
+          *reinterpret_cast<float4*>(W + i) =
+              make_float4(__fsub_rn(w[u].x, __fmul_rn(a.lr, v.x)), __fsub_rn(w[u].y, __fmul_rn(a.lr, v.y)),
+                          __fsub_rn(w[u].z, __fmul_rn(a.lr, v.z)), __fsub_rn(w[u].w, __fmul_rn(a.lr, v.w)));
       }
     }
   }
 }
 
 __device__ __forceinline__ void scatter_fast_tr(const StreamLaunchArgs& a, const ETile& t,
-                                                const Owner& o, float coef, const char* y,
+                                                const Owner& o, float coef, bool wm, const char* y,
                                                 float (*tile)[kTT + 1]) {
   const int r_end = min(t.r0 + kTT, o.rows);
   // Y rows c0..c0+63 hold block columns; 8 elements per thread, 32 rows per pass
@@ -500,7 +501,7 @@ __device__ __forceinline__ void scatter_fast_tr(const StreamLaunchArgs& a, const
   #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int r = t.r0 + rq + 16 * k;
-    if (r < r_end)
+    if (wm && r < r_end)
       w[k] = *reinterpret_cast<const float4*>(a.master + t.sdelta + int64_t(r) * o.cols + t.c0 + cq);
   }
   #pragma unroll
@@ -512,9 +513,10 @@ __device__ __forceinline__ void scatter_fast_tr(const StreamLaunchArgs& a, const
       const float4 v = make_float4(__fmul_rn(coef, tr[cq]), __fmul_rn(coef, tr[cq + 1]),
                                    __fmul_rn(coef, tr[cq + 2]), __fmul_rn(coef, tr[cq + 3]));
       *reinterpret_cast<float4*>(a.accum + i) = v;
-      *reinterpret_cast<float4*>(a.master + i) =
-          make_float4(__fsub_rn(w[k].x, __fmul_rn(a.lr, v.x)), __fsub_rn(w[k].y, __fmul_rn(a.lr, v.y)),
-                      __fsub_rn(w[k].z, __fmul_rn(a.lr, v.z)), __fsub_rn(w[k].w, __fmul_rn(a.lr, v.w)));
+      if (wm)
+        *reinterpret_cast<float4*>(a.master + i) =
+            make_float4(__fsub_rn(w[k].x, __fmul_rn(a.lr, v.x)), __fsub_rn(w[k].y, __fmul_rn(a.lr, v.y)),
+                        __fsub_rn(w[k].z, __fmul_rn(a.lr, v.z)), __fsub_rn(w[k].w, __fmul_rn(a.lr, v.w)));
     }
   }
 }
@@ -541,6 +543,52 @@ __device__ __forceinline__ void scatter_fast_aux(const StreamLaunchArgs& a, cons
         if (a.adam) adam_four(a, t.sdelta + i, v);
       }
     }
+  }
+}
+
+// Bounded workspace, final pass over a Muon tile whose unclipped update u
+// is parked in accum: accum = coef * u, master -= lr * coef * u.
+__device__ __forceinline__ float4 apply4(const StreamLaunchArgs& a, float coef, float* A, float* W) {
+  const float4 u = *reinterpret_cast<const float4*>(A);
+  const float4 w = *reinterpret_cast<const float4*>(W);
+  const float4 v = make_float4(__fmul_rn(coef, u.x), __fmul_rn(coef, u.y), __fmul_rn(coef, u.z),
+                               __fmul_rn(coef, u.w));
+  *reinterpret_cast<float4*>(W) =
+      make_float4(__fsub_rn(w.x, __fmul_rn(a.lr, v.x)), __fsub_rn(w.y, __fmul_rn(a.lr, v.y)),
+                  __fsub_rn(w.z, __fmul_rn(a.lr, v.z)), __fsub_rn(w.w, __fmul_rn(a.lr, v.w)));
+  return v;
+}
+
+__device__ __forceinline__ void apply_parked(const StreamLaunchArgs& a, const ETile& t, const Owner& o,
+                                             float coef) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  if (t.fast && t.kind == 0) {
+    const int64_t e0 = int64_t(t.r0) * o.cols, e1 = int64_t(t.r0 + t.nr) * o.cols;
+    for (int64_t i = e0 + 4 * threadIdx.x; i < e1; i += int64_t(4) * kStreamThreads) {
+      float* A = a.accum + t.sdelta + i;
+      *reinterpret_cast<float4*>(A) = apply4(a, coef, A, a.master + t.sdelta + i);
+    }
+    return;
+  }
+  if (t.fast) {   // 64 x 64 tile of a transposed block, 16 float4 per row
+    const int r_end = min(t.r0 + kTT, o.rows);
+    const int rq = threadIdx.x >> 4, cq = (threadIdx.x & 15) * 4;
+    for (int r = t.r0 + rq; r < r_end; r += kStreamThreads / 16) {
+      const int64_t i = t.sdelta + int64_t(r) * o.cols + t.c0 + cq;
+      *reinterpret_cast<float4*>(a.accum + i) = apply4(a, coef, a.accum + i, a.master + i);
+    }
+    return;
+  }
+  const Segment* segs = a.segs + o.seg_begin;
+  const int r_end = t.kind == 0 ? t.r0 + t.nr : min(t.r0 + kTT, o.rows);
+  const int c0 = t.kind == 0 ? 0 : t.c0, c_end = t.kind == 0 ? o.cols : min(t.c0 + kTT, o.cols);
+  for (int r = t.r0 + warp; r < r_end; r += nw) {
+    const int64_t rb = int64_t(r) * o.cols;
+    for_row(segs, o.seg_count, rb + c0, rb + c_end, lane, [&](int64_t, int64_t st) {
+      const float v = __fmul_rn(coef, a.accum[st]);
+      a.accum[st] = v;
+      a.master[st] = __fsub_rn(a.master[st], __fmul_rn(a.lr, v));
+    });
   }
 }
 
@@ -703,17 +751,27 @@ k_scatter(StreamLaunchArgs a) {
   __shared__ float tile[kTT][kTT + 1];
   // clip before Muon: the update is written unscaled (the gradient already
   // carried the coefficient); auxiliary gradients take coef either way
+  // Bounded workspace: park 1 (per wave) writes Muon updates only, unscaled
+  // and without the master when the coefficient is not known yet; park 2
+  // (final pass) applies it to the parked updates and writes the
+  // auxiliary parameters.
   const float coef = a.state->coef, lr = a.lr;
-  const float post = a.clip_mode == 1 ? 1.f : coef;
   const ETile t = a.etiles[blockIdx.x];
   const Owner o = a.owners[t.owner];
+  if (a.park == 2 && t.kind != 2) {
+    if (a.clip_mode == 0) apply_parked(a, t, o, coef);
+    return;
+  }
+  if (a.park == 1 && t.kind == 2) return;
+  const float post = (a.clip_mode == 1 || a.park == 1) ? 1.f : coef;
+  const bool wm = !(a.park == 1 && a.clip_mode == 0);
   const Segment* segs = a.segs + o.seg_begin;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   if (t.fast) {
     const char* yb = static_cast<const char*>(a.y) + o.x_off * ebytes(a.esize);
-    if (t.kind == 0) scatter_fast_rows(a, t, o, post, yb);
-    else if (t.kind == 1) scatter_fast_tr(a, t, o, post, yb, tile);
+    if (t.kind == 0) scatter_fast_rows(a, t, o, post, wm, yb);
+    else if (t.kind == 1) scatter_fast_tr(a, t, o, post, wm, yb, tile);
     else scatter_fast_aux(a, t, coef);
     return;
   }
@@ -741,7 +799,7 @@ k_scatter(StreamLaunchArgs a) {
       for_row(segs, o.seg_count, rb, rb + o.cols, lane, [&](int64_t rel, int64_t st) {
         const float v = __fmul_rn(post, load_ws(y, a.esize, int64_t(r) * o.ldx + (rel - rb), a.x_ps));
         a.accum[st] = v;
-        a.master[st] = __fsub_rn(a.master[st], __fmul_rn(lr, v));
+        if (wm) a.master[st] = __fsub_rn(a.master[st], __fmul_rn(lr, v));
       });
     }
   } else {
@@ -761,7 +819,7 @@ k_scatter(StreamLaunchArgs a) {
       for_row(segs, o.seg_count, rb + t.c0, rb + c_end, lane, [&](int64_t rel, int64_t st) {
         const float v = __fmul_rn(post, tile[rr][rel - rb - t.c0]);
         a.accum[st] = v;
-        a.master[st] = __fsub_rn(a.master[st], __fmul_rn(lr, v));
+        if (wm) a.master[st] = __fsub_rn(a.master[st], __fmul_rn(lr, v));
       });
     }
   }

@@ -256,3 +256,71 @@ def test_options_partition_independence_bitwise(torch, storage, nparts):
     for xa, xb in zip(*outs):
         for a, b in zip(xa, xb):
             assert np.array_equal(bits(a), bits(b))
+
+
+def _buffers(st, adam):
+    out = list(st.numpy())
+    if adam:
+        out += [st.exp_avg.cpu().numpy(), st.exp_avg_sq.cpu().numpy()]
+    return out
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+@pytest.mark.parametrize("mode", ["bf16", "fp32"])
+@pytest.mark.parametrize("clip_mode", ["update", "grad"])
+def test_bounded_workspace_bit_identical(torch, method, mode, clip_mode):
+    """workspace_budget runs the Newton-Schulz blocks in waves over a shared
+    workspace ('Run Muon once per optimizer step under ZeRO-3 ...', 'The
+    change': bounded per-rank buffers; 'Fix Muon optimizer under ZeRO CPU
+    offload and bound gather buffers': a byte cap on gathered parameters).
+    Every budget -- one block per wave, a few blocks, all -- gives the
+    unbounded step's bits, Adam state included."""
+    lay = mixed_layout()
+    outs, res = [], []
+    for budget in (0, 1, 40_000, 200_000, 1 << 40):
+        st = make_state(torch, lay, 68, adam=True)
+        res.append(nsg.read_result(nsg.step_ex(st.accum, st.momentum, st.master, lay.params,
+                                               lay.parts, BETA, LR, method, 5, CLIP, mode,
+                                               clip_mode=clip_mode, adam=adam_dict(st, 2),
+                                               workspace_budget=budget)))
+        outs.append(_buffers(st, True))
+    for k in range(1, len(outs)):
+        assert res[k] == res[0], k
+        for a, b in zip(outs[0], outs[k]):
+            assert np.array_equal(bits(a), bits(b)), k
+    assert nsg.device_error() == 0
+
+
+def test_bounded_workspace_gpt2_layers_and_memory(torch):
+    """Two GPT-2-small layers, P=8, 16 MiB budget: bit-identical to the
+    unbounded step, several waves, and the workspace stays within the budget
+    (every block here fits it)."""
+    lay = wl.gpt2_small_layout(layers=2)
+    budget = 16 << 20
+    outs = []
+    for b in (0, budget):
+        nsg.release_workspace()
+        st = make_state(torch, lay, 69)
+        nsg.step_ex(st.accum, st.momentum, st.master, lay.params, lay.parts, BETA, LR, "standard",
+                    5, CLIP, "bf16", workspace_budget=b)
+        outs.append(list(st.numpy()))
+        ws = nsg.get_stats()["workspace_bytes"]
+        if b:
+            assert ws <= budget + 4096, ws
+        else:
+            assert ws > 3 * budget, ws
+    for a, b in zip(*outs):
+        assert np.array_equal(bits(a), bits(b))
+    nsg.release_workspace()
+
+
+def test_bounded_workspace_overflow_skips(torch):
+    lay = mixed_layout()
+    st = make_state(torch, lay, 70)
+    st.accum[int(lay.params["offset"][1])] = float("nan")
+    before = st.numpy()
+    gres = nsg.read_result(nsg.step_ex(st.accum, st.momentum, st.master, lay.params, lay.parts,
+                                       BETA, LR, "gram", 5, CLIP, "bf16", workspace_budget=1))
+    assert gres["applied"] == 0
+    for a, b in zip(before, st.numpy()):
+        assert np.array_equal(bits(a), bits(b))
