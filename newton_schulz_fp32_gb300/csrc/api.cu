@@ -354,7 +354,8 @@ struct GemmPhase {
   int ab_es = 4;   // A/B operand bytes for the CUDA-core engine
   std::vector<GemmProblem> probs;
   std::vector<GemmTile> tiles;
-  DevBuf d_probs, d_maps, d_tiles;
+  std::vector<int> tile_off;   // persistent engines: CTA b runs tiles [off[b], off[b + 1])
+  DevBuf d_probs, d_maps, d_tiles, d_off;
   double flops = 0.0;   // algorithmic (full products)
   const float* conv_src = nullptr;
   void* conv_dst = nullptr;
@@ -406,12 +407,59 @@ struct PhaseBuilder {
   }
 };
 
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 1;
+  return n;
+}
+
+// Per-tile cost model of the persistent tensor-core engines, in units of
+// one K block of the main loop: the K blocks plus a fixed cost for the
+// tile's prologue and epilogue that the next tile's main loop cannot hide.
+double tile_cost(const GemmPhase& ph, const GemmTile& t) {
+  const GemmProblem& p = ph.probs[t.problem];
+  if (ph.engine == ENGINE_X3) return (p.K + 31) / 32 + 2.0;
+  return (p.K + kTcBK - 1) / kTcBK + 8.0;
+}
+
 int finish_phase(GemmPhase& ph) {
   if (ph.engine == ENGINE_CONVERT) return MUON_OK;
-  // heavy tiles first (K descending) for the static round-robin schedule
-  std::stable_sort(ph.tiles.begin(), ph.tiles.end(), [&](const GemmTile& a, const GemmTile& b) {
-    return ph.probs[a.problem].K > ph.probs[b.problem].K;
-  });
+  if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3) {
+    // Longest-processing-time-first assignment of tiles to one persistent
+    // CTA per SM: tiles by decreasing cost, each to the least loaded CTA;
+    // every CTA then runs its tiles contiguously, heaviest first.
+    const int n = static_cast<int>(ph.tiles.size());
+    const int nb = std::max(1, std::min(num_sms(), n));
+    std::vector<int> order(n);
+    for (int i = 0; i < n; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+      return tile_cost(ph, ph.tiles[a]) > tile_cost(ph, ph.tiles[b]);
+    });
+    std::vector<std::vector<int>> bins(nb);
+    std::vector<std::pair<double, int>> heap;   // (load, bin), min-heap
+    for (int b = 0; b < nb; ++b) heap.push_back({0.0, b});
+    auto cmp = [](const std::pair<double, int>& x, const std::pair<double, int>& y) {
+      return x.first > y.first || (x.first == y.first && x.second > y.second);
+    };
+    std::make_heap(heap.begin(), heap.end(), cmp);
+    for (int i : order) {
+      std::pop_heap(heap.begin(), heap.end(), cmp);
+      heap.back().first += tile_cost(ph, ph.tiles[i]);
+      bins[heap.back().second].push_back(i);
+      std::push_heap(heap.begin(), heap.end(), cmp);
+    }
+    std::vector<GemmTile> sorted;
+    sorted.reserve(n);
+    ph.tile_off.assign(1, 0);
+    for (int b = 0; b < nb; ++b) {
+      for (int i : bins[b]) sorted.push_back(ph.tiles[i]);
+      ph.tile_off.push_back(static_cast<int>(sorted.size()));
+    }
+    ph.tiles.swap(sorted);
+    MUON_CUDA_TRY(upload(ph.d_off, ph.tile_off));
+  }
   MUON_CUDA_TRY(upload(ph.d_probs, ph.probs));
   MUON_CUDA_TRY(upload(ph.d_tiles, ph.tiles));
   if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3) {
@@ -549,11 +597,15 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_
       for (const Owner& o : owners)
         if (o.is_muon)
           g.add(mk(xm(src, o), xm(src, o), 1, sm(S[0], o, se), none, o.m, o.m, o.n, 1, 1.f, 0.f, 0.f));
-      PhaseBuilder q = new_phase(eng, xe);   // B = c A A + b A
+      // B = c A A + b A.  On the BF16 tensor cores every tile is computed:
+      // with the addend in flight the epilogue has no buffer to stage a
+      // mirror, and scattered mirror stores cost more than the lower tiles.
+      const int q_sym = eng == ENGINE_TC ? 0 : 1;
+      PhaseBuilder q = new_phase(eng, xe);
       for (const Owner& o : owners)
         if (o.is_muon)
           q.add(mk(sm(S[0], o, se), sm(S[0], o, se), 1, sm(S[1], o, se), sm(S[0], o, se), o.m, o.m,
-                   o.m, 1, c, b, 0.f));
+                   o.m, q_sym, c, b, 0.f));
       PhaseBuilder u = new_phase(eng, xe);   // X' = B X + a X
       for (const Owner& o : owners)
         if (o.is_muon)
@@ -820,12 +872,14 @@ int enqueue_gemms(NsPlan& P, const StepState* state, int* err, cudaStream_t s) {
     if (ph->tiles.empty()) continue;
     if (ph->engine == ENGINE_TC) {
       if (launch_gemm_tc(ph->d_probs.as<GemmProblem>(), ph->d_maps.as<TcMaps>(),
-                         ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()), state, err,
+                         ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()),
+                         ph->d_off.as<int>(), static_cast<int>(ph->tile_off.size()) - 1, state, err,
                          s) != 0)
         return fail(MUON_ERR_CUDA, "tensor-core GEMM launch setup failed");
     } else if (ph->engine == ENGINE_X3) {
       if (launch_gemm_x3(ph->d_probs.as<GemmProblem>(), ph->d_maps.as<TcMaps>(),
-                         ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()), state, err,
+                         ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()),
+                         ph->d_off.as<int>(), static_cast<int>(ph->tile_off.size()) - 1, state, err,
                          s) != 0)
         return fail(MUON_ERR_CUDA, "split-3 tensor-core GEMM launch setup failed");
     } else {

@@ -54,7 +54,7 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 /*align*/ + 2
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps,
-          const GemmTile* __restrict__ tiles, int ntiles, const StepState* state,
+          const GemmTile* __restrict__ tiles, int ntiles, const int* __restrict__ tile_off, const StepState* state,
           int* err_flag) {
   if (state != nullptr && state->overflow) return;
   extern __shared__ uint8_t smem_raw[];
@@ -74,6 +74,10 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // this CTA's tiles: a host-balanced range, or round-robin
+  const int t_begin = tile_off ? tile_off[blockIdx.x] : static_cast<int>(blockIdx.x);
+  const int t_end = tile_off ? tile_off[blockIdx.x + 1] : ntiles;
+  const int t_step = tile_off ? 1 : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -107,7 +111,7 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
       int s = 0;
       uint32_t ph = 0;
       int last_problem = -1;
-      for (int ti = blockIdx.x; ti < ntiles && !*abort_flag; ti += gridDim.x) {
+      for (int ti = t_begin; ti < t_end && !*abort_flag; ti += t_step) {
         const GemmTile t = tiles[ti];
         const GemmProblem& p = probs[t.problem];
         const TcMaps* mp = maps + t.problem;
@@ -142,7 +146,7 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
       uint32_t ph = 0;
       int acc = 0;
       uint32_t acc_ph = 0;
-      for (int ti = blockIdx.x; ti < ntiles && !*abort_flag; ti += gridDim.x) {
+      for (int ti = t_begin; ti < t_end && !*abort_flag; ti += t_step) {
         const GemmTile t = tiles[ti];
         const GemmProblem& p = probs[t.problem];
         const int nk = (p.K + BK - 1) / BK;
@@ -186,10 +190,11 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
     const uint32_t ebuf_s = smem_u32(ebuf);
     const uint32_t dbuf_s = smem_u32(dbuf);
     uint32_t eph = 0u;
+    bool ebuf_mirrored = false;   // the last tile staged mirror chunks in ebuf
     int acc = 0;
     uint32_t acc_ph = 0;
     bool ok = true;
-    for (int ti = blockIdx.x; ti < ntiles && ok && !*abort_flag; ti += gridDim.x) {
+    for (int ti = t_begin; ti < t_end && ok && !*abort_flag; ti += t_step) {
       const GemmTile t = tiles[ti];
       const GemmProblem& p = probs[t.problem];     // read through L1, not held in registers
       const TcMaps* mp = maps + t.problem;
@@ -204,6 +209,7 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
         }
       const bool has_e = p.E != nullptr;
       if (has_e && todo && lane == 0) {   // prefetch the first addend chunk
+        if (ebuf_mirrored) tma_store_wait_read();   // a mirror store may still read ebuf
         mbar_expect_tx(e_bar(ew), EPI_E_BYTES);
         tma_load_2d(ebuf_s, &mp->e, t.tn * BN + (__ffs(todo) - 1) * 32, gm0, e_bar(ew));
       }
@@ -251,9 +257,12 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
           for (int j = 0; j < 32; ++j)
             if (gm0 + lane == gn0 + j) x[j] = __fadd_rn(x[j], p.gamma);
         }
-        store_chunk(p, mp, x, gm0, gn0, lane, p.symmetric && gn0 == gm0, dbuf, dbuf_s);
+        // without an addend the E buffer doubles as the mirror's staging box
+        store_chunk(p, mp, x, gm0, gn0, lane, p.symmetric && gn0 == gm0, dbuf, dbuf_s,
+                    has_e ? nullptr : ebuf, ebuf_s);
         __syncwarp();
       }
+      ebuf_mirrored = !has_e && p.symmetric;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -306,7 +315,8 @@ bool tc_available() {
 }
 
 int launch_gemm_tc(const GemmProblem* probs, const TcMaps* maps, const GemmTile* tiles,
-                   int ntiles, const StepState* state, int* err_flag, cudaStream_t s) {
+                   int ntiles, const int* tile_off, int nbins, const StepState* state,
+                   int* err_flag, cudaStream_t s) {
   if (ntiles <= 0) return 0;
   static bool attr_set = false;
   if (!attr_set) {
@@ -318,8 +328,9 @@ int launch_gemm_tc(const GemmProblem* probs, const TcMaps* maps, const GemmTile*
     cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
     attr_set = true;
   }
-  const int grid = ntiles < g_num_sms ? ntiles : g_num_sms;
-  k_gemm_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(probs, maps, tiles, ntiles, state, err_flag);
+  const int grid = tile_off ? nbins : (ntiles < g_num_sms ? ntiles : g_num_sms);
+  if (grid <= 0) return 0;
+  k_gemm_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(probs, maps, tiles, ntiles, tile_off, state, err_flag);
   return 0;
 }
 

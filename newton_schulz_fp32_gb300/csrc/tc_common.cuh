@@ -228,9 +228,13 @@ __device__ __forceinline__ void stage_and_store(uint8_t* dbuf, int lane, Fill fi
   __syncwarp();
 }
 
+// mbuf (bf16 outputs, optional): a second 2 KB box buffer; chunks above the
+// diagonal of a symmetric product are then mirrored by staging the
+// transposed chunk there and storing it with TMA as well.
 __device__ __forceinline__ void store_chunk(const GemmProblem& p, const TcMaps* mp, const float* x,
                                             int gm0, int gn0, int lane, bool diag, uint8_t* dbuf,
-                                            uint32_t dbuf_s) {
+                                            uint32_t dbuf_s, uint8_t* mbuf = nullptr,
+                                            uint32_t mbuf_s = 0) {
   // fields read once: later stores to D would force reloads through p
   const int M = p.M, N = p.N, des = p.d_es;
   const bool sym = p.symmetric != 0;
@@ -282,6 +286,19 @@ __device__ __forceinline__ void store_chunk(const GemmProblem& p, const TcMaps* 
       });
       if (lane == 0) tma_store_3d(&mp->d, gn0, gm0, b, dbuf_s);
     }
+  }
+  if (sym && des == 2 && mbuf != nullptr) {
+    // The store above waited for every earlier store to read its buffer, so
+    // mbuf is free.  Box row r = output row gn0 + r, box column = lane
+    // (output column gm0 + lane); TMA clips what falls outside the matrix.
+    #pragma unroll
+    for (int r = 0; r < 32; ++r)
+      *reinterpret_cast<__nv_bfloat16*>(mbuf + sw64(r, lane >> 3) + (lane & 7) * 2) =
+          __float2bfloat16_rn(x[r]);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) tma_store_2d(&mp->d, gm0, gn0, mbuf_s);
+    return;
   }
   if (sym && gm < M) {
     if (des == 2) {
