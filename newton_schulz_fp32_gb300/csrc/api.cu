@@ -345,7 +345,7 @@ int validate_and_build(const muon_param_t* params, int nparams, const muon_parti
 
 // ------------------------------------------------------------------ NS plan
 
-enum Engine { ENGINE_TC = 0, ENGINE_SIMT = 1, ENGINE_CONVERT = 2, ENGINE_X3 = 3 };
+enum Engine { ENGINE_TC = 0, ENGINE_SIMT = 1, ENGINE_CONVERT = 2, ENGINE_X3 = 3, ENGINE_TC2 = 4 };
 
 // One launch of the NS iteration: a grouped GEMM over every block, or (for
 // ENGINE_CONVERT) the fp32 -> bf16 rounding of a whole workspace region.
@@ -394,6 +394,7 @@ struct PhaseBuilder {
   void add(const GemmProblem& p) {
     int bm = kSimtTile, bn = kSimtTile;
     if (ph->engine == ENGINE_TC) { bm = kTcBM; bn = kTcBN; }
+    if (ph->engine == ENGINE_TC2) { bm = kTcPairBM; bn = kTcPairBN; }
     if (ph->engine == ENGINE_X3) { bm = kX3BM; bn = kX3BN; }
     const int idx = static_cast<int>(ph->probs.size());
     ph->probs.push_back(p);
@@ -421,17 +422,19 @@ int num_sms() {
 double tile_cost(const GemmPhase& ph, const GemmTile& t) {
   const GemmProblem& p = ph.probs[t.problem];
   if (ph.engine == ENGINE_X3) return (p.K + 31) / 32 + 2.0;
-  return (p.K + kTcBK - 1) / kTcBK + 8.0;
+  return (p.K + kTcBK - 1) / kTcBK + 8.0;   // the pair engine's K block is 64 as well
 }
 
 int finish_phase(GemmPhase& ph) {
   if (ph.engine == ENGINE_CONVERT) return MUON_OK;
-  if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3) {
+  if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3 || ph.engine == ENGINE_TC2) {
     // Longest-processing-time-first assignment of tiles to one persistent
-    // CTA per SM: tiles by decreasing cost, each to the least loaded CTA;
-    // every CTA then runs its tiles contiguously, heaviest first.
+    // CTA per SM (one CTA pair per two SMs for the pair engine): tiles by
+    // decreasing cost, each to the least loaded CTA; every CTA then runs
+    // its tiles contiguously, heaviest first.
     const int n = static_cast<int>(ph.tiles.size());
-    const int nb = std::max(1, std::min(num_sms(), n));
+    const int units = ph.engine == ENGINE_TC2 ? tc2_pairs() : num_sms();
+    const int nb = std::max(1, std::min(units, n));
     std::vector<int> order(n);
     for (int i = 0; i < n; ++i) order[i] = i;
     std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
@@ -462,11 +465,12 @@ int finish_phase(GemmPhase& ph) {
   }
   MUON_CUDA_TRY(upload(ph.d_probs, ph.probs));
   MUON_CUDA_TRY(upload(ph.d_tiles, ph.tiles));
-  if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3) {
+  if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3 || ph.engine == ENGINE_TC2) {
     std::vector<TcMaps> maps(ph.probs.size());
     for (size_t i = 0; i < ph.probs.size(); ++i) {
-      const bool ok = ph.engine == ENGINE_TC ? tc_encode_maps(ph.probs[i], &maps[i])
-                                             : x3_encode_maps(ph.probs[i], &maps[i]);
+      const bool ok = ph.engine == ENGINE_TC    ? tc_encode_maps(ph.probs[i], &maps[i])
+                      : ph.engine == ENGINE_TC2 ? tc2_encode_maps(ph.probs[i], &maps[i])
+                                                : x3_encode_maps(ph.probs[i], &maps[i]);
       if (!ok) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     }
     MUON_CUDA_TRY(upload(ph.d_maps, maps));
@@ -495,9 +499,12 @@ struct WsMat {
 //   P = c R R + b R + a I, Q <- P Q, T = P R, R = T P in FP32 with B read
 //   MN-major (no symmetry assumed: in floating point R and P are not
 //   exactly symmetric); then Y = bf16(Q) X0 (BF16 mode) or Q X0 (FP32 mode).
-// Engines: BF16 operands on the tensor cores (ENGINE_TC); FP32 operands on
-// the tensor cores through split-3 planes (ENGINE_X3); with MUON_GEMM=simt
-// everything runs on the CUDA-core kernel with plain bf16 / fp32 storage.
+// Engines: BF16 operands on the tensor cores, on SM pairs with 256 x 256
+// tiles (ENGINE_TC2) when every block has at least 192 rows, else on single
+// SMs with 128 x 256 tiles (ENGINE_TC; MUON_GEMM=tc1 forces it); FP32
+// operands on the tensor cores through split-3 planes (ENGINE_X3); with
+// MUON_GEMM=simt everything runs on the CUDA-core kernel with plain bf16 /
+// fp32 storage.
 // Element formats and region counts of a plan: X regions (m x n) in xe,
 // the m x m regions in se, nsq of them, and a bf16 copy of Q for the
 // CUDA-core gram path.
@@ -586,7 +593,12 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_
     return PhaseBuilder{P.phases.back().get()};
   };
   // engine for products whose operands have format es
-  auto engine_for = [&](int es) { return !tc ? ENGINE_SIMT : (es == 2 ? ENGINE_TC : ENGINE_X3); };
+  const char* genv = std::getenv("MUON_GEMM");
+  bool pairs = !(genv && std::strcmp(genv, "tc1") == 0);
+  for (const Owner& o : owners)
+    if (o.is_muon && o.m < 192) pairs = false;
+  const int bf16_engine = pairs ? ENGINE_TC2 : ENGINE_TC;
+  auto engine_for = [&](int es) { return !tc ? ENGINE_SIMT : (es == 2 ? bf16_engine : ENGINE_X3); };
 
   if (method == MUON_NS_STANDARD) {
     const int eng = engine_for(xe);
@@ -597,9 +609,10 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_
       for (const Owner& o : owners)
         if (o.is_muon)
           g.add(mk(xm(src, o), xm(src, o), 1, sm(S[0], o, se), none, o.m, o.m, o.n, 1, 1.f, 0.f, 0.f));
-      // B = c A A + b A.  On the BF16 tensor cores every tile is computed:
-      // with the addend in flight the epilogue has no buffer to stage a
-      // mirror, and scattered mirror stores cost more than the lower tiles.
+      // B = c A A + b A.  On single SMs every tile is computed: with the
+      // addend in flight that epilogue has no buffer to stage a mirror, and
+      // scattered mirror stores cost more than the lower tiles.  The pair
+      // engine mirrors through a buffer of its own.
       const int q_sym = eng == ENGINE_TC ? 0 : 1;
       PhaseBuilder q = new_phase(eng, xe);
       for (const Owner& o : owners)
@@ -653,7 +666,7 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_
     PhaseBuilder* yy = nullptr;
     if (bf16 && tc) {
       // bf16(Q) is exactly the hi plane of the split-3 Q
-      PhaseBuilder ph = new_phase(ENGINE_TC, 2);
+      PhaseBuilder ph = new_phase(bf16_engine, 2);
       for (const Owner& o : owners)
         if (o.is_muon) {
           WsMat q = sm(Qcur, o, fe);
@@ -870,7 +883,12 @@ int enqueue_gemms(NsPlan& P, const StepState* state, int* err, cudaStream_t s) {
     }
     PhaseScope sc(MUON_PHASE_NS_GEMM, s, ph->tiles.empty() ? 0 : 1, 0.0, ph->flops);
     if (ph->tiles.empty()) continue;
-    if (ph->engine == ENGINE_TC) {
+    if (ph->engine == ENGINE_TC2) {
+      if (launch_gemm_tc2(ph->d_probs.as<GemmProblem>(), ph->d_maps.as<TcMaps>(),
+                          ph->d_tiles.as<GemmTile>(), ph->d_off.as<int>(),
+                          static_cast<int>(ph->tile_off.size()) - 1, state, err, s) != 0)
+        return fail(MUON_ERR_CUDA, "tensor-core pair GEMM launch setup failed");
+    } else if (ph->engine == ENGINE_TC) {
       if (launch_gemm_tc(ph->d_probs.as<GemmProblem>(), ph->d_maps.as<TcMaps>(),
                          ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()),
                          ph->d_off.as<int>(), static_cast<int>(ph->tile_off.size()) - 1, state, err,

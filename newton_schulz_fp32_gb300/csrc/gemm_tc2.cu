@@ -1,0 +1,342 @@
+// Tensor-core matrix products on SM pairs: tcgen05.mma.cta_group::2 with
+// 256 x 256 output tiles, BF16 operands, FP32 accumulation in the tensor
+// memory of both SMs.
+//
+//   D = alpha * A op(B) + beta * E + gamma * I     (D, E bf16; epilogue fp32)
+//
+// A cluster of two CTAs (one SM pair) walks a host-balanced list of
+// (problem, 256 x 256 tile) pairs.  Per K block of 64, CTA r loads rows
+// [128 r, 128 r + 128) of the A tile and columns [128 r, 128 r + 128) of
+// the B tile into its own shared memory; the even CTA's single MMA thread
+// then issues M=256, N=256 MMAs that read both CTAs' halves, and each CTA
+// ends up holding its 128 rows x 256 columns of the tile in its tensor
+// memory.  Per K block an SM thus loads 32 KB for a 128 x 256 x 64 product
+// (the single-SM kernel loads 48 KB), which is what the main loop is bound
+// by on the smaller problems.
+//
+// Warp roles per CTA:
+//   warp 0      TMA producer (both CTAs), 5-stage ring of 32 KB stages; the
+//               loads of both CTAs complete on the even CTA's full barrier
+//   warp 1      TMEM allocation for the pair (512 columns: two 128 x 256
+//               FP32 accumulators per CTA); in the even CTA also the MMA
+//               issuer, whose commits release both CTAs' stages and
+//               accumulators
+//   warps 2-9   epilogue of this CTA's 128 rows, as in the single-SM kernel
+//               (addend prefetch by TMA, FP32 alpha/beta/gamma, BF16 TMA
+//               stores), with a buffer of its own for the transposed chunk
+//               of symmetric products, so those may carry an addend too
+//
+// Every wait is bounded: after ~2 s without progress a CTA records an error
+// code, stops issuing work, lets its copies in flight land, frees its
+// tensor memory and exits.
+#include <cuda_bf16.h>
+
+#include <cstring>
+
+#include "tc_common.cuh"
+
+namespace muon {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 256, BMC = 128, BN = 256, BK = 64;   // pair tile, rows per CTA
+constexpr int STAGES = 5;
+constexpr int A_BYTES = BMC * BK * 2;         // 16 KB
+constexpr int B_BYTES = (BN / 2) * BK * 2;    // 16 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;
+constexpr int EPI_WARPS = 8;
+constexpr int NTHREADS = 64 + 32 * EPI_WARPS;
+constexpr int EPI_E_BYTES = 32 * 32 * 2;
+constexpr int EPI_D_BYTES = 32 * 64;
+constexpr int EPI_M_BYTES = 32 * 64;                 // mirrored chunk of a symmetric product
+constexpr int EPI_WARP_BYTES = EPI_E_BYTES + EPI_D_BYTES + EPI_M_BYTES;
+constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 256;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(kTcPairBM == BM && kTcPairBN == BN, "tile shape shared with the planner");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps,
+           const GemmTile* __restrict__ tiles, const int* __restrict__ tile_off,
+           const StepState* state, int* err_flag) {
+  // uniform over the pair: both CTAs leave together
+  if (state != nullptr && state->overflow) return;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  uint8_t* epi_base = base_ptr + STAGES * STAGE_BYTES;
+  const uint32_t bar_base = base + STAGES * STAGE_BYTES + EPI_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES + EPI_BYTES);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int i) { return bar_base + 8u * (2 * STAGES + i); };
+  auto tempty_bar = [&](int i) { return bar_base + 8u * (2 * STAGES + 2 + i); };
+  auto e_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + 4 + w); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();      // 0: issues the MMAs
+  const int pair = blockIdx.x >> 1;
+  const int t_begin = tile_off[pair], t_end = tile_off[pair + 1];
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);                 // the even CTA's arrive + both CTAs' bytes
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull_bar(i), 1);
+      mbar_init(tempty_bar(i), 2 * EPI_WARPS);   // epilogue warps of both CTAs
+    }
+    for (int w = 0; w < EPI_WARPS; ++w) mbar_init(e_bar(w), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    // one warp of each CTA of the pair allocates, collectively
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();   // barriers of both CTAs initialised, tensor memory allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int last_problem = -1;
+      for (int ti = t_begin; ti < t_end && !*abort_flag; ++ti) {
+        const GemmTile t = tiles[ti];
+        const GemmProblem& p = probs[t.problem];
+        const TcMaps* mp = maps + t.problem;
+        if (t.problem != last_problem) {
+          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mp->a)));
+          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mp->b)));
+          last_problem = t.problem;
+        }
+        const int nk = (p.K + BK - 1) / BK;
+        const bool b_k = p.b_kmajor != 0;
+        const int row0 = t.tm * BM + static_cast<int>(rank) * BMC;        // this CTA's A rows
+        const int col0 = t.tn * BN + static_cast<int>(rank) * (BN / 2);   // this CTA's B columns
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, err_flag, ERR_TIMEOUT_PRODUCER)) break;
+          const uint32_t sa = base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const uint32_t fb = mapa_shared(full_bar(s), 0);
+          if (rank == 0) mbar_expect_tx(full_bar(s), 2 * STAGE_BYTES);
+          tma_load_2d_pair(sa, &mp->a, kb * BK, row0, fb);
+          if (b_k) {
+            tma_load_2d_pair(sb, &mp->b, kb * BK, col0, fb);
+          } else {
+            #pragma unroll
+            for (int j = 0; j < (BN / 2) / 64; ++j)
+              tma_load_2d_pair(sb + j * (64 * BK * 2), &mp->b, col0 + j * 64, kb * BK, fb);
+          }
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      for (int ti = t_begin; ti < t_end && !*abort_flag; ++ti) {
+        const GemmTile t = tiles[ti];
+        const GemmProblem& p = probs[t.problem];
+        const int nk = (p.K + BK - 1) / BK;
+        const bool b_k = p.b_kmajor != 0;
+        const uint32_t idesc = make_idesc(!b_k, BM, BN);
+        if (!mbar_wait(tempty_bar(acc), acc_ph ^ 1u, abort_flag, err_flag, ERR_TIMEOUT_MMA)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(full_bar(s), ph, abort_flag, err_flag, ERR_TIMEOUT_MMA)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          #pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = make_desc(sa + k * 32, 16, 1024, kSwizzle128);
+            const uint64_t bd = b_k ? make_desc(sb + k * 32, 16, 1024, kSwizzle128)
+                                    : make_desc(sb + k * 16 * 128, 64 * BK * 2, 1024, kSwizzle128);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit_pair(empty_bar(s), 0x3);   // frees this stage in both CTAs
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair(tfull_bar(acc), 0x3);   // both CTAs' accumulators ready
+        acc ^= 1;
+        if (acc == 0) acc_ph ^= 1u;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    const int c_lo = (ew >> 2) * 4;
+    uint8_t* ebuf = epi_base + ew * EPI_WARP_BYTES;
+    uint8_t* dbuf = ebuf + EPI_E_BYTES;
+    uint8_t* mbuf = dbuf + EPI_D_BYTES;
+    const uint32_t ebuf_s = smem_u32(ebuf);
+    const uint32_t dbuf_s = smem_u32(dbuf);
+    const uint32_t mbuf_s = smem_u32(mbuf);
+    uint32_t eph = 0u;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    bool ok = true;
+    for (int ti = t_begin; ti < t_end && ok && !*abort_flag; ++ti) {
+      const GemmTile t = tiles[ti];
+      const GemmProblem& p = probs[t.problem];
+      const TcMaps* mp = maps + t.problem;
+      const int gm0 = t.tm * BM + static_cast<int>(rank) * BMC + q * 32;
+      uint32_t todo = 0;
+      if (gm0 < p.M)
+        for (int c = c_lo; c < c_lo + 4; ++c) {
+          const int gn0 = t.tn * BN + c * 32;
+          if (gn0 < p.N && !(p.symmetric && gn0 < gm0)) todo |= 1u << c;
+        }
+      const bool has_e = p.E != nullptr;
+      if (has_e && todo && lane == 0) {
+        mbar_expect_tx(e_bar(ew), EPI_E_BYTES);
+        tma_load_2d(ebuf_s, &mp->e, t.tn * BN + (__ffs(todo) - 1) * 32, gm0, e_bar(ew));
+      }
+      if (!mbar_wait(tfull_bar(acc), acc_ph, abort_flag, err_flag, ERR_TIMEOUT_EPILOGUE)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t rest = todo;
+      while (rest) {
+        const int c = __ffs(rest) - 1;
+        rest &= rest - 1;
+        const int gn0 = t.tn * BN + c * 32;
+        float x[32];
+        tmem_ld32(tmem_base + static_cast<uint32_t>(acc * BN + c * 32) +
+                      (static_cast<uint32_t>(q * 32) << 16),
+                  x);
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = __fmul_rn(p.alpha, x[j]);
+        if (has_e) {
+          if (!mbar_wait(e_bar(ew), eph, abort_flag, err_flag, ERR_TIMEOUT_EPILOGUE)) {
+            ok = false;
+            break;
+          }
+          eph ^= 1u;
+          #pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint4 w = *reinterpret_cast<const uint4*>(ebuf + sw64(lane, g));
+            const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&w);
+            #pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float2 f = __bfloat1622float2(hh[u]);
+              x[g * 8 + 2 * u] = __fadd_rn(x[g * 8 + 2 * u], __fmul_rn(p.beta, f.x));
+              x[g * 8 + 2 * u + 1] = __fadd_rn(x[g * 8 + 2 * u + 1], __fmul_rn(p.beta, f.y));
+            }
+          }
+          __syncwarp();
+          if (rest && lane == 0) {
+            mbar_expect_tx(e_bar(ew), EPI_E_BYTES);
+            tma_load_2d(ebuf_s, &mp->e, t.tn * BN + (__ffs(rest) - 1) * 32, gm0, e_bar(ew));
+          }
+        }
+        if (p.gamma != 0.f) {
+          #pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (gm0 + lane == gn0 + j) x[j] = __fadd_rn(x[j], p.gamma);
+        }
+        store_chunk(p, mp, x, gm0, gn0, lane, p.symmetric && gn0 == gm0, dbuf, dbuf_s, mbuf,
+                    mbuf_s);
+        __syncwarp();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1u;
+    }
+    if (lane == 0) tma_store_wait_all();
+    __syncwarp();
+  }
+
+  if (*abort_flag) {
+    // an aborted pair may leave loads in flight that target this CTA's (or
+    // the peer's) barriers: let them land before either CTA exits
+    const unsigned long long t0 = globaltimer();
+    while (globaltimer() - t0 < 20000000ull) __nanosleep(100000);
+  }
+  __syncwarp();      // the aligned cluster barrier wants converged warps
+  tc_fence_before();
+  cluster_sync();   // no MMA, load or arrive of the pair is outstanding
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+int g_sms2 = 0;
+
+}  // namespace
+
+bool tc2_encode_maps(const GemmProblem& p, TcMaps* out) {
+  std::memset(out, 0, sizeof(TcMaps));
+  bool ok = encode_2d(&out->a, p.A, 2, p.K, p.M, p.lda, BK, BMC, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (p.b_kmajor)
+    ok = ok && encode_2d(&out->b, p.B, 2, p.K, p.N, p.ldb, BK, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    ok = ok && encode_2d(&out->b, p.B, 2, p.N, p.K, p.ldb, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (p.E != nullptr)
+    ok = ok && p.e_es == 2 &&
+         encode_2d(&out->e, p.E, 2, p.N, p.M, p.lde, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (p.d_es == 6)
+    ok = ok && encode_2d(&out->d, p.D, 2, p.N, p.M, p.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, 3, p.d_ps);
+  else
+    ok = ok && encode_2d(&out->d, p.D, p.d_es, p.N, p.M, p.ldd, p.d_es == 2 ? 32 : 16, 32,
+                         CU_TENSOR_MAP_SWIZZLE_64B);
+  return ok;
+}
+
+int tc2_pairs() {
+  if (g_sms2 == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms2, cudaDevAttrMultiProcessorCount, dev);
+  }
+  return g_sms2 / 2 > 0 ? g_sms2 / 2 : 1;
+}
+
+int launch_gemm_tc2(const GemmProblem* probs, const TcMaps* maps, const GemmTile* tiles,
+                    const int* tile_off, int npairs, const StepState* state, int* err_flag,
+                    cudaStream_t s) {
+  if (npairs <= 0) return 0;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+      return -1;
+    attr_set = true;
+  }
+  k_gemm_tc2<<<2 * npairs, NTHREADS, SMEM_BYTES, s>>>(probs, maps, tiles, tile_off, state, err_flag);
+  return 0;
+}
+
+}  // namespace muon

@@ -229,4 +229,15 @@ int launch_gemm_tc(const GemmProblem* probs, const TcMaps* maps, const GemmTile*
                    int ntiles, const int* tile_off, int nbins, const StepState* state,
                    int* err_flag, cudaStream_t s);
 
+// Tensor-core path on SM pairs (tcgen05 cta_group::2, clusters of two
+// CTAs), BF16 operands, 256 x 256 tiles; pair p runs tiles
+// [tile_off[p], tile_off[p + 1]).
+constexpr int kTcPairBM = 256;
+constexpr int kTcPairBN = 256;
+bool tc2_encode_maps(const GemmProblem& p, TcMaps* out);
+int tc2_pairs();   // SM pairs of the current device
+int launch_gemm_tc2(const GemmProblem* probs, const TcMaps* maps, const GemmTile* tiles,
+                    const int* tile_off, int npairs, const StepState* state, int* err_flag,
+                    cudaStream_t s);
+
 }  // namespace muon
