@@ -535,11 +535,87 @@ int ns_formats(int method, int mode, NsFormats& f) {
   return MUON_OK;
 }
 
-// Builds the GEMM phases of `owners` (their x_off / sq_off index regions of
-// x_elems / sq_elems elements).  The workspace is allocated unless `ext`
-// (at least ws_bytes(x_elems, sq_elems) bytes) is given.
-int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_elems,
-                  int method, int mode, int steps, NsPlan& P, char* ext = nullptr) {
+// Newton-Schulz problems of a plan.  A run of consecutive Muon blocks of
+// one shape whose X0 regions are adjacent is stacked into one problem of up
+// to `cap` rows (the engine's row tile) when the blocks have a multiple of
+// 32 rows: the Gram product of the stack (X X^T, or R = X0 X0^T) is masked
+// to its block diagonal, every later product of the iteration keeps the
+// zeros exactly, and each block's rows of the result are those of its own
+// iteration.  Each problem gets m x m regions of its own (sq_off, ldm).
+struct NsBlocks {
+  std::vector<Owner> probs;                 // m = stacked rows; ns_blk = rows per block
+  std::vector<std::pair<int, int>> members; // first owner index and block count
+  int64_t sq_elems = 0;
+  int cap = 0;
+  bool pairs = false;                       // BF16 products on SM pairs
+};
+
+NsBlocks ns_blocks(const std::vector<Owner>& owners, bool tc, bool bf16, int force_cap) {
+  const char* genv = std::getenv("MUON_GEMM");
+  const bool allow_pairs = tc && bf16 && !(genv && std::strcmp(genv, "tc1") == 0);
+  const char* senv = std::getenv("MUON_STACK");
+  const bool stack = !(senv && std::strcmp(senv, "0") == 0);   // MUON_STACK=0: one block per problem
+  auto group = [&](int cap) {
+    NsBlocks B;
+    if (!stack) cap = 0;
+    B.cap = cap;
+    int last = -2;
+    for (int i = 0; i < static_cast<int>(owners.size()); ++i) {
+      const Owner& o = owners[i];
+      if (!o.is_muon) continue;
+      bool extend = false;
+      if (cap > 0 && last == i - 1 && o.m % 32 == 0 && 2 * o.m <= cap) {
+        const Owner& prev = owners[i - 1];
+        extend = prev.m == o.m && prev.n == o.n && prev.ldx == o.ldx &&
+                 o.x_off == prev.x_off + int64_t(prev.m) * prev.ldx &&
+                 B.probs.back().m + o.m <= cap && B.probs.back().ns_blk == o.m;
+      }
+      if (extend) {
+        B.probs.back().m += o.m;
+        B.members.back().second += 1;
+      } else {
+        Owner q = o;
+        q.ns_blk = o.m;
+        B.probs.push_back(q);
+        B.members.push_back({i, 1});
+      }
+      last = i;
+    }
+    for (size_t k = 0; k < B.probs.size(); ++k) {
+      Owner& q = B.probs[k];
+      if (B.members[k].second == 1) q.ns_blk = 0;
+      q.ldm = static_cast<int32_t>(round_up(q.m, 8));
+      q.sq_off = B.sq_elems;
+      B.sq_elems += round_up(int64_t(q.m) * q.ldm, 64);
+    }
+    return B;
+  };
+  if (!tc) return group(0);
+  if (force_cap >= 0) {
+    NsBlocks B = group(force_cap);
+    B.pairs = allow_pairs && force_cap == kTcPairBM;
+    return B;
+  }
+  if (allow_pairs) {
+    NsBlocks B = group(kTcPairBM);
+    bool ok = true;
+    for (const Owner& q : B.probs) ok = ok && q.m >= 192;   // a 256-row tile at least 3/4 used
+    if (ok) {
+      B.pairs = true;
+      return B;
+    }
+  }
+  return group(128);
+}
+
+// Builds the GEMM phases of `owners` (their x_off index an X region of
+// x_elems elements; the m x m regions are laid out per NS problem).  The
+// workspace is allocated unless `ext` is given, in which case the m x m
+// regions hold ext_sq elements (at least the problems' need) and the
+// problems are stacked with rows cap `force_cap`.
+int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method, int mode,
+                  int steps, NsPlan& P, char* ext = nullptr, int64_t ext_sq = 0,
+                  int force_cap = -1) {
   const bool bf16 = mode == MUON_OPERANDS_BF16;
   NsFormats F;
   int rc0 = ns_formats(method, mode, F);
@@ -550,6 +626,13 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_
   const bool need_qbf = F.need_qbf;
   auto bytes_of = NsFormats::bytes_of;
   auto eb = [](int es) { return int64_t(es == 6 ? 2 : es); };
+  const NsBlocks NB = ns_blocks(owners, tc, bf16, force_cap);
+  const std::vector<Owner>& probs = NB.probs;
+  int64_t sq_elems = NB.sq_elems;
+  if (ext) {
+    if (ext_sq < sq_elems) return fail(MUON_ERR_INVALID, "internal: wave workspace too small");
+    sq_elems = ext_sq;
+  }
   P.esize = xe;
   P.x_ps = xe == 6 ? x_elems : 0;
   P.method = method;
@@ -593,11 +676,12 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_
     return PhaseBuilder{P.phases.back().get()};
   };
   // engine for products whose operands have format es
-  const char* genv = std::getenv("MUON_GEMM");
-  bool pairs = !(genv && std::strcmp(genv, "tc1") == 0);
-  for (const Owner& o : owners)
-    if (o.is_muon && o.m < 192) pairs = false;
-  const int bf16_engine = pairs ? ENGINE_TC2 : ENGINE_TC;
+  const int bf16_engine = NB.pairs ? ENGINE_TC2 : ENGINE_TC;
+  // Gram products of stacked blocks are masked to the block diagonal
+  auto gram = [](GemmProblem p, const Owner& o) {
+    p.blk = o.ns_blk;
+    return p;
+  };
   auto engine_for = [&](int es) { return !tc ? ENGINE_SIMT : (es == 2 ? bf16_engine : ENGINE_X3); };
 
   if (method == MUON_NS_STANDARD) {
@@ -606,21 +690,22 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_
       char* src = X[st & 1];
       char* dst = X[(st + 1) & 1];
       PhaseBuilder g = new_phase(eng, xe);   // A = X X^T
-      for (const Owner& o : owners)
+      for (const Owner& o : probs)
         if (o.is_muon)
-          g.add(mk(xm(src, o), xm(src, o), 1, sm(S[0], o, se), none, o.m, o.m, o.n, 1, 1.f, 0.f, 0.f));
+          g.add(gram(mk(xm(src, o), xm(src, o), 1, sm(S[0], o, se), none, o.m, o.m, o.n, 1, 1.f, 0.f,
+                        0.f), o));
       // B = c A A + b A.  On single SMs every tile is computed: with the
       // addend in flight that epilogue has no buffer to stage a mirror, and
       // scattered mirror stores cost more than the lower tiles.  The pair
       // engine mirrors through a buffer of its own.
       const int q_sym = eng == ENGINE_TC ? 0 : 1;
       PhaseBuilder q = new_phase(eng, xe);
-      for (const Owner& o : owners)
+      for (const Owner& o : probs)
         if (o.is_muon)
           q.add(mk(sm(S[0], o, se), sm(S[0], o, se), 1, sm(S[1], o, se), sm(S[0], o, se), o.m, o.m,
                    o.m, q_sym, c, b, 0.f));
       PhaseBuilder u = new_phase(eng, xe);   // X' = B X + a X
-      for (const Owner& o : owners)
+      for (const Owner& o : probs)
         if (o.is_muon)
           u.add(mk(sm(S[1], o, se), xm(src, o), 0, xm(dst, o), xm(src, o), o.m, o.n, o.m, 0, 1.f, a,
                    0.f));
@@ -630,21 +715,22 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_
     char *R = S[0], *Pm = S[1], *Qa = S[2], *Qb = S[3], *T = S[4];
     const int rec = tc ? ENGINE_X3 : ENGINE_SIMT;
     PhaseBuilder g0 = new_phase(engine_for(xe), xe);   // R = X0 X0^T
-    for (const Owner& o : owners)
+    for (const Owner& o : probs)
       if (o.is_muon)
-        g0.add(mk(xm(X[0], o), xm(X[0], o), 1, sm(R, o, fe), none, o.m, o.m, o.n, 1, 1.f, 0.f, 0.f));
+        g0.add(gram(mk(xm(X[0], o), xm(X[0], o), 1, sm(R, o, fe), none, o.m, o.m, o.n, 1, 1.f, 0.f,
+                       0.f), o));
     char* Qcur = Qa;
     for (int k = 0; k < steps; ++k) {
       char* Pk = (k == 0) ? Qa : Pm;   // Q1 = P0 (Q0 = I)
       PhaseBuilder pp = new_phase(rec, fe);   // P = c R R + b R + a I
-      for (const Owner& o : owners)
+      for (const Owner& o : probs)
         if (o.is_muon)
           pp.add(mk(sm(R, o, fe), sm(R, o, fe), 0, sm(Pk, o, fe), sm(R, o, fe), o.m, o.m, o.m, 0, c, b,
                     a));
       if (k > 0) {
         char* Qn = (Qcur == Qa) ? Qb : Qa;
         PhaseBuilder qq = new_phase(rec, fe);   // Q <- P Q
-        for (const Owner& o : owners)
+        for (const Owner& o : probs)
           if (o.is_muon)
             qq.add(mk(sm(Pk, o, fe), sm(Qcur, o, fe), 0, sm(Qn, o, fe), none, o.m, o.m, o.m, 0, 1.f,
                       0.f, 0.f));
@@ -652,12 +738,12 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_
       }
       if (k < steps - 1) {
         PhaseBuilder tt = new_phase(rec, fe);   // T = P R
-        for (const Owner& o : owners)
+        for (const Owner& o : probs)
           if (o.is_muon)
             tt.add(mk(sm(Pk, o, fe), sm(R, o, fe), 0, sm(T, o, fe), none, o.m, o.m, o.m, 0, 1.f, 0.f,
                       0.f));
         PhaseBuilder rr = new_phase(rec, fe);   // R = T P
-        for (const Owner& o : owners)
+        for (const Owner& o : probs)
           if (o.is_muon)
             rr.add(mk(sm(T, o, fe), sm(Pk, o, fe), 0, sm(R, o, fe), none, o.m, o.m, o.m, 0, 1.f, 0.f,
                       0.f));
@@ -667,7 +753,7 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_
     if (bf16 && tc) {
       // bf16(Q) is exactly the hi plane of the split-3 Q
       PhaseBuilder ph = new_phase(bf16_engine, 2);
-      for (const Owner& o : owners)
+      for (const Owner& o : probs)
         if (o.is_muon) {
           WsMat q = sm(Qcur, o, fe);
           q.es = 2;
@@ -683,13 +769,13 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int64_t sq_
       cv.conv_dst = Qbf;
       cv.conv_n = sq_elems;
       PhaseBuilder ph = new_phase(ENGINE_SIMT, 2);
-      for (const Owner& o : owners)
+      for (const Owner& o : probs)
         if (o.is_muon)
           ph.add(mk(WsMat{Qbf + 2 * o.sq_off, 2, 0, o.ldm}, xm(X[0], o), 0, xm(X[1], o), none, o.m,
                     o.n, o.m, 0, 1.f, 0.f, 0.f));
     } else {   // FP32 mode: Y = Q X0 in FP32 (split-3 or fp32)
       PhaseBuilder ph = new_phase(engine_for(xe), xe);
-      for (const Owner& o : owners)
+      for (const Owner& o : probs)
         if (o.is_muon)
           ph.add(mk(sm(Qcur, o, fe), xm(X[0], o), 0, xm(X[1], o), none, o.m, o.n, o.m, 0, 1.f, 0.f,
                     0.f));
@@ -783,36 +869,41 @@ int get_table_plan(const muon_param_t* params, int nparams, const muon_partition
   return MUON_OK;
 }
 
-// Splits the Muon owners, in order, into waves whose workspace fits
-// `budget` bytes (an owner larger than the budget is a wave of its own) and
-// builds one plan per wave over a shared workspace.
+// Splits the NS problems (stacks of Muon blocks, in owner order) into waves
+// whose workspace fits `budget` bytes (a problem larger than the budget is
+// a wave of its own) and builds one plan per wave over a shared workspace.
 int build_wave_plan(const Layout& L, int method, int mode, int steps, uint64_t budget, NsPlan& P) {
   NsFormats F;
   int rc = ns_formats(method, mode, F);
   if (rc != MUON_OK) return rc;
+  const NsBlocks NB = ns_blocks(L.owners, F.tc, mode == MUON_OPERANDS_BF16, -1);
   // The shared workspace holds the largest wave's m x n regions and the
   // largest wave's m x m regions, which may come from different waves, so
-  // an owner joins the current wave only while those running maxima still
+  // a problem joins the current wave only while those running maxima still
   // fit the budget.
   std::vector<Owner> owners = L.owners;
-  std::vector<std::vector<int>> waves;
+  std::vector<std::vector<int>> waves;   // owner indices per wave
   int64_t cx = 0, csq = 0, mx = 0, msq = 0;
-  for (int i = 0; i < static_cast<int>(owners.size()); ++i) {
-    Owner& o = owners[i];
-    if (!o.is_muon) continue;
-    const int64_t ox = round_up(int64_t(o.m) * o.ldx, 64), osq = round_up(int64_t(o.m) * o.ldm, 64);
+  for (size_t k = 0; k < NB.probs.size(); ++k) {
+    const Owner& q = NB.probs[k];
+    const int first = NB.members[k].first, count = NB.members[k].second;
+    int64_t ox = 0;
+    for (int i = first; i < first + count; ++i)
+      ox += round_up(int64_t(owners[i].m) * owners[i].ldx, 64);
+    const int64_t osq = round_up(int64_t(q.m) * q.ldm, 64);
     if (waves.empty() ||
         F.ws_bytes(std::max(mx, cx + ox), std::max(msq, csq + osq)) > budget) {
       waves.emplace_back();
       cx = csq = 0;
     }
-    o.x_off = cx;
-    o.sq_off = csq;
-    cx += ox;
+    for (int i = first; i < first + count; ++i) {   // members stay adjacent
+      owners[i].x_off = cx;
+      cx += round_up(int64_t(owners[i].m) * owners[i].ldx, 64);
+      waves.back().push_back(i);
+    }
     csq += osq;
     mx = std::max(mx, cx);
     msq = std::max(msq, csq);
-    waves.back().push_back(i);
   }
   MUON_CUDA_TRY(P.ws.alloc(F.ws_bytes(mx, msq) + 256));
   MUON_CUDA_TRY(upload(P.d_owners, owners));
@@ -834,7 +925,7 @@ int build_wave_plan(const Layout& L, int method, int mode, int steps, uint64_t b
     std::vector<Owner> wo;
     for (int i : waves[w]) wo.push_back(owners[i]);
     std::unique_ptr<NsPlan> sub(new NsPlan());
-    rc = build_ns_plan(wo, mx, msq, method, mode, steps, *sub, P.ws.as<char>());
+    rc = build_ns_plan(wo, mx, method, mode, steps, *sub, P.ws.as<char>(), msq, NB.cap);
     if (rc != MUON_OK) return rc;
     P.flops += sub->flops;
     P.x0 = sub->x0;
@@ -858,7 +949,7 @@ int get_ns_plan(TablePlan& tp, int method, int mode, int steps, uint64_t budget,
   }
   std::unique_ptr<NsPlan> P(new NsPlan());
   int rc = budget ? build_wave_plan(tp.L, method, mode, steps, budget, *P)
-                  : build_ns_plan(tp.L.owners, tp.L.x_elems, tp.L.sq_elems, method, mode, steps, *P);
+                  : build_ns_plan(tp.L.owners, tp.L.x_elems, method, mode, steps, *P);
   if (rc != MUON_OK) return rc;
   *out = P.get();
   tp.ns[k] = std::move(P);
@@ -1230,7 +1321,7 @@ extern "C" int muon_newton_schulz(const void* X, void* Y, int rows, int cols, in
     MUON_CUDA_TRY(np->tile_sum.alloc(sizeof(double) * (np->ntiles + 1)));
     MUON_CUDA_TRY(np->err.alloc(sizeof(int)));
     MUON_CUDA_TRY(cudaMemset(np->err.p, 0, sizeof(int)));
-    rc = build_ns_plan(np->owners, np->x_elems, np->sq_elems, ns_method, operand_mode, ns_steps,
+    rc = build_ns_plan(np->owners, np->x_elems, ns_method, operand_mode, ns_steps,
                        np->ns);
     if (rc != MUON_OK) return rc;
     sp = np.get();

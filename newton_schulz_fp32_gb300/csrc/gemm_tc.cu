@@ -229,6 +229,10 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
                   x);
         #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] = __fmul_rn(p.alpha, x[j]);
+        if (p.blk != 0 && gm0 / p.blk != gn0 / p.blk) {   // across stacked blocks
+          #pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = 0.f;
+        }
         if (has_e) {
           if (!mbar_wait(e_bar(ew), eph, abort_flag, err_flag, ERR_TIMEOUT_EPILOGUE)) {
             ok = false;

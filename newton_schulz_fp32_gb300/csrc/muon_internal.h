@@ -53,6 +53,8 @@ struct Owner {
   int32_t ldm;          // leading dimension of the m x m workspace matrices
   int64_t x_off;        // element offset of this owner in each m x n region
   int64_t sq_off;       // element offset of this owner in each m x m region
+  int32_t ns_blk;       // NS plans only: rows per stacked block (0: not stacked)
+  int32_t ns_pad;
 };
 
 // Pass-1 tile: owner elements [rel_begin, rel_begin + len).  Thread t sums
@@ -125,7 +127,10 @@ struct GemmProblem {
   int32_t symmetric;
   float alpha, beta, gamma;
   int32_t d_es, e_es;   // 2 bf16, 4 fp32, 6 split-3 (three bf16 planes)
-  int32_t pad;
+  // > 0: the problem stacks independent blocks of `blk` rows (a multiple of
+  // 32); output chunks whose row and column fall in different blocks are
+  // written as zeros (Gram products of stacked blocks)
+  int32_t blk;
   // split-3 operands: element distance between the hi, mid and lo planes
   int64_t a_ps, b_ps, d_ps, e_ps;
 };

@@ -369,3 +369,35 @@ def test_llama3_8b_config_sampled(torch):
     nsg.release_workspace()
     torch.cuda.empty_cache()
     assert nsg.device_error() == 0
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+@pytest.mark.parametrize("mode", ["bf16", "fp32"])
+def test_stacked_head_blocks_match_separate_blocks(torch, method, mode):
+    """Consecutive equal head blocks (GPT-2 Q/K: 12 blocks of 64 x 768) run
+    stacked into block-diagonal problems of up to 256 rows; the step must
+    agree with one problem per block (MUON_STACK=0) within the operand
+    mode's rule, and both with the oracle on a sampled block."""
+    lay = wl.gpt2_small_layout(layers=1, nparts=2)
+    seed = 77
+    g = wl.gaussian_grads(lay, seed, 0, wl.loguniform_sigmas(lay, seed, 1e-3, 1e-1))
+    m = wl.gaussian_grads(lay, seed, 1, None, bf16=False)
+    outs = []
+    for stack in ("1", "0"):
+        nsg.release_workspace()
+        os.environ["MUON_STACK"] = stack
+        try:
+            st = GpuState(torch, wl.pack(lay, g), wl.pack(lay, m), wl.pack(lay, m))
+            before = st.numpy()
+            nsg.step(st.accum, st.momentum, st.master, lay.params, lay.parts, BETA, LR, method, 5,
+                     0.0, mode)
+            outs.append(wl.unpack(lay, st.accum.cpu().numpy()))
+        finally:
+            os.environ.pop("MUON_STACK", None)
+            nsg.release_workspace()
+    for k, spec in enumerate(lay.specs):
+        assert_close_update(outs[0][k], outs[1][k], mode, f"stacked vs separate {spec.name}")
+    res = om.muon_step_flat(*before, lay.params, lay.parts, BETA, LR, method, 5, 0.0,
+                            ORACLE_MODE[mode])
+    want = wl.unpack(lay, res[0])
+    assert_close_update(outs[0][0], want[0], mode, "stacked Q vs oracle")
