@@ -386,16 +386,36 @@ struct NsPlan {
   std::vector<std::unique_ptr<NsPlan>> waves;
   std::vector<WaveRange> ranges;
   DevBuf d_owners;
+  // Sums of squares of the update, written by the last product's epilogue
+  // (per tile and epilogue warp, problems in owner order; null when the
+  // last product runs on the CUDA cores)
+  DevBuf ssq;
+  double* ssq_ptr = nullptr;
+  int64_t n_ssq = 0;
 };
+
+void engine_tile(int engine, int& bm, int& bn) {
+  bm = bn = kSimtTile;
+  if (engine == ENGINE_TC) { bm = kTcBM; bn = kTcBN; }
+  if (engine == ENGINE_TC2) { bm = kTcPairBM; bn = kTcPairBN; }
+  if (engine == ENGINE_X3) { bm = kX3BM; bn = kX3BN; }
+}
+
+// Slots of the fused sums of squares for problems of m x n outputs.
+int64_t ssq_slots(int engine, int m, int n) {
+  int bm, bn;
+  engine_tile(engine, bm, bn);
+  return int64_t((m + bm - 1) / bm) * ((n + bn - 1) / bn) * kSsqSlots;
+}
 
 // Adds one GEMM D = alpha A op(B) + beta E + gamma I (per block) to a phase.
 struct PhaseBuilder {
   GemmPhase* ph;
-  void add(const GemmProblem& p) {
-    int bm = kSimtTile, bn = kSimtTile;
-    if (ph->engine == ENGINE_TC) { bm = kTcBM; bn = kTcBN; }
-    if (ph->engine == ENGINE_TC2) { bm = kTcPairBM; bn = kTcPairBN; }
-    if (ph->engine == ENGINE_X3) { bm = kX3BM; bn = kX3BN; }
+  // useful: the fraction of the product's 2 M N K flops that is algorithmic
+  // work (stacked blocks: rows per block / stacked rows)
+  void add(const GemmProblem& p, double useful = 1.0) {
+    int bm, bn;
+    engine_tile(ph->engine, bm, bn);
     const int idx = static_cast<int>(ph->probs.size());
     ph->probs.push_back(p);
     const int tm_n = (p.M + bm - 1) / bm, tn_n = (p.N + bn - 1) / bn;
@@ -404,7 +424,7 @@ struct PhaseBuilder {
         if (p.symmetric && tn * bn + bn - 1 < tm * bm) continue;   // strictly lower tile
         ph->tiles.push_back({idx, tm, tn});
       }
-    ph->flops += 2.0 * p.M * double(p.N) * p.K;
+    ph->flops += 2.0 * p.M * double(p.N) * p.K * useful;
   }
 };
 
@@ -615,7 +635,7 @@ NsBlocks ns_blocks(const std::vector<Owner>& owners, bool tc, bool bf16, int for
 // problems are stacked with rows cap `force_cap`.
 int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method, int mode,
                   int steps, NsPlan& P, char* ext = nullptr, int64_t ext_sq = 0,
-                  int force_cap = -1) {
+                  int force_cap = -1, double* ext_ssq = nullptr) {
   const bool bf16 = mode == MUON_OPERANDS_BF16;
   NsFormats F;
   int rc0 = ns_formats(method, mode, F);
@@ -677,6 +697,7 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
   };
   // engine for products whose operands have format es
   const int bf16_engine = NB.pairs ? ENGINE_TC2 : ENGINE_TC;
+  auto fs = [](const Owner& o) { return o.ns_blk ? double(o.ns_blk) / o.m : 1.0; };
   // Gram products of stacked blocks are masked to the block diagonal
   auto gram = [](GemmProblem p, const Owner& o) {
     p.blk = o.ns_blk;
@@ -693,7 +714,7 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
       for (const Owner& o : probs)
         if (o.is_muon)
           g.add(gram(mk(xm(src, o), xm(src, o), 1, sm(S[0], o, se), none, o.m, o.m, o.n, 1, 1.f, 0.f,
-                        0.f), o));
+                        0.f), o), fs(o));
       // B = c A A + b A.  On single SMs every tile is computed: with the
       // addend in flight that epilogue has no buffer to stage a mirror, and
       // scattered mirror stores cost more than the lower tiles.  The pair
@@ -703,12 +724,12 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
       for (const Owner& o : probs)
         if (o.is_muon)
           q.add(mk(sm(S[0], o, se), sm(S[0], o, se), 1, sm(S[1], o, se), sm(S[0], o, se), o.m, o.m,
-                   o.m, q_sym, c, b, 0.f));
+                   o.m, q_sym, c, b, 0.f), fs(o));
       PhaseBuilder u = new_phase(eng, xe);   // X' = B X + a X
       for (const Owner& o : probs)
         if (o.is_muon)
           u.add(mk(sm(S[1], o, se), xm(src, o), 0, xm(dst, o), xm(src, o), o.m, o.n, o.m, 0, 1.f, a,
-                   0.f));
+                   0.f), fs(o));
     }
     P.y = X[steps & 1];
   } else {
@@ -718,7 +739,7 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
     for (const Owner& o : probs)
       if (o.is_muon)
         g0.add(gram(mk(xm(X[0], o), xm(X[0], o), 1, sm(R, o, fe), none, o.m, o.m, o.n, 1, 1.f, 0.f,
-                       0.f), o));
+                       0.f), o), fs(o));
     char* Qcur = Qa;
     for (int k = 0; k < steps; ++k) {
       char* Pk = (k == 0) ? Qa : Pm;   // Q1 = P0 (Q0 = I)
@@ -726,14 +747,14 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
       for (const Owner& o : probs)
         if (o.is_muon)
           pp.add(mk(sm(R, o, fe), sm(R, o, fe), 0, sm(Pk, o, fe), sm(R, o, fe), o.m, o.m, o.m, 0, c, b,
-                    a));
+                    a), fs(o));
       if (k > 0) {
         char* Qn = (Qcur == Qa) ? Qb : Qa;
         PhaseBuilder qq = new_phase(rec, fe);   // Q <- P Q
         for (const Owner& o : probs)
           if (o.is_muon)
             qq.add(mk(sm(Pk, o, fe), sm(Qcur, o, fe), 0, sm(Qn, o, fe), none, o.m, o.m, o.m, 0, 1.f,
-                      0.f, 0.f));
+                      0.f, 0.f), fs(o));
         Qcur = Qn;
       }
       if (k < steps - 1) {
@@ -741,12 +762,12 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
         for (const Owner& o : probs)
           if (o.is_muon)
             tt.add(mk(sm(Pk, o, fe), sm(R, o, fe), 0, sm(T, o, fe), none, o.m, o.m, o.m, 0, 1.f, 0.f,
-                      0.f));
+                      0.f), fs(o));
         PhaseBuilder rr = new_phase(rec, fe);   // R = T P
         for (const Owner& o : probs)
           if (o.is_muon)
             rr.add(mk(sm(T, o, fe), sm(Pk, o, fe), 0, sm(R, o, fe), none, o.m, o.m, o.m, 0, 1.f, 0.f,
-                      0.f));
+                      0.f), fs(o));
       }
     }
     PhaseBuilder* yy = nullptr;
@@ -758,7 +779,7 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
           WsMat q = sm(Qcur, o, fe);
           q.es = 2;
           q.ps = 0;
-          ph.add(mk(q, xm(X[0], o), 0, xm(X[1], o), none, o.m, o.n, o.m, 0, 1.f, 0.f, 0.f));
+          ph.add(mk(q, xm(X[0], o), 0, xm(X[1], o), none, o.m, o.n, o.m, 0, 1.f, 0.f, 0.f), fs(o));
         }
       yy = nullptr;
     } else if (need_qbf) {   // CUDA-core path: round Q to bf16, then Y = Q X0
@@ -772,16 +793,38 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
       for (const Owner& o : probs)
         if (o.is_muon)
           ph.add(mk(WsMat{Qbf + 2 * o.sq_off, 2, 0, o.ldm}, xm(X[0], o), 0, xm(X[1], o), none, o.m,
-                    o.n, o.m, 0, 1.f, 0.f, 0.f));
+                    o.n, o.m, 0, 1.f, 0.f, 0.f), fs(o));
     } else {   // FP32 mode: Y = Q X0 in FP32 (split-3 or fp32)
       PhaseBuilder ph = new_phase(engine_for(xe), xe);
       for (const Owner& o : probs)
         if (o.is_muon)
           ph.add(mk(sm(Qcur, o, fe), xm(X[0], o), 0, xm(X[1], o), none, o.m, o.n, o.m, 0, 1.f, 0.f,
-                    0.f));
+                    0.f), fs(o));
     }
     (void)yy;
     P.y = X[1];
+  }
+  // The last product's epilogue writes the sums of squares of the update,
+  // problems in owner order (into ext_ssq for a wave of a bounded plan).
+  if (!P.phases.empty()) {
+    GemmPhase& last = *P.phases.back();
+    if (last.engine == ENGINE_TC || last.engine == ENGINE_TC2 || last.engine == ENGINE_X3) {
+      int64_t n = 0;
+      for (const GemmProblem& q : last.probs) n += ssq_slots(last.engine, q.M, q.N);
+      double* buf = ext_ssq;
+      if (buf == nullptr) {
+        MUON_CUDA_TRY(P.ssq.alloc(sizeof(double) * std::max<int64_t>(n, 1)));
+        MUON_CUDA_TRY(cudaMemset(P.ssq.p, 0, sizeof(double) * std::max<int64_t>(n, 1)));
+        buf = P.ssq.as<double>();
+      }
+      int64_t off = 0;
+      for (GemmProblem& q : last.probs) {
+        q.ssq = buf + off;
+        off += ssq_slots(last.engine, q.M, q.N);
+      }
+      P.ssq_ptr = buf;
+      P.n_ssq = n;
+    }
   }
   for (auto& ph : P.phases) {
     int rc = finish_phase(*ph);
@@ -883,6 +926,7 @@ int build_wave_plan(const Layout& L, int method, int mode, int steps, uint64_t b
   // fit the budget.
   std::vector<Owner> owners = L.owners;
   std::vector<std::vector<int>> waves;   // owner indices per wave
+  std::vector<size_t> wave_prob0;        // first problem of each wave
   int64_t cx = 0, csq = 0, mx = 0, msq = 0;
   for (size_t k = 0; k < NB.probs.size(); ++k) {
     const Owner& q = NB.probs[k];
@@ -894,6 +938,7 @@ int build_wave_plan(const Layout& L, int method, int mode, int steps, uint64_t b
     if (waves.empty() ||
         F.ws_bytes(std::max(mx, cx + ox), std::max(msq, csq + osq)) > budget) {
       waves.emplace_back();
+      wave_prob0.push_back(k);
       cx = csq = 0;
     }
     for (int i = first; i < first + count; ++i) {   // members stay adjacent
@@ -907,6 +952,21 @@ int build_wave_plan(const Layout& L, int method, int mode, int steps, uint64_t b
   }
   MUON_CUDA_TRY(P.ws.alloc(F.ws_bytes(mx, msq) + 256));
   MUON_CUDA_TRY(upload(P.d_owners, owners));
+  // fused sums of squares of all waves in one buffer, problems in owner order
+  const int last_engine = !F.tc ? ENGINE_SIMT
+                          : (mode == MUON_OPERANDS_BF16 ? (NB.pairs ? ENGINE_TC2 : ENGINE_TC)
+                                                        : ENGINE_X3);
+  std::vector<int64_t> ssq_off(NB.probs.size() + 1, 0);
+  for (size_t k = 0; k < NB.probs.size(); ++k)
+    ssq_off[k + 1] = ssq_off[k] + (last_engine == ENGINE_SIMT ? 0
+                                   : ssq_slots(last_engine, NB.probs[k].m, NB.probs[k].n));
+  if (last_engine != ENGINE_SIMT) {
+    const int64_t n = std::max<int64_t>(ssq_off.back(), 1);
+    MUON_CUDA_TRY(P.ssq.alloc(sizeof(double) * n));
+    MUON_CUDA_TRY(cudaMemset(P.ssq.p, 0, sizeof(double) * n));
+    P.ssq_ptr = P.ssq.as<double>();
+    P.n_ssq = ssq_off.back();
+  }
   P.esize = F.xe;
   P.x_ps = F.xe == 6 ? mx : 0;
   P.use_tc = F.tc;
@@ -925,7 +985,8 @@ int build_wave_plan(const Layout& L, int method, int mode, int steps, uint64_t b
     std::vector<Owner> wo;
     for (int i : waves[w]) wo.push_back(owners[i]);
     std::unique_ptr<NsPlan> sub(new NsPlan());
-    rc = build_ns_plan(wo, mx, method, mode, steps, *sub, P.ws.as<char>(), msq, NB.cap);
+    rc = build_ns_plan(wo, mx, method, mode, steps, *sub, P.ws.as<char>(), msq, NB.cap,
+                       P.ssq_ptr ? P.ssq_ptr + ssq_off[wave_prob0[w]] : nullptr);
     if (rc != MUON_OK) return rc;
     P.flops += sub->flops;
     P.x0 = sub->x0;
@@ -1201,9 +1262,15 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
     rc = enqueue_gemms(*P, a.state, tp->d_err.as<int>(), s);
     if (rc != MUON_OK) return rc;
     {
-      PhaseScope sc(MUON_PHASE_NORM, s, (a.n_ytiles && !pre ? 1 : 0) + 1, pre ? 0.0 : me * P->esize,
-                    0.0);
-      if (!pre) launch_update_sumsq(a, s);
+      const bool fused = P->ssq_ptr != nullptr;   // the last product summed the squares
+      PhaseScope sc(MUON_PHASE_NORM, s, (a.n_ytiles && !pre && !fused ? 1 : 0) + 1,
+                    pre || fused ? 0.0 : me * P->esize, 0.0);
+      if (fused) {
+        a.ytile_sum = P->ssq_ptr;
+        a.n_ytiles = static_cast<int>(P->n_ssq);
+      } else if (!pre) {
+        launch_update_sumsq(a, s);
+      }
       launch_finalize(a, s);
     }
     {
@@ -1228,7 +1295,7 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
       }
       rc = enqueue_gemms(*P->waves[w], a.state, tp->d_err.as<int>(), s);
       if (rc != MUON_OK) return rc;
-      if (!pre) {
+      if (!pre && P->ssq_ptr == nullptr) {
         b.ytiles = tp->d_ytiles.as<YTile>() + R.y0;
         b.ytile_sum = tp->d_ysum.as<double>() + R.y0;
         b.n_ytiles = R.y1 - R.y0;
@@ -1245,6 +1312,10 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
       }
     }
     {
+      if (P->ssq_ptr != nullptr) {
+        a.ytile_sum = P->ssq_ptr;
+        a.n_ytiles = static_cast<int>(P->n_ssq);
+      }
       PhaseScope sc(MUON_PHASE_NORM, s, 1, 0.0, 0.0);
       launch_finalize(a, s);
     }

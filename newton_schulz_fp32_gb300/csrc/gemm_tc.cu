@@ -218,6 +218,7 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
         break;
       }
       tc_fence_after();
+      float ssq = 0.f;   // this warp's sum of squares of the tile (last product only)
       uint32_t rest = todo;
       while (rest) {
         const int c = __ffs(rest) - 1;
@@ -261,12 +262,16 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
           for (int j = 0; j < 32; ++j)
             if (gm0 + lane == gn0 + j) x[j] = __fadd_rn(x[j], p.gamma);
         }
+        if (p.ssq != nullptr) ssq = chunk_sumsq(x, p.d_es, ssq);
         // without an addend the E buffer doubles as the mirror's staging box
         store_chunk(p, mp, x, gm0, gn0, lane, p.symmetric && gn0 == gm0, dbuf, dbuf_s,
                     has_e ? nullptr : ebuf, ebuf_s);
         __syncwarp();
       }
       ebuf_mirrored = !has_e && p.symmetric;
+      if (p.ssq != nullptr)
+        warp_sumsq_store(p.ssq + (int64_t(t.tm) * ((p.N + BN - 1) / BN) + t.tn) * kSsqSlots + ew, ssq,
+                         lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));

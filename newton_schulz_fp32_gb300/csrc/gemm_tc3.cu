@@ -220,6 +220,7 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
         break;
       }
       tc_fence_after();
+      float ssq = 0.f;   // this warp's sum of squares of the tile (last product only)
       uint32_t rest = todo;
       while (rest) {
         const int c = __ffs(rest) - 1;
@@ -271,9 +272,13 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
           for (int j = 0; j < 32; ++j)
             if (gm0 + lane == gn0 + j) x[j] = __fadd_rn(x[j], p.gamma);
         }
+        if (p.ssq != nullptr) ssq = chunk_sumsq(x, p.d_es, ssq);
         store_chunk(p, mp, x, gm0, gn0, lane, p.symmetric && gn0 == gm0, dbuf, dbuf_s);
         __syncwarp();
       }
+      if (p.ssq != nullptr)
+        warp_sumsq_store(p.ssq + (int64_t(t.tm) * ((p.N + BN - 1) / BN) + t.tn) * kSsqSlots + ew, ssq,
+                         lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(0));

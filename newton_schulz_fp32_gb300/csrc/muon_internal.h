@@ -133,7 +133,12 @@ struct GemmProblem {
   int32_t blk;
   // split-3 operands: element distance between the hi, mid and lo planes
   int64_t a_ps, b_ps, d_ps, e_ps;
+  // non-null on the last product of the iteration: each epilogue warp writes
+  // the sum of squares of the values it stored (as stored: bf16-rounded for
+  // bf16 outputs) to ssq[(tm * tiles_n + tn) * kSsqSlots + its slot]
+  double* ssq;
 };
+constexpr int kSsqSlots = 16;   // per output tile: 2 CTAs x 8 epilogue warps at most
 
 struct GemmTile {
   int32_t problem;

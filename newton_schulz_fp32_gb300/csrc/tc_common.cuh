@@ -374,6 +374,27 @@ __device__ __forceinline__ void store_chunk(const GemmProblem& p, const TcMaps* 
   }
 }
 
+// Sum of squares of one chunk's values as stored (bf16-rounded for bf16
+// outputs; FP32 and split-3 outputs hold the value exactly), accumulated in
+// FP32 in column order.
+__device__ __forceinline__ float chunk_sumsq(const float* x, int d_es, float acc) {
+  #pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float v = d_es == 2 ? __bfloat162float(__float2bfloat16_rn(x[j])) : x[j];
+    acc = __fmaf_rn(v, v, acc);
+  }
+  return acc;
+}
+
+// A warp's per-lane sums, added in a fixed shuffle order in double; lane 0
+// writes the total.
+__device__ __forceinline__ void warp_sumsq_store(double* dst, float acc, int lane) {
+  double d = acc;
+  #pragma unroll
+  for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+  if (lane == 0) *dst = d;
+}
+
 // ------------------------------------------------------------------ host side
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
