@@ -355,11 +355,22 @@ struct GemmPhase {
   std::vector<GemmProblem> probs;
   std::vector<GemmTile> tiles;
   std::vector<int> tile_off;   // persistent engines: CTA b runs tiles [off[b], off[b + 1])
+  int program = -1;            // pair engine: the task program this phase belongs to
+  bool program_head = false;   // its first phase: the one launch of the program
   DevBuf d_probs, d_maps, d_tiles, d_off;
   double flops = 0.0;   // algorithmic (full products)
   const float* conv_src = nullptr;
   void* conv_dst = nullptr;
   int64_t conv_n = 0;
+};
+
+struct PairProgram {
+  int first_phase = 0, nphases = 0;
+  std::vector<GemmProblem> probs;
+  std::vector<PairTask> tasks;
+  int ncounters = 1;
+  double flops = 0.0;
+  DevBuf d_probs, d_maps, d_tasks, d_counters;
 };
 
 // Tile ranges of one wave of a bounded-workspace plan (owner order).
@@ -392,6 +403,7 @@ struct NsPlan {
   DevBuf ssq;
   double* ssq_ptr = nullptr;
   int64_t n_ssq = 0;
+  std::vector<std::unique_ptr<PairProgram>> programs;
 };
 
 void engine_tile(int engine, int& bm, int& bn) {
@@ -446,15 +458,14 @@ double tile_cost(const GemmPhase& ph, const GemmTile& t) {
 }
 
 int finish_phase(GemmPhase& ph) {
-  if (ph.engine == ENGINE_CONVERT) return MUON_OK;
-  if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3 || ph.engine == ENGINE_TC2) {
+  if (ph.engine == ENGINE_CONVERT || ph.engine == ENGINE_TC2) return MUON_OK;   // see PairProgram
+  if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3) {
     // Longest-processing-time-first assignment of tiles to one persistent
     // CTA per SM (one CTA pair per two SMs for the pair engine): tiles by
     // decreasing cost, each to the least loaded CTA; every CTA then runs
     // its tiles contiguously, heaviest first.
     const int n = static_cast<int>(ph.tiles.size());
-    const int units = ph.engine == ENGINE_TC2 ? tc2_pairs() : num_sms();
-    const int nb = std::max(1, std::min(units, n));
+    const int nb = std::max(1, std::min(num_sms(), n));
     std::vector<int> order(n);
     for (int i = 0; i < n; ++i) order[i] = i;
     std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
@@ -485,16 +496,77 @@ int finish_phase(GemmPhase& ph) {
   }
   MUON_CUDA_TRY(upload(ph.d_probs, ph.probs));
   MUON_CUDA_TRY(upload(ph.d_tiles, ph.tiles));
-  if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3 || ph.engine == ENGINE_TC2) {
+  if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3) {
     std::vector<TcMaps> maps(ph.probs.size());
     for (size_t i = 0; i < ph.probs.size(); ++i) {
-      const bool ok = ph.engine == ENGINE_TC    ? tc_encode_maps(ph.probs[i], &maps[i])
-                      : ph.engine == ENGINE_TC2 ? tc2_encode_maps(ph.probs[i], &maps[i])
-                                                : x3_encode_maps(ph.probs[i], &maps[i]);
+      const bool ok = ph.engine == ENGINE_TC ? tc_encode_maps(ph.probs[i], &maps[i])
+                                             : x3_encode_maps(ph.probs[i], &maps[i]);
       if (!ok) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     }
     MUON_CUDA_TRY(upload(ph.d_maps, maps));
   }
+  return MUON_OK;
+}
+
+// Consecutive pair-engine phases of a plan run as one task program: the
+// problems of all its phases in one array, one task per output tile, and
+// for every phase after the first, each tile of NS problem j waits for the
+// tiles of problem j's previous product (every epilogue warp of both CTAs
+// of each adds one to its counter).  Tasks are ordered wave by wave (groups of consecutive
+// problems), phase by phase inside a wave, heavy tiles first inside a
+// (wave, phase), so a wave's operands tend to stay in L2 from one product
+// to the next while the other waves fill the gaps.
+
+int build_pair_program(std::vector<std::unique_ptr<GemmPhase>>& phases, int a, int b,
+                       int waves, PairProgram& G) {
+  G.first_phase = a;
+  G.nphases = b - a;
+  const int np = static_cast<int>(phases[a]->probs.size());
+  for (int k = a; k < b; ++k)
+    if (static_cast<int>(phases[k]->probs.size()) != np)
+      return fail(MUON_ERR_INVALID, "internal: pair phases of unequal problem counts");
+  // tiles of (phase, problem)
+  std::vector<std::vector<std::vector<GemmTile>>> tl(b - a, std::vector<std::vector<GemmTile>>(np));
+  for (int k = a; k < b; ++k) {
+    for (const GemmTile& t : phases[k]->tiles) tl[k - a][t.problem].push_back(t);
+    for (const GemmProblem& q : phases[k]->probs) G.probs.push_back(q);
+    G.flops += phases[k]->flops;
+  }
+  auto counter = [&](int k, int j) { return 1 + k * np + j; };
+  G.ncounters = 1 + (b - a) * np;
+  waves = std::max(1, std::min(waves, np));
+  for (int w = 0; w < waves; ++w) {
+    const int j0 = int(int64_t(np) * w / waves), j1 = int(int64_t(np) * (w + 1) / waves);
+    for (int k = 0; k < b - a; ++k) {
+      std::vector<PairTask> group;
+      for (int j = j0; j < j1; ++j) {
+        const GemmProblem& q = phases[a + k]->probs[j];
+        for (const GemmTile& t : tl[k][j]) {
+          PairTask pt{};
+          pt.problem = k * np + j;
+          pt.tm = t.tm;
+          pt.tn = t.tn;
+          pt.dep = k > 0 ? counter(k - 1, j) : -1;
+          pt.dep_target = k > 0 ? kPairArrivals * static_cast<int>(tl[k - 1][j].size()) : 0;
+          pt.done = k + 1 < b - a ? counter(k, j) : -1;
+          pt.nk = (q.K + kTcBK - 1) / kTcBK;
+          pt.b_kmajor = q.b_kmajor;
+          group.push_back(pt);
+        }
+      }
+      std::stable_sort(group.begin(), group.end(), [&](const PairTask& x, const PairTask& y) {
+        return G.probs[x.problem].K > G.probs[y.problem].K;
+      });
+      G.tasks.insert(G.tasks.end(), group.begin(), group.end());
+    }
+  }
+  std::vector<TcMaps> maps(G.probs.size());
+  for (size_t i = 0; i < G.probs.size(); ++i)
+    if (!tc2_encode_maps(G.probs[i], &maps[i])) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  MUON_CUDA_TRY(upload(G.d_probs, G.probs));
+  MUON_CUDA_TRY(upload(G.d_maps, maps));
+  MUON_CUDA_TRY(upload(G.d_tasks, G.tasks));
+  MUON_CUDA_TRY(G.d_counters.alloc(sizeof(int) * G.ncounters));
   return MUON_OK;
 }
 
@@ -831,6 +903,23 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
     if (rc != MUON_OK) return rc;
     P.flops += ph->flops;
   }
+  // runs of consecutive pair-engine phases become task programs
+  const char* wenv = std::getenv("MUON_FLOW_WAVES");
+  const int flow_waves = wenv ? std::max(1, std::atoi(wenv)) : 1;
+  const char* fenv = std::getenv("MUON_FLOW");
+  const bool flow = !(fenv && std::strcmp(fenv, "0") == 0);   // MUON_FLOW=0: a program per phase
+  for (int k = 0; k < static_cast<int>(P.phases.size());) {
+    if (P.phases[k]->engine != ENGINE_TC2) { ++k; continue; }
+    int e = k + 1;
+    while (flow && e < static_cast<int>(P.phases.size()) && P.phases[e]->engine == ENGINE_TC2) ++e;
+    std::unique_ptr<PairProgram> G(new PairProgram());
+    int rc = build_pair_program(P.phases, k, e, flow_waves, *G);
+    if (rc != MUON_OK) return rc;
+    for (int i = k; i < e; ++i) P.phases[i]->program = static_cast<int>(P.programs.size());
+    P.phases[k]->program_head = true;
+    P.programs.push_back(std::move(G));
+    k = e;
+  }
   return MUON_OK;
 }
 
@@ -1033,14 +1122,19 @@ int enqueue_gemms(NsPlan& P, const StepState* state, int* err, cudaStream_t s) {
       launch_convert_bf16(ph->conv_src, ph->conv_dst, ph->conv_n, state, s);
       continue;
     }
+    if (ph->engine == ENGINE_TC2) {
+      if (!ph->program_head) continue;   // launched with its program's first phase
+      PairProgram& G = *P.programs[ph->program];
+      PhaseScope sc(MUON_PHASE_NS_GEMM, s, G.tasks.empty() ? 0 : 1, 0.0, G.flops);
+      if (launch_gemm_tc2(G.d_probs.as<GemmProblem>(), G.d_maps.as<TcMaps>(),
+                          G.d_tasks.as<PairTask>(), static_cast<int>(G.tasks.size()),
+                          G.d_counters.as<int>(), G.ncounters, state, err, s) != 0)
+        return fail(MUON_ERR_CUDA, "tensor-core pair GEMM launch setup failed");
+      continue;
+    }
     PhaseScope sc(MUON_PHASE_NS_GEMM, s, ph->tiles.empty() ? 0 : 1, 0.0, ph->flops);
     if (ph->tiles.empty()) continue;
-    if (ph->engine == ENGINE_TC2) {
-      if (launch_gemm_tc2(ph->d_probs.as<GemmProblem>(), ph->d_maps.as<TcMaps>(),
-                          ph->d_tiles.as<GemmTile>(), ph->d_off.as<int>(),
-                          static_cast<int>(ph->tile_off.size()) - 1, state, err, s) != 0)
-        return fail(MUON_ERR_CUDA, "tensor-core pair GEMM launch setup failed");
-    } else if (ph->engine == ENGINE_TC) {
+    if (ph->engine == ENGINE_TC) {
       if (launch_gemm_tc(ph->d_probs.as<GemmProblem>(), ph->d_maps.as<TcMaps>(),
                          ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()),
                          ph->d_off.as<int>(), static_cast<int>(ph->tile_off.size()) - 1, state, err,

@@ -4,27 +4,41 @@
 //
 //   D = alpha * A op(B) + beta * E + gamma * I     (D, E bf16; epilogue fp32)
 //
-// A cluster of two CTAs (one SM pair) walks a host-balanced list of
-// (problem, 256 x 256 tile) pairs.  Per K block of 64, CTA r loads rows
-// [128 r, 128 r + 128) of the A tile and columns [128 r, 128 r + 128) of
-// the B tile into its own shared memory; the even CTA's single MMA thread
-// then issues M=256, N=256 MMAs that read both CTAs' halves, and each CTA
-// ends up holding its 128 rows x 256 columns of the tile in its tensor
-// memory.  Per K block an SM thus loads 32 KB for a 128 x 256 x 64 product
-// (the single-SM kernel loads 48 KB), which is what the main loop is bound
-// by on the smaller problems.
+// One persistent cluster of two CTAs per SM pair takes tasks -- (problem,
+// 256 x 256 tile) -- from a task list in order through a global counter.
+// A task may name a dependency: a counter that the tiles of an earlier
+// product of the same Newton-Schulz problem raise when their outputs are
+// in memory; the task's operands are loaded only once it has reached its
+// target.  All products of an iteration can so run in one launch (a
+// dataflow over the problems): a problem's next product starts as soon as
+// its previous one is complete, whatever the other problems are doing,
+// instead of waiting at a launch boundary for every problem's previous
+// product.  Tasks depend only on earlier tasks and every cluster is
+// resident, so the earliest unfinished task can always progress.
+//
+// Per K block of 64, CTA r loads rows [128 r, 128 r + 128) of the A tile and
+// columns [128 r, 128 r + 128) of the B tile into its own shared memory; the
+// even CTA's single MMA thread issues M=256, N=256 MMAs that read both
+// halves, and each CTA ends up holding its 128 rows x 256 columns of the
+// tile in its tensor memory.  Per K block an SM loads 32 KB for a
+// 128 x 256 x 64 product (a single-SM 128 x 256 tile needs 48 KB).
 //
 // Warp roles per CTA:
 //   warp 0      TMA producer (both CTAs), 5-stage ring of 32 KB stages; the
-//               loads of both CTAs complete on the even CTA's full barrier
+//               loads of both CTAs complete on the even CTA's full barrier.
+//               In the even CTA it also fetches the tasks, waits for their
+//               dependencies and publishes them to both CTAs through a
+//               4-slot task ring.
 //   warp 1      TMEM allocation for the pair (512 columns: two 128 x 256
 //               FP32 accumulators per CTA); in the even CTA also the MMA
 //               issuer, whose commits release both CTAs' stages and
 //               accumulators
-//   warps 2-9   epilogue of this CTA's 128 rows, as in the single-SM kernel
-//               (addend prefetch by TMA, FP32 alpha/beta/gamma, BF16 TMA
-//               stores), with a buffer of its own for the transposed chunk
-//               of symmetric products, so those may carry an addend too
+//   warps 2-9   epilogue of this CTA's 128 rows: addend chunks by TMA,
+//               FP32 alpha/beta/gamma, BF16 TMA stores, a buffer of its own
+//               for the transposed chunk of symmetric products; then, for
+//               tasks that others depend on, the warps wait for their stores
+//               to complete and one raises the task's counter (release, GPU
+//               scope): a tile is complete at 2 arrivals, one per CTA.
 //
 // Every wait is bounded: after ~2 s without progress a CTA records an error
 // code, stops issuing work, lets its copies in flight land, frees its
@@ -53,15 +67,52 @@ constexpr int EPI_D_BYTES = 32 * 64;
 constexpr int EPI_M_BYTES = 32 * 64;                 // mirrored chunk of a symmetric product
 constexpr int EPI_WARP_BYTES = EPI_E_BYTES + EPI_D_BYTES + EPI_M_BYTES;
 constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 256;
+constexpr int TASK_SLOTS = 4;
+constexpr int SLOT_INTS = 6;   // task ring entry: index, problem, tm, tn, nk | b_kmajor << 16, done
+constexpr int kEpiBarrier = 1;                        // named barrier of the epilogue warps
+// full, empty per stage; tfull, tempty per accumulator; E per epilogue
+// warp; task full, task empty per task slot
+constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS + 2 * TASK_SLOTS;
+constexpr int TASK_CONSUMERS = 2 + 2 * EPI_WARPS;     // peer producer, MMA, epilogue warps of both
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 512;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(kTcPairBM == BM && kTcPairBN == BN, "tile shape shared with the planner");
+static_assert(NUM_BARS * 8 + 8 + 4 * SLOT_INTS * TASK_SLOTS <= 512, "barrier and task-ring area");
+static_assert(kTcPairBM == BM && kTcPairBN == BN && kTcBK == BK, "tile shape shared with the planner");
+constexpr int ERR_TIMEOUT_DEP = 4;
+
+// A task as published in the ring: everything the MMA issuer needs, so it
+// issues without dependent global loads.
+struct TaskInfo {
+  int ti, problem, tm, tn, nk, bk, done;
+};
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait for a dependency counter to reach `target`.
+__device__ __forceinline__ bool wait_counter(const int* ctr, int target, volatile int* abort_flag,
+                                             int* err_flag) {
+  if (ld_acquire(ctr) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire(ctr) >= target) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      *abort_flag = 1;
+      if (err_flag) atomicExch(err_flag, ERR_TIMEOUT_DEP);
+      return false;
+    }
+  }
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps,
-           const GemmTile* __restrict__ tiles, const int* __restrict__ tile_off,
-           const StepState* state, int* err_flag) {
+           const PairTask* __restrict__ tasks, int ntasks, int* counters, const StepState* state,
+           int* err_flag) {
   // uniform over the pair: both CTAs leave together
   if (state != nullptr && state->overflow) return;
   extern __shared__ uint8_t smem_raw[];
@@ -76,13 +127,17 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
   auto tfull_bar = [&](int i) { return bar_base + 8u * (2 * STAGES + i); };
   auto tempty_bar = [&](int i) { return bar_base + 8u * (2 * STAGES + 2 + i); };
   auto e_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + 4 + w); };
+  auto qfull_bar = [&](int i) { return bar_base + 8u * (2 * STAGES + 4 + EPI_WARPS + i); };
+  auto qempty_bar = [&](int i) {
+    return bar_base + 8u * (2 * STAGES + 4 + EPI_WARPS + TASK_SLOTS + i);
+  };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS) + 1;
+  int* task_slot = reinterpret_cast<int*>(bars + NUM_BARS) + 2;    // TASK_SLOTS x SLOT_INTS
+  const uint32_t task_slot_s = smem_u32(task_slot);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();      // 0: issues the MMAs
-  const int pair = blockIdx.x >> 1;
-  const int t_begin = tile_off[pair], t_end = tile_off[pair + 1];
+  const uint32_t rank = cluster_ctarank();      // 0: fetches tasks and issues the MMAs
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -94,6 +149,10 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
       mbar_init(tempty_bar(i), 2 * EPI_WARPS);   // epilogue warps of both CTAs
     }
     for (int w = 0; w < EPI_WARPS; ++w) mbar_init(e_bar(w), 1);
+    for (int i = 0; i < TASK_SLOTS; ++i) {
+      mbar_init(qfull_bar(i), 1);                // the even CTA's producer publishes
+      mbar_init(qempty_bar(i), TASK_CONSUMERS);  // used in the even CTA
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -112,23 +171,74 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // Task ring, consumer side: the next task (ti = -1: no more); the slot is
+  // then handed back to the even CTA's producer.
+  auto take_task = [&](int& slot, uint32_t& qph) -> TaskInfo {
+    TaskInfo r{-1, 0, 0, 0, 0, 0, -1};
+    if (!mbar_wait_cluster(qfull_bar(slot), qph, abort_flag, err_flag, ERR_TIMEOUT_MMA)) return r;
+    const volatile int* e = task_slot + slot * SLOT_INTS;
+    r.ti = e[0];
+    r.problem = e[1];
+    r.tm = e[2];
+    r.tn = e[3];
+    r.nk = e[4] & 0xffff;
+    r.bk = e[4] >> 16;
+    r.done = e[5];
+    mbar_arrive_cluster(mapa_shared(qempty_bar(slot), 0));
+    if (++slot == TASK_SLOTS) { slot = 0; qph ^= 1u; }
+    return r;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
+      int qs = 0;
+      uint32_t qph = 0;
       int last_problem = -1;
-      for (int ti = t_begin; ti < t_end && !*abort_flag; ++ti) {
-        const GemmTile t = tiles[ti];
-        const GemmProblem& p = probs[t.problem];
+      // the even CTA fetches one task ahead, so the atomic's round trip
+      // overlaps the loads of the task before
+      int next = rank == 0 ? atomicAdd(counters, 1) : -1;
+      while (!*abort_flag) {
+        TaskInfo t{-1, 0, 0, 0, 0, 0, -1};
+        if (rank == 0) {
+          // take the fetched task, wait for its dependency, publish it
+          if (!mbar_wait_cluster(qempty_bar(qs), qph ^ 1u, abort_flag, err_flag, ERR_TIMEOUT_PRODUCER))
+            break;
+          const int ti = next < ntasks ? next : -1;
+          if (ti >= 0) {
+            next = atomicAdd(counters, 1);
+            const PairTask pt = tasks[ti];
+            t = TaskInfo{ti, pt.problem, pt.tm, pt.tn, pt.nk, pt.b_kmajor != 0 ? 1 : 0, pt.done};
+            if (pt.dep >= 0 && !wait_counter(counters + pt.dep, pt.dep_target, abort_flag, err_flag))
+              break;
+          }
+          const int e[SLOT_INTS] = {t.ti, t.problem, t.tm, t.tn, t.nk | (t.bk << 16), t.done};
+          const uint32_t remote = mapa_shared(task_slot_s + 4u * SLOT_INTS * qs, 1);
+          #pragma unroll
+          for (int i = 0; i < SLOT_INTS; ++i) {
+            task_slot[qs * SLOT_INTS + i] = e[i];
+            asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote + 4u * i), "r"(e[i]) : "memory");
+          }
+          mbar_arrive(qfull_bar(qs));
+          mbar_arrive_cluster(mapa_shared(qfull_bar(qs), 1));
+          if (++qs == TASK_SLOTS) { qs = 0; qph ^= 1u; }
+        } else {
+          t = take_task(qs, qph);
+        }
+        if (t.ti < 0) break;
+        // the operands were written by other SMs (generic release / acquire
+        // above); order the TMA reads after that
+        asm volatile("fence.proxy.async;" ::: "memory");
         const TcMaps* mp = maps + t.problem;
         if (t.problem != last_problem) {
           asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mp->a)));
           asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mp->b)));
           last_problem = t.problem;
         }
-        const int nk = (p.K + BK - 1) / BK;
-        const bool b_k = p.b_kmajor != 0;
+        const int nk = t.nk;
+        const bool b_k = t.bk != 0;
         const int row0 = t.tm * BM + static_cast<int>(rank) * BMC;        // this CTA's A rows
         const int col0 = t.tn * BN + static_cast<int>(rank) * (BN / 2);   // this CTA's B columns
         for (int kb = 0; kb < nk; ++kb) {
@@ -156,11 +266,13 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
       uint32_t ph = 0;
       int acc = 0;
       uint32_t acc_ph = 0;
-      for (int ti = t_begin; ti < t_end && !*abort_flag; ++ti) {
-        const GemmTile t = tiles[ti];
-        const GemmProblem& p = probs[t.problem];
-        const int nk = (p.K + BK - 1) / BK;
-        const bool b_k = p.b_kmajor != 0;
+      int qs = 0;
+      uint32_t qph = 0;
+      while (!*abort_flag) {
+        const TaskInfo t = take_task(qs, qph);
+        if (t.ti < 0) break;
+        const int nk = t.nk;
+        const bool b_k = t.bk != 0;
         const uint32_t idesc = make_idesc(!b_k, BM, BN);
         if (!mbar_wait(tempty_bar(acc), acc_ph ^ 1u, abort_flag, err_flag, ERR_TIMEOUT_MMA)) break;
         tc_fence_after();
@@ -201,9 +313,25 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
     uint32_t eph = 0u;
     int acc = 0;
     uint32_t acc_ph = 0;
+    int qs = 0;
+    uint32_t qph = 0;
     bool ok = true;
-    for (int ti = t_begin; ti < t_end && ok && !*abort_flag; ++ti) {
-      const GemmTile t = tiles[ti];
+    while (ok && !*abort_flag) {
+      // lane 0 takes the task for the warp and hands the slot back
+      TaskInfo t{-1, 0, 0, 0, 0, 0, -1};
+      if (lane == 0) {
+        t = take_task(qs, qph);
+      } else if (++qs == TASK_SLOTS) {
+        qs = 0;
+        qph ^= 1u;
+      }
+      t.ti = __shfl_sync(0xffffffffu, t.ti, 0);
+      if (t.ti < 0) break;
+      t.problem = __shfl_sync(0xffffffffu, t.problem, 0);
+      t.tm = __shfl_sync(0xffffffffu, t.tm, 0);
+      t.tn = __shfl_sync(0xffffffffu, t.tn, 0);
+      t.done = __shfl_sync(0xffffffffu, t.done, 0);
+      asm volatile("fence.proxy.async;" ::: "memory");   // addends come from other SMs
       const GemmProblem& p = probs[t.problem];
       const TcMaps* mp = maps + t.problem;
       const int gm0 = t.tm * BM + static_cast<int>(rank) * BMC + q * 32;
@@ -272,14 +400,28 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
                     mbuf_s);
         __syncwarp();
       }
+      if (!ok) break;
       if (p.ssq != nullptr)
-        warp_sumsq_store(p.ssq + (int64_t(t.tm) * ((p.N + BN - 1) / BN) + t.tn) * kSsqSlots + static_cast<int>(rank) * 8 + ew, ssq,
-                         lane);
+        warp_sumsq_store(p.ssq + (int64_t(t.tm) * ((p.N + BN - 1) / BN) + t.tn) * kSsqSlots +
+                             static_cast<int>(rank) * 8 + ew,
+                         ssq, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
       acc ^= 1;
       if (acc == 0) acc_ph ^= 1u;
+      if (t.done >= 0) {
+        // Later tasks read this tile: once every epilogue warp's stores are
+        // complete in memory, raise the counter with release semantics (one
+        // arrival per CTA).
+        if (lane == 0) tma_store_wait_all();
+        __syncwarp();
+        asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(32 * EPI_WARPS) : "memory");
+        if (ew == 0 && lane == 0) {
+          asm volatile("fence.proxy.async;" ::: "memory");
+          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(counters + t.done) : "memory");
+        }
+      }
     }
     if (lane == 0) tma_store_wait_all();
     __syncwarp();
@@ -333,10 +475,10 @@ int tc2_pairs() {
   return g_sms2 / 2 > 0 ? g_sms2 / 2 : 1;
 }
 
-int launch_gemm_tc2(const GemmProblem* probs, const TcMaps* maps, const GemmTile* tiles,
-                    const int* tile_off, int npairs, const StepState* state, int* err_flag,
-                    cudaStream_t s) {
-  if (npairs <= 0) return 0;
+int launch_gemm_tc2(const GemmProblem* probs, const TcMaps* maps, const PairTask* tasks,
+                    int ntasks, int* counters, int ncounters, const StepState* state,
+                    int* err_flag, cudaStream_t s) {
+  if (ntasks <= 0) return 0;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -344,7 +486,11 @@ int launch_gemm_tc2(const GemmProblem* probs, const TcMaps* maps, const GemmTile
       return -1;
     attr_set = true;
   }
-  k_gemm_tc2<<<2 * npairs, NTHREADS, SMEM_BYTES, s>>>(probs, maps, tiles, tile_off, state, err_flag);
+  // task counter and dependency counters start from zero on every launch
+  if (cudaMemsetAsync(counters, 0, sizeof(int) * ncounters, s) != cudaSuccess) return -1;
+  const int pairs = ntasks < tc2_pairs() ? ntasks : tc2_pairs();
+  k_gemm_tc2<<<2 * pairs, NTHREADS, SMEM_BYTES, s>>>(probs, maps, tasks, ntasks, counters, state,
+                                                     err_flag);
   return 0;
 }
 

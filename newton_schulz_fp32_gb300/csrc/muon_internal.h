@@ -240,14 +240,27 @@ int launch_gemm_tc(const GemmProblem* probs, const TcMaps* maps, const GemmTile*
                    int* err_flag, cudaStream_t s);
 
 // Tensor-core path on SM pairs (tcgen05 cta_group::2, clusters of two
-// CTAs), BF16 operands, 256 x 256 tiles; pair p runs tiles
-// [tile_off[p], tile_off[p + 1]).
+// CTAs), BF16 operands, 256 x 256 tiles, fed from a task list.
 constexpr int kTcPairBM = 256;
 constexpr int kTcPairBN = 256;
+constexpr int kPairArrivals = 2;   // one arrival per CTA of the pair per tile
+// One output tile of one product.  dep >= 0: its operands are ready when
+// counters[dep] >= dep_target (each tile of an earlier product of the same
+// NS problem adds kPairArrivals when its outputs are in memory);
+// done >= 0: the counter this tile raises.  counters[0] hands out tasks.
+struct PairTask {
+  int32_t problem;
+  int32_t tm, tn;
+  int32_t dep, dep_target;
+  int32_t done;
+  int32_t nk;        // K blocks of 64
+  int32_t b_kmajor;  // the problem's B layout
+};
 bool tc2_encode_maps(const GemmProblem& p, TcMaps* out);
 int tc2_pairs();   // SM pairs of the current device
-int launch_gemm_tc2(const GemmProblem* probs, const TcMaps* maps, const GemmTile* tiles,
-                    const int* tile_off, int npairs, const StepState* state, int* err_flag,
-                    cudaStream_t s);
+// Zeroes counters[0, ncounters) on `s`, then runs the tasks.
+int launch_gemm_tc2(const GemmProblem* probs, const TcMaps* maps, const PairTask* tasks,
+                    int ntasks, int* counters, int ncounters, const StepState* state,
+                    int* err_flag, cudaStream_t s);
 
 }  // namespace muon

@@ -105,6 +105,34 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Bounded wait with cluster-scope acquire: for barriers that other CTAs of
+// the cluster arrive on to hand over data they wrote.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, int* err_flag, int code) {
+  auto try_once = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_once()) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (try_once()) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      *abort_flag = 1;
+      if (err_flag) atomicExch(err_flag, code);
+      return false;
+    }
+  }
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
   asm volatile(
