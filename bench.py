@@ -29,12 +29,13 @@ import workloads as wl  # noqa: E402
 METRIC = "Muon step time & NS TFLOP/s (% of GB300 bf16 dense peak) plus HBM GB/s, 1 GPU"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes per launch of the bf16 tensor-core GEMM in this workload, from
-# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum averaged over
-# the 15 launches of one step; command in profiles/gpt2_step_launches.md),
-# valid only for the kernel sources it was taken on (hash below).
-GEMM_TRAFFIC = {"bytes_per_launch": 205.12e6, "sources_sha256_16": "0cfc9f09745dbc35",
-                "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc.cu",
+# DRAM bytes per launch of the BF16 pair GEMM in this workload (one launch
+# runs all NS products of the step), from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum averaged over two launches;
+# command in profiles/gpt2_step_launches.md), valid only for the kernel
+# sources it was taken on (hash below).
+GEMM_TRAFFIC = {"bytes_per_launch": 3.7189e9, "sources_sha256_16": "b87e496d6fd55824",
+                "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
                           "newton_schulz_fp32_gb300/csrc/tc_common.cuh"]}
 
 
@@ -403,14 +404,18 @@ def run_llama(args, peaks, peak_src):
         for mb in range(2):
             nsg.accumulate(acc, grads[mb], 0.5, overwrite=(mb == 0), params=P, parts=Q, stream=stream)
         nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, "standard", 5, 0.0, args.mode, result=res,
-                 stream=stream)
+                 stream=stream, options=opts)
+    # --workspace-budget: the NS blocks run in waves whose workspace fits it
+    opts = nsg.step_options(workspace_budget=args.workspace_budget) if args.workspace_budget else None
     ms, ph = timed(torch, nsg, step, args.steps, args.warmup, stream)
     flops = ns_formula_flops(lay, "standard")
     g = ph["ns_gemm"]
     hbm = [k for k in ph if k != "ns_gemm" and ph[k]["ms"] > 0]
     print(json.dumps({"metric": "Muon step time", "value": ms, "unit": "ms",
                       "config": {"workload": "llama3-8b muon step, 6.98G params, P=64, gas=2, "
-                                             "standard NS x5", "operand_mode": args.mode},
+                                             "standard NS x5", "operand_mode": args.mode,
+                                 "workspace_budget_bytes": args.workspace_budget},
+                      "workspace_bytes": nsg.get_stats()["workspace_bytes"],
                       "ns_tflops": flops / (g["ms"] / args.steps * 1e-3) / 1e12,
                       "ns_flops_per_step": flops,
                       "hbm_gbs": sum(ph[k]["bytes"] for k in hbm) / (sum(ph[k]["ms"] for k in hbm) * 1e-3) / 1e9,
@@ -431,6 +436,8 @@ def main():
     ap.add_argument("--workload", default="gpt2", choices=["gpt2", "sweep", "ragged", "llama"],
                     help="gpt2 is the benchmark line; sweep and ragged print extra lines")
     ap.add_argument("--shapes", default="", help="sweep shapes, e.g. 4096x4096,4096x16384")
+    ap.add_argument("--workspace-budget", type=int, default=0,
+                    help="llama workload: NS workspace cap in bytes (0: unbounded)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.workload != "gpt2" and args.impl == "ours":

@@ -354,10 +354,9 @@ struct GemmPhase {
   int ab_es = 4;   // A/B operand bytes for the CUDA-core engine
   std::vector<GemmProblem> probs;
   std::vector<GemmTile> tiles;
-  std::vector<int> tile_off;   // persistent engines: CTA b runs tiles [off[b], off[b + 1])
   int program = -1;            // pair engine: the task program this phase belongs to
   bool program_head = false;   // its first phase: the one launch of the program
-  DevBuf d_probs, d_maps, d_tiles, d_off;
+  DevBuf d_probs, d_maps, d_tiles;
   double flops = 0.0;   // algorithmic (full products)
   const float* conv_src = nullptr;
   void* conv_dst = nullptr;
@@ -440,60 +439,12 @@ struct PhaseBuilder {
   }
 };
 
-int num_sms() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-    return 1;
-  return n;
-}
-
-// Per-tile cost model of the persistent tensor-core engines, in units of
-// one K block of the main loop: the K blocks plus a fixed cost for the
-// tile's prologue and epilogue that the next tile's main loop cannot hide.
-double tile_cost(const GemmPhase& ph, const GemmTile& t) {
-  const GemmProblem& p = ph.probs[t.problem];
-  if (ph.engine == ENGINE_X3) return (p.K + 31) / 32 + 2.0;
-  return (p.K + kTcBK - 1) / kTcBK + 8.0;   // the pair engine's K block is 64 as well
-}
-
 int finish_phase(GemmPhase& ph) {
   if (ph.engine == ENGINE_CONVERT || ph.engine == ENGINE_TC2) return MUON_OK;   // see PairProgram
-  if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3) {
-    // Longest-processing-time-first assignment of tiles to one persistent
-    // CTA per SM (one CTA pair per two SMs for the pair engine): tiles by
-    // decreasing cost, each to the least loaded CTA; every CTA then runs
-    // its tiles contiguously, heaviest first.
-    const int n = static_cast<int>(ph.tiles.size());
-    const int nb = std::max(1, std::min(num_sms(), n));
-    std::vector<int> order(n);
-    for (int i = 0; i < n; ++i) order[i] = i;
-    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
-      return tile_cost(ph, ph.tiles[a]) > tile_cost(ph, ph.tiles[b]);
-    });
-    std::vector<std::vector<int>> bins(nb);
-    std::vector<std::pair<double, int>> heap;   // (load, bin), min-heap
-    for (int b = 0; b < nb; ++b) heap.push_back({0.0, b});
-    auto cmp = [](const std::pair<double, int>& x, const std::pair<double, int>& y) {
-      return x.first > y.first || (x.first == y.first && x.second > y.second);
-    };
-    std::make_heap(heap.begin(), heap.end(), cmp);
-    for (int i : order) {
-      std::pop_heap(heap.begin(), heap.end(), cmp);
-      heap.back().first += tile_cost(ph, ph.tiles[i]);
-      bins[heap.back().second].push_back(i);
-      std::push_heap(heap.begin(), heap.end(), cmp);
-    }
-    std::vector<GemmTile> sorted;
-    sorted.reserve(n);
-    ph.tile_off.assign(1, 0);
-    for (int b = 0; b < nb; ++b) {
-      for (int i : bins[b]) sorted.push_back(ph.tiles[i]);
-      ph.tile_off.push_back(static_cast<int>(sorted.size()));
-    }
-    ph.tiles.swap(sorted);
-    MUON_CUDA_TRY(upload(ph.d_off, ph.tile_off));
-  }
+  // heavy tiles first (K descending) for the static round-robin schedule
+  std::stable_sort(ph.tiles.begin(), ph.tiles.end(), [&](const GemmTile& a, const GemmTile& b) {
+    return ph.probs[a.problem].K > ph.probs[b.problem].K;
+  });
   MUON_CUDA_TRY(upload(ph.d_probs, ph.probs));
   MUON_CUDA_TRY(upload(ph.d_tiles, ph.tiles));
   if (ph.engine == ENGINE_TC || ph.engine == ENGINE_X3) {
@@ -1136,14 +1087,12 @@ int enqueue_gemms(NsPlan& P, const StepState* state, int* err, cudaStream_t s) {
     if (ph->tiles.empty()) continue;
     if (ph->engine == ENGINE_TC) {
       if (launch_gemm_tc(ph->d_probs.as<GemmProblem>(), ph->d_maps.as<TcMaps>(),
-                         ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()),
-                         ph->d_off.as<int>(), static_cast<int>(ph->tile_off.size()) - 1, state, err,
+                         ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()), state, err,
                          s) != 0)
         return fail(MUON_ERR_CUDA, "tensor-core GEMM launch setup failed");
     } else if (ph->engine == ENGINE_X3) {
       if (launch_gemm_x3(ph->d_probs.as<GemmProblem>(), ph->d_maps.as<TcMaps>(),
-                         ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()),
-                         ph->d_off.as<int>(), static_cast<int>(ph->tile_off.size()) - 1, state, err,
+                         ph->d_tiles.as<GemmTile>(), static_cast<int>(ph->tiles.size()), state, err,
                          s) != 0)
         return fail(MUON_ERR_CUDA, "split-3 tensor-core GEMM launch setup failed");
     } else {

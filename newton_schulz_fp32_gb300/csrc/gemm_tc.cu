@@ -54,7 +54,7 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 /*align*/ + 2
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps,
-          const GemmTile* __restrict__ tiles, int ntiles, const int* __restrict__ tile_off, const StepState* state,
+          const GemmTile* __restrict__ tiles, int ntiles, const StepState* state,
           int* err_flag) {
   if (state != nullptr && state->overflow) return;
   extern __shared__ uint8_t smem_raw[];
@@ -74,10 +74,6 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // this CTA's tiles: a host-balanced range, or round-robin
-  const int t_begin = tile_off ? tile_off[blockIdx.x] : static_cast<int>(blockIdx.x);
-  const int t_end = tile_off ? tile_off[blockIdx.x + 1] : ntiles;
-  const int t_step = tile_off ? 1 : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -111,7 +107,7 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
       int s = 0;
       uint32_t ph = 0;
       int last_problem = -1;
-      for (int ti = t_begin; ti < t_end && !*abort_flag; ti += t_step) {
+      for (int ti = blockIdx.x; ti < ntiles && !*abort_flag; ti += gridDim.x) {
         const GemmTile t = tiles[ti];
         const GemmProblem& p = probs[t.problem];
         const TcMaps* mp = maps + t.problem;
@@ -146,7 +142,7 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
       uint32_t ph = 0;
       int acc = 0;
       uint32_t acc_ph = 0;
-      for (int ti = t_begin; ti < t_end && !*abort_flag; ti += t_step) {
+      for (int ti = blockIdx.x; ti < ntiles && !*abort_flag; ti += gridDim.x) {
         const GemmTile t = tiles[ti];
         const GemmProblem& p = probs[t.problem];
         const int nk = (p.K + BK - 1) / BK;
@@ -194,7 +190,7 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
     int acc = 0;
     uint32_t acc_ph = 0;
     bool ok = true;
-    for (int ti = t_begin; ti < t_end && ok && !*abort_flag; ti += t_step) {
+    for (int ti = blockIdx.x; ti < ntiles && ok && !*abort_flag; ti += gridDim.x) {
       const GemmTile t = tiles[ti];
       const GemmProblem& p = probs[t.problem];     // read through L1, not held in registers
       const TcMaps* mp = maps + t.problem;
@@ -324,8 +320,7 @@ bool tc_available() {
 }
 
 int launch_gemm_tc(const GemmProblem* probs, const TcMaps* maps, const GemmTile* tiles,
-                   int ntiles, const int* tile_off, int nbins, const StepState* state,
-                   int* err_flag, cudaStream_t s) {
+                   int ntiles, const StepState* state, int* err_flag, cudaStream_t s) {
   if (ntiles <= 0) return 0;
   static bool attr_set = false;
   if (!attr_set) {
@@ -337,9 +332,8 @@ int launch_gemm_tc(const GemmProblem* probs, const TcMaps* maps, const GemmTile*
     cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
     attr_set = true;
   }
-  const int grid = tile_off ? nbins : (ntiles < g_num_sms ? ntiles : g_num_sms);
-  if (grid <= 0) return 0;
-  k_gemm_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(probs, maps, tiles, ntiles, tile_off, state, err_flag);
+  const int grid = ntiles < g_num_sms ? ntiles : g_num_sms;
+  k_gemm_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(probs, maps, tiles, ntiles, state, err_flag);
   return 0;
 }
 

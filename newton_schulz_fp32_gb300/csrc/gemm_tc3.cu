@@ -54,7 +54,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps,
-          const GemmTile* __restrict__ tiles, int ntiles, const int* __restrict__ tile_off, const StepState* state, int* err_flag) {
+          const GemmTile* __restrict__ tiles, int ntiles, const StepState* state, int* err_flag) {
   if (state != nullptr && state->overflow) return;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -71,10 +71,6 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // this CTA's tiles: a host-balanced range, or round-robin
-  const int t_begin = tile_off ? tile_off[blockIdx.x] : static_cast<int>(blockIdx.x);
-  const int t_end = tile_off ? tile_off[blockIdx.x + 1] : ntiles;
-  const int t_step = tile_off ? 1 : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -107,7 +103,7 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      for (int ti = t_begin; ti < t_end && !*abort_flag; ti += t_step) {
+      for (int ti = blockIdx.x; ti < ntiles && !*abort_flag; ti += gridDim.x) {
         const GemmTile t = tiles[ti];
         const GemmProblem& p = probs[t.problem];
         const TcMaps* mp = maps + t.problem;
@@ -140,7 +136,7 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
       int s = 0;
       uint32_t ph = 0;
       uint32_t acc_ph = 0;
-      for (int ti = t_begin; ti < t_end && !*abort_flag; ti += t_step) {
+      for (int ti = blockIdx.x; ti < ntiles && !*abort_flag; ti += gridDim.x) {
         const GemmTile t = tiles[ti];
         const GemmProblem& p = probs[t.problem];
         const int nk = (p.K + BK - 1) / BK;
@@ -196,7 +192,7 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
     uint32_t eph = 0u;
     uint32_t acc_ph = 0;
     bool ok = true;
-    for (int ti = t_begin; ti < t_end && ok && !*abort_flag; ti += t_step) {
+    for (int ti = blockIdx.x; ti < ntiles && ok && !*abort_flag; ti += gridDim.x) {
       const GemmTile t = tiles[ti];
       const GemmProblem& p = probs[t.problem];
       const TcMaps* mp = maps + t.problem;
@@ -321,8 +317,7 @@ bool x3_encode_maps(const GemmProblem& p, TcMaps* out) {
 }
 
 int launch_gemm_x3(const GemmProblem* probs, const TcMaps* maps, const GemmTile* tiles, int ntiles,
-                   const int* tile_off, int nbins, const StepState* state, int* err_flag,
-                   cudaStream_t s) {
+                   const StepState* state, int* err_flag, cudaStream_t s) {
   if (ntiles <= 0) return 0;
   static bool attr_set = false;
   if (!attr_set) {
@@ -334,9 +329,8 @@ int launch_gemm_x3(const GemmProblem* probs, const TcMaps* maps, const GemmTile*
     cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
     attr_set = true;
   }
-  const int grid = tile_off ? nbins : (ntiles < g_sms ? ntiles : g_sms);
-  if (grid <= 0) return 0;
-  k_gemm_x3<<<grid, NTHREADS, SMEM_BYTES, s>>>(probs, maps, tiles, ntiles, tile_off, state, err_flag);
+  const int grid = ntiles < g_sms ? ntiles : g_sms;
+  k_gemm_x3<<<grid, NTHREADS, SMEM_BYTES, s>>>(probs, maps, tiles, ntiles, state, err_flag);
   return 0;
 }
 

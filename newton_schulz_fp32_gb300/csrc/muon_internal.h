@@ -218,11 +218,8 @@ constexpr int kSimtTile = 128;
 // FP32-accurate products on the BF16 tensor cores from split-3 operands
 // (three exact bf16 planes per FP32 matrix; gemm_tc3.cu).
 bool x3_encode_maps(const GemmProblem& p, TcMaps* out);
-// tile_off: CTA b runs tiles [tile_off[b], tile_off[b + 1]) of `tiles`
-// (nbins CTAs); NULL: round-robin over min(ntiles, SMs) CTAs.
 int launch_gemm_x3(const GemmProblem* probs, const TcMaps* maps, const GemmTile* tiles, int ntiles,
-                   const int* tile_off, int nbins, const StepState* state, int* err_flag,
-                   cudaStream_t s);
+                   const StepState* state, int* err_flag, cudaStream_t s);
 constexpr int kX3BM = 128, kX3BN = 128;
 
 // Sets (msg != nullptr) or clears the text muon_last_error() returns.
@@ -236,8 +233,7 @@ bool tc_available();
 // Encodes the TMA descriptors of one problem; false if the driver refuses.
 bool tc_encode_maps(const GemmProblem& p, TcMaps* out);
 int launch_gemm_tc(const GemmProblem* probs, const TcMaps* maps, const GemmTile* tiles,
-                   int ntiles, const int* tile_off, int nbins, const StepState* state,
-                   int* err_flag, cudaStream_t s);
+                   int ntiles, const StepState* state, int* err_flag, cudaStream_t s);
 
 // Tensor-core path on SM pairs (tcgen05 cta_group::2, clusters of two
 // CTAs), BF16 operands, 256 x 256 tiles, fed from a task list.

@@ -259,7 +259,7 @@ extern "C" int muon_newton_schulz_noalloc(const void* X, void* Y, int rows, int 
     const GemmTile* tl = d_tiles + o.tile_list * kMaxTilesPerList;
     const int nt = g_lists[o.tile_list].count;
     if (o.engine == ENG_TC) {
-      if (launch_gemm_tc(d_probs + i, d_maps + i, tl, nt, nullptr, 0, nullptr, err_flag, s) != 0)
+      if (launch_gemm_tc(d_probs + i, d_maps + i, tl, nt, nullptr, err_flag, s) != 0)
         return nofail(MUON_ERR_CUDA, "tensor-core GEMM launch setup failed");
     } else {
       launch_gemm_simt(d_probs + i, tl, nt, o.ab_es, nullptr, s);
