@@ -69,10 +69,10 @@ constexpr int EPI_WARP_BYTES = EPI_E_BYTES + EPI_D_BYTES + EPI_M_BYTES;
 constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
 constexpr int TASK_SLOTS = 4;
 constexpr int SLOT_INTS = 6;   // task ring entry: index, problem, tm, tn, nk | b_kmajor << 16, done
-constexpr int kEpiBarrier = 1;                        // named barrier of the epilogue warps
 // full, empty per stage; tfull, tempty per accumulator; E per epilogue
 // warp; task full, task empty per task slot
 constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS + 2 * TASK_SLOTS;
+constexpr int kEpiBarrier = 1;   // named barrier of the epilogue warps
 constexpr int TASK_CONSUMERS = 2 + 2 * EPI_WARPS;     // peer producer, MMA, epilogue warps of both
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 512;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -131,6 +131,7 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
   auto qempty_bar = [&](int i) {
     return bar_base + 8u * (2 * STAGES + 4 + EPI_WARPS + TASK_SLOTS + i);
   };
+
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS) + 1;
   int* task_slot = reinterpret_cast<int*>(bars + NUM_BARS) + 2;    // TASK_SLOTS x SLOT_INTS
@@ -153,6 +154,7 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
       mbar_init(qfull_bar(i), 1);                // the even CTA's producer publishes
       mbar_init(qempty_bar(i), TASK_CONSUMERS);  // used in the even CTA
     }
+
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -316,6 +318,7 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
     int qs = 0;
     uint32_t qph = 0;
     bool ok = true;
+    bool finished = false;   // left the loop on the end-of-tasks marker
     while (ok && !*abort_flag) {
       // lane 0 takes the task for the warp and hands the slot back
       TaskInfo t{-1, 0, 0, 0, 0, 0, -1};
@@ -326,7 +329,10 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
         qph ^= 1u;
       }
       t.ti = __shfl_sync(0xffffffffu, t.ti, 0);
-      if (t.ti < 0) break;
+      if (t.ti < 0) {
+        finished = !*abort_flag;
+        break;
+      }
       t.problem = __shfl_sync(0xffffffffu, t.problem, 0);
       t.tm = __shfl_sync(0xffffffffu, t.tm, 0);
       t.tn = __shfl_sync(0xffffffffu, t.tn, 0);
@@ -422,6 +428,13 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
           asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(counters + t.done) : "memory");
         }
       }
+    }
+    if (!finished) {
+      // A warp that gives up owes at most the one epilogue barrier the others
+      // may be waiting in (none can pass it without this warp); arriving
+      // there lets them reach the loop top and see the abort.
+      __syncwarp();
+      asm volatile("bar.arrive %0, %1;" ::"n"(kEpiBarrier), "n"(32 * EPI_WARPS) : "memory");
     }
     if (lane == 0) tma_store_wait_all();
     __syncwarp();
