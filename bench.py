@@ -256,22 +256,45 @@ def run_gpu(args, rank, world):
     if nsg.device_error() != 0:
         raise RuntimeError("a kernel reported a device error during the timed region")
 
-    # ---- end to end: host grads -> device, the step, result -> host
+    # ---- end to end: host grads -> device, the step, result -> host.
+    # Every step copies its micro-batches from pinned host memory on a copy
+    # stream (micro-batch i waits until the step before has accumulated its
+    # buffer) and reads its result back; the compute stream accumulates
+    # micro-batch i once it has arrived, so the next step's copies overlap
+    # this step's Newton-Schulz.  The host reads each step's result.
     h2d = sum(g.numel() * 2 for g in g_host)
+    copy_stream = torch.cuda.Stream()
+    copied = [torch.cuda.Event() for _ in range(gas)]
+    consumed = [torch.cuda.Event() for _ in range(gas)]
+    res_ready = [torch.cuda.Event() for _ in range(2)]
+    res_hosts = [res_host, torch.zeros(4, dtype=torch.int32).pin_memory()]
     e2 = torch.cuda.Event(enable_timing=True)
     e3 = torch.cuda.Event(enable_timing=True)
     barrier()
     t_wall = time.perf_counter()
     e2.record(stream)
-    for _ in range(args.steps):
-        with torch.cuda.stream(stream):
-            for i in range(gas):
+    copy_stream.wait_event(e2)
+    for k in range(args.steps):
+        for i in range(gas):
+            if k > 0:
+                copy_stream.wait_event(consumed[i])
+            with torch.cuda.stream(copy_stream):
                 g_dev[i].copy_(g_host[i], non_blocking=True)
-        step(g_dev)
+            copied[i].record(copy_stream)
+        for mb in range(gas):
+            stream.wait_event(copied[mb])
+            nsg.accumulate(acc, g_dev[mb], 1.0 / gas, overwrite=(mb == 0), params=P, parts=Q,
+                           stream=stream)
+            consumed[mb].record(stream)
+        nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, args.ns_method, 5, 0.05, args.mode, result=res,
+                 stream=stream)
         with torch.cuda.stream(stream):
-            res_host.copy_(res, non_blocking=True)
-        stream.synchronize()
+            res_hosts[k & 1].copy_(res, non_blocking=True)
+        res_ready[k & 1].record(stream)
+        if k > 0:
+            res_ready[(k - 1) & 1].synchronize()   # the host reads the previous step's result
     e3.record(stream)
+    res_ready[(args.steps - 1) & 1].synchronize()
     barrier()
     wall_ms = 1000.0 * (time.perf_counter() - t_wall) / args.steps
     e2e_ms = max(e2.elapsed_time(e3) / args.steps, wall_ms)
