@@ -175,9 +175,15 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
 
   // Task ring, consumer side: the next task (ti = -1: no more); the slot is
   // then handed back to the even CTA's producer.
+  // In the even CTA the producer and the consumers share the CTA, so
+  // CTA-scope acquire / release suffice; the odd CTA synchronises with the
+  // even CTA's producer at cluster scope.
   auto take_task = [&](int& slot, uint32_t& qph) -> TaskInfo {
     TaskInfo r{-1, 0, 0, 0, 0, 0, -1};
-    if (!mbar_wait_cluster(qfull_bar(slot), qph, abort_flag, err_flag, ERR_TIMEOUT_MMA)) return r;
+    const bool got = rank == 0
+        ? mbar_wait(qfull_bar(slot), qph, abort_flag, err_flag, ERR_TIMEOUT_MMA)
+        : mbar_wait_cluster(qfull_bar(slot), qph, abort_flag, err_flag, ERR_TIMEOUT_MMA);
+    if (!got) return r;
     const volatile int* e = task_slot + slot * SLOT_INTS;
     r.ti = e[0];
     r.problem = e[1];
@@ -186,7 +192,8 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
     r.nk = e[4] & 0xffff;
     r.bk = e[4] >> 16;
     r.done = e[5];
-    mbar_arrive_cluster(mapa_shared(qempty_bar(slot), 0));
+    if (rank == 0) mbar_arrive(qempty_bar(slot));
+    else mbar_arrive_cluster(mapa_shared(qempty_bar(slot), 0));
     if (++slot == TASK_SLOTS) { slot = 0; qph ^= 1u; }
     return r;
   };
