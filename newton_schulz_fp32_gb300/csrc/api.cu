@@ -486,28 +486,56 @@ int build_pair_program(std::vector<std::unique_ptr<GemmPhase>>& phases, int a, i
   auto counter = [&](int k, int j) { return 1 + k * np + j; };
   G.ncounters = 1 + (b - a) * np;
   waves = std::max(1, std::min(waves, np));
-  for (int w = 0; w < waves; ++w) {
-    const int j0 = int(int64_t(np) * w / waves), j1 = int(int64_t(np) * (w + 1) / waves);
-    for (int k = 0; k < b - a; ++k) {
-      std::vector<PairTask> group;
-      for (int j = j0; j < j1; ++j) {
-        const GemmProblem& q = phases[a + k]->probs[j];
-        for (const GemmTile& t : tl[k][j]) {
-          PairTask pt{};
-          pt.problem = k * np + j;
-          pt.tm = t.tm;
-          pt.tn = t.tn;
-          pt.dep = k > 0 ? counter(k - 1, j) : -1;
-          pt.dep_target = k > 0 ? kPairArrivals * static_cast<int>(tl[k - 1][j].size()) : 0;
-          pt.done = k + 1 < b - a ? counter(k, j) : -1;
-          pt.nk = (q.K + kTcBK - 1) / kTcBK;
-          pt.b_kmajor = q.b_kmajor;
-          group.push_back(pt);
-        }
+  // Units (product k, problem j) in wavefront order: unit (k, j) has key
+  // j + k * lag, ties by k; lag >= np is product-major.  A unit always
+  // follows the previous product of its problem, so dependencies point
+  // backwards; a small lag keeps a problem's products close together (its
+  // operands stay in L2) but leaves less slack before each dependency.
+  // (GPT-2-small, 120 problems: lag 4 / 8 / 16 / 32 / 64 / product-major
+  // gave 1.274 / 1.194 / 1.145 / 1.135 / 1.134 / 1.158 ms per iteration)
+  const char* lenv = std::getenv("MUON_FLOW_LAG");
+  const int lag = lenv ? std::max(1, std::atoi(lenv)) : std::max(1, np / 2);
+  auto make_tasks = [&](int k, int j, std::vector<PairTask>& out) {
+    const GemmProblem& q = phases[a + k]->probs[j];
+    for (const GemmTile& t : tl[k][j]) {
+      PairTask pt{};
+      pt.problem = k * np + j;
+      pt.tm = t.tm;
+      pt.tn = t.tn;
+      pt.dep = k > 0 ? counter(k - 1, j) : -1;
+      pt.dep_target = k > 0 ? kPairArrivals * static_cast<int>(tl[k - 1][j].size()) : 0;
+      pt.done = k + 1 < b - a ? counter(k, j) : -1;
+      pt.nk = (q.K + kTcBK - 1) / kTcBK;
+      pt.b_kmajor = q.b_kmajor;
+      out.push_back(pt);
+    }
+  };
+  auto heavy_first = [&](std::vector<PairTask>& group) {
+    std::stable_sort(group.begin(), group.end(), [&](const PairTask& x, const PairTask& y) {
+      return G.probs[x.problem].K > G.probs[y.problem].K;
+    });
+  };
+  if (lag >= np) {
+    for (int w = 0; w < waves; ++w) {
+      const int j0 = int(int64_t(np) * w / waves), j1 = int(int64_t(np) * (w + 1) / waves);
+      for (int k = 0; k < b - a; ++k) {
+        std::vector<PairTask> group;
+        for (int j = j0; j < j1; ++j) make_tasks(k, j, group);
+        heavy_first(group);
+        G.tasks.insert(G.tasks.end(), group.begin(), group.end());
       }
-      std::stable_sort(group.begin(), group.end(), [&](const PairTask& x, const PairTask& y) {
-        return G.probs[x.problem].K > G.probs[y.problem].K;
-      });
+    }
+  } else {
+    // group the units of one key together, heavy tiles first within it
+    const int nk_prod = b - a;
+    const int64_t max_key = int64_t(np - 1) + int64_t(nk_prod - 1) * lag;
+    for (int64_t key = 0; key <= max_key; ++key) {
+      std::vector<PairTask> group;
+      for (int k = 0; k < nk_prod; ++k) {
+        const int64_t j = key - int64_t(k) * lag;
+        if (j >= 0 && j < np) make_tasks(k, static_cast<int>(j), group);
+      }
+      heavy_first(group);
       G.tasks.insert(G.tasks.end(), group.begin(), group.end());
     }
   }
