@@ -34,8 +34,9 @@
 //               issuer, whose commits release both CTAs' stages and
 //               accumulators
 //   warps 2-9   epilogue of this CTA's 128 rows: addend chunks by TMA,
-//               FP32 alpha/beta/gamma, BF16 TMA stores, a buffer of its own
-//               for the transposed chunk of symmetric products; then, for
+//               FP32 alpha/beta/gamma, BF16 TMA stores through two
+//               alternating boxes, a box of its own for the transposed chunk
+//               of symmetric products; then, for
 //               tasks that others depend on, the warps wait for their stores
 //               to complete and one raises the task's counter (release, GPU
 //               scope): a tile is complete at 2 arrivals, one per CTA.
@@ -65,7 +66,7 @@ constexpr int NTHREADS = 64 + 32 * EPI_WARPS;
 constexpr int EPI_E_BYTES = 32 * 32 * 2;
 constexpr int EPI_D_BYTES = 32 * 64;
 constexpr int EPI_M_BYTES = 32 * 64;                 // mirrored chunk of a symmetric product
-constexpr int EPI_WARP_BYTES = EPI_E_BYTES + EPI_D_BYTES + EPI_M_BYTES;
+constexpr int EPI_WARP_BYTES = EPI_E_BYTES + 2 * EPI_D_BYTES + EPI_M_BYTES;   // two output boxes
 constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
 constexpr int TASK_SLOTS = 4;
 constexpr int SLOT_INTS = 6;   // task ring entry: index, problem, tm, tn, nk | b_kmajor << 16, done
@@ -315,7 +316,11 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
     const int c_lo = (ew >> 2) * 4;
     uint8_t* ebuf = epi_base + ew * EPI_WARP_BYTES;
     uint8_t* dbuf = ebuf + EPI_E_BYTES;
-    uint8_t* mbuf = dbuf + EPI_D_BYTES;
+    uint8_t* mbuf = dbuf + 2 * EPI_D_BYTES;
+    // bulk groups committed by lane 0, and the count right after the last
+    // store out of each box: a box may be refilled once at most (groups -
+    // that count) newer groups still read their sources
+    int groups = 0, g_d[2] = {0, 0}, g_m = 0, dsel = 0;
     const uint32_t ebuf_s = smem_u32(ebuf);
     const uint32_t dbuf_s = smem_u32(dbuf);
     const uint32_t mbuf_s = smem_u32(mbuf);
@@ -355,10 +360,12 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
           if (gn0 < p.N && !(p.symmetric && gn0 < gm0)) todo |= 1u << c;
         }
       const bool has_e = p.E != nullptr;
-      if (has_e && todo && lane == 0) {
+      // addend chunks arrive by TMA one chunk ahead
+      auto load_e = [&](int c) {   // lane 0
         mbar_expect_tx(e_bar(ew), EPI_E_BYTES);
-        tma_load_2d(ebuf_s, &mp->e, t.tn * BN + (__ffs(todo) - 1) * 32, gm0, e_bar(ew));
-      }
+        tma_load_2d(ebuf_s, &mp->e, t.tn * BN + c * 32, gm0, e_bar(ew));
+      };
+      if (has_e && todo && lane == 0) load_e(__ffs(todo) - 1);
       if (!mbar_wait(tfull_bar(acc), acc_ph, abort_flag, err_flag, ERR_TIMEOUT_EPILOGUE)) {
         ok = false;
         break;
@@ -386,9 +393,10 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
             break;
           }
           eph ^= 1u;
+          const uint8_t* eb = ebuf;
           #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            const uint4 w = *reinterpret_cast<const uint4*>(ebuf + sw64(lane, g));
+            const uint4 w = *reinterpret_cast<const uint4*>(eb + sw64(lane, g));
             const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&w);
             #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -398,10 +406,7 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
             }
           }
           __syncwarp();
-          if (rest && lane == 0) {
-            mbar_expect_tx(e_bar(ew), EPI_E_BYTES);
-            tma_load_2d(ebuf_s, &mp->e, t.tn * BN + (__ffs(rest) - 1) * 32, gm0, e_bar(ew));
-          }
+          if (rest && lane == 0) load_e(__ffs(rest) - 1);
         }
         if (p.gamma != 0.f) {
           #pragma unroll
@@ -409,8 +414,46 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
             if (gm0 + lane == gn0 + j) x[j] = __fadd_rn(x[j], p.gamma);
         }
         if (p.ssq != nullptr) ssq = chunk_sumsq(x, p.d_es, ssq);
-        store_chunk(p, mp, x, gm0, gn0, lane, p.symmetric && gn0 == gm0, dbuf, dbuf_s, mbuf,
-                    mbuf_s);
+        const bool diag = p.symmetric && gn0 == gm0;
+        if (p.d_es == 2 && !diag) {
+          // BF16 box through alternating staging boxes, then the mirror
+          const int b = dsel;
+          dsel ^= 1;
+          uint8_t* db = dbuf + b * EPI_D_BYTES;
+          if (lane == 0) bulk_wait_read_n(groups - g_d[b]);
+          __syncwarp();
+          #pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            __nv_bfloat162 h[4];
+            #pragma unroll
+            for (int u = 0; u < 4; ++u)
+              h[u] = __floats2bfloat162_rn(x[8 * g + 2 * u], x[8 * g + 2 * u + 1]);
+            *reinterpret_cast<uint4*>(db + sw64(lane, g)) = *reinterpret_cast<const uint4*>(h);
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) tma_store_2d(&mp->d, gn0, gm0, dbuf_s + b * EPI_D_BYTES);
+          g_d[b] = ++groups;
+          if (p.symmetric) {
+            if (lane == 0) bulk_wait_read_n(groups - g_m);
+            __syncwarp();
+            #pragma unroll
+            for (int r = 0; r < 32; ++r)
+              *reinterpret_cast<__nv_bfloat16*>(mbuf + sw64(r, lane >> 3) + (lane & 7) * 2) =
+                  __float2bfloat16_rn(x[r]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) tma_store_2d(&mp->d, gm0, gn0, mbuf_s);
+            g_m = ++groups;
+          }
+        } else {
+          // diagonal chunks (direct stores) and FP32 / split-3 outputs: the
+          // general writer, which first waits for every earlier store to
+          // have read its box
+          store_chunk(p, mp, x, gm0, gn0, lane, diag, dbuf, dbuf_s);
+          if (!diag) groups += p.d_es == 6 ? 3 : (gn0 + 16 < p.N ? 2 : 1);
+          g_d[0] = g_d[1] = g_m = groups;
+        }
         __syncwarp();
       }
       if (!ok) break;
