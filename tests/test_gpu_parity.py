@@ -401,3 +401,68 @@ def test_stacked_head_blocks_match_separate_blocks(torch, method, mode):
                             ORACLE_MODE[mode])
     want = wl.unpack(lay, res[0])
     assert_close_update(outs[0][0], want[0], mode, "stacked Q vs oracle")
+
+
+@pytest.mark.parametrize("env", [{"MUON_FLOW": "0"}, {"MUON_FLOW_LAG": "1"},
+                                 {"MUON_FLOW_LAG": "1000"}, {"MUON_FLOW_WAVES": "3", "MUON_FLOW_LAG": "1000"}])
+def test_pair_dataflow_schedule_is_bitwise_neutral(torch, env):
+    """The SM-pair kernel's task order and dependency counters change only
+    when tiles run, never what they compute: one launch per product, the
+    tightest wavefront, product-major order and grouped waves all give the
+    default schedule's bits.  A dependency released too early would read a
+    half-written operand and differ."""
+    lay = wl.gpt2_small_layout(layers=2, nparts=4)
+    seed = 78
+    g = wl.gaussian_grads(lay, seed, 0, wl.loguniform_sigmas(lay, seed, 1e-3, 1e-1))
+    m = wl.gaussian_grads(lay, seed, 1, None, bf16=False)
+    outs = []
+    for e in ({}, env):
+        nsg.release_workspace()
+        old = {k: os.environ.get(k) for k in e}
+        os.environ.update(e)
+        try:
+            st = GpuState(torch, wl.pack(lay, g), wl.pack(lay, m), wl.pack(lay, m))
+            nsg.step(st.accum, st.momentum, st.master, lay.params, lay.parts, BETA, LR, "standard",
+                     5, CLIP, "bf16")
+            outs.append(st.numpy())
+        finally:
+            for k, v in old.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+            nsg.release_workspace()
+    for a, b in zip(*outs):
+        assert np.array_equal(bits(a), bits(b))
+    assert nsg.device_error() == 0
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_pair_kernel_matches_single_sm_kernel(torch, method):
+    """BF16 products on SM pairs (256x256 tiles, cta_group::2) against the
+    single-SM kernel (128x256 tiles, MUON_GEMM=tc1) on one GPT-2 layer, both
+    by the BF16 rule, and both against the oracle on a sampled block."""
+    lay = wl.gpt2_small_layout(layers=1, nparts=2)
+    seed = 79
+    g = wl.gaussian_grads(lay, seed, 0, wl.loguniform_sigmas(lay, seed, 1e-3, 1e-1))
+    m = wl.gaussian_grads(lay, seed, 1, None, bf16=False)
+    outs = []
+    for path in (None, "tc1"):
+        nsg.release_workspace()
+        if path:
+            os.environ["MUON_GEMM"] = path
+        try:
+            st = GpuState(torch, wl.pack(lay, g), wl.pack(lay, m), wl.pack(lay, m))
+            before = st.numpy()
+            nsg.step(st.accum, st.momentum, st.master, lay.params, lay.parts, BETA, LR, method, 5,
+                     0.0, "bf16")
+            outs.append(wl.unpack(lay, st.accum.cpu().numpy()))
+        finally:
+            os.environ.pop("MUON_GEMM", None)
+            nsg.release_workspace()
+    for k, spec in enumerate(lay.specs):
+        assert_close_update(outs[0][k], outs[1][k], "bf16", f"pairs vs single SM {spec.name}")
+    res = om.muon_step_flat(*before, lay.params, lay.parts, BETA, LR, method, 5, 0.0, "bf16")
+    want = wl.unpack(lay, res[0])
+    for o in outs:
+        assert_close_update(o[4], want[4], "bf16", "MLP-up vs oracle")
