@@ -799,21 +799,24 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
         if (o.is_muon)
           pp.add(mk(sm(R, o, fe), sm(R, o, fe), 0, sm(Pk, o, fe), sm(R, o, fe), o.m, o.m, o.m, 0, c, b,
                     a), fs(o));
-      if (k > 0) {
-        char* Qn = (Qcur == Qa) ? Qb : Qa;
-        PhaseBuilder qq = new_phase(rec, fe);   // Q <- P Q
+      // Q <- P Q and T = P R need only P: one phase, each block's two
+      // products side by side so they share P's panels in L2
+      const bool q_upd = k > 0, t_upd = k < steps - 1;
+      char* Qn = (Qcur == Qa) ? Qb : Qa;
+      {
+        PhaseBuilder qt = new_phase(rec, fe);
         for (const Owner& o : probs)
-          if (o.is_muon)
-            qq.add(mk(sm(Pk, o, fe), sm(Qcur, o, fe), 0, sm(Qn, o, fe), none, o.m, o.m, o.m, 0, 1.f,
-                      0.f, 0.f), fs(o));
-        Qcur = Qn;
+          if (o.is_muon) {
+            if (q_upd)
+              qt.add(mk(sm(Pk, o, fe), sm(Qcur, o, fe), 0, sm(Qn, o, fe), none, o.m, o.m, o.m, 0, 1.f,
+                        0.f, 0.f), fs(o));
+            if (t_upd)
+              qt.add(mk(sm(Pk, o, fe), sm(R, o, fe), 0, sm(T, o, fe), none, o.m, o.m, o.m, 0, 1.f, 0.f,
+                        0.f), fs(o));
+          }
       }
-      if (k < steps - 1) {
-        PhaseBuilder tt = new_phase(rec, fe);   // T = P R
-        for (const Owner& o : probs)
-          if (o.is_muon)
-            tt.add(mk(sm(Pk, o, fe), sm(R, o, fe), 0, sm(T, o, fe), none, o.m, o.m, o.m, 0, 1.f, 0.f,
-                      0.f), fs(o));
+      if (q_upd) Qcur = Qn;
+      if (t_upd) {
         PhaseBuilder rr = new_phase(rec, fe);   // R = T P
         for (const Owner& o : probs)
           if (o.is_muon)

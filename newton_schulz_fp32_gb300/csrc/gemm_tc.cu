@@ -147,7 +147,12 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
         const GemmProblem& p = probs[t.problem];
         const int nk = (p.K + BK - 1) / BK;
         const bool b_k = p.b_kmajor != 0;
-        const uint32_t idesc = make_idesc(!b_k, BM, BN);
+        // MMA width: the tile's columns inside the matrix, rounded up to the
+        // B operand's swizzle atom (32 rows K-major, 64 elements MN-major);
+        // the epilogue reads no column beyond it
+        const int n_rem = p.N - t.tn * BN;
+        const int n_eff = min(BN, b_k ? (n_rem + 31) & ~31 : (n_rem + 63) & ~63);
+        const uint32_t idesc = make_idesc(!b_k, BM, n_eff);
         if (!mbar_wait(tempty_bar(acc), acc_ph ^ 1u, abort_flag, err_flag, ERR_TIMEOUT_MMA)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);

@@ -12,7 +12,7 @@
 //   D = alpha * A op(B) + beta * E + gamma * I
 //
 // Layout: 128 x 128 output tiles, K steps of 32 (64-byte rows, 64-byte
-// swizzle), 4-stage ring of 3 A planes + 3 B planes (48 KB per stage).
+// swizzle), 3-stage ring of 3 A planes + 3 B planes (48 KB per stage).
 // Warp 0: TMA producer; warp 1: TMEM allocation and MMA issue; warps 2-5:
 // epilogue (32 rows each): sums the addend's three planes, adds alpha*acc,
 // gamma on the diagonal, and writes D as three planes (or bf16 / fp32),
@@ -29,28 +29,146 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BN = 128, BK = 32;
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int PLANE_A = BM * BK * 2;        // 8 KB
 constexpr int PLANE_B = BN * BK * 2;        // 8 KB
 constexpr int STAGE_BYTES = 3 * PLANE_A + 3 * PLANE_B;
-// Accumulation: four fp32 accumulators of 128 columns (all 512 TMEM
-// columns); K-block kb accumulates into slot kb % 4 and the epilogue adds the
-// slots with round-to-nearest fp32 additions.  The tensor cores' fp32
-// accumulation truncates at every MMA, and the error of a chain grows with
-// its length, so four interleaved chains keep FP32-level accuracy on long K.
-// One tile is in flight at a time (no room left for a second buffer).
-constexpr int KSPLIT = 4;
-constexpr int TMEM_COLS = KSPLIT * BN;
+// Accumulation: the tensor cores' fp32 accumulation truncates at every MMA
+// and the error of a chain grows with its length, so a tile accumulates in
+// several interleaved chains (K block kb into chain kb % chains) that the
+// epilogue adds with round-to-nearest fp32 additions.  TMEM holds two
+// buffers of 256 columns (two 128-column chains each).  Tiles with at most
+// kNarrowNk K blocks use two chains in one buffer, so the next tile's MMAs
+// overlap this tile's epilogue; longer tiles use four chains over both.
+constexpr int BUF_COLS = 2 * BN;
+constexpr int TMEM_COLS = 2 * BUF_COLS;
+constexpr int kNarrowNk = 16;
 constexpr int EPI_WARPS = 4;
 constexpr int NTHREADS = 64 + 32 * EPI_WARPS;
-constexpr int EPI_E_BYTES = 3 * 32 * 32 * 2;   // three bf16 addend planes of a 32 x 32 chunk
-constexpr int EPI_D_BYTES = 32 * 64;           // one 64-byte-row output box
-constexpr int EPI_WARP_BYTES = EPI_E_BYTES + EPI_D_BYTES;
+// Per epilogue warp: an addend buffer, an output box and a mirror box, each
+// a 32 x 32 chunk of three bf16 planes (2 KB each; a bf16 output uses the
+// first plane, an fp32 output two 16-column boxes).
+constexpr int CHUNK_BYTES = 3 * 32 * 32 * 2;
+constexpr int EPI_WARP_BYTES = 3 * CHUNK_BYTES;
 constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
 constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 256;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
+// Two floats to a packed bf16 pair, each rounded to nearest even (PTX
+// cvt.rn.bf16x2.f32; the first argument lands in the low half).
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// split3 of 32 values, two at a time: pk[b][u] holds plane b (hi, mid, lo)
+// of x[2u] (low half) and x[2u + 1] (high half).  Bit for bit the planes
+// split3 gives, with one conversion per plane and pair.
+__device__ __forceinline__ void split3_pack(const float* x, uint32_t (&pk)[3][16]) {
+  #pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const float x0 = x[2 * u], x1 = x[2 * u + 1];
+    const uint32_t h = bf16x2_rn(x0, x1);
+    const float r0 = __fsub_rn(x0, __uint_as_float(h << 16));
+    const float r1 = __fsub_rn(x1, __uint_as_float(h & 0xFFFF0000u));
+    const uint32_t m = bf16x2_rn(r0, r1);
+    const float l0 = __fsub_rn(r0, __uint_as_float(m << 16));
+    const float l1 = __fsub_rn(r1, __uint_as_float(m & 0xFFFF0000u));
+    pk[0][u] = h;
+    pk[1][u] = m;
+    pk[2][u] = bf16x2_rn(l0, l1);
+  }
+}
+
+// TMEM column of accumulation chain c of a tile whose first buffer is buf.
+__device__ __forceinline__ uint32_t chain_col(int buf, int c) {
+  return static_cast<uint32_t>(((buf + (c >> 1)) & 1) * BUF_COLS + (c & 1) * BN);
+}
+
+// The chunk's values (lane = row, x[j] = column j) in the output format:
+// des 6: pk[b][u] holds plane b of columns 2u, 2u+1; des 2: pk[0] the bf16
+// values; des 4: the fp32 values are taken from x.
+__device__ __forceinline__ void pack_chunk(const float* x, int des, uint32_t (&pk)[3][16]) {
+  if (des == 6) {
+    split3_pack(x, pk);
+  } else if (des == 2) {
+    #pragma unroll
+    for (int u = 0; u < 16; ++u) pk[0][u] = bf16x2_rn(x[2 * u], x[2 * u + 1]);
+  }
+}
+
+// Stages the chunk by rows: box row `lane` = the lane's 32 values.
+__device__ __forceinline__ void stage_rows(uint8_t* buf, const float* x, const uint32_t (&pk)[3][16],
+                                           int lane, int des) {
+  if (des == 4) {
+    #pragma unroll
+    for (int b = 0; b < 2; ++b)
+      #pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const float* xs = x + 16 * b + 4 * g;
+        *reinterpret_cast<uint4*>(buf + b * 2048 + sw64(lane, g)) =
+            make_uint4(__float_as_uint(xs[0]), __float_as_uint(xs[1]), __float_as_uint(xs[2]),
+                       __float_as_uint(xs[3]));
+      }
+    return;
+  }
+  const int planes = des == 6 ? 3 : 1;
+  #pragma unroll
+  for (int b = 0; b < 3; ++b) {
+    if (b >= planes) break;
+    #pragma unroll
+    for (int g = 0; g < 4; ++g)
+      *reinterpret_cast<uint4*>(buf + b * 2048 + sw64(lane, g)) =
+          make_uint4(pk[b][4 * g], pk[b][4 * g + 1], pk[b][4 * g + 2], pk[b][4 * g + 3]);
+  }
+}
+
+// Stages the chunk transposed: box row r, column `lane` = x[r], for rows
+// r > lane only when lower_only (the mirror half of a diagonal chunk).
+__device__ __forceinline__ void stage_cols(uint8_t* buf, const float* x, const uint32_t (&pk)[3][16],
+                                           int lane, int des, bool lower_only) {
+  if (des == 4) {
+    uint8_t* bb = buf + (lane >> 4) * 2048;
+    const int cl = lane & 15;
+    #pragma unroll
+    for (int r = 0; r < 32; ++r)
+      if (!lower_only || r > lane)
+        *reinterpret_cast<float*>(bb + sw64(r, cl >> 2) + (cl & 3) * 4) = x[r];
+    return;
+  }
+  const int planes = des == 6 ? 3 : 1;
+  #pragma unroll
+  for (int b = 0; b < 3; ++b) {
+    if (b >= planes) break;
+    #pragma unroll
+    for (int r = 0; r < 32; ++r)
+      if (!lower_only || r > lane)
+        *reinterpret_cast<uint16_t*>(buf + b * 2048 + sw64(r, lane >> 3) + (lane & 7) * 2) =
+            static_cast<uint16_t>((r & 1) ? (pk[b][r >> 1] >> 16) : (pk[b][r >> 1] & 0xFFFFu));
+  }
+}
+
+// Issues the TMA store(s) of one staged box at (column x0, row y0) of D and
+// returns the number of bulk groups committed (one per store).  An fp32
+// chunk is two 16-column boxes; the second is skipped when it starts past
+// the last column.
+__device__ __forceinline__ int issue_box(const TcMaps* mp, uint32_t buf_s, int x0, int y0, int des,
+                                         int ncols) {
+  if (des == 6) {
+    tma_store_3d(&mp->d, x0, y0, 0, buf_s);
+    return 1;
+  }
+  if (des == 2) {
+    tma_store_2d(&mp->d, x0, y0, buf_s);
+    return 1;
+  }
+  tma_store_2d(&mp->d, x0, y0, buf_s);
+  if (x0 + 16 >= ncols) return 1;
+  tma_store_2d(&mp->d, x0 + 16, y0, buf_s + 2048);
+  return 2;
+}
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps,
@@ -135,22 +253,33 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      uint32_t acc_ph = 0;
+      int buf = 0;        // first TMEM buffer of the next tile
+      uint32_t bph = 0;   // bit b: use parity of buffer b
       for (int ti = blockIdx.x; ti < ntiles && !*abort_flag; ti += gridDim.x) {
         const GemmTile t = tiles[ti];
         const GemmProblem& p = probs[t.problem];
         const int nk = (p.K + BK - 1) / BK;
+        const int chains = nk <= kNarrowNk ? 2 : 4;
+        const int nbuf = chains / 2;
         const bool b_k = p.b_kmajor != 0;
-        const uint32_t idesc = make_idesc(!b_k, BM, BN);
-        if (!mbar_wait(tempty_bar(0), acc_ph ^ 1u, abort_flag, err_flag, ERR_TIMEOUT_MMA)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base;
+        // MMA width: the tile's columns inside the matrix, rounded up to 32
+        // (the epilogue reads no column beyond it)
+        const int n_eff = min(BN, (p.N - t.tn * BN + 31) & ~31);
+        const uint32_t idesc = make_idesc(!b_k, BM, n_eff);
         bool ok = true;
+        for (int i = 0; i < nbuf && ok; ++i) {
+          const int b = (buf + i) & 1;
+          ok = mbar_wait(tempty_bar(b), ((bph >> b) & 1u) ^ 1u, abort_flag, err_flag, ERR_TIMEOUT_MMA);
+        }
+        if (!ok) break;
+        tc_fence_after();
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(full_bar(s), ph, abort_flag, err_flag, ERR_TIMEOUT_MMA)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = base + s * STAGE_BYTES;
           const uint32_t sb = sa + 3 * PLANE_A;
+          const int c = kb % chains;
+          const uint32_t d_tmem = tmem_base + chain_col(buf, c);
           #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks) {
             // the six plane products, smallest first: lo*hi, hi*lo, mid*mid,
@@ -167,18 +296,21 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
               const uint64_t bd = b_k ? make_desc(sb + pb * PLANE_B + ks * 32, 16, 512, kSwizzle64)
                                       : make_desc(sb + pb * PLANE_B + ks * 16 * 64, 32 * BK * 2, 512,
                                                   kSwizzle64);
-              // slot kb % KSPLIT; the first MMA into a slot overwrites it
-              const bool first = kb < KSPLIT && ks == 0 && q == 0;
-              umma_bf16(d_tmem + static_cast<uint32_t>((kb % KSPLIT) * BN), ad, bd, idesc,
-                        first ? 0u : 1u);
+              // the first MMA into a chain overwrites it
+              const bool first = kb < chains && ks == 0 && q == 0;
+              umma_bf16(d_tmem, ad, bd, idesc, first ? 0u : 1u);
             }
           }
           umma_commit(empty_bar(s));
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        umma_commit(tfull_bar(0));
-        acc_ph ^= 1u;
+        for (int i = 0; i < nbuf; ++i) {
+          const int b = (buf + i) & 1;
+          umma_commit(tfull_bar(b));
+          bph ^= 1u << b;
+        }
+        buf = (buf + nbuf) & 1;
       }
     }
   } else {
@@ -186,16 +318,26 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
     const int q = warp & 3;
     const int ew = warp - 2;
     uint8_t* ebuf = epi_base + ew * EPI_WARP_BYTES;
-    uint8_t* dbuf = ebuf + EPI_E_BYTES;
+    uint8_t* dbuf = ebuf + CHUNK_BYTES;
+    uint8_t* mbuf = dbuf + CHUNK_BYTES;
     const uint32_t ebuf_s = smem_u32(ebuf);
     const uint32_t dbuf_s = smem_u32(dbuf);
+    const uint32_t mbuf_s = smem_u32(mbuf);
     uint32_t eph = 0u;
-    uint32_t acc_ph = 0;
+    int buf = 0;
+    uint32_t bph = 0;
+    // bulk groups committed by lane 0 so far, and the count right after the
+    // last store from the output box and from the mirror box
+    int groups = 0, g_d = 0, g_m = 0;
     bool ok = true;
     for (int ti = blockIdx.x; ti < ntiles && ok && !*abort_flag; ti += gridDim.x) {
       const GemmTile t = tiles[ti];
       const GemmProblem& p = probs[t.problem];
       const TcMaps* mp = maps + t.problem;
+      const int nk = (p.K + BK - 1) / BK;
+      const int chains = nk <= kNarrowNk ? 2 : 4;
+      const int nbuf = chains / 2;
+      const int used = min(chains, nk);   // chains that were written
       const int gm0 = t.tm * BM + q * 32;
       uint32_t todo = 0;
       if (gm0 < p.M)
@@ -205,17 +347,18 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
         }
       const bool has_e = p.E != nullptr;
       auto load_e = [&](int c) {
-        mbar_expect_tx(e_bar(ew), EPI_E_BYTES);
-        #pragma unroll
-        for (int pl = 0; pl < 3; ++pl)
-          tma_load_3d(ebuf_s + pl * 2048, &mp->e, t.tn * BN + c * 32, gm0, pl, e_bar(ew));
+        mbar_expect_tx(e_bar(ew), CHUNK_BYTES);
+        tma_load_3d(ebuf_s, &mp->e, t.tn * BN + c * 32, gm0, 0, e_bar(ew));
       };
       if (has_e && todo && lane == 0) load_e(__ffs(todo) - 1);
-      if (!mbar_wait(tfull_bar(0), acc_ph, abort_flag, err_flag, ERR_TIMEOUT_EPILOGUE)) {
-        ok = false;
-        break;
+      for (int i = 0; i < nbuf && ok; ++i) {
+        const int b = (buf + i) & 1;
+        ok = mbar_wait(tfull_bar(b), (bph >> b) & 1u, abort_flag, err_flag, ERR_TIMEOUT_EPILOGUE);
       }
+      if (!ok) break;
       tc_fence_after();
+      const int des = p.d_es;
+      const bool sym = p.symmetric != 0;
       float ssq = 0.f;   // this warp's sum of squares of the tile (last product only)
       uint32_t rest = todo;
       while (rest) {
@@ -223,13 +366,11 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
         rest &= rest - 1;
         const int gn0 = t.tn * BN + c * 32;
         float x[32];
-        const uint32_t tcol = tmem_base + static_cast<uint32_t>(c * 32) +
-                              (static_cast<uint32_t>(q * 32) << 16);
-        tmem_ld32(tcol, x);
-        const int used = min(KSPLIT, (p.K + BK - 1) / BK);   // slots that were written
-        for (int sl = 1; sl < used; ++sl) {
+        const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+        tmem_ld32(tmem_base + chain_col(buf, 0) + static_cast<uint32_t>(c * 32) + lanes, x);
+        for (int ch = 1; ch < used; ++ch) {
           float y[32];
-          tmem_ld32(tcol + sl * BN, y);
+          tmem_ld32(tmem_base + chain_col(buf, ch) + static_cast<uint32_t>(c * 32) + lanes, y);
           #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = __fadd_rn(x[j], y[j]);
         }
@@ -268,17 +409,45 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
           for (int j = 0; j < 32; ++j)
             if (gm0 + lane == gn0 + j) x[j] = __fadd_rn(x[j], p.gamma);
         }
-        if (p.ssq != nullptr) ssq = chunk_sumsq(x, p.d_es, ssq);
-        store_chunk(p, mp, x, gm0, gn0, lane, p.symmetric && gn0 == gm0, dbuf, dbuf_s);
+        if (p.ssq != nullptr) ssq = chunk_sumsq(x, des, ssq);
+        uint32_t pk[3][16];
+        pack_chunk(x, des, pk);
+        // the output box: rows of this chunk; a diagonal chunk of a
+        // symmetric product takes its strictly lower half from the upper
+        // half (transposed), so D is exactly symmetric
+        const bool diag = sym && gn0 == gm0;
+        if (lane == 0) bulk_wait_read_n(groups - g_d);
         __syncwarp();
+        stage_rows(dbuf, x, pk, lane, des);
+        if (diag) {
+          __syncwarp();
+          stage_cols(dbuf, x, pk, lane, des, true);
+        }
+        fence_async_smem();
+        __syncwarp();
+        groups += lane == 0 ? issue_box(mp, dbuf_s, gn0, gm0, des, p.N) : (des == 4 && gn0 + 16 < p.N ? 2 : 1);
+        g_d = groups;
+        if (sym && !diag) {   // the mirror chunk at (gn0, gm0)
+          if (lane == 0) bulk_wait_read_n(groups - g_m);
+          __syncwarp();
+          stage_cols(mbuf, x, pk, lane, des, false);
+          fence_async_smem();
+          __syncwarp();
+          groups += lane == 0 ? issue_box(mp, mbuf_s, gm0, gn0, des, p.M) : (des == 4 && gm0 + 16 < p.M ? 2 : 1);
+          g_m = groups;
+        }
       }
       if (p.ssq != nullptr)
         warp_sumsq_store(p.ssq + (int64_t(t.tm) * ((p.N + BN - 1) / BN) + t.tn) * kSsqSlots + ew, ssq,
                          lane);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(0));
-      acc_ph ^= 1u;
+      for (int i = 0; i < nbuf; ++i) {
+        const int b = (buf + i) & 1;
+        if (lane == 0) mbar_arrive(tempty_bar(b));
+        bph ^= 1u << b;
+      }
+      buf = (buf + nbuf) & 1;
     }
     if (lane == 0) tma_store_wait_all();
     __syncwarp();
@@ -298,6 +467,23 @@ int g_sms = 0;
 
 }  // namespace
 
+namespace {
+// A map over three bf16 planes `pstride` elements apart whose box spans all
+// three: one TMA copy moves a whole 32 x 32 split-3 chunk.
+bool encode_planes_box(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld,
+                       int64_t pstride) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer), 3};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), static_cast<cuuint64_t>(pstride * 2)};
+  cuuint32_t box[3] = {32, 32, 3};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
 bool x3_encode_maps(const GemmProblem& p, TcMaps* out) {
   std::memset(out, 0, sizeof(TcMaps));
   bool ok = encode_2d(&out->a, p.A, 2, p.K, p.M, p.lda, BK, BM, CU_TENSOR_MAP_SWIZZLE_64B, 3, p.a_ps);
@@ -305,11 +491,11 @@ bool x3_encode_maps(const GemmProblem& p, TcMaps* out) {
     ok = ok && encode_2d(&out->b, p.B, 2, p.K, p.N, p.ldb, BK, BN, CU_TENSOR_MAP_SWIZZLE_64B, 3, p.b_ps);
   else
     ok = ok && encode_2d(&out->b, p.B, 2, p.N, p.K, p.ldb, 32, BK, CU_TENSOR_MAP_SWIZZLE_64B, 3, p.b_ps);
+  // addend and split-3 output boxes carry all three planes of a 32 x 32 chunk
   if (p.E != nullptr)
-    ok = ok && p.e_es == 6 &&
-         encode_2d(&out->e, p.E, 2, p.N, p.M, p.lde, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, 3, p.e_ps);
+    ok = ok && p.e_es == 6 && encode_planes_box(&out->e, p.E, p.N, p.M, p.lde, p.e_ps);
   if (p.d_es == 6)
-    ok = ok && encode_2d(&out->d, p.D, 2, p.N, p.M, p.ldd, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, 3, p.d_ps);
+    ok = ok && encode_planes_box(&out->d, p.D, p.N, p.M, p.ldd, p.d_ps);
   else
     ok = ok && encode_2d(&out->d, p.D, p.d_es, p.N, p.M, p.ldd, p.d_es == 2 ? 32 : 16, 32,
                          CU_TENSOR_MAP_SWIZZLE_64B);
