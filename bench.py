@@ -78,7 +78,8 @@ def gpt2_workload(ns_method, mode):
     w0 = wl.pack(lay, wl.gaussian_grads(lay, seed, 101, None, bf16=False))
     desc = (f"gpt2-small muon step: 12 layers (q,k 12-head, v, o 768x768; up 3072x768; "
             f"down 768x3072), 84.9M params, P=8, align 128, gas=4 bf16 grads, "
-            f"{ns_method} NS x5, {mode} operands, clip 0.05")
+            f"{ns_method} NS x5, {mode} operands, clip 0.05; the 4th micro-batch is "
+            f"accumulated inside the step's first pass")
     return lay, grads, m0, w0, gas, desc
 
 
@@ -212,13 +213,18 @@ def run_gpu(args, rank, world):
         res_host = torch.zeros(4, dtype=torch.int32).pin_memory()
     torch.cuda.synchronize()
     P, Q = lay.params, lay.parts
+    # the last micro-batch is accumulated by the step itself, in its first
+    # read of accum (muon_step_ex last_grad: the same arithmetic, one read
+    # and one write of accum fewer)
+    fold = nsg.step_options(last_grad=g_dev[gas - 1], last_grad_scale=1.0 / gas,
+                            last_grad_overwrite=(gas == 1))
 
     def step(grad_list):
-        for mb in range(gas):
+        for mb in range(gas - 1):
             nsg.accumulate(acc, grad_list[mb], 1.0 / gas, overwrite=(mb == 0), params=P, parts=Q,
                            stream=stream)
         nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, args.ns_method, 5, 0.05, args.mode, result=res,
-                 stream=stream)
+                 stream=stream, options=fold)
 
     # warm-up (plans are built on the first call)
     for _ in range(args.warmup):
@@ -266,6 +272,13 @@ def run_gpu(args, rank, world):
     copy_stream = torch.cuda.Stream()
     copied = [torch.cuda.Event() for _ in range(gas)]
     consumed = [torch.cuda.Event() for _ in range(gas)]
+    # the folded last micro-batch is read until the step's first pass ends,
+    # so it alternates between two device buffers: the next step's copy of
+    # it need not wait for this step's Newton-Schulz
+    g_last = [g_dev[gas - 1], torch.empty_like(g_dev[gas - 1])]
+    folds = [fold, nsg.step_options(last_grad=g_last[1], last_grad_scale=1.0 / gas,
+                                    last_grad_overwrite=(gas == 1))]
+    consumed_last = [torch.cuda.Event() for _ in range(2)]
     res_ready = [torch.cuda.Event() for _ in range(2)]
     res_hosts = [res_host, torch.zeros(4, dtype=torch.int32).pin_memory()]
     e2 = torch.cuda.Event(enable_timing=True)
@@ -275,19 +288,25 @@ def run_gpu(args, rank, world):
     e2.record(stream)
     copy_stream.wait_event(e2)
     for k in range(args.steps):
+        b = k & 1
         for i in range(gas):
-            if k > 0:
+            last = i == gas - 1
+            if last and k > 1:
+                copy_stream.wait_event(consumed_last[b])
+            elif not last and k > 0:
                 copy_stream.wait_event(consumed[i])
             with torch.cuda.stream(copy_stream):
-                g_dev[i].copy_(g_host[i], non_blocking=True)
+                (g_last[b] if last else g_dev[i]).copy_(g_host[i], non_blocking=True)
             copied[i].record(copy_stream)
-        for mb in range(gas):
+        for mb in range(gas - 1):
             stream.wait_event(copied[mb])
             nsg.accumulate(acc, g_dev[mb], 1.0 / gas, overwrite=(mb == 0), params=P, parts=Q,
                            stream=stream)
             consumed[mb].record(stream)
+        stream.wait_event(copied[gas - 1])
         nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, args.ns_method, 5, 0.05, args.mode, result=res,
-                 stream=stream)
+                 stream=stream, options=folds[b])
+        consumed_last[b].record(stream)
         with torch.cuda.stream(stream):
             res_hosts[k & 1].copy_(res, non_blocking=True)
         res_ready[k & 1].record(stream)
@@ -424,12 +443,13 @@ def run_llama(args, peaks, peak_src):
     P, Q = lay.params, lay.parts
 
     def step():
-        for mb in range(2):
-            nsg.accumulate(acc, grads[mb], 0.5, overwrite=(mb == 0), params=P, parts=Q, stream=stream)
+        nsg.accumulate(acc, grads[0], 0.5, overwrite=True, params=P, parts=Q, stream=stream)
         nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, "standard", 5, 0.0, args.mode, result=res,
                  stream=stream, options=opts)
+    # the second micro-batch is folded into the step's first pass;
     # --workspace-budget: the NS blocks run in waves whose workspace fits it
-    opts = nsg.step_options(workspace_budget=args.workspace_budget) if args.workspace_budget else None
+    opts = nsg.step_options(workspace_budget=args.workspace_budget, last_grad=grads[1],
+                            last_grad_scale=0.5)
     ms, ph = timed(torch, nsg, step, args.steps, args.warmup, stream)
     flops = ns_formula_flops(lay, "standard")
     g = ph["ns_gemm"]

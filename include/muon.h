@@ -182,7 +182,18 @@ MUON_API int muon_step(float* accum, float* momentum, float* master,
  *              update is parked in accum, and a final pass applies the clip
  *              coefficient (with MUON_CLIP_GRAD the coefficient is known
  *              before the waves and updates are written directly).  Results
- *              are bit-identical to the unbounded step. */
+ *              are bit-identical to the unbounded step.
+ *   last_grad  non-NULL: the last micro-batch's gradients, accumulated by
+ *              the step itself in its first read of accum, before the
+ *              overflow check: accum[s] = (last_grad_overwrite ? 0 :
+ *              accum[s]) + last_grad_scale * float(last_grad[s]) on every
+ *              element some parameter covers, then the step.  The same
+ *              arithmetic as muon_accumulate with those arguments followed
+ *              by the step (bit-identical accum, momentum, master and
+ *              result, a skipped step included), one read and one write of
+ *              accum fewer.  last_grad must be 8-byte aligned.
+ * struct_size is sizeof(muon_step_options_t), or MUON_STEP_OPTIONS_V1_SIZE
+ * for callers built against the layout that ends at workspace_budget. */
 typedef enum { MUON_CLIP_UPDATE = 0, MUON_CLIP_GRAD = 1 } muon_clip_mode_t;
 
 typedef struct muon_step_options {
@@ -195,7 +206,12 @@ typedef struct muon_step_options {
   float* exp_avg;        /* device, when aux_adam */
   float* exp_avg_sq;     /* device, when aux_adam */
   uint64_t workspace_budget;
+  /* -- absent when struct_size == MUON_STEP_OPTIONS_V1_SIZE -- */
+  const uint16_t* last_grad;    /* device bf16, accum's layout, or NULL */
+  float last_grad_scale;
+  int32_t last_grad_overwrite;
 } muon_step_options_t;
+#define MUON_STEP_OPTIONS_V1_SIZE 64   /* struct_size of the layout without last_grad */
 
 /* muon_step with options (NULL = defaults).  Errors as muon_step, plus
  * MUON_ERR_INVALID for a bad struct_size, a non-finite or negative

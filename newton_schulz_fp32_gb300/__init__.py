@@ -58,7 +58,12 @@ class StepOptions(ctypes.Structure):
                 ("adam_lr", ctypes.c_float), ("adam_beta1", ctypes.c_float),
                 ("adam_beta2", ctypes.c_float), ("adam_eps", ctypes.c_float),
                 ("adam_step", ctypes.c_int64), ("exp_avg", ctypes.c_void_p),
-                ("exp_avg_sq", ctypes.c_void_p), ("workspace_budget", ctypes.c_uint64)]
+                ("exp_avg_sq", ctypes.c_void_p), ("workspace_budget", ctypes.c_uint64),
+                ("last_grad", ctypes.c_void_p), ("last_grad_scale", ctypes.c_float),
+                ("last_grad_overwrite", ctypes.c_int32)]
+
+
+STEP_OPTIONS_V1_SIZE = 64   # struct_size of the layout that ends at workspace_budget
 
 
 class PhaseTime(ctypes.Structure):
@@ -147,14 +152,22 @@ def accumulate(accum, grad, scale: float, overwrite: bool = False, params=None, 
 
 
 def step_options(clip_mode="update", grad_scale: float = 1.0, adam: dict | None = None,
-                 workspace_budget: int = 0) -> StepOptions:
+                 workspace_budget: int = 0, last_grad=None, last_grad_scale: float = 1.0,
+                 last_grad_overwrite: bool = False) -> StepOptions:
     """A muon_step_options_t.  adam: dict(lr, beta1, beta2, eps, step,
-    exp_avg, exp_avg_sq) with device float buffers in accum's layout."""
+    exp_avg, exp_avg_sq) with device float buffers in accum's layout.
+    last_grad: the last micro-batch's bf16 gradients (accum's layout), which
+    the step accumulates itself, as accumulate(accum, last_grad,
+    last_grad_scale, last_grad_overwrite) would."""
     o = StepOptions()
     o.struct_size = ctypes.sizeof(StepOptions)
     o.clip_mode = CLIP_MODES[clip_mode] if isinstance(clip_mode, str) else int(clip_mode)
     o.grad_scale = grad_scale
     o.workspace_budget = int(workspace_budget)
+    if last_grad is not None:
+        o.last_grad = _ptr(last_grad)
+        o.last_grad_scale = last_grad_scale
+        o.last_grad_overwrite = int(last_grad_overwrite)
     if adam is not None:
         o.aux_adam = 1
         o.adam_lr, o.adam_beta1 = adam["lr"], adam["beta1"]
@@ -190,11 +203,13 @@ def step(accum, momentum, master, params, parts, beta: float, lr: float, ns_meth
 def step_ex(accum, momentum, master, params, parts, beta: float, lr: float, ns_method="gram",
             ns_steps: int = 5, clip: float = 0.0, operand_mode="bf16", clip_mode="update",
             grad_scale: float = 1.0, adam: dict | None = None, workspace_budget: int = 0,
+            last_grad=None, last_grad_scale: float = 1.0, last_grad_overwrite: bool = False,
             result=None, stream=None):
     """muon_step_ex with its options as keyword arguments."""
     return step(accum, momentum, master, params, parts, beta, lr, ns_method, ns_steps, clip,
                 operand_mode, result, stream,
-                step_options(clip_mode, grad_scale, adam, workspace_budget))
+                step_options(clip_mode, grad_scale, adam, workspace_budget, last_grad,
+                             last_grad_scale, last_grad_overwrite))
 
 
 def read_result(result) -> dict:

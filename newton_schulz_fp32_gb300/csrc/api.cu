@@ -1214,9 +1214,25 @@ int apply_options(const muon_step_options_t* opts, StreamLaunchArgs& a) {
   a.reduce_mode = 0;
   a.adam = 0;
   a.park = 0;
+  a.last_grad = nullptr;
+  a.last_scale = 1.f;
+  a.last_overwrite = 0;
   if (!opts) return MUON_OK;
-  if (opts->struct_size != static_cast<int32_t>(sizeof(muon_step_options_t)))
-    return fail(MUON_ERR_INVALID, "opts->struct_size must be sizeof(muon_step_options_t)");
+  const bool v2 = opts->struct_size == static_cast<int32_t>(sizeof(muon_step_options_t));
+  if (!v2 && opts->struct_size != MUON_STEP_OPTIONS_V1_SIZE)
+    return fail(MUON_ERR_INVALID,
+                "opts->struct_size must be sizeof(muon_step_options_t) or MUON_STEP_OPTIONS_V1_SIZE");
+  if (v2 && opts->last_grad) {
+    if (reinterpret_cast<uintptr_t>(opts->last_grad) % 8)
+      return fail(MUON_ERR_INVALID, "last_grad must be 8-byte aligned");
+    if (!std::isfinite(opts->last_grad_scale))
+      return fail(MUON_ERR_INVALID, "last_grad_scale must be finite");
+    if (opts->last_grad_overwrite != 0 && opts->last_grad_overwrite != 1)
+      return fail(MUON_ERR_INVALID, "last_grad_overwrite must be 0 or 1");
+    a.last_grad = opts->last_grad;
+    a.last_scale = opts->last_grad_scale;
+    a.last_overwrite = opts->last_grad_overwrite;
+  }
   if (opts->clip_mode != MUON_CLIP_UPDATE && opts->clip_mode != MUON_CLIP_GRAD)
     return fail(MUON_ERR_INVALID, "unknown clip_mode");
   if (!std::isfinite(opts->grad_scale) || opts->grad_scale < 0.f)
@@ -1310,17 +1326,22 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
 
   const double me = double(L.muon_elems), ae = double(L.aux_elems);
   MUON_CUDA_TRY(cudaMemsetAsync(a.state, 0, sizeof(StepState), s));
+  // a folded last micro-batch adds a bf16 read and an accum write; when it
+  // overwrites, accum's old value is not read
+  const double lg = a.last_grad ? (me + ae) * (a.last_overwrite ? 2 : 6) : 0.0;
   if (!pre) {
-    PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 1 : 0) + 1, me * 8 + ae * 4, 0.0);
+    PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 1 : 0) + 1, me * 8 + ae * 4 + lg, 0.0);
     a.reduce_mode = 0;
     launch_reduce(a, s);
+    a.last_grad = nullptr;   // accum now holds the full gradient
     launch_owner_norm(a, s);
   } else {
     // gradient norm over every parameter, clip coefficient, then the
     // per-block momentum norms of the clipped gradients
-    PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 2 : 0) + 2, me * 12 + ae * 4, 0.0);
+    PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 2 : 0) + 2, me * 12 + ae * 4 + lg, 0.0);
     a.reduce_mode = 1;
     launch_reduce(a, s);
+    a.last_grad = nullptr;
     launch_finalize_pre(a, s);
     a.reduce_mode = 2;
     launch_reduce(a, s);

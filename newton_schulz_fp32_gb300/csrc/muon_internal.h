@@ -187,6 +187,10 @@ struct StreamLaunchArgs {
   float* exp_avg;
   float* exp_avg_sq;
   int park;              // bounded workspace: scatter writes the unclipped update to accum only
+  // non-null: the first k_reduce pass accumulates this micro-batch into accum first
+  const uint16_t* last_grad;
+  float last_scale;
+  int last_overwrite;
 };
 
 void launch_accumulate(float* accum, const uint16_t* grad, const Run* runs, int nruns,

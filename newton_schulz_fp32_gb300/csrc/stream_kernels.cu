@@ -224,9 +224,15 @@ k_reduce(StreamLaunchArgs a) {
   const int ngroups = (t.len + 3) / 4;
   float acc = 0.f;
   bool bad = false;
+  // a folded last micro-batch: accum = (overwrite ? 0 : accum) + scale * g,
+  // written back before the element is used (muon_accumulate's arithmetic)
+  const uint16_t* LG = a.last_grad;
+  const float ls = a.last_scale;
+  const int lo = a.last_overwrite;
   if (t.fast) {
-    const float* G = a.accum + t.sdelta + tb;
+    float* G = a.accum + t.sdelta + tb;
     const float* M = a.momentum + t.sdelta + tb;
+    const uint16_t* GL = LG ? LG + t.sdelta + tb : nullptr;
     constexpr int U = 4;
     for (int g0 = threadIdx.x; g0 < ngroups; g0 += NT * U) {
       float4 gv[U], mv[U];
@@ -234,7 +240,17 @@ k_reduce(StreamLaunchArgs a) {
       for (int u = 0; u < U; ++u) {
         const int g = g0 + u * NT;
         if (g < ngroups) {
-          gv[u] = *reinterpret_cast<const float4*>(G + 4 * g);
+          if (GL) {
+            const uint2 b = *reinterpret_cast<const uint2*>(GL + 4 * g);
+            const float4 old = lo ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(G + 4 * g);
+            gv[u].x = acc_one(old.x, __uint_as_float(b.x << 16), ls, lo);
+            gv[u].y = acc_one(old.y, __uint_as_float(b.x & 0xffff0000u), ls, lo);
+            gv[u].z = acc_one(old.z, __uint_as_float(b.y << 16), ls, lo);
+            gv[u].w = acc_one(old.w, __uint_as_float(b.y & 0xffff0000u), ls, lo);
+            *reinterpret_cast<float4*>(G + 4 * g) = gv[u];
+          } else {
+            gv[u] = *reinterpret_cast<const float4*>(G + 4 * g);
+          }
           mv[u] = use_m ? *reinterpret_cast<const float4*>(M + 4 * g) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
@@ -258,7 +274,12 @@ k_reduce(StreamLaunchArgs a) {
         if (si < 0) si = find_seg(segs, o.seg_count, rel);
         while (rel >= segs[si].rel_begin + segs[si].len) ++si;
         const int64_t st = segs[si].storage_begin + (rel - segs[si].rel_begin);
-        reduce_one(a, a.accum[st], use_m ? a.momentum[st] : 0.f, use_m, c, acc, bad);
+        float gr = a.accum[st];
+        if (LG) {
+          gr = acc_one(gr, bf16_bits_to_float(LG[st]), ls, lo);
+          a.accum[st] = gr;
+        }
+        reduce_one(a, gr, use_m ? a.momentum[st] : 0.f, use_m, c, acc, bad);
       }
     }
   }

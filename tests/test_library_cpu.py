@@ -108,8 +108,13 @@ def _step_ex(lib, opts, ptrs=(FAKE, FAKE, FAKE)):
 
 
 def test_step_options_struct_layout():
-    assert ctypes.sizeof(nsg.StepOptions) == 64
+    # muon.h: the original layout ends at workspace_budget (64 bytes); the
+    # folded last micro-batch follows it
+    assert ctypes.sizeof(nsg.StepOptions) == 80
     assert nsg.StepOptions.adam_step.offset == 32 and nsg.StepOptions.workspace_budget.offset == 56
+    assert nsg.StepOptions.last_grad.offset == nsg.STEP_OPTIONS_V1_SIZE == 64
+    assert nsg.StepOptions.last_grad_scale.offset == 72
+    assert nsg.StepOptions.last_grad_overwrite.offset == 76
 
 
 def test_step_options_rejected_on_host(lib):
@@ -125,6 +130,12 @@ def test_step_options_rejected_on_host(lib):
     cases.append((nsg.step_options(adam=dict(adam, step=0)), "adam_step"))
     cases.append((nsg.step_options(adam=dict(adam, beta2=1.0)), "betas"))
     cases.append((nsg.step_options(adam=dict(adam, eps=-1.0)), "adam_eps"))
+    cases.append((nsg.step_options(last_grad=FAKE + 2), "8-byte"))
+    cases.append((nsg.step_options(last_grad=FAKE, last_grad_scale=float("nan")), "last_grad_scale"))
+    o = nsg.step_options(last_grad=FAKE); o.last_grad_overwrite = 2
+    cases.append((o, "last_grad_overwrite"))
+    o = nsg.step_options(); o.struct_size = 72
+    cases.append((o, "struct_size"))
     for opts, word in cases:
         rc = _step_ex(lib, opts)
         assert rc == nsg.MUON_ERR_INVALID, (word, rc)
@@ -142,5 +153,8 @@ def test_valid_options_without_gpu_fail_cleanly(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     adam = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, step=3, exp_avg=FAKE, exp_avg_sq=FAKE)
-    for opts in (None, nsg.step_options(), nsg.step_options("grad", 2.0 ** -10, adam)):
+    v1 = nsg.step_options(last_grad=FAKE + 2)   # ignored: the fields are absent in a v1 struct
+    v1.struct_size = nsg.STEP_OPTIONS_V1_SIZE
+    for opts in (None, nsg.step_options(), nsg.step_options("grad", 2.0 ** -10, adam),
+                 nsg.step_options(last_grad=FAKE, last_grad_scale=0.25), v1):
         assert _step_ex(lib, opts) == nsg.MUON_ERR_CUDA
