@@ -786,11 +786,17 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
   } else {
     char *R = S[0], *Pm = S[1], *Qa = S[2], *Qb = S[3], *T = S[4];
     const int rec = tc ? ENGINE_X3 : ENGINE_SIMT;
-    PhaseBuilder g0 = new_phase(engine_for(xe), xe);   // R = X0 X0^T
+    // R = X0 X0^T.  On single SMs (blocks below 192 rows) every tile is
+    // computed: a 128-row block is one tile either way, and that kernel
+    // mirrors split-3 outputs element by element, which cost more than the
+    // lower tiles (ragged 8192-block step: 1.26 -> 0.41 ms for this product)
+    const int r0_eng = engine_for(xe);
+    const int r0_sym = r0_eng == ENGINE_TC ? 0 : 1;
+    PhaseBuilder g0 = new_phase(r0_eng, xe);
     for (const Owner& o : probs)
       if (o.is_muon)
-        g0.add(gram(mk(xm(X[0], o), xm(X[0], o), 1, sm(R, o, fe), none, o.m, o.m, o.n, 1, 1.f, 0.f,
-                       0.f), o), fs(o));
+        g0.add(gram(mk(xm(X[0], o), xm(X[0], o), 1, sm(R, o, fe), none, o.m, o.m, o.n, r0_sym, 1.f,
+                       0.f, 0.f), o), fs(o));
     char* Qcur = Qa;
     for (int k = 0; k < steps; ++k) {
       char* Pk = (k == 0) ? Qa : Pm;   // Q1 = P0 (Q0 = I)
