@@ -82,6 +82,23 @@ __device__ __forceinline__ void split3_pack(const float* x, uint32_t (&pk)[3][16
   }
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
+// MN-major B whose columns come in whole groups of 32 is read through a
+// 4-D view (32 columns, K rows, column groups, planes), so one copy moves a
+// stage's whole B tile (4 groups x 3 planes); other MN-major B tiles are
+// copied one 32-column group and plane at a time.
+__host__ __device__ inline bool b_grouped(const GemmProblem& p) {
+  return p.b_kmajor == 0 && p.N % 32 == 0;
+}
+
 // TMEM column of accumulation chain c of a tile whose first buffer is buf.
 __device__ __forceinline__ uint32_t chain_col(int buf, int c) {
   return static_cast<uint32_t>(((buf + (c >> 1)) & 1) * BUF_COLS + (c & 1) * BN);
@@ -227,22 +244,25 @@ k_gemm_x3(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
         const TcMaps* mp = maps + t.problem;
         const int nk = (p.K + BK - 1) / BK;
         const bool b_k = p.b_kmajor != 0;
+        const bool b_g = b_grouped(p);
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, err_flag, ERR_TIMEOUT_PRODUCER)) break;
           const uint32_t sa = base + s * STAGE_BYTES;
           const uint32_t sb = sa + 3 * PLANE_A;
           mbar_expect_tx(full_bar(s), STAGE_BYTES);
-          #pragma unroll
-          for (int pl = 0; pl < 3; ++pl) {
-            tma_load_3d(sa + pl * PLANE_A, &mp->a, kb * BK, t.tm * BM, pl, full_bar(s));
-            if (b_k) {
-              tma_load_3d(sb + pl * PLANE_B, &mp->b, kb * BK, t.tn * BN, pl, full_bar(s));
-            } else {
+          // A and K-major B: one box of all three planes each
+          tma_load_3d(sa, &mp->a, kb * BK, t.tm * BM, 0, full_bar(s));
+          if (b_k) {
+            tma_load_3d(sb, &mp->b, kb * BK, t.tn * BN, 0, full_bar(s));
+          } else if (b_g) {
+            tma_load_4d(sb, &mp->b, 0, kb * BK, t.tn * (BN / 32), 0, full_bar(s));
+          } else {
+            #pragma unroll
+            for (int pl = 0; pl < 3; ++pl)
               #pragma unroll
               for (int j = 0; j < BN / 32; ++j)
                 tma_load_3d(sb + pl * PLANE_B + j * (32 * BK * 2), &mp->b, t.tn * BN + j * 32,
                             kb * BK, pl, full_bar(s));
-            }
           }
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
@@ -468,15 +488,32 @@ int g_sms = 0;
 }  // namespace
 
 namespace {
+// 4-D view of an MN-major split-3 B (K rows of N columns, N % 32 == 0):
+// (32 columns, K rows, N / 32 column groups, 3 planes); a box of
+// (32, BK, BN / 32, 3) lands in shared memory as [plane][group][row][32].
+bool encode_b_grouped(CUtensorMap* m, const GemmProblem& p) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {32, static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.N / 32), 3};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(p.ldb * 2), 64,
+                           static_cast<cuuint64_t>(p.b_ps * 2)};
+  cuuint32_t box[4] = {32, BK, BN / 32, 3};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p.B), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A map over three bf16 planes `pstride` elements apart whose box spans all
-// three: one TMA copy moves a whole 32 x 32 split-3 chunk.
+// three: one TMA copy moves a whole split-3 box (an operand tile of one
+// K step, or a 32 x 32 addend or output chunk).
 bool encode_planes_box(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld,
-                       int64_t pstride) {
+                       int64_t pstride, uint32_t box_inner = 32, uint32_t box_outer = 32) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer), 3};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), static_cast<cuuint64_t>(pstride * 2)};
-  cuuint32_t box[3] = {32, 32, 3};
+  cuuint32_t box[3] = {box_inner, box_outer, 3};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -486,9 +523,12 @@ bool encode_planes_box(CUtensorMap* m, const void* base, int64_t inner, int64_t 
 
 bool x3_encode_maps(const GemmProblem& p, TcMaps* out) {
   std::memset(out, 0, sizeof(TcMaps));
-  bool ok = encode_2d(&out->a, p.A, 2, p.K, p.M, p.lda, BK, BM, CU_TENSOR_MAP_SWIZZLE_64B, 3, p.a_ps);
+  // A and K-major B: boxes of all three planes (one copy per stage each)
+  bool ok = encode_planes_box(&out->a, p.A, p.K, p.M, p.lda, p.a_ps, BK, BM);
   if (p.b_kmajor)
-    ok = ok && encode_2d(&out->b, p.B, 2, p.K, p.N, p.ldb, BK, BN, CU_TENSOR_MAP_SWIZZLE_64B, 3, p.b_ps);
+    ok = ok && encode_planes_box(&out->b, p.B, p.K, p.N, p.ldb, p.b_ps, BK, BN);
+  else if (b_grouped(p))
+    ok = ok && encode_b_grouped(&out->b, p);
   else
     ok = ok && encode_2d(&out->b, p.B, 2, p.N, p.K, p.ldb, 32, BK, CU_TENSOR_MAP_SWIZZLE_64B, 3, p.b_ps);
   // addend and split-3 output boxes carry all three planes of a 32 x 32 chunk
