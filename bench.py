@@ -391,7 +391,7 @@ def run_ragged(args, peaks, peak_src):
     import newton_schulz_fp32_gb300 as nsg
     nsg.build()
     seed = wl.CONFIG_SEED["ragged"]
-    lay = wl.ragged_layout(8192, seed=seed)
+    lay = wl.ragged_layout(args.ragged_count, seed=seed)
     rng = wl.rng_for(seed, 1)
     scales = 10.0 ** rng.uniform(-5, 0, len(lay.specs))
     mats = [(wl.rng_for(seed, 2, i).standard_normal((s.rows, s.cols), dtype=np.float32)
@@ -412,7 +412,8 @@ def run_ragged(args, peaks, peak_src):
     ms, ph = timed(torch, nsg, step, args.steps, args.warmup, stream)
     flops = ns_formula_flops(lay, "gram")
     print(json.dumps({"metric": "Muon step time", "value": ms, "unit": "ms",
-                      "config": {"workload": "ragged 8192 matrices, gram NS x5", "operand_mode": args.mode,
+                      "config": {"workload": f"ragged {args.ragged_count} matrices, gram NS x5",
+                                 "operand_mode": args.mode,
                                  "elements": lay.n_muon_elements},
                       "ns_tflops_gram_flops": flops / (ph["ns_gemm"]["ms"] / args.steps * 1e-3) / 1e12,
                       "phases_ms_per_step": {k: ph[k]["ms"] / args.steps for k in ph}}))
@@ -479,6 +480,9 @@ def main():
     ap.add_argument("--workload", default="gpt2", choices=["gpt2", "sweep", "ragged", "llama"],
                     help="gpt2 is the benchmark line; sweep and ragged print extra lines")
     ap.add_argument("--shapes", default="", help="sweep shapes, e.g. 4096x4096,4096x16384")
+    ap.add_argument("--ragged-count", type=int, default=8192,
+                    help="ragged workload: number of matrices (a smaller count keeps profiler "
+                         "captures small; the same shape distribution)")
     ap.add_argument("--workspace-budget", type=int, default=0,
                     help="llama workload: NS workspace cap in bytes (0: unbounded)")
     args = ap.parse_args()
