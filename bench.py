@@ -325,25 +325,41 @@ def run_gpu(args, rank, world):
     return lay, desc, ms, e2e_ms, h2d, phases, clk, launches
 
 
-def timed(torch, nsg, fn, steps, warmup, stream):
+def timed(torch, nsg, fn, steps, warmup, stream, prepare=None):
     """Warm-up, then CUDA-event time of `steps` calls on `stream`, with the
-    library's per-phase profile over the timed calls."""
+    library's per-phase profile over the timed calls.  prepare(), if given,
+    runs before every call outside the timed spans (each call is then timed
+    by its own event pair and the spans are summed)."""
     for _ in range(warmup):
+        if prepare:
+            prepare()
         fn()
     torch.cuda.synchronize()
     nsg.profile_read(reset=True)
     nsg.profile_enable(True)
+    spans = []
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        fn()
-    e1.record(stream)
+    if prepare is None:
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+    else:
+        for _ in range(steps):
+            prepare()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            spans.append((a, b))
     torch.cuda.synchronize()
     nsg.profile_enable(False)
     phases = nsg.profile_read(reset=True)
     if nsg.device_error() != 0:
         raise RuntimeError("a kernel reported a device error")
-    return e0.elapsed_time(e1) / steps, phases
+    if prepare is None:
+        return e0.elapsed_time(e1) / steps, phases
+    return sum(a.elapsed_time(b) for a, b in spans) / steps, phases
 
 
 def run_sweep(args, peaks, peak_src):
@@ -404,12 +420,14 @@ def run_ragged(args, peaks, peak_src):
     res = torch.zeros(4, dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
 
-    def step():
+    def refill():   # the step consumes accum: fresh gradients, outside the timed span
         with torch.cuda.stream(stream):
             acc.copy_(g0)
+
+    def step():
         nsg.step(acc, mom, mst, lay.params, lay.parts, 0.95, 0.02, "gram", 5, 0.0, args.mode,
                  result=res, stream=stream)
-    ms, ph = timed(torch, nsg, step, args.steps, args.warmup, stream)
+    ms, ph = timed(torch, nsg, step, args.steps, args.warmup, stream, prepare=refill)
     flops = ns_formula_flops(lay, "gram")
     print(json.dumps({"metric": "Muon step time", "value": ms, "unit": "ms",
                       "config": {"workload": f"ragged {args.ragged_count} matrices, gram NS x5",
