@@ -301,6 +301,11 @@ typedef struct muon_phase_time {
 } muon_phase_time_t;
 
 MUON_API int muon_profile_enable(int on);
+/* As muon_profile_enable, for the phases whose bit (1 << muon_phase_t) is
+ * set in mask only (0 = off); fewer events perturb a timed run less.  Calls
+ * issued while their stream is captured into a CUDA graph record the events
+ * as nodes of the graph, timed again by every replay. */
+MUON_API int muon_profile_enable_phases(uint32_t mask);
 MUON_API int muon_profile_read(muon_phase_time_t* out, int nphases, int reset);
 
 #ifdef __cplusplus

@@ -35,7 +35,7 @@ PHASES = ["accumulate", "reduce", "gather", "ns_gemm", "norm", "scatter"]
 EXPORTED = ["muon_accumulate", "muon_step", "muon_newton_schulz", "muon_get_stats",
             "muon_last_error", "muon_release_workspace", "muon_device_error",
             "muon_profile_enable", "muon_profile_read", "muon_newton_schulz_noalloc",
-            "muon_step_ex"]
+            "muon_step_ex", "muon_profile_enable_phases"]
 CLIP_MODES = {"update": 0, "grad": 1}
 
 
@@ -98,10 +98,12 @@ def lib():
         L.muon_last_error.restype = ctypes.c_char_p
         L.muon_release_workspace.restype = None
         L.muon_profile_enable.argtypes = [I]
+        L.muon_profile_enable_phases.argtypes = [ctypes.c_uint32]
         L.muon_profile_read.argtypes = [ctypes.POINTER(PhaseTime), I, I]
         for name in ("muon_accumulate", "muon_step", "muon_step_ex", "muon_newton_schulz",
                      "muon_newton_schulz_noalloc", "muon_get_stats",
-                     "muon_device_error", "muon_profile_enable", "muon_profile_read"):
+                     "muon_device_error", "muon_profile_enable", "muon_profile_read",
+                     "muon_profile_enable_phases"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -256,8 +258,15 @@ def device_error() -> int:
     return int(lib().muon_device_error())
 
 
-def profile_enable(on: bool = True):
-    _check(lib().muon_profile_enable(int(on)))
+def profile_enable(on: bool = True, phases=None):
+    """Time every phase (on), none, or only `phases` (names from PHASES)."""
+    if phases is None:
+        _check(lib().muon_profile_enable(int(on)))
+    else:
+        mask = 0
+        for name in phases:
+            mask |= 1 << PHASES.index(name)
+        _check(lib().muon_profile_enable_phases(mask if on else 0))
 
 
 def profile_read(reset: bool = False) -> dict:

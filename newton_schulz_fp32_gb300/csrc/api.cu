@@ -86,7 +86,7 @@ struct PendingEvent {
   cudaEvent_t start, stop;
   double bytes, flops;
 };
-bool g_profile = false;
+uint32_t g_profile = 0;   // phases (bit 1 << muon_phase_t) whose launches are timed
 std::vector<PendingEvent> g_pending;
 std::vector<cudaEvent_t> g_event_pool;
 muon_phase_time_t g_phase[MUON_PHASE_COUNT];
@@ -102,6 +102,17 @@ cudaEvent_t get_event() {
   return e;
 }
 
+// Records a profiling event on s.  While s is being captured into a CUDA
+// graph the record becomes an event node of the graph (external record),
+// so every replay of the graph times the phase again.
+void record_event(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) == cudaSuccess && st == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 // Brackets one launch group with events (when profiling) and counts kernels.
 struct PhaseScope {
   int phase, kernels;
@@ -110,17 +121,17 @@ struct PhaseScope {
   cudaEvent_t a = nullptr, b = nullptr;
   PhaseScope(int ph, cudaStream_t st, int nkern, double by, double fl)
       : phase(ph), kernels(nkern), bytes(by), flops(fl), s(st) {
-    if (g_profile && nkern > 0) {
+    if ((g_profile >> ph & 1u) && nkern > 0) {
       a = get_event();
       b = get_event();
-      cudaEventRecord(a, s);
+      record_event(a, s);
     }
   }
   ~PhaseScope() {
     g_cnt.launches_last += kernels;
     g_cnt.launches_total += kernels;
     if (a) {
-      cudaEventRecord(b, s);
+      record_event(b, s);
       g_pending.push_back({phase, a, b, bytes, flops});
       g_phase[phase].launches += kernels;
     }
@@ -1565,7 +1576,13 @@ extern "C" int muon_device_error(void) {
 
 extern "C" int muon_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(g_mu);
-  g_profile = on != 0;
+  g_profile = on != 0 ? (1u << MUON_PHASE_COUNT) - 1u : 0u;
+  return MUON_OK;
+}
+
+extern "C" int muon_profile_enable_phases(uint32_t mask) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_profile = mask & ((1u << MUON_PHASE_COUNT) - 1u);
   return MUON_OK;
 }
 
