@@ -344,11 +344,18 @@ def run_gpu(args, rank, world):
     wall_ms = 1000.0 * (time.perf_counter() - t_wall) / args.steps
     e2e_ms = max(e2.elapsed_time(e3) / args.steps, wall_ms)
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+        ms, e2e_ms = max_over_ranks([ms, e2e_ms], "cuda")
     return lay, desc, ms, e2e_ms, h2d, phases, clk, launches
+
+
+def max_over_ranks(values, device):
+    """Each value's maximum over the ranks of the default process group (the
+    slowest replica sets the whole job's time)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
 
 
 def timed(torch, nsg, fn, steps, warmup, stream, prepare=None):
