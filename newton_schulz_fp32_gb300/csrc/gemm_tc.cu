@@ -185,7 +185,9 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // TMEM lane quarter this warp may read
     const int ew = warp - 2;                      // epilogue warp 0..7
-    const int c_lo = (ew >> 2) * 4;               // its chunks: columns [32 c_lo, 32 c_lo + 128)
+    // the two warps of a lane quarter take alternate 32-column chunks, so the
+    // upper-triangle chunks of a diagonal tile are shared evenly
+    const int c_par = ew >> 2;
     uint8_t* ebuf = epi_base + ew * EPI_WARP_BYTES;
     uint8_t* dbuf = ebuf + EPI_E_BYTES;
     const uint32_t ebuf_s = smem_u32(ebuf);
@@ -204,7 +206,7 @@ k_gemm_tc(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ maps
       // products not strictly below the diagonal (32-aligned both ways)
       uint32_t todo = 0;
       if (gm0 < p.M)
-        for (int c = c_lo; c < c_lo + 4; ++c) {
+        for (int c = c_par; c < BN / 32; c += 2) {
           const int gn0 = t.tn * BN + c * 32;
           if (gn0 < p.N && !(p.symmetric && gn0 < gm0)) todo |= 1u << c;
         }

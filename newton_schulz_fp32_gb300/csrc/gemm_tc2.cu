@@ -313,7 +313,10 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int ew = warp - 2;
-    const int c_lo = (ew >> 2) * 4;
+    // the two warps of a lane quarter take alternate 32-column chunks, so
+    // the upper-triangle chunks of a diagonal tile (and their mirrors) are
+    // shared evenly between them
+    const int c_par = ew >> 2;
     uint8_t* ebuf = epi_base + ew * EPI_WARP_BYTES;
     uint8_t* dbuf = ebuf + EPI_E_BYTES;
     uint8_t* mbuf = dbuf + 2 * EPI_D_BYTES;
@@ -355,7 +358,7 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
       const int gm0 = t.tm * BM + static_cast<int>(rank) * BMC + q * 32;
       uint32_t todo = 0;
       if (gm0 < p.M)
-        for (int c = c_lo; c < c_lo + 4; ++c) {
+        for (int c = c_par; c < BN / 32; c += 2) {
           const int gn0 = t.tn * BN + c * 32;
           if (gn0 < p.N && !(p.symmetric && gn0 < gm0)) todo |= 1u << c;
         }
