@@ -34,7 +34,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # (dram__bytes_read.sum + dram__bytes_write.sum averaged over two launches;
 # command in profiles/gpt2_step_launches.md), valid only for the kernel
 # sources it was taken on (hash below).
-GEMM_TRAFFIC = {"bytes_per_launch": 3.8479e9, "sources_sha256_16": "2bc68bf014d92824",
+GEMM_TRAFFIC = {"bytes_per_launch": 3.8489e9, "sources_sha256_16": "3ef1b59e79164675",
                 "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
                           "newton_schulz_fp32_gb300/csrc/tc_common.cuh"]}
 
