@@ -579,8 +579,8 @@ struct WsMat {
 //   float64 are exact), so mirroring changes no value.
 // gram: R0 = X0 X0^T (symmetric), then the m x m recurrence
 //   P = c R R + b R + a I, Q <- P Q, T = P R, R = T P in FP32 with B read
-//   MN-major (no symmetry assumed: in floating point R and P are not
-//   exactly symmetric); then Y = bf16(Q) X0 (BF16 mode) or Q X0 (FP32 mode).
+//   MN-major, upper tiles mirrored (each product is symmetric in exact
+//   arithmetic); then Y = bf16(Q) X0 (BF16 mode) or Q X0 (FP32 mode).
 // Engines: BF16 operands on the tensor cores, on SM pairs with 256 x 256
 // tiles (ENGINE_TC2) when every block has at least 192 rows, else on single
 // SMs with 128 x 256 tiles (ENGINE_TC; MUON_GEMM=tc1 forces it); FP32
@@ -809,13 +809,19 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
         g0.add(gram(mk(xm(X[0], o), xm(X[0], o), 1, sm(R, o, fe), none, o.m, o.m, o.n, r0_sym, 1.f,
                        0.f, 0.f), o), fs(o));
     char* Qcur = Qa;
+    // Every matrix of the recurrence is a polynomial in R0 in exact
+    // arithmetic, so every product (R R, P Q, P R, T P) is symmetric: only
+    // tiles touching the upper triangle are computed and mirrored, which
+    // halves the work on large blocks and keeps each iterate exactly
+    // symmetric.
+    const int rs = 1;
     for (int k = 0; k < steps; ++k) {
       char* Pk = (k == 0) ? Qa : Pm;   // Q1 = P0 (Q0 = I)
       PhaseBuilder pp = new_phase(rec, fe);   // P = c R R + b R + a I
       for (const Owner& o : probs)
         if (o.is_muon)
-          pp.add(mk(sm(R, o, fe), sm(R, o, fe), 0, sm(Pk, o, fe), sm(R, o, fe), o.m, o.m, o.m, 0, c, b,
-                    a), fs(o));
+          pp.add(mk(sm(R, o, fe), sm(R, o, fe), 0, sm(Pk, o, fe), sm(R, o, fe), o.m, o.m, o.m, rs, c,
+                    b, a), fs(o));
       // Q <- P Q and T = P R need only P: one phase, each block's two
       // products side by side so they share P's panels in L2
       const bool q_upd = k > 0, t_upd = k < steps - 1;
@@ -825,11 +831,11 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
         for (const Owner& o : probs)
           if (o.is_muon) {
             if (q_upd)
-              qt.add(mk(sm(Pk, o, fe), sm(Qcur, o, fe), 0, sm(Qn, o, fe), none, o.m, o.m, o.m, 0, 1.f,
+              qt.add(mk(sm(Pk, o, fe), sm(Qcur, o, fe), 0, sm(Qn, o, fe), none, o.m, o.m, o.m, rs, 1.f,
                         0.f, 0.f), fs(o));
             if (t_upd)
-              qt.add(mk(sm(Pk, o, fe), sm(R, o, fe), 0, sm(T, o, fe), none, o.m, o.m, o.m, 0, 1.f, 0.f,
-                        0.f), fs(o));
+              qt.add(mk(sm(Pk, o, fe), sm(R, o, fe), 0, sm(T, o, fe), none, o.m, o.m, o.m, rs, 1.f,
+                        0.f, 0.f), fs(o));
           }
       }
       if (q_upd) Qcur = Qn;
@@ -837,8 +843,8 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
         PhaseBuilder rr = new_phase(rec, fe);   // R = T P
         for (const Owner& o : probs)
           if (o.is_muon)
-            rr.add(mk(sm(T, o, fe), sm(Pk, o, fe), 0, sm(R, o, fe), none, o.m, o.m, o.m, 0, 1.f, 0.f,
-                      0.f), fs(o));
+            rr.add(mk(sm(T, o, fe), sm(Pk, o, fe), 0, sm(R, o, fe), none, o.m, o.m, o.m, rs, 1.f,
+                      0.f, 0.f), fs(o));
       }
     }
     PhaseBuilder* yy = nullptr;
