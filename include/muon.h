@@ -25,16 +25,22 @@
  *     device; host pointers are ordinary host memory and are only read
  *     during the call (tables are copied; the caller may free them after).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
- *     GPU work is enqueued asynchronously on it; no call synchronises the
- *     host except the first muon_step for a new table set (see below).
+ *     GPU work is enqueued asynchronously on it.  Only calls that create a
+ *     plan (below) and the diagnostic calls muon_device_error,
+ *     muon_profile_read and muon_release_workspace synchronise the host.
+ *     Once its plans exist, a sequence of muon_accumulate / muon_step /
+ *     muon_step_ex calls may be captured into a CUDA graph and replayed.
  *   - Return value: MUON_OK (0) or a negative MUON_ERR_* code.  On error
  *     nothing has been enqueued, and muon_last_error() describes it.
  *   - The caller owns every buffer it passes.  The library owns a per-table
- *     workspace (device memory) and plan, created on the first muon_step
- *     with a given table set and freed by muon_release_workspace().
- *     Creating a plan calls cudaMalloc and copies tables to the device, so
- *     that first call synchronises and must not be stream-captured.
- *   - Calls are not thread-safe with respect to each other.
+ *     workspace (device memory) and plans, created on the first muon_step
+ *     with a given table set (and on the first call with new NS settings or
+ *     a new workspace budget; muon_newton_schulz per shape) and freed by
+ *     muon_release_workspace().  Creating a plan calls cudaMalloc and copies
+ *     tables to the device, so such a call synchronises and must not be
+ *     stream-captured.
+ *   - Calls serialise on one library-wide lock; muon_last_error() reports
+ *     the last error of any thread.
  */
 #ifndef MUON_H
 #define MUON_H
