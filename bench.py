@@ -4,9 +4,11 @@ Default workload: the GPT-2-small parameter set (12 layers of Q, K (12
 heads), V, O 768x768, MLP up 3072x768 and down 768x3072; 84.9M elements,
 8 partitions, 128 alignment), four BF16 micro-batches accumulated in FP32,
 then one Muon step (5 standard Newton-Schulz steps, BF16 operands, clip
-0.05).  One timed step = 4 x accumulate + 1 x muon_step, all kernels of the
-library, inputs resident in HBM.  Every state buffer is 340 MB, larger than
-the 129 MB L2, so no flush is needed between steps.
+0.05).  One timed step = 3 x muon_accumulate + 1 x muon_step_ex that
+accumulates the 4th micro-batch in its first pass, all kernels of the
+library, inputs resident in HBM; the K timed steps are recorded into one
+CUDA graph and timed as one replay.  Every state buffer is 340 MB, larger
+than the 129 MB L2, so no flush is needed between steps.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 instead, on a bounded sample of the same workload.
