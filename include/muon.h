@@ -270,6 +270,26 @@ MUON_API int muon_newton_schulz_noalloc(const void* X, void* Y, int rows, int co
 /* Host-side counters (no GPU work).  Returns MUON_OK. */
 MUON_API int muon_get_stats(muon_stats_t* out);
 
+/* What a step over these tables would do, computed on the host alone (no
+ * CUDA call, no GPU needed): the tables are validated as muon_step
+ * validates them (same errors), and the Newton-Schulz grouping is the one
+ * the tensor-core path of a GB300 uses for ns_method and operand_mode. */
+typedef struct muon_table_info {
+  int64_t muon_params;      /* parameters with use_muon = 1 */
+  int64_t muon_blocks;      /* their head blocks: Newton-Schulz calls per step */
+  int64_t ns_problems;      /* after stacking equal consecutive blocks */
+  int32_t pair_engine;      /* 1: BF16 products on SM pairs (256-row tiles) */
+  int32_t stack_rows;       /* rows cap of a stack (0: no stacking) */
+  int64_t muon_elements;    /* elements of the Muon parameters */
+  int64_t aux_elements;     /* elements of the auxiliary parameters */
+  int64_t padding_elements; /* flat indices inside partitions no parameter covers */
+  int64_t segments;         /* (block or auxiliary parameter) x partition runs */
+  uint64_t workspace_bytes; /* the unbounded plan's Newton-Schulz work regions */
+} muon_table_info_t;
+MUON_API int muon_describe_tables(const muon_param_t* params, int nparams,
+                                  const muon_partition_t* parts, int nparts, int ns_method,
+                                  int operand_mode, muon_table_info_t* out);
+
 /* Message for the last error on this thread ("" if none). */
 MUON_API const char* muon_last_error(void);
 

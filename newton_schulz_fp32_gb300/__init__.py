@@ -35,7 +35,7 @@ PHASES = ["accumulate", "reduce", "gather", "ns_gemm", "norm", "scatter"]
 EXPORTED = ["muon_accumulate", "muon_step", "muon_newton_schulz", "muon_get_stats",
             "muon_last_error", "muon_release_workspace", "muon_device_error",
             "muon_profile_enable", "muon_profile_read", "muon_newton_schulz_noalloc",
-            "muon_step_ex", "muon_profile_enable_phases"]
+            "muon_step_ex", "muon_profile_enable_phases", "muon_describe_tables"]
 CLIP_MODES = {"update": 0, "grad": 1}
 
 
@@ -64,6 +64,15 @@ class StepOptions(ctypes.Structure):
 
 
 STEP_OPTIONS_V1_SIZE = 64   # struct_size of the layout that ends at workspace_budget
+
+
+class TableInfo(ctypes.Structure):
+    """muon_table_info_t."""
+    _fields_ = [("muon_params", ctypes.c_int64), ("muon_blocks", ctypes.c_int64),
+                ("ns_problems", ctypes.c_int64), ("pair_engine", ctypes.c_int32),
+                ("stack_rows", ctypes.c_int32), ("muon_elements", ctypes.c_int64),
+                ("aux_elements", ctypes.c_int64), ("padding_elements", ctypes.c_int64),
+                ("segments", ctypes.c_int64), ("workspace_bytes", ctypes.c_uint64)]
 
 
 class PhaseTime(ctypes.Structure):
@@ -99,11 +108,12 @@ def lib():
         L.muon_release_workspace.restype = None
         L.muon_profile_enable.argtypes = [I]
         L.muon_profile_enable_phases.argtypes = [ctypes.c_uint32]
+        L.muon_describe_tables.argtypes = [P, I, P, I, I, I, ctypes.POINTER(TableInfo)]
         L.muon_profile_read.argtypes = [ctypes.POINTER(PhaseTime), I, I]
         for name in ("muon_accumulate", "muon_step", "muon_step_ex", "muon_newton_schulz",
                      "muon_newton_schulz_noalloc", "muon_get_stats",
                      "muon_device_error", "muon_profile_enable", "muon_profile_read",
-                     "muon_profile_enable_phases"):
+                     "muon_profile_enable_phases", "muon_describe_tables"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -212,6 +222,20 @@ def step_ex(accum, momentum, master, params, parts, beta: float, lr: float, ns_m
                 operand_mode, result, stream,
                 step_options(clip_mode, grad_scale, adam, workspace_budget, last_grad,
                              last_grad_scale, last_grad_overwrite))
+
+
+def describe_tables(params, parts, ns_method="gram", operand_mode="bf16") -> dict:
+    """muon_describe_tables: what a step over these tables would do, on the
+    host alone (validation, block and stacking counts, workspace size)."""
+    p, np_ = _table(params, PARAM_DTYPE)
+    q, nq = _table(parts, PART_DTYPE)
+    method = NS_METHODS[ns_method] if isinstance(ns_method, str) else int(ns_method)
+    mode = OPERAND_MODES[operand_mode] if isinstance(operand_mode, str) else int(operand_mode)
+    info = TableInfo()
+    _check(lib().muon_describe_tables(p.ctypes.data if np_ else None, np_,
+                                      q.ctypes.data if nq else None, nq, method, mode,
+                                      ctypes.byref(info)))
+    return {name: getattr(info, name) for name, _ in TableInfo._fields_}
 
 
 def read_result(result) -> dict:

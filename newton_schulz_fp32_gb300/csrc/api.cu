@@ -602,18 +602,25 @@ struct NsFormats {
   }
 };
 
-int ns_formats(int method, int mode, NsFormats& f) {
+// Element formats of a plan given whether the tensor-core kernels run.
+void ns_formats_for(bool tc, int method, int mode, NsFormats& f) {
   const bool bf16 = mode == MUON_OPERANDS_BF16;
-  const char* env = std::getenv("MUON_GEMM");
-  const bool force_simt = env && std::strcmp(env, "simt") == 0;
-  f.tc = !force_simt && tc_available();
-  if (bf16 && !f.tc && !force_simt)
-    return fail(MUON_ERR_UNSUPPORTED, "BF16 operand mode needs an sm_103 (GB300) GPU");
+  f.tc = tc;
   f.xe = bf16 ? 2 : (f.tc ? 6 : 4);
   f.fe = f.tc ? 6 : 4;
   f.se = method == MUON_NS_STANDARD ? f.xe : f.fe;
   f.nsq = method == MUON_NS_STANDARD ? 2 : 5;
   f.need_qbf = method == MUON_NS_GRAM && bf16 && !f.tc;
+}
+
+int ns_formats(int method, int mode, NsFormats& f) {
+  const bool bf16 = mode == MUON_OPERANDS_BF16;
+  const char* env = std::getenv("MUON_GEMM");
+  const bool force_simt = env && std::strcmp(env, "simt") == 0;
+  const bool tc = !force_simt && tc_available();
+  if (bf16 && !tc && !force_simt)
+    return fail(MUON_ERR_UNSUPPORTED, "BF16 operand mode needs an sm_103 (GB300) GPU");
+  ns_formats_for(tc, method, mode, f);
   return MUON_OK;
 }
 
@@ -1608,5 +1615,36 @@ extern "C" int muon_profile_read(muon_phase_time_t* out, int nphases, int reset)
   if (out)
     for (int i = 0; i < nphases && i < MUON_PHASE_COUNT; ++i) out[i] = g_phase[i];
   if (reset) std::memset(g_phase, 0, sizeof(g_phase));
+  return MUON_OK;
+}
+
+extern "C" int muon_describe_tables(const muon_param_t* params, int nparams,
+                                    const muon_partition_t* parts, int nparts, int ns_method,
+                                    int operand_mode, muon_table_info_t* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_err.clear();
+  if (!out) return fail(MUON_ERR_INVALID, "out is NULL");
+  int rc = check_method(ns_method, 5, operand_mode);
+  if (rc != MUON_OK) return rc;
+  Layout L;
+  rc = validate_and_build(params, nparams, parts, nparts, L);
+  if (rc != MUON_OK) return rc;
+  const bool bf16 = operand_mode == MUON_OPERANDS_BF16;
+  const NsBlocks NB = ns_blocks(L.owners, true, bf16, -1);   // as on a GB300
+  NsFormats F;
+  ns_formats_for(true, ns_method, operand_mode, F);
+  std::memset(out, 0, sizeof(*out));
+  out->muon_params = L.n_muon_params;
+  out->muon_blocks = L.n_muon_owners;
+  out->ns_problems = static_cast<int64_t>(NB.probs.size());
+  out->pair_engine = NB.pairs ? 1 : 0;
+  out->stack_rows = NB.cap;
+  out->muon_elements = L.muon_elems;
+  out->aux_elements = L.aux_elems;
+  int64_t in_parts = 0;
+  for (int i = 0; i < nparts; ++i) in_parts += parts[i].flat_end - parts[i].flat_begin;
+  out->padding_elements = in_parts - L.muon_elems - L.aux_elems;
+  out->segments = static_cast<int64_t>(L.segs.size());
+  out->workspace_bytes = L.n_muon_owners ? F.ws_bytes(L.x_elems, NB.sq_elems) + 256 : 0;
   return MUON_OK;
 }
