@@ -105,3 +105,15 @@ def test_describe_rejects_what_the_step_rejects(lib):
     assert "heads" in lib.muon_last_error().decode() or "num_heads" in lib.muon_last_error().decode()
     with pytest.raises(nsg.MuonError):
         nsg.describe_tables(wl.tiny_layout().params, wl.tiny_layout().parts, 7, "bf16")
+
+
+def test_auxiliary_only_and_empty_tables(lib):
+    lay = wl.build_layout([[wl.ParamSpec("ln", 1, 768, use_muon=False),
+                            wl.ParamSpec("emb", 40, 96, use_muon=False)]], 128, 2)
+    d = nsg.describe_tables(lay.params, lay.parts)
+    assert d["muon_params"] == d["muon_blocks"] == d["ns_problems"] == 0
+    assert d["aux_elements"] == 768 + 40 * 96 and d["workspace_bytes"] == 0
+    total = int(sum(int(q["flat_end"]) - int(q["flat_begin"]) for q in lay.parts))
+    assert d["padding_elements"] == total - 768 - 40 * 96
+    e = nsg.describe_tables([], [])   # (the engine choice is vacuous without blocks)
+    assert all(v == 0 for k, v in e.items() if k not in ("stack_rows", "pair_engine"))
