@@ -183,6 +183,95 @@ def test_bf16_mode_one_step_brute_force():
     assert np.array_equal(Y, np.array(X1, np.float32))
 
 
+def _gram_bf16_brute(G, steps, r_in_bf16=False, q_to_bf16=True):
+    """The gram method in BF16-operand mode written as scalar loops, with
+    the rounding points of the reading: X0 = bf16(G / d); R0 = fl32(sum of
+    bf16 products); per step P = fl32(fl32(c * RR) + fl32(b * R)) (+ a on
+    the diagonal, one more float32 addition), Q <- fl32(P Q) (Q1 = P),
+    T = fl32(P R) and R = fl32(T P) except after the last step; finally
+    Y = bf16(fl32(bf16(Q) X0)).  r_in_bf16 / q_to_bf16 switch the two
+    rounding points a plausible mistake would move."""
+    f32 = np.float32
+    a, b, c = 3.4445, -4.7750, 2.0315
+    m, n = G.shape
+    assert m <= n
+    d = f32(np.sqrt(float(np.sum(G.astype(np.float64) ** 2))) + 1e-7)
+    X = [[_rne_bf16_scalar(f32(G[i, j]) / d) for j in range(n)] for i in range(m)]
+
+    def rr(v):
+        return _rne_bf16_scalar(v) if r_in_bf16 else v
+
+    def prod(L, Rt, i, j, K):
+        return f32(sum(float(L[i][k]) * float(Rt[k][j]) for k in range(K)))
+
+    Xt = [[X[j][i] for j in range(m)] for i in range(n)]
+    R = [[rr(prod(X, Xt, i, j, n)) for j in range(m)] for i in range(m)]
+    Q = None
+    for k in range(steps):
+        P = []
+        for i in range(m):
+            row = []
+            for j in range(m):
+                v = f32(f32(f32(c) * prod(R, R, i, j, m)) + f32(f32(b) * f32(R[i][j])))
+                if i == j:
+                    v = f32(v + f32(a))
+                row.append(v)
+            P.append(row)
+        Q = P if k == 0 else [[prod(P, Q, i, j, m) for j in range(m)] for i in range(m)]
+        if k < steps - 1:
+            T = [[prod(P, R, i, j, m) for j in range(m)] for i in range(m)]
+            R = [[rr(prod(T, P, i, j, m)) for j in range(m)] for i in range(m)]
+    Qy = [[_rne_bf16_scalar(q) if q_to_bf16 else q for q in row] for row in Q]
+    return np.array([[_rne_bf16_scalar(prod(Qy, X, i, j, m)) for j in range(n)]
+                     for i in range(m)], np.float32)
+
+
+GRAM_BRUTE_CASES = [(np.array([[0.3, -1.2, 0.7], [2.0, 0.1, -0.4]], np.float32), 1),
+                    (np.array([[0.3, -1.2, 0.7], [2.0, 0.1, -0.4]], np.float32), 2),
+                    (wl.rng_for(31).standard_normal((3, 5)).astype(np.float32), 1),
+                    (wl.rng_for(31).standard_normal((3, 5)).astype(np.float32), 2),
+                    (wl.rng_for(32).standard_normal((3, 5)).astype(np.float32), 3)]
+
+
+@pytest.mark.parametrize("case", range(len(GRAM_BRUTE_CASES)))
+def test_gram_bf16_mode_brute_force(case):
+    """One, two and three gram steps on 2x3 and 3x5 matrices, scalar loops
+    against the oracle, bit for bit (the BF16-mode gram reading: FP32
+    recurrence, Q rounded to bf16 before Y)."""
+    G, steps = GRAM_BRUTE_CASES[case]
+    want = _gram_bf16_brute(G, steps)
+    assert np.array_equal(ons.newton_schulz(G, "gram", steps, "bf16"), want)
+    # the transposed input takes the same path (rows > cols is transposed)
+    assert np.array_equal(ons.newton_schulz(G.T.copy(), "gram", steps, "bf16"), want.T)
+
+
+def _planted_gram(r_in_bf16, q_to_bf16):
+    """The oracle's BF16-mode gram with one rounding point moved."""
+    def bad(X0, steps, mode):
+        a, b, c = ons.A_COEF, ons.B_COEF, ons.C_COEF
+        rr = (lambda M: obf.round_bf16(M)) if r_in_bf16 else (lambda M: M)
+        R = rr(ons._gemm_f32(X0, X0.T, 1.0))
+        Q = None
+        for k in range(steps):
+            P = ons._gemm_f32(R, R, c, R, b, gamma=a)
+            Q = P if k == 0 else ons._gemm_f32(P, Q, 1.0)
+            if k < steps - 1:
+                R = rr(ons._gemm_f32(ons._gemm_f32(P, R, 1.0), P, 1.0))
+        return ons._gemm_bf16(obf.round_bf16(Q) if q_to_bf16 else Q, X0, 1.0)
+    return bad
+
+
+@pytest.mark.parametrize("plant", [(True, True), (False, False)],
+                         ids=["R kept in bf16", "Q not rounded before Y"])
+def test_planted_gram_bf16_rounding_points_are_caught(monkeypatch, plant):
+    monkeypatch.setattr(ons, "_gram", _planted_gram(*plant))
+    caught = 0
+    for G, steps in GRAM_BRUTE_CASES:
+        caught += not np.array_equal(ons.newton_schulz(G, "gram", steps, "bf16"),
+                                     _gram_bf16_brute(G, steps))
+    assert caught >= 3
+
+
 # ------------------------------------------------------------ planted mistakes
 
 def test_planted_wrong_coefficient_sign_is_caught(monkeypatch):
@@ -402,9 +491,29 @@ def test_bad_tables_raise():
         om.muon_step_flat(acc, acc, acc, bad, lay.parts, 0.95, 0.02)
 
 
+def _f32_round(x):
+    """Nearest float32 of a Python float (IEEE round to nearest even), by
+    the C library's double -> float conversion inside struct."""
+    import struct
+    return struct.unpack("<f", struct.pack("<f", x))[0]
+
+
 def test_accumulate_rounding_sequence():
-    g = wl.to_bf16_values(np.array([1.0, 3.0, 0.1, -7.5], np.float32))
-    a = om.accumulate(None, g, 1.0 / 3.0, overwrite=True)
-    assert np.array_equal(a, np.float32(1.0 / 3.0) * g)
-    b = om.accumulate(a, g, 1.0 / 3.0)
-    assert np.array_equal(b, a + np.float32(1.0 / 3.0) * g)
+    """Each micro-batch adds fl32(fl32(scale) * g) to the FP32 accumulator
+    with one FP32 rounding per operation.  The expected values come from
+    Python floats (exact here: products of two float32 values and sums of
+    two close float32 values fit a double) rounded to float32 by struct,
+    not from numpy."""
+    g1 = wl.to_bf16_values(wl.rng_for(33).standard_normal(64).astype(np.float32))
+    g2 = wl.to_bf16_values(wl.rng_for(34).standard_normal(64).astype(np.float32))
+    s32 = _f32_round(1.0 / 3.0)
+    want_a = [_f32_round(s32 * float(x)) for x in g1]
+    a = om.accumulate(None, g1, 1.0 / 3.0, overwrite=True)
+    assert a.tolist() == want_a
+    want_b = [_f32_round(x + _f32_round(s32 * float(y))) for x, y in zip(want_a, g2)]
+    b = om.accumulate(a, g2, 1.0 / 3.0)
+    assert b.tolist() == want_b
+    # the inputs tell the two roundings apart: a fused multiply-add (the
+    # product left unrounded) gives other values on some elements
+    fused = [_f32_round(x + s32 * float(y)) for x, y in zip(want_a, g2)]
+    assert sum(u != v for u, v in zip(want_b, fused)) >= 5
