@@ -240,16 +240,23 @@ MUON_API int muon_step_ex(float* accum, float* momentum, float* master,
 MUON_API int muon_newton_schulz(const void* X, void* Y, int rows, int cols, int io_dtype,
                        int ns_method, int ns_steps, int operand_mode, void* stream);
 
-/* Newton-Schulz of one matrix, exactly as muon_newton_schulz (same
- * arguments, kernels and results), for callers that cannot allocate device
- * memory: code that runs while a stream is being captured into a CUDA
- * graph, processes whose device memory belongs to an allocator that must
- * not be bypassed, runtimes that forbid allocation after start-up.  It
- * calls no cudaMalloc/cudaFree and no allocating library routine; all of
- * its scratch (norm partials, the X and m x m work matrices, GEMM and TMA
- * descriptors) sits in one fixed 16 MiB __device__ array inside the
- * library, which every GPU that loads the library holds until the process
- * exits.  The pages have no counterpart of this entry point.
+/* Newton-Schulz of one matrix (the arguments and the computation of
+ * muon_newton_schulz) with no device allocation, for callers that cannot
+ * call cudaMalloc: processes whose device memory is handed out by another
+ * allocator that reserves it up front (a framework's caching allocator,
+ * which a direct cudaMalloc would bypass or find exhausted), and runtimes
+ * that forbid allocation once they serve (cudaMalloc may synchronise the
+ * device and stall a latency-bound loop).  It calls no cudaMalloc/cudaFree
+ * and no allocating library routine; all of its scratch (norm partials,
+ * the X and m x m work matrices, GEMM and TMA descriptors) sits in one
+ * fixed 16 MiB __device__ array inside the library, which every GPU that
+ * loads the library holds until the process exits.  The pages have no
+ * counterpart of this entry point.
+ *   Kernels: BF16-operand products run on the single-SM tensor-core
+ *   kernel; FP32-operand products and gram's m x m recurrence run on the
+ *   CUDA-core FP32 GEMM (muon_newton_schulz uses SM pairs and the split-3
+ *   tensor-core products there), so the two entries agree within the
+ *   operand mode's tolerance, not bit for bit.
  *   Limits: rows * cols <= MUON_NOALLOC_MAX_ELEMS, min(rows, cols) <=
  *   MUON_NOALLOC_MAX_MIN_DIM, max(rows, cols) <= MUON_NOALLOC_MAX_DIM;
  *   larger matrices return MUON_ERR_UNSUPPORTED (see muon_last_error()).
@@ -257,9 +264,12 @@ MUON_API int muon_newton_schulz(const void* X, void* Y, int rows, int cols, int 
  *   (cudaGetSymbolAddress, with that device current) and keeps it; make
  *   that first call before any stream capture.
  *   All calls share the one array and leave their contents in it: two
- *   calls whose work overlaps on the GPU (different streams or host
- *   threads) race and corrupt each other's results.
- *   The descriptors are copied from host memory on `stream` each call. */
+ *   calls whose work overlaps on the GPU (different streams) race and
+ *   corrupt each other's results.  Host threads may call concurrently: a
+ *   call holds the library lock while it builds its descriptors and copies
+ *   them (from host arrays that the next call reuses) onto `stream`.
+ *   A bounded wait that runs out in its tensor-core products records a
+ *   code that muon_device_error reports. */
 #define MUON_NOALLOC_MAX_ELEMS 1048576
 #define MUON_NOALLOC_MAX_MIN_DIM 512
 #define MUON_NOALLOC_MAX_DIM 16384
@@ -289,6 +299,28 @@ typedef struct muon_table_info {
 MUON_API int muon_describe_tables(const muon_param_t* params, int nparams,
                                   const muon_partition_t* parts, int nparts, int ns_method,
                                   int operand_mode, muon_table_info_t* out);
+
+/* Cross-checks for tests (not a production setting): plans built after
+ * the call route the Newton-Schulz products through another kernel or
+ * schedule, so tests can compare them with the product path.  Existing
+ * plans keep what they were built with (muon_release_workspace drops them).
+ * Every knob's default is the product path.
+ *   MUON_TEST_GEMM        0 default; 1 CUDA-core GEMM for every product;
+ *                         2 single-SM tensor-core kernel instead of SM pairs
+ *   MUON_TEST_STACK       1 default (equal consecutive blocks stacked); 0 off
+ *   MUON_TEST_FLOW        1 default (one SM-pair launch per iteration);
+ *                         0 one launch per product
+ *   MUON_TEST_FLOW_LAG    0 default (half the problems); k >= 1
+ *   MUON_TEST_FLOW_WAVES  1 default; k >= 1 groups of problems
+ * Errors: MUON_ERR_INVALID for an unknown knob or value. */
+typedef enum {
+  MUON_TEST_GEMM = 0,
+  MUON_TEST_STACK = 1,
+  MUON_TEST_FLOW = 2,
+  MUON_TEST_FLOW_LAG = 3,
+  MUON_TEST_FLOW_WAVES = 4
+} muon_test_knob_t;
+MUON_API int muon_testing_set(int knob, int value);
 
 /* Message for the last error on this thread ("" if none). */
 MUON_API const char* muon_last_error(void);

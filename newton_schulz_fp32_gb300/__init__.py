@@ -35,7 +35,8 @@ PHASES = ["accumulate", "reduce", "gather", "ns_gemm", "norm", "scatter"]
 EXPORTED = ["muon_accumulate", "muon_step", "muon_newton_schulz", "muon_get_stats",
             "muon_last_error", "muon_release_workspace", "muon_device_error",
             "muon_profile_enable", "muon_profile_read", "muon_newton_schulz_noalloc",
-            "muon_step_ex", "muon_profile_enable_phases", "muon_describe_tables"]
+            "muon_step_ex", "muon_profile_enable_phases", "muon_describe_tables",
+            "muon_testing_set"]
 CLIP_MODES = {"update": 0, "grad": 1}
 
 
@@ -110,10 +111,12 @@ def lib():
         L.muon_profile_enable_phases.argtypes = [ctypes.c_uint32]
         L.muon_describe_tables.argtypes = [P, I, P, I, I, I, ctypes.POINTER(TableInfo)]
         L.muon_profile_read.argtypes = [ctypes.POINTER(PhaseTime), I, I]
+        L.muon_testing_set.argtypes = [I, I]
         for name in ("muon_accumulate", "muon_step", "muon_step_ex", "muon_newton_schulz",
                      "muon_newton_schulz_noalloc", "muon_get_stats",
                      "muon_device_error", "muon_profile_enable", "muon_profile_read",
-                     "muon_profile_enable_phases", "muon_describe_tables"):
+                     "muon_profile_enable_phases", "muon_describe_tables",
+                     "muon_testing_set"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -299,3 +302,34 @@ def profile_read(reset: bool = False) -> dict:
     return {name: {"launches": arr[i].launches, "ms": arr[i].total_ms,
                    "bytes": arr[i].algorithmic_bytes, "flops": arr[i].algorithmic_flops}
             for i, name in enumerate(PHASES)}
+
+
+# muon_testing_set knobs and their product-path defaults
+TEST_KNOBS = {"gemm": (0, 0), "stack": (1, 1), "flow": (2, 1), "flow_lag": (3, 0),
+              "flow_waves": (4, 1)}
+TEST_GEMM = {"default": 0, "simt": 1, "tc1": 2}
+
+
+class testing:
+    """Cross-check context for tests: plans built inside it route the
+    Newton-Schulz products as the knobs say (gemm="simt" CUDA-core GEMM,
+    gemm="tc1" single-SM tensor-core kernel, stack=0, flow=0, flow_lag=k,
+    flow_waves=k).  Plans are dropped on entry and exit, and every knob
+    returns to its product-path default on exit."""
+
+    def __init__(self, **knobs):
+        self.knobs = knobs
+
+    def __enter__(self):
+        release_workspace()
+        for name, value in self.knobs.items():
+            if name == "gemm" and isinstance(value, str):
+                value = TEST_GEMM[value]
+            _check(lib().muon_testing_set(TEST_KNOBS[name][0], int(value)))
+        return self
+
+    def __exit__(self, *exc):
+        release_workspace()
+        for knob, default in TEST_KNOBS.values():
+            _check(lib().muon_testing_set(knob, default))
+        return False

@@ -81,6 +81,17 @@ struct Counters {
 Counters g_cnt;
 std::mutex g_mu;
 
+// Cross-check settings (muon_testing_set): plans built while they differ
+// from the defaults run other kernels or schedules.
+struct TestKnobs {
+  int gemm = 0;         // 0 product path, 1 CUDA-core GEMM everywhere, 2 no SM pairs
+  int stack = 1;        // 0: one NS problem per block
+  int flow = 1;         // 0: one pair launch per product
+  int flow_lag = 0;     // pair task wavefront lag (0: half the problems)
+  int flow_waves = 1;   // pair task order by groups of problems
+};
+TestKnobs g_knobs;
+
 struct PendingEvent {
   int phase;
   cudaEvent_t start, stop;
@@ -504,8 +515,7 @@ int build_pair_program(std::vector<std::unique_ptr<GemmPhase>>& phases, int a, i
   // operands stay in L2) but leaves less slack before each dependency.
   // (GPT-2-small, 120 problems: lag 4 / 8 / 16 / 32 / 64 / product-major
   // gave 1.274 / 1.194 / 1.145 / 1.135 / 1.134 / 1.158 ms per iteration)
-  const char* lenv = std::getenv("MUON_FLOW_LAG");
-  const int lag = lenv ? std::max(1, std::atoi(lenv)) : std::max(1, np / 2);
+  const int lag = g_knobs.flow_lag > 0 ? g_knobs.flow_lag : std::max(1, np / 2);
   auto make_tasks = [&](int k, int j, std::vector<PairTask>& out) {
     const GemmProblem& q = phases[a + k]->probs[j];
     for (const GemmTile& t : tl[k][j]) {
@@ -583,10 +593,10 @@ struct WsMat {
 //   arithmetic); then Y = bf16(Q) X0 (BF16 mode) or Q X0 (FP32 mode).
 // Engines: BF16 operands on the tensor cores, on SM pairs with 256 x 256
 // tiles (ENGINE_TC2) when every block has at least 192 rows, else on single
-// SMs with 128 x 256 tiles (ENGINE_TC; MUON_GEMM=tc1 forces it); FP32
-// operands on the tensor cores through split-3 planes (ENGINE_X3); with
-// MUON_GEMM=simt everything runs on the CUDA-core kernel with plain bf16 /
-// fp32 storage.
+// SMs with 128 x 256 tiles (ENGINE_TC; the MUON_TEST_GEMM cross-check can
+// force it); FP32 operands on the tensor cores through split-3 planes
+// (ENGINE_X3); the CUDA-core cross-check runs everything on the CUDA-core
+// kernel with plain bf16 / fp32 storage.
 // Element formats and region counts of a plan: X regions (m x n) in xe,
 // the m x m regions in se, nsq of them, and a bf16 copy of Q for the
 // CUDA-core gram path.
@@ -615,8 +625,7 @@ void ns_formats_for(bool tc, int method, int mode, NsFormats& f) {
 
 int ns_formats(int method, int mode, NsFormats& f) {
   const bool bf16 = mode == MUON_OPERANDS_BF16;
-  const char* env = std::getenv("MUON_GEMM");
-  const bool force_simt = env && std::strcmp(env, "simt") == 0;
+  const bool force_simt = g_knobs.gemm == 1;
   const bool tc = !force_simt && tc_available();
   if (bf16 && !tc && !force_simt)
     return fail(MUON_ERR_UNSUPPORTED, "BF16 operand mode needs an sm_103 (GB300) GPU");
@@ -640,10 +649,8 @@ struct NsBlocks {
 };
 
 NsBlocks ns_blocks(const std::vector<Owner>& owners, bool tc, bool bf16, int force_cap) {
-  const char* genv = std::getenv("MUON_GEMM");
-  const bool allow_pairs = tc && bf16 && !(genv && std::strcmp(genv, "tc1") == 0);
-  const char* senv = std::getenv("MUON_STACK");
-  const bool stack = !(senv && std::strcmp(senv, "0") == 0);   // MUON_STACK=0: one block per problem
+  const bool allow_pairs = tc && bf16 && g_knobs.gemm != 2;
+  const bool stack = g_knobs.stack != 0;
   auto group = [&](int cap) {
     NsBlocks B;
     if (!stack) cap = 0;
@@ -916,10 +923,8 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
     P.flops += ph->flops;
   }
   // runs of consecutive pair-engine phases become task programs
-  const char* wenv = std::getenv("MUON_FLOW_WAVES");
-  const int flow_waves = wenv ? std::max(1, std::atoi(wenv)) : 1;
-  const char* fenv = std::getenv("MUON_FLOW");
-  const bool flow = !(fenv && std::strcmp(fenv, "0") == 0);   // MUON_FLOW=0: a program per phase
+  const int flow_waves = std::max(1, g_knobs.flow_waves);
+  const bool flow = g_knobs.flow != 0;   // 0: a program per phase
   for (int k = 0; k < static_cast<int>(P.phases.size());) {
     if (P.phases[k]->engine != ENGINE_TC2) { ++k; continue; }
     int e = k + 1;
@@ -1183,6 +1188,8 @@ void set_last_error(const char* msg) {
   if (msg) g_err = msg;
   else g_err.clear();
 }
+
+std::mutex& library_mutex() { return g_mu; }
 
 }  // namespace muon
 
@@ -1584,7 +1591,38 @@ extern "C" int muon_device_error(void) {
   };
   for (auto& tp : g_plans) check(tp->d_err);
   for (auto& sp : g_single) check(sp->err);
+  const int na = noalloc_take_device_error();
+  if (na) worst = na;
   return worst;
+}
+
+extern "C" int muon_testing_set(int knob, int value) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_err.clear();
+  switch (knob) {
+    case MUON_TEST_GEMM:
+      if (value < 0 || value > 2) return fail(MUON_ERR_INVALID, "MUON_TEST_GEMM takes 0, 1 or 2");
+      g_knobs.gemm = value;
+      return MUON_OK;
+    case MUON_TEST_STACK:
+      if (value != 0 && value != 1) return fail(MUON_ERR_INVALID, "MUON_TEST_STACK takes 0 or 1");
+      g_knobs.stack = value;
+      return MUON_OK;
+    case MUON_TEST_FLOW:
+      if (value != 0 && value != 1) return fail(MUON_ERR_INVALID, "MUON_TEST_FLOW takes 0 or 1");
+      g_knobs.flow = value;
+      return MUON_OK;
+    case MUON_TEST_FLOW_LAG:
+      if (value < 0) return fail(MUON_ERR_INVALID, "MUON_TEST_FLOW_LAG takes a value >= 0");
+      g_knobs.flow_lag = value;
+      return MUON_OK;
+    case MUON_TEST_FLOW_WAVES:
+      if (value < 1) return fail(MUON_ERR_INVALID, "MUON_TEST_FLOW_WAVES takes a value >= 1");
+      g_knobs.flow_waves = value;
+      return MUON_OK;
+    default:
+      return fail(MUON_ERR_INVALID, "unknown testing knob");
+  }
 }
 
 extern "C" int muon_profile_enable(int on) {

@@ -7,6 +7,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -228,6 +229,11 @@ constexpr int kX3BM = 128, kX3BN = 128;
 
 // Sets (msg != nullptr) or clears the text muon_last_error() returns.
 void set_last_error(const char* msg);
+// The lock every entry point holds for the whole call.
+std::mutex& library_mutex();
+// The allocation-free entry's device error flag on every device that has
+// used it: the first nonzero code, cleared once read (0 = none).
+int noalloc_take_device_error();
 
 // Tensor-core (tcgen05) path, BF16 operands.
 constexpr int kTcBM = 128;

@@ -1,15 +1,20 @@
 // muon_newton_schulz_noalloc: Newton-Schulz of one matrix without any
 // device allocation.
 //
-// Some callers cannot call cudaMalloc: code running while a CUDA stream is
-// being captured into a graph, processes whose device memory is owned by
-// another allocator that must not be bypassed, and embedded runtimes that
-// forbid allocation after start-up.  For them this entry point runs the same
-// kernels as muon_newton_schulz, but every byte of scratch it needs (norm
+// Some callers cannot call cudaMalloc: processes whose device memory is
+// handed out by another allocator that reserves it up front (a direct
+// cudaMalloc would bypass it or find the memory gone), and runtimes that
+// forbid allocation once they serve (cudaMalloc can synchronise the device
+// and stall them).  For them this entry point computes what
+// muon_newton_schulz computes, but every byte of scratch it needs (norm
 // partial sums, the X / X^T products, the m x m matrices, GEMM descriptors
 // and TMA tensor maps) lives in one file-scope __device__ array of fixed
 // size.  The array exists on every GPU that loads the library, from module
-// load until the process exits.
+// load until the process exits.  BF16-operand products run on the
+// single-SM tensor-core kernel; FP32-operand products and gram's m x m
+// recurrence run on the CUDA-core FP32 GEMM (the allocating entry uses SM
+// pairs and split-3 tensor-core products there), so results agree with
+// muon_newton_schulz within the operand mode's tolerance.
 //
 // Limits: rows * cols <= 2^20, min(rows, cols) <= 512, max(rows, cols) <=
 // 16384; the array is 16 MiB.
@@ -18,7 +23,14 @@
 // it names a host-side stand-in), so the first call on each device asks the
 // runtime for the address with cudaGetSymbolAddress, with that device
 // current, and keeps it.  Every call shares the array: two calls whose work
-// overlaps on the GPU (different streams, or different host threads) race.
+// overlaps on the GPU (different streams) race.  The host-side plan tables
+// below are shared too, so a call holds the library lock from the address
+// lookup until its last copy has been enqueued.
+//
+// The word at the start of the array is the error flag of the tensor-core
+// GEMM's bounded waits.  It is zero when the module loads and is cleared
+// only when muon_device_error reads it, so a code is not lost before it is
+// queried.
 #include <cstring>
 
 #include "muon_internal.h"
@@ -92,9 +104,23 @@ int tile_list_for(int engine, int M, int N, int sym, int* nlists) {
 
 using namespace muon;
 
+int muon::noalloc_take_device_error() {   // the caller holds the library lock
+  int worst = 0;
+  for (int dev = 0; dev < kMaxDevices; ++dev) {
+    if (g_scratch_addr[dev] == nullptr) continue;
+    int v = 0;
+    if (cudaMemcpy(&v, g_scratch_addr[dev], sizeof(int), cudaMemcpyDefault) == cudaSuccess && v) {
+      if (!worst) worst = v;
+      cudaMemset(g_scratch_addr[dev], 0, sizeof(int));
+    }
+  }
+  return worst;
+}
+
 extern "C" int muon_newton_schulz_noalloc(const void* X, void* Y, int rows, int cols, int io_dtype,
                                           int ns_method, int ns_steps, int operand_mode,
                                           void* stream) {
+  std::lock_guard<std::mutex> lk(library_mutex());
   set_last_error(nullptr);
   if (!X || !Y || X == Y) return nofail(MUON_ERR_INVALID, "X, Y must be distinct device arrays");
   if (rows < 1 || cols < 1) return nofail(MUON_ERR_INVALID, "rows and cols must be >= 1");
@@ -238,8 +264,7 @@ extern "C" int muon_newton_schulz_noalloc(const void* X, void* Y, int rows, int 
   }
   for (int l = 0; l < nlists; ++l)
     std::memcpy(h_tiles + l * kMaxTilesPerList, g_lists[l].tiles, sizeof(GemmTile) * g_lists[l].count);
-  if (cudaMemsetAsync(err_flag, 0, sizeof(int), s) != cudaSuccess ||
-      cudaMemcpyAsync(d_probs, h_probs, sizeof(GemmProblem) * nops, cudaMemcpyHostToDevice, s) !=
+  if (cudaMemcpyAsync(d_probs, h_probs, sizeof(GemmProblem) * nops, cudaMemcpyHostToDevice, s) !=
           cudaSuccess ||
       cudaMemcpyAsync(d_maps, g_maps, sizeof(TcMaps) * nops, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(d_tiles, h_tiles, sizeof(GemmTile) * kMaxTilesPerList * nlists,

@@ -4,7 +4,6 @@ Each test builds seeded inputs with ``workloads``, runs the library on the
 GPU and the oracle on the CPU from the same inputs, and compares with the
 rules in ``harness``: bit-exact for accumulation, momentum, ownership,
 padding and skips; per-matrix tolerances for the Newton-Schulz update."""
-import os
 
 import numpy as np
 import pytest
@@ -225,16 +224,10 @@ def test_tensor_core_path_matches_cuda_core_path(torch, method, mode):
     else:
         X = to_dev(G, torch)
     outs = []
-    for path in (None, "simt"):
-        nsg.release_workspace()
-        if path:
-            os.environ["MUON_GEMM"] = path
-        try:
+    for path in ("default", "simt"):
+        with nsg.testing(gemm=path):
             outs.append(nsg.newton_schulz(X, ns_method=method, operand_mode=mode)
                         .float().cpu().numpy())
-        finally:
-            os.environ.pop("MUON_GEMM", None)
-            nsg.release_workspace()
     assert_close_update(outs[0], outs[1], mode, f"tensor vs cuda cores {method} {mode}")
     want = ons.newton_schulz(G, method, 5, ORACLE_MODE[mode])
     for o in outs:
@@ -376,25 +369,20 @@ def test_llama3_8b_config_sampled(torch):
 def test_stacked_head_blocks_match_separate_blocks(torch, method, mode):
     """Consecutive equal head blocks (GPT-2 Q/K: 12 blocks of 64 x 768) run
     stacked into block-diagonal problems of up to 256 rows; the step must
-    agree with one problem per block (MUON_STACK=0) within the operand
+    agree with one problem per block (stacking off) within the operand
     mode's rule, and both with the oracle on a sampled block."""
     lay = wl.gpt2_small_layout(layers=1, nparts=2)
     seed = 77
     g = wl.gaussian_grads(lay, seed, 0, wl.loguniform_sigmas(lay, seed, 1e-3, 1e-1))
     m = wl.gaussian_grads(lay, seed, 1, None, bf16=False)
     outs = []
-    for stack in ("1", "0"):
-        nsg.release_workspace()
-        os.environ["MUON_STACK"] = stack
-        try:
+    for stack in (1, 0):
+        with nsg.testing(stack=stack):
             st = GpuState(torch, wl.pack(lay, g), wl.pack(lay, m), wl.pack(lay, m))
             before = st.numpy()
             nsg.step(st.accum, st.momentum, st.master, lay.params, lay.parts, BETA, LR, method, 5,
                      0.0, mode)
             outs.append(wl.unpack(lay, st.accum.cpu().numpy()))
-        finally:
-            os.environ.pop("MUON_STACK", None)
-            nsg.release_workspace()
     for k, spec in enumerate(lay.specs):
         assert_close_update(outs[0][k], outs[1][k], mode, f"stacked vs separate {spec.name}")
     res = om.muon_step_flat(*before, lay.params, lay.parts, BETA, LR, method, 5, 0.0,
@@ -403,9 +391,9 @@ def test_stacked_head_blocks_match_separate_blocks(torch, method, mode):
     assert_close_update(outs[0][0], want[0], mode, "stacked Q vs oracle")
 
 
-@pytest.mark.parametrize("env", [{"MUON_FLOW": "0"}, {"MUON_FLOW_LAG": "1"},
-                                 {"MUON_FLOW_LAG": "1000"}, {"MUON_FLOW_WAVES": "3", "MUON_FLOW_LAG": "1000"}])
-def test_pair_dataflow_schedule_is_bitwise_neutral(torch, env):
+@pytest.mark.parametrize("knobs", [{"flow": 0}, {"flow_lag": 1}, {"flow_lag": 1000},
+                                   {"flow_waves": 3, "flow_lag": 1000}])
+def test_pair_dataflow_schedule_is_bitwise_neutral(torch, knobs):
     """The SM-pair kernel's task order and dependency counters change only
     when tiles run, never what they compute: one launch per product, the
     tightest wavefront, product-major order and grouped waves all give the
@@ -416,22 +404,12 @@ def test_pair_dataflow_schedule_is_bitwise_neutral(torch, env):
     g = wl.gaussian_grads(lay, seed, 0, wl.loguniform_sigmas(lay, seed, 1e-3, 1e-1))
     m = wl.gaussian_grads(lay, seed, 1, None, bf16=False)
     outs = []
-    for e in ({}, env):
-        nsg.release_workspace()
-        old = {k: os.environ.get(k) for k in e}
-        os.environ.update(e)
-        try:
+    for e in ({}, knobs):
+        with nsg.testing(**e):
             st = GpuState(torch, wl.pack(lay, g), wl.pack(lay, m), wl.pack(lay, m))
             nsg.step(st.accum, st.momentum, st.master, lay.params, lay.parts, BETA, LR, "standard",
                      5, CLIP, "bf16")
             outs.append(st.numpy())
-        finally:
-            for k, v in old.items():
-                if v is None:
-                    os.environ.pop(k, None)
-                else:
-                    os.environ[k] = v
-            nsg.release_workspace()
     for a, b in zip(*outs):
         assert np.array_equal(bits(a), bits(b))
     assert nsg.device_error() == 0
@@ -440,26 +418,20 @@ def test_pair_dataflow_schedule_is_bitwise_neutral(torch, env):
 @pytest.mark.parametrize("method", ["standard", "gram"])
 def test_pair_kernel_matches_single_sm_kernel(torch, method):
     """BF16 products on SM pairs (256x256 tiles, cta_group::2) against the
-    single-SM kernel (128x256 tiles, MUON_GEMM=tc1) on one GPT-2 layer, both
+    single-SM kernel (128x256 tiles, the "tc1" cross-check) on one GPT-2 layer, both
     by the BF16 rule, and both against the oracle on a sampled block."""
     lay = wl.gpt2_small_layout(layers=1, nparts=2)
     seed = 79
     g = wl.gaussian_grads(lay, seed, 0, wl.loguniform_sigmas(lay, seed, 1e-3, 1e-1))
     m = wl.gaussian_grads(lay, seed, 1, None, bf16=False)
     outs = []
-    for path in (None, "tc1"):
-        nsg.release_workspace()
-        if path:
-            os.environ["MUON_GEMM"] = path
-        try:
+    for path in ("default", "tc1"):
+        with nsg.testing(gemm=path):
             st = GpuState(torch, wl.pack(lay, g), wl.pack(lay, m), wl.pack(lay, m))
             before = st.numpy()
             nsg.step(st.accum, st.momentum, st.master, lay.params, lay.parts, BETA, LR, method, 5,
                      0.0, "bf16")
             outs.append(wl.unpack(lay, st.accum.cpu().numpy()))
-        finally:
-            os.environ.pop("MUON_GEMM", None)
-            nsg.release_workspace()
     for k, spec in enumerate(lay.specs):
         assert_close_update(outs[0][k], outs[1][k], "bf16", f"pairs vs single SM {spec.name}")
     res = om.muon_step_flat(*before, lay.params, lay.parts, BETA, LR, method, 5, 0.0, "bf16")
