@@ -1,14 +1,18 @@
 """Benchmark of the Muon optimizer step on GB300.
 
-Default workload: the GPT-2-small parameter set (12 layers of Q, K (12
-heads), V, O 768x768, MLP up 3072x768 and down 768x3072; 84.9M elements,
-8 partitions, 128 alignment), four BF16 micro-batches accumulated in FP32,
-then one Muon step (5 standard Newton-Schulz steps, BF16 operands, clip
-0.05).  One timed step = 3 x muon_accumulate + 1 x muon_step_ex that
-accumulates the 4th micro-batch in its first pass, all kernels of the
-library, inputs resident in HBM; the K timed steps are recorded into one
-CUDA graph and timed as one replay.  Every state buffer is 340 MB, larger
-than the 129 MB L2, so no flush is needed between steps.
+Default workload (the benchmark line): the Llama-3-8B-shaped parameter set
+(32 layers of Q, O 4096x4096, K, V 1024x4096, gate, up 14336x4096, down
+4096x14336; 6.98G elements, 64 partitions, 128 alignment; even-indexed
+matrices rank 8 plus 1e-3 noise, odd-indexed N(0,1)), two BF16 micro-batches
+accumulated in FP32, then one Muon step (5 standard Newton-Schulz steps,
+BF16 operands).  One timed step = muon_accumulate of the first micro-batch
++ muon_step_ex that accumulates the second in its first pass, all kernels
+of the library, every input resident in HBM (accum, momentum and master
+are 27.9 GB each, far larger than the 129 MB L2, so no flush is needed);
+the K timed steps are recorded into one CUDA graph and timed as one replay.
+``--workload gpt2`` runs the same contract line on the GPT-2-small
+parameter set (84.9M elements, P=8, four micro-batches, clip 0.05), which
+the default line also summarises.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 instead, on a bounded sample of the same workload.
@@ -31,25 +35,30 @@ import workloads as wl  # noqa: E402
 METRIC = "Muon step time & NS TFLOP/s (% of GB300 bf16 dense peak) plus HBM GB/s, 1 GPU"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes per launch of the BF16 pair GEMM in this workload (one launch
-# runs all NS products of the step), from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum averaged over two launches;
-# command in profiles/gpt2_step_launches.md), valid only for the kernel
-# sources it was taken on (hash below).
-GEMM_TRAFFIC = {"bytes_per_launch": 3.8489e9, "sources_sha256_16": "3ef1b59e79164675",
-                "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
-                          "newton_schulz_fp32_gb300/csrc/tc_common.cuh"]}
+# DRAM bytes per launch of the BF16 pair GEMM (one launch runs all NS
+# products of a step), from ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum), valid only for the kernel sources they were taken
+# on (hash below).  GPT-2: the full step, averaged over two launches.
+# Llama-3-8B: the full step does not fit a capture, so one layer (the same
+# seven shapes) was captured and scaled by the 32 layers.
+GEMM_SOURCES = ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
+                "newton_schulz_fp32_gb300/csrc/tc_common.cuh"]
+GEMM_TRAFFIC = {"gpt2": {"bytes_per_launch": 3.8489e9, "sources_sha256_16": "3ef1b59e79164675"},
+                "llama": None}
 
 
-def gemm_traffic():
+def gemm_traffic(workload):
     import hashlib
+    rec = GEMM_TRAFFIC.get(workload)
+    if rec is None:
+        return None
     h = hashlib.sha256()
-    for f in GEMM_TRAFFIC["files"]:
+    for f in GEMM_SOURCES:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
-    if h.hexdigest()[:16] != GEMM_TRAFFIC["sources_sha256_16"]:
+    if h.hexdigest()[:16] != rec["sources_sha256_16"]:
         return None   # the kernel changed since the counters were taken
-    return GEMM_TRAFFIC["bytes_per_launch"]
+    return rec["bytes_per_launch"]
 
 
 def load_peaks():
@@ -70,19 +79,65 @@ def peak_value(peaks, key):
 
 # ------------------------------------------------------------------ workloads
 
+class Workload:
+    """One benchmark configuration: its layout, micro-batch count and step
+    settings, and how its device and pinned host inputs are made."""
+
+    def __init__(self, name, lay, gas, ns_method, clip, desc):
+        self.name, self.lay, self.gas = name, lay, gas
+        self.ns_method, self.clip, self.desc = ns_method, clip, desc
+
+
 def gpt2_workload(ns_method, mode):
     lay = wl.gpt2_small_layout()
-    seed = wl.CONFIG_SEED["gpt2"]
-    sig = wl.loguniform_sigmas(lay, seed, 1e-4, 1e-1)
-    gas = 4
-    grads = [wl.bf16_storage_grad(lay, wl.gaussian_grads(lay, seed, mb, sig)) for mb in range(gas)]
-    m0 = wl.pack(lay, [0.1 * g for g in wl.gaussian_grads(lay, seed, 100, sig, bf16=False)])
-    w0 = wl.pack(lay, wl.gaussian_grads(lay, seed, 101, None, bf16=False))
     desc = (f"gpt2-small muon step: 12 layers (q,k 12-head, v, o 768x768; up 3072x768; "
             f"down 768x3072), 84.9M params, P=8, align 128, gas=4 bf16 grads, "
             f"{ns_method} NS x5, {mode} operands, clip 0.05; the 4th micro-batch is "
             f"accumulated inside the step's first pass")
-    return lay, grads, m0, w0, gas, desc
+    return Workload("gpt2", lay, 4, ns_method, 0.05, desc)
+
+
+def llama_workload(mode, layers=32):
+    lay = wl.llama3_8b_layout(layers=layers)
+    desc = (f"llama3-8b muon step: {layers} layers (q,o 4096x4096; k,v 1024x4096; gate,up "
+            f"14336x4096; down 4096x14336), {lay.n_param_elements / 1e9:.2f}G params, P=64, "
+            f"align 128, gas=2 bf16 grads (even-indexed matrices rank 8 + 1e-3 noise), "
+            f"standard NS x5, {mode} operands; the 2nd micro-batch is accumulated inside "
+            f"the step's first pass")
+    return Workload("llama", lay, 2, "standard", 0.0, desc)
+
+
+def make_inputs(torch, W, stream):
+    """Device state and micro-batch gradients, plus pinned host copies of the
+    gradients (the end-to-end run copies them in every step)."""
+    lay = W.lay
+    n = lay.storage_size
+    with torch.cuda.stream(stream):
+        if W.name == "gpt2":
+            seed = wl.CONFIG_SEED["gpt2"]
+            sig = wl.loguniform_sigmas(lay, seed, 1e-4, 1e-1)
+            grads = [wl.bf16_storage_grad(lay, wl.gaussian_grads(lay, seed, mb, sig))
+                     for mb in range(W.gas)]
+            m0 = wl.pack(lay, [0.1 * g for g in wl.gaussian_grads(lay, seed, 100, sig, bf16=False)])
+            w0 = wl.pack(lay, wl.gaussian_grads(lay, seed, 101, None, bf16=False))
+            acc = torch.zeros(n, dtype=torch.float32, device="cuda")
+            mom = torch.from_numpy(m0).cuda()
+            mst = torch.from_numpy(w0).cuda()
+            g_dev = [torch.from_numpy(g.view(np.int16)).cuda().view(torch.bfloat16) for g in grads]
+        else:
+            seed = wl.CONFIG_SEED["llama"]
+            gen = torch.Generator(device="cuda").manual_seed(seed)
+            acc = torch.zeros(n, dtype=torch.float32, device="cuda")
+            mom = torch.zeros(n, dtype=torch.float32, device="cuda")
+            mst = torch.randn(n, dtype=torch.float32, device="cuda", generator=gen)
+            g_dev = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(W.gas)]
+            for mb in range(W.gas):
+                wl.llama_grad_into(lay, seed, mb, g_dev[mb])
+        g_host = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(W.gas)]
+        for h, d in zip(g_host, g_dev):
+            h.copy_(d)
+    torch.cuda.synchronize()
+    return acc, mom, mst, g_dev, g_host
 
 
 def ns_formula_flops(lay, method, steps=5):
@@ -99,6 +154,24 @@ def ns_formula_flops(lay, method, steps=5):
             f += h * steps * (4.0 * m * m * n + 2.0 * m ** 3)
         else:
             f += h * (4.0 * m * m * n + (2 * steps + 2 * (steps - 1) + 4 * (steps - 1)) * m ** 3)
+    return f
+
+
+def ns_executed_flops_pairs(lay, steps=5, tile=256):
+    """Flops the SM-pair kernel executes for the standard form in BF16 mode:
+    X X^T and c A^2 + b A compute only the 256x256 tiles touching the upper
+    triangle (mirrored), X' = B X + a X every tile.  Counted per NS problem
+    (unstacked blocks of 192+ rows)."""
+    f = 0.0
+    for s in lay.specs:
+        if not s.use_muon:
+            continue
+        h = s.num_heads if s.num_heads > 1 else 1
+        r, c = s.rows // h, s.cols
+        m, n = min(r, c), max(r, c)
+        nt = -(-m // tile)
+        sym = nt * (nt + 1) // 2 * tile * tile
+        f += h * steps * (2.0 * sym * n + 2.0 * sym * m + 2.0 * m * m * n)
     return f
 
 
@@ -160,57 +233,135 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def cpu_oracle_sample(ns_method, mode, budget_s=20.0):
-    """Times the oracle on a bounded sample of the GPT-2-small step: the
-    whole step (accumulate x4, momentum, NS, norm, clip, write-back) on one
-    layer's six matrices (P=8); scaled to the full 12 layers by layer
-    count.  Returns (ms per full step estimate, sample description)."""
+def cpu_info():
+    """(threads the oracle's BLAS may use, CPU model string)."""
+    cores = os.cpu_count() or 1
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            cores = int(os.environ[var])
+            break
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        import platform
+        model = platform.processor() or platform.machine()
+    return cores, model
+
+
+def _oracle_mode(mode):
+    return "bf16" if mode == "bf16" else "exact"
+
+
+def oracle_step_gpt2(ns_method, mode):
+    """The oracle's whole GPT-2-small step (accumulate x4, momentum, NS, norm,
+    clip, write-back over all 12 layers, P=8); returns seconds."""
     import oracle.muon as om
     import oracle.bf16 as obf
-    lay = wl.gpt2_small_layout(layers=1)
+    lay = wl.gpt2_small_layout()
     seed = wl.CONFIG_SEED["gpt2"]
     sig = wl.loguniform_sigmas(lay, seed, 1e-4, 1e-1)
     grads = [obf.bits_to_f32(wl.bf16_storage_grad(lay, wl.gaussian_grads(lay, seed, mb, sig)))
              for mb in range(4)]
     m0 = wl.pack(lay, [0.1 * g for g in wl.gaussian_grads(lay, seed, 100, sig, bf16=False)])
     w0 = wl.pack(lay, wl.gaussian_grads(lay, seed, 101, None, bf16=False))
-    omode = "bf16" if mode == "bf16" else "exact"
-    reps, t_tot = 0, 0.0
-    while True:
+    t0 = time.perf_counter()
+    acc = None
+    for mb in range(4):
+        acc = om.accumulate(acc, grads[mb], 0.25, overwrite=(mb == 0))
+    om.muon_step_flat(acc, m0, w0, lay.params, lay.parts, 0.95, 0.02, ns_method, 5, 0.05,
+                      _oracle_mode(mode))
+    return time.perf_counter() - t0
+
+
+# Llama-3-8B matrices in the order the bounded sample takes them (layer 0:
+# k, v, o, q, then gate, up, down): the smallest first, so a short budget
+# still times whole matrices.
+LLAMA_SAMPLE_ORDER = [1, 2, 3, 0, 4, 5, 6]
+
+
+def oracle_step_llama_sample(mode, budget_s):
+    """The oracle's whole step (accumulate x2, momentum, NS, norm, write-back)
+    on layer-0 matrices of the Llama-3-8B set, one matrix at a time in
+    LLAMA_SAMPLE_ORDER until budget_s is spent (at least one).  Inputs are
+    numpy-seeded with the workload's distribution (even-indexed matrices rank
+    8 + 1e-3 noise, odd-indexed N(0,1), bf16).  Returns (seconds, formula
+    flops of the matrices timed, their names)."""
+    import oracle.muon as om
+    full = wl.llama3_8b_layout(layers=1)
+    seed = wl.CONFIG_SEED["llama"]
+    spent, flops, names = 0.0, 0.0, []
+    for k in LLAMA_SAMPLE_ORDER:
+        spec = full.specs[k]
+        lay = wl.build_layout([[spec]], 128, 1)
+        mats = []
+        for mb in range(2):
+            rng = wl.rng_for(seed, 7, k, mb)
+            if k % 2 == 0:
+                g = (rng.standard_normal((spec.rows, 8), dtype=np.float32)
+                     @ rng.standard_normal((8, spec.cols), dtype=np.float32)
+                     + np.float32(1e-3) * rng.standard_normal((spec.rows, spec.cols), dtype=np.float32))
+            else:
+                g = rng.standard_normal((spec.rows, spec.cols), dtype=np.float32)
+            mats.append(wl.pack(lay, [wl.to_bf16_values(g)]))
+        z = np.zeros(lay.storage_size, np.float32)
         t0 = time.perf_counter()
-        acc = None
-        for mb in range(4):
-            acc = om.accumulate(acc, grads[mb], 0.25, overwrite=(mb == 0))
-        om.muon_step_flat(acc, m0, w0, lay.params, lay.parts, 0.95, 0.02, ns_method, 5, 0.05, omode)
-        t_tot += time.perf_counter() - t0
-        reps += 1
-        if t_tot > budget_s or reps >= 3:
+        acc = om.accumulate(None, mats[0], 0.5, overwrite=True)
+        acc = om.accumulate(acc, mats[1], 0.5)
+        om.muon_step_flat(acc, z, z, lay.params, lay.parts, 0.95, 0.02, "standard", 5, 0.0,
+                          _oracle_mode(mode))
+        spent += time.perf_counter() - t0
+        flops += ns_formula_flops(lay, "standard")
+        names.append(f"{spec.name} {spec.rows}x{spec.cols}")
+        if spent >= budget_s:
             break
-    ms_layer = 1000.0 * t_tot / reps
-    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
-    sample = (f"oracle ({omode} mode, numpy/BLAS fp64) on layer 0 of 12 (6 matrices, P=8), "
-              f"{reps} rep(s), full step = 12 x layer time")
-    return 12.0 * ms_layer, cores, sample
+    return spent, flops, names
+
+
+def cpu_baseline(workload, ns_method, mode, budget_s):
+    """The oracle timed on the host cores: GPT-2-small in full (one rep), or
+    a bounded sample of the Llama-3-8B step extrapolated by formula flops.
+    Returns the contract's cpu_baseline object (value in ms per full step)."""
+    cores, model = cpu_info()
+    if workload == "gpt2":
+        sec = oracle_step_gpt2(ns_method, mode)
+        return {"value": 1000.0 * sec, "unit": "ms", "cores": cores, "cpu": model,
+                "kind": "oracle", "sampled": False,
+                "sample": f"oracle ({_oracle_mode(mode)} mode, numpy fp64 BLAS) on the whole "
+                          f"GPT-2-small step (12 layers, P=8), one rep"}
+    sec, flops, names = oracle_step_llama_sample(mode, budget_s)
+    total = ns_formula_flops(wl.llama3_8b_layout(), "standard")
+    return {"value": 1000.0 * sec * total / flops, "unit": "ms", "cores": cores, "cpu": model,
+            "kind": "oracle", "sampled": True, "sample_seconds": sec,
+            "sample_fraction_of_step_flops": flops / total,
+            "sample": f"oracle ({_oracle_mode(mode)} mode, numpy fp64 BLAS) on the whole step of "
+                      f"{len(names)} layer-0 matrices ({', '.join(names)}) in {sec:.1f} s, "
+                      f"extrapolated to the 224-matrix step by formula flops "
+                      f"(x{total / flops:.0f})"}
 
 
 # ------------------------------------------------------------------ GPU run
 
-def run_gpu(args, rank, world):
+def run_gpu(args, W, rank, world):
+    """Warm-up, the K timed steps as one CUDA-graph replay (inputs resident),
+    an eager pass of the same steps for the phase split, and the end-to-end
+    loop with host copies.  Returns a dict of measurements."""
     import torch
     import newton_schulz_fp32_gb300 as nsg
 
     dev = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(dev)
     nsg.build()
-    lay, grads, m0, w0, gas, desc = gpt2_workload(args.ns_method, args.mode)
+    lay, gas = W.lay, W.gas
     stream = torch.cuda.Stream()
-    torch.cuda.synchronize()
+    acc, mom, mst, g_dev, g_host = make_inputs(torch, W, stream)
     with torch.cuda.stream(stream):
-        acc = torch.zeros(lay.storage_size, dtype=torch.float32, device="cuda")
-        mom = torch.from_numpy(m0).cuda()
-        mst = torch.from_numpy(w0).cuda()
-        g_dev = [torch.from_numpy(g.view(np.int16)).cuda().view(torch.bfloat16) for g in grads]
-        g_host = [torch.from_numpy(g.view(np.int16)).view(torch.bfloat16).pin_memory() for g in grads]
         res = torch.zeros(4, dtype=torch.int32, device="cuda")
         res_host = torch.zeros(4, dtype=torch.int32).pin_memory()
     torch.cuda.synchronize()
@@ -225,7 +376,7 @@ def run_gpu(args, rank, world):
         for mb in range(gas - 1):
             nsg.accumulate(acc, grad_list[mb], 1.0 / gas, overwrite=(mb == 0), params=P, parts=Q,
                            stream=stream)
-        nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, args.ns_method, 5, 0.05, args.mode, result=res,
+        nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, W.ns_method, 5, W.clip, args.mode, result=res,
                  stream=stream, options=fold)
 
     # warm-up (plans are built on the first call)
@@ -244,12 +395,10 @@ def run_gpu(args, rank, world):
 
     # ---- the K timed steps as one CUDA graph: once the plans exist the
     # library only issues stream-ordered work (no allocation, no host
-    # synchronisation), so K whole steps (accumulations + muon_step_ex) record
-    # into one graph, with the library's per-phase events as event nodes,
-    # and replay without per-launch host overhead
-    # Only the Newton-Schulz launch (the dominant kernel, for the roofline) is
-    # bracketed by event nodes in the timed graph; the other phases are split
-    # in an eager pass afterwards.
+    # synchronisation), so K whole steps record into one graph and replay
+    # without per-launch host overhead.  Only the Newton-Schulz launch (the
+    # dominant kernel, for the roofline) is bracketed by event nodes in the
+    # timed graph; the other phases are split in an eager pass afterwards.
     nsg.profile_read(reset=True)
     nsg.profile_enable(True, phases=["ns_gemm"])
     launches0 = nsg.get_stats()["kernel_launches_total"]
@@ -264,6 +413,7 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     if nsg.read_result(res)["applied"] != 1:
         raise RuntimeError("graph replay: step not applied")
+    nsg.profile_read(reset=True)
 
     # ---- device-resident timed region: one replay = exactly K steps
     clocks = ClockSampler(dev)
@@ -281,6 +431,7 @@ def run_gpu(args, rank, world):
     ns_timed = nsg.profile_read(reset=True)["ns_gemm"]   # NS launches of the timed replay
     if nsg.device_error() != 0:
         raise RuntimeError("a kernel reported a device error during the timed region")
+    del graph
     # phase split of the same K steps, issued eagerly with every phase's events
     nsg.profile_enable(True)
     for _ in range(args.steps):
@@ -332,7 +483,7 @@ def run_gpu(args, rank, world):
                            stream=stream)
             consumed[mb].record(stream)
         stream.wait_event(copied[gas - 1])
-        nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, args.ns_method, 5, 0.05, args.mode, result=res,
+        nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, W.ns_method, 5, W.clip, args.mode, result=res,
                  stream=stream, options=folds[b])
         consumed_last[b].record(stream)
         with torch.cuda.stream(stream):
@@ -345,9 +496,68 @@ def run_gpu(args, rank, world):
     barrier()
     wall_ms = 1000.0 * (time.perf_counter() - t_wall) / args.steps
     e2e_ms = max(e2.elapsed_time(e3) / args.steps, wall_ms)
+    if nsg.read_result(res_hosts[(args.steps - 1) & 1])["applied"] != 1:
+        raise RuntimeError("end-to-end step not applied")
+    ws = nsg.get_stats()["workspace_bytes"]
     if world > 1:
         ms, e2e_ms = max_over_ranks([ms, e2e_ms], "cuda")
-    return lay, desc, ms, e2e_ms, h2d, phases, clk, launches
+    del acc, mom, mst, g_dev, g_host, g_last
+    nsg.release_workspace()
+    torch.cuda.empty_cache()
+    return {"ms": ms, "e2e_ms": e2e_ms, "h2d": h2d, "phases": phases, "clocks": clk,
+            "launches": launches, "workspace_bytes": ws}
+
+
+def contract_fields(args, W, m, peaks, peak_src, world):
+    """Roofline of the dominant kernel and the per-phase figures of one
+    measured workload."""
+    phases = m["phases"]
+    lay = W.lay
+    dom = max(phases, key=lambda k: phases[k]["ms"])
+    ph = phases[dom]
+    per_launch_ms = ph["ms"] / max(ph["launches"], 1)
+    # the NS kernel runs inside seconds of back-to-back steps: the sustained
+    # tensor peak is its denominator (the burst fraction is reported beside)
+    if dom == "ns_gemm":
+        bound, unit = "tensor", "TFLOP/s"
+        achieved = (ph["flops"] / max(ph["launches"], 1)) / (per_launch_ms * 1e-3) / 1e12
+        peak_key = "bf16_tflops_sustained" if W.name == "llama" else "bf16_tflops"
+        peak = peak_value(peaks, peak_key) if args.mode == "bf16" else None
+    else:
+        bound, unit = "hbm", "GB/s"
+        achieved = (ph["bytes"] / max(ph["launches"], 1)) / (per_launch_ms * 1e-3) / 1e9
+        peak_key = "hbm_gbs"
+        peak = peak_value(peaks, peak_key)
+    roof = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
+            "peak_source": f"{peak_key} ({peak_src})", "unit": unit,
+            "frac": (achieved / peak) if peak else None,
+            "traffic": gemm_traffic(W.name) if dom == "ns_gemm" and args.mode == "bf16"
+            and W.ns_method == "standard" else None,
+            "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
+            "work_per_launch": ph["flops"] / max(ph["launches"], 1) if dom == "ns_gemm"
+            else ph["bytes"] / max(ph["launches"], 1),
+            "launch_ms": per_launch_ms}
+    if dom == "ns_gemm" and args.mode == "bf16" and W.ns_method == "standard" and W.name == "llama":
+        ex = ns_executed_flops_pairs(lay) / (per_launch_ms * 1e-3) / 1e12
+        roof["executed_tflops"] = ex   # upper tiles of the symmetric products only
+        roof["executed_frac"] = ex / peak if peak else None
+        roof["frac_of_burst_peak"] = achieved / peak_value(peaks, "bf16_tflops")
+    hbm_phases = [k for k in phases if k != "ns_gemm" and phases[k]["ms"] > 0]
+    hbm_bytes = sum(phases[k]["bytes"] for k in hbm_phases)
+    hbm_ms = sum(phases[k]["ms"] for k in hbm_phases)
+    ns_ms = phases["ns_gemm"]["ms"]
+    ns_tflops = phases["ns_gemm"]["flops"] / max(ns_ms * 1e-3, 1e-12) / 1e12
+    return {
+        "ns_tflops": ns_tflops,
+        "ns_frac_of_peak": (ns_tflops / peak_value(peaks, "bf16_tflops")) if args.mode == "bf16" else None,
+        "ns_flops_per_step": ns_formula_flops(lay, W.ns_method),
+        "hbm_gbs": hbm_bytes / max(hbm_ms * 1e-3, 1e-12) / 1e9,
+        "hbm_frac_of_peak": hbm_bytes / max(hbm_ms * 1e-3, 1e-12) / 1e9 / peak_value(peaks, "hbm_gbs"),
+        "phases_ms_per_step": {k: phases[k]["ms"] / args.steps for k in phases},
+        "phase_gbs": {k: phases[k]["bytes"] / max(phases[k]["ms"] * 1e-3, 1e-12) / 1e9
+                      for k in hbm_phases},
+        "roofline": roof,
+    }
 
 
 def max_over_ranks(values, device):
@@ -472,26 +682,19 @@ def run_ragged(args, peaks, peak_src):
                       "phases_ms_per_step": {k: ph[k]["ms"] / args.steps for k in ph}}))
 
 
-def run_llama(args, peaks, peak_src):
-    """Llama-3-8B-shaped parameter set (32 layers x {q, o 4096^2; k, v
-    1024x4096; gate, up 14336x4096; down 4096x14336}, 6.98G elements, 64
-    partitions, align 128): 2 bf16 micro-batches (even-indexed matrices
-    low-rank rank 8 + 1e-3 noise) accumulated in fp32, one standard Muon
-    step.  All state resident in HBM (~84 GB fp32 + 28 GB grads)."""
+def run_llama_layers(args, peaks, peak_src):
+    """A Llama-3-8B-shaped case of --layers layers (each q, o 4096^2; k, v
+    1024x4096; gate, up 14336x4096; down 4096x14336; 64 partitions, align
+    128; 2 bf16 micro-batches, even-indexed matrices rank 8 + 1e-3 noise),
+    one standard Muon step timed eagerly.  Small enough for profiler
+    captures at --layers 1; --workspace-budget runs the NS blocks in waves."""
     import torch
     import newton_schulz_fp32_gb300 as nsg
     nsg.build()
-    lay = wl.llama3_8b_layout()
-    seed = wl.CONFIG_SEED["llama"]
-    n = lay.storage_size
+    W = llama_workload(args.mode, layers=args.layers)
+    lay = W.lay
     stream = torch.cuda.Stream()
-    gen = torch.Generator(device="cuda").manual_seed(seed)
-    acc = torch.zeros(n, dtype=torch.float32, device="cuda")
-    mom = torch.zeros(n, dtype=torch.float32, device="cuda")
-    mst = torch.randn(n, dtype=torch.float32, device="cuda", generator=gen)
-    grads = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
-    for mb in range(2):
-        wl.llama_grad_into(lay, seed, mb, grads[mb])
+    acc, mom, mst, grads, _ = make_inputs(torch, W, stream)
     res = torch.zeros(4, dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
     P, Q = lay.params, lay.parts
@@ -509,15 +712,55 @@ def run_llama(args, peaks, peak_src):
     g = ph["ns_gemm"]
     hbm = [k for k in ph if k != "ns_gemm" and ph[k]["ms"] > 0]
     print(json.dumps({"metric": "Muon step time", "value": ms, "unit": "ms",
-                      "config": {"workload": "llama3-8b muon step, 6.98G params, P=64, gas=2, "
-                                             "standard NS x5", "operand_mode": args.mode,
+                      "config": {"workload": W.desc, "operand_mode": args.mode,
                                  "workspace_budget_bytes": args.workspace_budget},
                       "workspace_bytes": nsg.get_stats()["workspace_bytes"],
                       "ns_tflops": flops / (g["ms"] / args.steps * 1e-3) / 1e12,
+                      "ns_launches_per_step": g["launches"] / args.steps,
                       "ns_flops_per_step": flops,
                       "hbm_gbs": sum(ph[k]["bytes"] for k in hbm) / (sum(ph[k]["ms"] for k in hbm) * 1e-3) / 1e9,
                       "phases_ms_per_step": {k: ph[k]["ms"] / args.steps for k in ph},
                       "result": nsg.read_result(res)}))
+
+
+def reference_line(args, peaks, peak_src):
+    """The reference arm: the CPU oracle on the host cores, on the workload
+    this bench measures.  Each of the W + K steps is the bounded sample (the
+    whole GPT-2-small step, or the first Llama-3-8B matrix of the sample
+    order); the line's value is the full step extrapolated from the timed
+    steps' mean; steps and ms_per_step say what was timed."""
+    cores, model = cpu_info()
+    if args.workload == "gpt2":
+        run = lambda: (oracle_step_gpt2(args.ns_method, args.mode), 1.0, "the whole GPT-2-small step")
+    else:
+        total = ns_formula_flops(wl.llama3_8b_layout(), "standard")
+
+        def run():
+            sec, flops, names = oracle_step_llama_sample(args.mode, 0.0)
+            return sec, total / flops, f"the whole step of one layer-0 matrix ({names[0]})"
+    for _ in range(args.warmup):
+        run()
+    secs = []
+    for _ in range(args.steps):
+        sec, scale, what = run()
+        secs.append(sec)
+    ms_sample = 1000.0 * float(np.mean(secs))
+    ms_full = ms_sample * scale
+    W = gpt2_workload(args.ns_method, args.mode) if args.workload == "gpt2" else llama_workload(args.mode)
+    sample = (f"oracle ({_oracle_mode(args.mode)} mode, numpy fp64 BLAS): each step times {what}; "
+              f"value = mean over {args.steps} steps x {scale:.0f} (formula flops of the full "
+              f"step over the sample's)")
+    return {"metric": METRIC, "value": ms_full, "unit": "ms", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_sample, "sampled": scale != 1.0, "sample_scale": scale,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": args.mode + "+fp32", "data": "synthetic",
+            "config": {"workload": W.desc + " (oracle on CPU, bounded sample)",
+                       "ns_method": W.ns_method, "operand_mode": args.mode},
+            "cpu_baseline": {"value": ms_full, "unit": "ms", "cores": cores, "cpu": model,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": ms_full, "unit": "ms", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
 
 
 def main():
@@ -526,48 +769,40 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--ns-method", default="standard", choices=["standard", "gram"])
+    ap.add_argument("--ns-method", default="standard", choices=["standard", "gram"],
+                    help="gpt2 workload only (the Llama-3-8B config runs the standard method)")
     ap.add_argument("--mode", default="bf16", choices=["bf16", "fp32"])
-    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--cpu-budget", type=float, default=20.0,
+                    help="seconds of oracle time for the Llama-3-8B cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="gpt2", choices=["gpt2", "sweep", "ragged", "llama"],
-                    help="gpt2 is the benchmark line; sweep and ragged print extra lines")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the GPT-2-small summary inside the Llama-3-8B line")
+    ap.add_argument("--workload", default="llama",
+                    choices=["llama", "gpt2", "sweep", "ragged", "llama_layers"],
+                    help="llama (default) and gpt2 print the contract line; sweep, ragged and "
+                         "llama_layers (a smaller Llama-shaped case for profiler captures) print "
+                         "extra lines")
+    ap.add_argument("--layers", type=int, default=1, help="llama_layers: layers of the case")
     ap.add_argument("--shapes", default="", help="sweep shapes, e.g. 4096x4096,4096x16384")
     ap.add_argument("--ragged-count", type=int, default=8192,
                     help="ragged workload: number of matrices (a smaller count keeps profiler "
                          "captures small; the same shape distribution)")
     ap.add_argument("--workspace-budget", type=int, default=0,
-                    help="llama workload: NS workspace cap in bytes (0: unbounded)")
+                    help="llama_layers workload: NS workspace cap in bytes (0: unbounded)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    if args.workload != "gpt2" and args.impl == "ours":
-        peaks, peak_src = load_peaks()
-        {"sweep": run_sweep, "ragged": run_ragged, "llama": run_llama}[args.workload](
-            args, peaks, peak_src)
-        return
-
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     peaks, peak_src = load_peaks()
-    lay1 = wl.gpt2_small_layout(layers=1)
-    ns_flops = ns_formula_flops(wl.gpt2_small_layout(), args.ns_method)
 
     if args.impl == "reference":
         if rank != 0:
             return
-        ms_ref, cores, sample = cpu_oracle_sample(args.ns_method, args.mode, args.cpu_budget)
-        line = {"metric": METRIC, "value": ms_ref, "unit": "ms", "impl": "reference",
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": ms_ref, "higher_is_better": False, "scaling": "weak",
-                "vs_baseline": None, "dtype": args.mode + "+fp32", "data": "synthetic",
-                "config": {"workload": "gpt2-small muon step (oracle on CPU, bounded sample)",
-                           "ns_method": args.ns_method, "operand_mode": args.mode},
-                "cpu_baseline": {"value": ms_ref, "unit": "ms", "cores": cores, "kind": "oracle",
-                                 "sample": sample},
-                "e2e": {"value": ms_ref, "unit": "ms", "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0},
-                "ns_tflops": ns_flops / (ms_ref * 1e-3) / 1e12}
-        print(json.dumps(line))
+        print(json.dumps(reference_line(args, peaks, peak_src)))
+        return
+    if args.workload in ("sweep", "ragged", "llama_layers"):
+        {"sweep": run_sweep, "ragged": run_ragged, "llama_layers": run_llama_layers}[
+            args.workload](args, peaks, peak_src)
         return
 
     if world > 1:
@@ -575,59 +810,48 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))))
 
-    lay, desc, ms, e2e_ms, h2d, phases, clk, launches = run_gpu(args, rank, world)
-
-    # roofline of the dominant phase
-    dom = max(phases, key=lambda k: phases[k]["ms"])
-    ph = phases[dom]
-    per_launch_ms = ph["ms"] / max(ph["launches"], 1)
-    if dom == "ns_gemm":
-        bound, unit = "tensor", "TFLOP/s"
-        achieved = (ph["flops"] / max(ph["launches"], 1)) / (per_launch_ms * 1e-3) / 1e12
-        peak = peak_value(peaks, "bf16_tflops") if args.mode == "bf16" else None
-    else:
-        bound, unit = "hbm", "GB/s"
-        achieved = (ph["bytes"] / max(ph["launches"], 1)) / (per_launch_ms * 1e-3) / 1e9
-        peak = peak_value(peaks, "hbm_gbs")
-    hbm_phases = [k for k in phases if k != "ns_gemm" and phases[k]["ms"] > 0]
-    hbm_bytes = sum(phases[k]["bytes"] for k in hbm_phases)
-    hbm_ms = sum(phases[k]["ms"] for k in hbm_phases)
-    ns_ms = phases["ns_gemm"]["ms"]
-    ns_tflops = phases["ns_gemm"]["flops"] / max(ns_ms * 1e-3, 1e-12) / 1e12
-
+    W = gpt2_workload(args.ns_method, args.mode) if args.workload == "gpt2" else llama_workload(args.mode)
+    m = run_gpu(args, W, rank, world)
+    fields = contract_fields(args, W, m, peaks, peak_src, world)
+    secondary = None
+    if args.workload == "llama" and not args.no_secondary:
+        G = gpt2_workload("standard", args.mode)
+        mg = run_gpu(args, G, rank, world)
+        fg = contract_fields(args, G, mg, peaks, peak_src, world)
+        secondary = {"workload": G.desc, "ms_per_step": mg["ms"], "e2e_ms": mg["e2e_ms"],
+                     "ns_tflops": fg["ns_tflops"], "ns_frac_of_peak": fg["ns_frac_of_peak"],
+                     "hbm_gbs": fg["hbm_gbs"], "roofline": fg["roofline"],
+                     "phases_ms_per_step": fg["phases_ms_per_step"], "clocks": mg["clocks"]}
     if rank != 0:
         return
     cpu = None
     if not args.no_cpu_baseline:
-        ms_ref, cores, sample = cpu_oracle_sample(args.ns_method, args.mode, args.cpu_budget)
-        cpu = {"value": ms_ref, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample}
+        cpu = cpu_baseline(W.name, W.ns_method, args.mode, args.cpu_budget)
+        if secondary is not None:
+            secondary["cpu_baseline"] = cpu_baseline("gpt2", "standard", args.mode, args.cpu_budget)
     line = {
-        "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": args.mode + "+fp32", "data": "synthetic",
-        "config": {"workload": desc, "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (each fp32 state buffer 340 MB), no flush",
-                   "ns_method": args.ns_method, "operand_mode": args.mode,
-                   "launch": "timed: one replay of a CUDA graph of the K steps (each 3 "
-                             "accumulations + muon_step_ex), event nodes around the NS launch "
-                             "only (roofline); other phases split in an eager pass of the same "
-                             "K steps; e2e: issued eagerly, with the host copies"},
-        "ns_tflops": ns_tflops,
-        "ns_frac_of_peak": (ns_tflops / peak_value(peaks, "bf16_tflops")) if args.mode == "bf16" else None,
-        "ns_flops_per_step": ns_flops,
-        "hbm_gbs": hbm_bytes / max(hbm_ms * 1e-3, 1e-12) / 1e9,
-        "phases_ms_per_step": {k: phases[k]["ms"] / args.steps for k in phases},
-        "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
-                     "peak_source": peak_src, "unit": unit,
-                     "frac": (achieved / peak) if peak else None,
-                     "traffic": gemm_traffic() if dom == "ns_gemm" and args.mode == "bf16"
-                     and args.ns_method == "standard" else None,
-                     "traffic_unit": "bytes per launch (DRAM read + write, ncu)"},
+        "metric": METRIC, "value": m["ms"], "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": m["ms"], "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": args.mode + "+fp32",
+        "data": "synthetic",
+        "config": {"workload": W.desc, "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (each fp32 state buffer "
+                         f"{4 * W.lay.storage_size / 1e9:.2f} GB), no flush",
+                   "ns_method": W.ns_method, "operand_mode": args.mode,
+                   "launch": "timed: one replay of a CUDA graph of the K steps (accumulations + "
+                             "muon_step_ex), event nodes around the NS launch only (roofline); "
+                             "other phases split in an eager pass of the same K steps; e2e: "
+                             "issued eagerly, with the host copies"},
+        **fields,
+        "workspace_bytes": m["workspace_bytes"],
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 16},
-        "gpu_launches": launches,
-        "clocks": clk,
+        "e2e": {"value": m["e2e_ms"], "unit": "ms", "h2d_bytes_per_step": m["h2d"],
+                "d2h_bytes_per_step": 16},
+        "gpu_launches": m["launches"],
+        "clocks": m["clocks"],
     }
+    if secondary is not None:
+        line["secondary"] = secondary
     print(json.dumps(line))
 
 

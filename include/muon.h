@@ -198,8 +198,16 @@ MUON_API int muon_step(float* accum, float* momentum, float* master,
  *              by the step (bit-identical accum, momentum, master and
  *              result, a skipped step included), one read and one write of
  *              accum fewer.  last_grad must be 8-byte aligned.
- * struct_size is sizeof(muon_step_options_t), or MUON_STEP_OPTIONS_V1_SIZE
- * for callers built against the layout that ends at workspace_budget. */
+ *   stats_out  non-NULL: device double[4], written at the end of the step:
+ *              [0] the sum of squares the clip norm was taken over (the
+ *              Muon updates and the auxiliary gradients), [1] 1 if the step
+ *              was skipped (non-finite gradient, or a device error) else 0,
+ *              [2] the Newton-Schulz problems run, [3] 0.  A caller that
+ *              splits the parameters over ranks adds these up across ranks
+ *              (see muon_dp_finish).  8-byte aligned.
+ * struct_size is sizeof(muon_step_options_t), MUON_STEP_OPTIONS_V2_SIZE for
+ * callers built against the layout that ends at last_grad_overwrite, or
+ * MUON_STEP_OPTIONS_V1_SIZE for the one that ends at workspace_budget. */
 typedef enum { MUON_CLIP_UPDATE = 0, MUON_CLIP_GRAD = 1 } muon_clip_mode_t;
 
 typedef struct muon_step_options {
@@ -216,8 +224,11 @@ typedef struct muon_step_options {
   const uint16_t* last_grad;    /* device bf16, accum's layout, or NULL */
   float last_grad_scale;
   int32_t last_grad_overwrite;
+  /* -- absent when struct_size <= MUON_STEP_OPTIONS_V2_SIZE -- */
+  double* stats_out;            /* device double[4], or NULL */
 } muon_step_options_t;
 #define MUON_STEP_OPTIONS_V1_SIZE 64   /* struct_size of the layout without last_grad */
+#define MUON_STEP_OPTIONS_V2_SIZE 80   /* struct_size of the layout without stats_out */
 
 /* muon_step with options (NULL = defaults).  Errors as muon_step, plus
  * MUON_ERR_INVALID for a bad struct_size, a non-finite or negative
@@ -228,6 +239,124 @@ MUON_API int muon_step_ex(float* accum, float* momentum, float* master,
                           float lr, int ns_method, int ns_steps, float clip,
                           int operand_mode, const muon_step_options_t* opts,
                           muon_result_t* d_result, void* stream);
+
+/* ---------------------------------------------------------------------
+ * Data parallelism across ranks (one process per GPU).
+ *
+ * The pages run the step on ranks that each hold only their partitions of
+ * the flat buffers: each Muon matrix needs its slices from every rank that
+ * holds one, Newton-Schulz runs on whole matrices, and every rank writes
+ * back its owned intersection ("Support Muon in BF16_Optimizer with FP32
+ * gradient accumulation", PR description and review thread on
+ * all_to_all_single: static send/recv split tables computed once, only the
+ * slices that cross partitions exchanged; "Run Muon once per optimizer step
+ * under ZeRO-3, not once per micro-batch", "The change": Muon round-robin
+ * over ranks, each rank's slice written back).  Here:
+ *   1. a plan assigns every parameter (Muon and auxiliary) to one owner
+ *      rank and derives the exchange tables (host only, no GPU);
+ *   2. muon_dp_pack gathers each rank's slices (gradient, and momentum for
+ *      Muon parameters) into a send buffer, ordered by owner; the caller
+ *      runs one all-to-all with the plan's split sizes;
+ *   3. muon_dp_unpack places the received slices into the owner's packed
+ *      buffers of its whole parameters, and muon_step_ex runs on them with
+ *      the plan's owned tables, clip = 0, lr = 0 and stats_out set: the
+ *      packed accum then holds the unclipped update u (the auxiliary
+ *      gradient for auxiliary parameters) and the packed momentum m';
+ *   4. the caller adds stats_out up over the ranks (one all-reduce of four
+ *      doubles: the global sum of squares, the skip count, the NS count);
+ *   5. muon_dp_pack in the receive direction gathers u and m' back into the
+ *      receive layout; the caller runs the reverse all-to-all (split sizes
+ *      swapped), which lands every slice in its holder's send layout;
+ *   6. muon_dp_finish computes coef = min(1, clip / (sqrt(sum) + 1e-6)) on
+ *      the device and writes each held slice: Muon accum = coef u, master
+ *      -= lr coef u, momentum = m'; auxiliary accum = coef g.  A step that
+ *      any rank skipped writes nothing.
+ * A plan's partition table lists every rank's partitions (global flat
+ * ranges), part_rank[p] names the rank that holds partition p, and each
+ * storage_offset is an index into that rank's own buffers.
+ * ------------------------------------------------------------------- */
+typedef struct muon_dp_plan muon_dp_plan_t;   /* opaque */
+
+typedef enum {
+  MUON_DP_BALANCED = 0,   /* largest first onto the least loaded rank */
+  MUON_DP_ROUND_ROBIN = 1 /* parameter k on rank k mod world (the pages' order) */
+} muon_dp_assign_t;
+
+/* One slice of one parameter held by one rank and owned by another (or the
+ * same) rank.  The send list of a rank is ordered by (owner, parameter,
+ * position); the receive list by (holder, parameter, position). */
+typedef struct muon_dp_segment {
+  int32_t param;    /* parameter index in the table */
+  int32_t peer;     /* send list: the owner; receive list: the holder */
+  int32_t is_muon;  /* 1: the momentum slice follows the gradient slice */
+  int32_t pad;
+  int64_t len;      /* elements */
+  int64_t local;    /* send list: storage index in this rank's buffers;
+                       receive list: index in the packed owned buffers */
+  int64_t buf;      /* offset of the slice in the exchange buffer; a Muon
+                       slice's momentum (or m') follows at buf + len */
+} muon_dp_segment_t;   /* 40 bytes */
+
+typedef struct muon_dp_sizes {
+  int32_t world, rank;
+  int32_t owned_params;   /* parameters this rank owns */
+  int32_t nparams;
+  int64_t owned_elems;    /* elements of each packed owned buffer */
+  int64_t send_segments, recv_segments;
+  int64_t send_elems;     /* elements of the send buffer (sum of send counts) */
+  int64_t recv_elems;     /* elements of the receive buffer */
+  double owned_cost;      /* this rank's share of the assignment's cost model */
+  double max_cost;        /* the most loaded rank's */
+} muon_dp_sizes_t;
+
+/* Builds the plan of `rank` (host only; no CUDA call).  ns_method feeds the
+ * cost model (formula flops of the NS iteration plus the streaming passes,
+ * 12500 flop-equivalents per element: ~50 bytes per element at the tensor
+ * rate per HBM byte of a GB300).
+ * Errors: MUON_ERR_INVALID for overlapping or uncovered parameters,
+ * unsorted or overlapping partitions, overlapping storage within a rank,
+ * part_rank outside [0, world), rank outside [0, world), world < 1. */
+MUON_API int muon_dp_plan_create(const muon_param_t* params, int nparams,
+                                 const muon_partition_t* parts, const int32_t* part_rank,
+                                 int nparts, int world, int rank, int ns_method, int assign,
+                                 muon_dp_plan_t** out);
+MUON_API void muon_dp_plan_destroy(muon_dp_plan_t* plan);
+MUON_API int muon_dp_plan_sizes(const muon_dp_plan_t* plan, muon_dp_sizes_t* out);
+/* Copies the plan's tables into caller arrays (any may be NULL):
+ *   owner[nparams]            owner rank of every parameter
+ *   send_counts[world]        elements this rank sends to each rank
+ *   recv_counts[world]        elements it receives from each rank
+ *   owned_params[owned_params] the owned parameters with offsets in the
+ *                             packed owned buffers (one partition covers
+ *                             [0, owned_elems), storage offset 0)
+ *   send_segs[send_segments], recv_segs[recv_segments] */
+MUON_API int muon_dp_plan_tables(const muon_dp_plan_t* plan, int32_t* owner,
+                                 int64_t* send_counts, int64_t* recv_counts,
+                                 muon_param_t* owned_params, muon_dp_segment_t* send_segs,
+                                 muon_dp_segment_t* recv_segs);
+
+/* Exchange buffers (device float).  direction MUON_DP_SEND: for every send
+ * segment, buf[seg.buf + i] = a[seg.local + i] and, for Muon slices,
+ * buf[seg.buf + seg.len + i] = b[seg.local + i] (a = accum, b = momentum,
+ * this rank's storage buffers).  MUON_DP_RECV: the same over the receive
+ * segments (a, b = the packed owned buffers).  muon_dp_unpack is the
+ * inverse copy.  The first device call of a plan uploads its segments
+ * (cudaMalloc; must not be stream-captured).  Errors: MUON_ERR_INVALID for
+ * NULL buffers, MUON_ERR_CUDA. */
+typedef enum { MUON_DP_SEND = 0, MUON_DP_RECV = 1 } muon_dp_direction_t;
+MUON_API int muon_dp_pack(muon_dp_plan_t* plan, int direction, float* buf, const float* a,
+                          const float* b, void* stream);
+MUON_API int muon_dp_unpack(muon_dp_plan_t* plan, int direction, const float* buf, float* a,
+                            float* b, void* stream);
+
+/* The write-back of step 6 above, on this rank's storage buffers, from the
+ * reverse exchange's buffer (send layout: u, then m' for Muon slices) and
+ * the all-reduced stats (device double[4], as muon_step_ex's stats_out
+ * summed over the ranks).  Writes d_result (applied = 0 when stats[1] > 0,
+ * ns_calls = stats[2], global_norm, clip_coef) for every rank alike. */
+MUON_API int muon_dp_finish(muon_dp_plan_t* plan, const float* buf, float* accum,
+                            float* momentum, float* master, const double* stats, float lr,
+                            float clip, muon_result_t* d_result, void* stream);
 
 /* Newton-Schulz orthogonalisation of one rows x cols row-major matrix:
  * normalise by the Frobenius norm (+1e-7), transpose if rows > cols,

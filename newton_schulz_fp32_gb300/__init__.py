@@ -36,7 +36,9 @@ EXPORTED = ["muon_accumulate", "muon_step", "muon_newton_schulz", "muon_get_stat
             "muon_last_error", "muon_release_workspace", "muon_device_error",
             "muon_profile_enable", "muon_profile_read", "muon_newton_schulz_noalloc",
             "muon_step_ex", "muon_profile_enable_phases", "muon_describe_tables",
-            "muon_testing_set"]
+            "muon_testing_set", "muon_dp_plan_create", "muon_dp_plan_destroy",
+            "muon_dp_plan_sizes", "muon_dp_plan_tables", "muon_dp_pack", "muon_dp_unpack",
+            "muon_dp_finish"]
 CLIP_MODES = {"update": 0, "grad": 1}
 
 
@@ -61,10 +63,11 @@ class StepOptions(ctypes.Structure):
                 ("adam_step", ctypes.c_int64), ("exp_avg", ctypes.c_void_p),
                 ("exp_avg_sq", ctypes.c_void_p), ("workspace_budget", ctypes.c_uint64),
                 ("last_grad", ctypes.c_void_p), ("last_grad_scale", ctypes.c_float),
-                ("last_grad_overwrite", ctypes.c_int32)]
+                ("last_grad_overwrite", ctypes.c_int32), ("stats_out", ctypes.c_void_p)]
 
 
 STEP_OPTIONS_V1_SIZE = 64   # struct_size of the layout that ends at workspace_budget
+STEP_OPTIONS_V2_SIZE = 80   # struct_size of the layout that ends at last_grad_overwrite
 
 
 class TableInfo(ctypes.Structure):
@@ -168,17 +171,21 @@ def accumulate(accum, grad, scale: float, overwrite: bool = False, params=None, 
 
 def step_options(clip_mode="update", grad_scale: float = 1.0, adam: dict | None = None,
                  workspace_budget: int = 0, last_grad=None, last_grad_scale: float = 1.0,
-                 last_grad_overwrite: bool = False) -> StepOptions:
+                 last_grad_overwrite: bool = False, stats_out=None) -> StepOptions:
     """A muon_step_options_t.  adam: dict(lr, beta1, beta2, eps, step,
     exp_avg, exp_avg_sq) with device float buffers in accum's layout.
     last_grad: the last micro-batch's bf16 gradients (accum's layout), which
     the step accumulates itself, as accumulate(accum, last_grad,
-    last_grad_scale, last_grad_overwrite) would."""
+    last_grad_scale, last_grad_overwrite) would.  stats_out: a device
+    float64[4] the step fills with (sum of squares of the clip norm, skipped,
+    NS problems, 0)."""
     o = StepOptions()
     o.struct_size = ctypes.sizeof(StepOptions)
     o.clip_mode = CLIP_MODES[clip_mode] if isinstance(clip_mode, str) else int(clip_mode)
     o.grad_scale = grad_scale
     o.workspace_budget = int(workspace_budget)
+    if stats_out is not None:
+        o.stats_out = _ptr(stats_out)
     if last_grad is not None:
         o.last_grad = _ptr(last_grad)
         o.last_grad_scale = last_grad_scale

@@ -1191,6 +1191,12 @@ void set_last_error(const char* msg) {
 
 std::mutex& library_mutex() { return g_mu; }
 
+int validate_tables(const muon_param_t* params, int nparams, const muon_partition_t* parts,
+                    int nparts) {
+  Layout L;
+  return validate_and_build(params, nparams, parts, nparts, L);
+}
+
 }  // namespace muon
 
 // ==================================================================== C ABI
@@ -1254,11 +1260,19 @@ int apply_options(const muon_step_options_t* opts, StreamLaunchArgs& a) {
   a.last_grad = nullptr;
   a.last_scale = 1.f;
   a.last_overwrite = 0;
+  a.stats_out = nullptr;
   if (!opts) return MUON_OK;
-  const bool v2 = opts->struct_size == static_cast<int32_t>(sizeof(muon_step_options_t));
+  const bool v3 = opts->struct_size == static_cast<int32_t>(sizeof(muon_step_options_t));
+  const bool v2 = v3 || opts->struct_size == MUON_STEP_OPTIONS_V2_SIZE;
   if (!v2 && opts->struct_size != MUON_STEP_OPTIONS_V1_SIZE)
     return fail(MUON_ERR_INVALID,
-                "opts->struct_size must be sizeof(muon_step_options_t) or MUON_STEP_OPTIONS_V1_SIZE");
+                "opts->struct_size must be sizeof(muon_step_options_t), MUON_STEP_OPTIONS_V2_SIZE "
+                "or MUON_STEP_OPTIONS_V1_SIZE");
+  if (v3 && opts->stats_out) {
+    if (reinterpret_cast<uintptr_t>(opts->stats_out) % 8)
+      return fail(MUON_ERR_INVALID, "stats_out must be 8-byte aligned");
+    a.stats_out = opts->stats_out;
+  }
   if (v2 && opts->last_grad) {
     if (reinterpret_cast<uintptr_t>(opts->last_grad) % 8)
       return fail(MUON_ERR_INVALID, "last_grad must be 8-byte aligned");

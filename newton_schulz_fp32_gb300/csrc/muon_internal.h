@@ -192,6 +192,8 @@ struct StreamLaunchArgs {
   const uint16_t* last_grad;
   float last_scale;
   int last_overwrite;
+  // non-null: k_finalize writes {sum of squares, skipped, NS problems, 0}
+  double* stats_out;
 };
 
 void launch_accumulate(float* accum, const uint16_t* grad, const Run* runs, int nruns,
@@ -231,6 +233,10 @@ constexpr int kX3BM = 128, kX3BN = 128;
 void set_last_error(const char* msg);
 // The lock every entry point holds for the whole call.
 std::mutex& library_mutex();
+// The table checks of muon_step (host only): MUON_OK or the error it would
+// report, with muon_last_error() set.
+int validate_tables(const muon_param_t* params, int nparams, const muon_partition_t* parts,
+                    int nparts);
 // The allocation-free entry's device error flag on every device that has
 // used it: the first nonzero code, cleared once read (0 = none).
 int noalloc_take_device_error();

@@ -144,6 +144,10 @@ extern "C" int muon_newton_schulz_noalloc(const void* X, void* Y, int rows, int 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return nofail(MUON_ERR_CUDA, "cudaGetDevice failed");
+  // The TMA descriptors are encoded by a driver call, which needs the
+  // device's context current on this host thread; a thread whose first CUDA
+  // call this is has none yet, and cudaSetDevice makes it current.
+  if (cudaSetDevice(dev) != cudaSuccess) return nofail(MUON_ERR_CUDA, "cudaSetDevice failed");
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);

@@ -745,6 +745,12 @@ k_finalize(StreamLaunchArgs a) {
       a.state->coef = 0.f;
       muon_result_t r{0, 0, 0.f, 0.f};
       *a.result = r;
+      if (a.stats_out) {
+        a.stats_out[0] = 0.0;
+        a.stats_out[1] = 1.0;
+        a.stats_out[2] = 0.0;
+        a.stats_out[3] = 0.0;
+      }
     }
     return;
   }
@@ -761,6 +767,12 @@ k_finalize(StreamLaunchArgs a) {
     a.state->applied = applied;
     muon_result_t r{applied, a.ns_calls, a.state->norm, a.state->coef};
     *a.result = r;
+    if (a.stats_out) {
+      a.stats_out[0] = a.state->sumsq;
+      a.stats_out[1] = applied == 1 ? 0.0 : 1.0;
+      a.stats_out[2] = static_cast<double>(a.ns_calls);
+      a.stats_out[3] = 0.0;
+    }
   }
 }
 

@@ -93,6 +93,20 @@ def adam_update(g, exp_avg, exp_avg_sq, w, lr, beta1, beta2, eps, step):
     return m, v, w_new
 
 
+def write_back(u, w, post, lr, mode, use_muon):
+    """The write-back of one parameter (or any slice of it, element by
+    element): v = post * u and, for a Muon parameter, w - lr * v.  exact
+    mode keeps a Muon update in float64 until both results are rounded to
+    float32 once; otherwise every operation is float32.  An auxiliary
+    parameter's master is returned unchanged.  Returns (v, new w)."""
+    w = np.asarray(w, np.float32)
+    if mode == "exact" and use_muon:
+        v64 = post * np.asarray(u, np.float64)
+        return v64.astype(np.float32), (w.astype(np.float64) - lr * v64).astype(np.float32)
+    v = np.asarray(u, np.float32) if post == 1.0 else np.float32(post) * np.asarray(u, np.float32)
+    return v, (w - np.float32(lr) * v if use_muon else w)
+
+
 def muon_step_full(mats, beta, lr, method="gram", steps=ns.DEFAULT_STEPS, clip=0.0,
                    mode="exact", clip_mode="update", grad_scale=1.0, adam=None):
     """One optimizer step on full matrices (no partition tables).
@@ -161,16 +175,10 @@ def muon_step_full(mats, beta, lr, method="gram", steps=ns.DEFAULT_STEPS, clip=0
 
     updates, masters, ea, eas = [], [], [], []
     for d, u in zip(mats, us):
-        w = np.asarray(d["w"], np.float32)
-        if mode == "exact" and d["use_muon"]:
-            v64 = post * np.asarray(u, np.float64)
-            v = v64.astype(np.float32)
-            w_new = (w.astype(np.float64) - lr * v64).astype(np.float32)
-        else:
-            v = np.asarray(u, np.float32) if post == 1.0 else np.float32(post) * np.asarray(u, np.float32)
-            w_new = w - np.float32(lr) * v if d["use_muon"] else w
+        v, w_new = write_back(u, d["w"], post, lr, mode, d["use_muon"])
         if adam is not None and not d["use_muon"]:
-            m1, v2, w_new = adam_update(v, d["exp_avg"], d["exp_avg_sq"], w, **adam)
+            m1, v2, w_new = adam_update(v, d["exp_avg"], d["exp_avg_sq"],
+                                        np.asarray(d["w"], np.float32), **adam)
             ea.append(m1)
             eas.append(v2)
         else:

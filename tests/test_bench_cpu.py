@@ -1,6 +1,6 @@
 """The bench's reference arm runs on the host alone (the oracle timed on a
-bounded sample of the GPT-2-small step) and prints the contract's single
-JSON line."""
+bounded sample of the Llama-3-8B step, extrapolated by formula flops) and
+prints the contract's single JSON line, whose fields say what was timed."""
 import json
 import os
 import subprocess
@@ -22,8 +22,13 @@ def test_reference_arm_prints_one_contract_line():
                 "cpu_baseline", "e2e"):
         assert key in d, key
     assert d["impl"] == "reference" and d["unit"] == "ms" and d["higher_is_better"] is False
-    assert d["value"] > 0 and d["value"] == d["ms_per_step"] == d["cpu_baseline"]["value"]
+    assert d["value"] > 0 and d["value"] == d["cpu_baseline"]["value"]
+    assert d["steps"] == 1 and d["warmup"] == 3
+    # a sampled arm: ms_per_step is the time of one timed (sample) step, and
+    # the value is that time scaled to the whole step
+    assert d["sampled"] is True and d["sample_scale"] > 1
+    assert abs(d["value"] - d["ms_per_step"] * d["sample_scale"]) <= 1e-6 * d["value"]
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["cpu"]
     assert d["e2e"] == {"value": d["value"], "unit": "ms", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}

@@ -275,12 +275,15 @@ def test_gpt2_small_config(torch):
         assert_close_update(u_un[k] / gres["clip_coef"], u_or, "bf16", spec.name)
 
 
-def test_ragged_small_matrices_gram(torch):
+@pytest.mark.parametrize("nparts", [1, 8])
+def test_ragged_small_matrices_gram(torch, nparts):
     """8192 matrices, rows from {32..256}, cols from {128..1024}, half tall;
     fp32 grads N(0,1) x 10^U(-5,0) written straight into accum; one gram
-    step.  64 sampled matrices against the oracle, all in the band."""
+    step.  64 sampled matrices against the oracle, all in the band.  P = 1
+    is the plain reading of the config; P = 8 puts partition boundaries
+    through the packed small matrices of both orientations."""
     seed = wl.CONFIG_SEED["ragged"]
-    lay = wl.ragged_layout(8192, seed=seed)
+    lay = wl.ragged_layout(8192, nparts=nparts, seed=seed)
     rng = wl.rng_for(seed, 1)
     scales = 10.0 ** rng.uniform(-5, 0, len(lay.specs))
     mats = [(wl.rng_for(seed, 2, i).standard_normal((s.rows, s.cols)) * scales[i]).astype(np.float32)
@@ -315,7 +318,9 @@ def test_llama3_8b_config_sampled(torch):
     mom = torch.zeros(n, dtype=torch.float32, device="cuda")
     mst = torch.zeros(n, dtype=torch.float32, device="cuda")
     grad = torch.empty(n, dtype=torch.bfloat16, device="cuda")
-    sample = [1, 7 * 31 + 1, 7 * 31 + 2]          # k of layer 0, k and v of layer 31
+    # k (1024x4096), o (4096^2) and up (14336x4096) of layer 0; k, v and
+    # down (4096x14336) of layer 31
+    sample = [1, 3, 5, 7 * 31 + 1, 7 * 31 + 2, 7 * 31 + 6]
     g_host = {k: [] for k in sample}
     for mb in range(2):
         wl.llama_grad_into(lay, seed, mb, grad)

@@ -24,9 +24,15 @@ hold at any size:
 Tolerances: the probe compares a result rounded at every product (BF16:
 A, B and X rounded to bf16, relative 2^-9 each, over terms of size up to
 |b|, |c| ~ 5 that cancel to ~1) with exact arithmetic on the same X_k;
-3e-2 relative in BF16 mode, 1e-4 in FP32 mode (split-3 products carry
-~1e-6).  A wrong coefficient, a dropped term or a transposed operand moves
-the probe by O(1).  Band edges get 2% (BF16) / 1e-4 (FP32)."""
+3e-2 relative in BF16 mode, 1e-4 in FP32 mode for the standard form
+(split-3 products carry ~1e-6, and X_k is the very iterate X_{k+1} was made
+from).  The gram form's k- and (k+1)-step outputs come from separate runs
+of the recurrence (Q_k X0 is formed anew each run), so the probe sees both
+runs' rounding, amplified by up to a = 3.4 through the step map; its FP32
+bound is the FP32 parity rule's rtol, 1e-3 (the compiled-NS check of
+"Support Muon in BF16_Optimizer with FP32 gradient accumulation",
+validation table).  A wrong coefficient, a dropped term or a transposed
+operand moves the probe by O(1).  Band edges get 2% (BF16) / 1e-4 (FP32)."""
 import numpy as np
 import pytest
 
@@ -38,7 +44,8 @@ pytestmark = pytest.mark.gpu
 
 A, B, C = ons.A_COEF, ons.B_COEF, ons.C_COEF
 F_MAX, F_MIN = 1.2024, 0.6818       # quintic's local max f(0.5545), local min f(1.0501)
-PROBE_TOL = {"bf16": 3e-2, "fp32": 1e-4}
+PROBE_TOL = {("bf16", "standard"): 3e-2, ("bf16", "gram"): 3e-2,
+             ("fp32", "standard"): 1e-4, ("fp32", "gram"): 1e-3}
 BAND_TOL = {"bf16": 2e-2, "fp32": 1e-4}
 
 
@@ -96,9 +103,14 @@ CASES = [
     (8192, 8192, "standard", "bf16"),
     (8192, 8192, "gram", "bf16"),
     (8192, 8192, "standard", "fp32"),
+    (8192, 8192, "gram", "fp32"),
     (16384, 16384, "standard", "bf16"),
+    (16384, 16384, "gram", "bf16"),
+    (16384, 16384, "standard", "fp32"),
+    (16384, 16384, "gram", "fp32"),
     (4096, 16384, "standard", "bf16"),
     (4096, 16384, "gram", "bf16"),
+    (4096, 16384, "gram", "fp32"),
     (16384, 4096, "standard", "bf16"),
     (16384, 4096, "standard", "fp32"),
 ]
@@ -114,7 +126,7 @@ def test_full_size_step_map_and_band(torch, rows, cols, method, mode):
         outs[k] = canon64(torch, Y)
     torch.cuda.synchronize()
     assert nsg.device_error() == 0
-    tol = PROBE_TOL[mode]
+    tol = PROBE_TOL[(mode, method)]
     # step 0 -> 1 from X_0 formed here
     G = canon64(torch, X)
     X0 = G / (torch.linalg.norm(G) + 1e-7)

@@ -109,12 +109,13 @@ def _step_ex(lib, opts, ptrs=(FAKE, FAKE, FAKE)):
 
 def test_step_options_struct_layout():
     # muon.h: the original layout ends at workspace_budget (64 bytes); the
-    # folded last micro-batch follows it
-    assert ctypes.sizeof(nsg.StepOptions) == 80
+    # folded last micro-batch follows it (80), then the statistics pointer
+    assert ctypes.sizeof(nsg.StepOptions) == 88
     assert nsg.StepOptions.adam_step.offset == 32 and nsg.StepOptions.workspace_budget.offset == 56
     assert nsg.StepOptions.last_grad.offset == nsg.STEP_OPTIONS_V1_SIZE == 64
     assert nsg.StepOptions.last_grad_scale.offset == 72
     assert nsg.StepOptions.last_grad_overwrite.offset == 76
+    assert nsg.StepOptions.stats_out.offset == nsg.STEP_OPTIONS_V2_SIZE == 80
 
 
 def test_step_options_rejected_on_host(lib):
@@ -136,6 +137,7 @@ def test_step_options_rejected_on_host(lib):
     cases.append((o, "last_grad_overwrite"))
     o = nsg.step_options(); o.struct_size = 72
     cases.append((o, "struct_size"))
+    cases.append((nsg.step_options(stats_out=FAKE + 4), "stats_out"))
     for opts, word in cases:
         rc = _step_ex(lib, opts)
         assert rc == nsg.MUON_ERR_INVALID, (word, rc)
@@ -155,6 +157,9 @@ def test_valid_options_without_gpu_fail_cleanly(lib):
     adam = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, step=3, exp_avg=FAKE, exp_avg_sq=FAKE)
     v1 = nsg.step_options(last_grad=FAKE + 2)   # ignored: the fields are absent in a v1 struct
     v1.struct_size = nsg.STEP_OPTIONS_V1_SIZE
+    v2 = nsg.step_options(stats_out=FAKE + 4)   # ignored: absent in a v2 struct
+    v2.struct_size = nsg.STEP_OPTIONS_V2_SIZE
     for opts in (None, nsg.step_options(), nsg.step_options("grad", 2.0 ** -10, adam),
-                 nsg.step_options(last_grad=FAKE, last_grad_scale=0.25), v1):
+                 nsg.step_options(last_grad=FAKE, last_grad_scale=0.25), v1, v2,
+                 nsg.step_options(stats_out=FAKE)):
         assert _step_ex(lib, opts) == nsg.MUON_ERR_CUDA
