@@ -107,7 +107,7 @@ def llama_workload(mode, layers=32):
     return Workload("llama", lay, 2, "standard", 0.0, desc)
 
 
-def make_inputs(torch, W, stream):
+def make_inputs(torch, W, stream, host_copies=True):
     """Device state and micro-batch gradients, plus pinned host copies of the
     gradients (the end-to-end run copies them in every step)."""
     lay = W.lay
@@ -133,9 +133,11 @@ def make_inputs(torch, W, stream):
             g_dev = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(W.gas)]
             for mb in range(W.gas):
                 wl.llama_grad_into(lay, seed, mb, g_dev[mb])
-        g_host = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(W.gas)]
-        for h, d in zip(g_host, g_dev):
-            h.copy_(d)
+        g_host = []
+        if host_copies:
+            g_host = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(W.gas)]
+            for h, d in zip(g_host, g_dev):
+                h.copy_(d)
     torch.cuda.synchronize()
     return acc, mom, mst, g_dev, g_host
 
@@ -349,9 +351,10 @@ def cpu_baseline(workload, ns_method, mode, budget_s):
 # ------------------------------------------------------------------ GPU run
 
 def run_gpu(args, W, rank, world):
-    """Warm-up, the K timed steps as one CUDA-graph replay (inputs resident),
-    an eager pass of the same steps for the phase split, and the end-to-end
-    loop with host copies.  Returns a dict of measurements."""
+    """One GPU, all partitions emulated on it: warm-up, the K timed steps as
+    one CUDA-graph replay (inputs resident), an eager pass of the same steps
+    for the phase split, and the end-to-end loop with host copies.  Returns
+    a dict of measurements."""
     import torch
     import newton_schulz_fp32_gb300 as nsg
 
@@ -387,11 +390,7 @@ def run_gpu(args, W, rank, world):
     if r["applied"] != 1:
         raise RuntimeError(f"warm-up step not applied: {r}")
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-        torch.cuda.synchronize()
+    barrier = torch.cuda.synchronize
 
     # ---- the K timed steps as one CUDA graph: once the plans exist the
     # library only issues stream-ordered work (no allocation, no host
@@ -499,13 +498,120 @@ def run_gpu(args, W, rank, world):
     if nsg.read_result(res_hosts[(args.steps - 1) & 1])["applied"] != 1:
         raise RuntimeError("end-to-end step not applied")
     ws = nsg.get_stats()["workspace_bytes"]
-    if world > 1:
-        ms, e2e_ms = max_over_ranks([ms, e2e_ms], "cuda")
     del acc, mom, mst, g_dev, g_host, g_last
     nsg.release_workspace()
     torch.cuda.empty_cache()
     return {"ms": ms, "e2e_ms": e2e_ms, "h2d": h2d, "phases": phases, "clocks": clk,
             "launches": launches, "workspace_bytes": ws}
+
+
+def run_dp(args, W, rank, world):
+    """The data-parallel step over `world` ranks (one process per GPU, NCCL):
+    the workload's parameter set cut into one partition per rank (128
+    alignment), each rank holding only its own partition of accum, momentum
+    and master and its partition of each micro-batch's gradients.  One step
+    = the micro-batches accumulated into the local partition, then the
+    data-parallel Muon step (exchange to owners, Newton-Schulz on whole
+    matrices, all-reduce of the norm statistics, exchange back, write-back).
+    Returns the measurements of this rank (times are maxima over ranks)."""
+    import torch
+    import torch.distributed as dist
+    import newton_schulz_fp32_gb300 as nsg
+    from newton_schulz_fp32_gb300 import dp
+
+    dev = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(dev)
+    nsg.build()
+    lay = wl.llama3_8b_layout(nparts=world) if W.name == "llama" else \
+        wl.gpt2_small_layout(nparts=world)
+    gas = W.gas
+    pr = np.arange(len(lay.parts), dtype=np.int32) % world
+    parts_local, sizes = dp.local_partition_table(lay.parts, pr, world)
+    n = sizes[rank]
+    pieces = [(int(lay.parts["storage_offset"][p]), int(parts_local["storage_offset"][p]),
+               int(lay.parts["flat_end"][p] - lay.parts["flat_begin"][p]))
+              for p in range(len(lay.parts)) if pr[p] == rank]
+    plan = dp.DPPlan(lay.params, parts_local, pr, world, rank, W.ns_method)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        W_full = Workload(W.name, lay, gas, W.ns_method, W.clip, W.desc)
+        acc_f, mom_f, mst_f, g_f, _ = make_inputs(torch, W_full, stream, host_copies=False)
+
+        def local(t):
+            out = torch.empty(n, dtype=t.dtype, device="cuda")
+            for g0, l0, k in pieces:
+                out[l0:l0 + k].copy_(t[g0:g0 + k])
+            return out
+        acc, mom, mst = local(acc_f), local(mom_f), local(mst_f)
+        g_dev = [local(g) for g in g_f]
+        del acc_f, mom_f, mst_f, g_f
+        g_host = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(gas)]
+        for h, d in zip(g_host, g_dev):
+            h.copy_(d)
+        res = torch.zeros(4, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    D = dp.DataParallelMuon(plan)
+
+    def step():
+        for mb in range(gas):
+            nsg.accumulate(acc, g_dev[mb], 1.0 / gas, overwrite=(mb == 0), n=n, stream=stream)
+        D.step(acc, mom, mst, 0.95, 0.02, W.ns_method, 5, W.clip, args.mode, result=res,
+               stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if nsg.read_result(res)["applied"] != 1:
+        raise RuntimeError("warm-up step not applied")
+
+    def barrier():
+        dist.barrier()
+        torch.cuda.synchronize()
+
+    launches0 = nsg.get_stats()["kernel_launches_total"]
+    clocks = ClockSampler(dev)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    clk = clocks.stop()
+    launches = nsg.get_stats()["kernel_launches_total"] - launches0
+    if nsg.device_error() != 0:
+        raise RuntimeError("a kernel reported a device error during the timed region")
+    # end to end: the local gradients from pinned host memory every step,
+    # the step, the result read back
+    h2d = sum(g.numel() * 2 for g in g_host)
+    res_host = torch.zeros(4, dtype=torch.int32).pin_memory()
+    barrier()
+    t_wall = time.perf_counter()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.steps):
+        with torch.cuda.stream(stream):
+            for d, h in zip(g_dev, g_host):
+                d.copy_(h, non_blocking=True)
+        step()
+        with torch.cuda.stream(stream):
+            res_host.copy_(res, non_blocking=True)
+        stream.synchronize()
+    e3.record(stream)
+    barrier()
+    e2e_ms = max(e2.elapsed_time(e3) / args.steps,
+                 1000.0 * (time.perf_counter() - t_wall) / args.steps)
+    if nsg.read_result(res_host)["applied"] != 1:
+        raise RuntimeError("end-to-end step not applied")
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], "cuda")
+    return {"ms": ms, "e2e_ms": e2e_ms, "h2d": h2d, "clocks": clk, "launches": launches,
+            "layout": lay, "owned_params": int(plan.sizes["owned_params"]),
+            "balance": plan.sizes["owned_cost"] / max(plan.sizes["max_cost"], 1e-30),
+            "exchange_elems_per_step": 2 * (plan.send_elems + plan.recv_elems)}
 
 
 def contract_fields(args, W, m, peaks, peak_src, world):
@@ -763,6 +869,35 @@ def reference_line(args, peaks, peak_src):
                     "d2h_bytes_per_step": 0}}
 
 
+def dp_line(args, W, m, world):
+    """The contract line of a data-parallel run (N ranks, strong scaling:
+    the same parameter set over more GPUs)."""
+    lay = m["layout"]
+    desc = W.desc.replace("P=64", f"P={world}").replace("P=8", f"P={world}")
+    return {
+        "metric": METRIC, "value": m["ms"], "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": m["ms"], "higher_is_better": False,
+        "scaling": "strong", "vs_baseline": None, "dtype": args.mode + "+fp32",
+        "data": "synthetic",
+        "config": {"workload": desc + "; data parallel: each rank holds one partition, "
+                                      "matrices spread over owner ranks, NCCL all-to-all of "
+                                      "the slices each way and one all-reduce of the norm "
+                                      "statistics",
+                   "parallelism": f"dp{world}", "ns_method": W.ns_method,
+                   "operand_mode": args.mode,
+                   "l2": f"inputs larger than L2 ({4 * lay.storage_size / world / 1e9:.2f} GB of "
+                         "fp32 state per rank and buffer), no flush",
+                   "launch": "eager; K steps between events, barrier on both sides, max over ranks"},
+        "ns_flops_per_step": ns_formula_flops(lay, W.ns_method),
+        "ns_tflops_whole_job": ns_formula_flops(lay, W.ns_method) / (m["ms"] * 1e-3) / 1e12,
+        "rank0_owned_params": m["owned_params"], "rank0_load_vs_max": m["balance"],
+        "exchange_elems_per_step_rank0": m["exchange_elems_per_step"],
+        "roofline": None, "cpu_baseline": None,
+        "e2e": {"value": m["e2e_ms"], "unit": "ms", "h2d_bytes_per_step": m["h2d"],
+                "d2h_bytes_per_step": 16},
+        "gpu_launches": m["launches"], "clocks": m["clocks"]}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -783,6 +918,8 @@ def main():
                          "llama_layers (a smaller Llama-shaped case for profiler captures) print "
                          "extra lines")
     ap.add_argument("--layers", type=int, default=1, help="llama_layers: layers of the case")
+    ap.add_argument("--dp", action="store_true",
+                    help="run the data-parallel path even on one rank (one-rank NCCL group)")
     ap.add_argument("--shapes", default="", help="sweep shapes, e.g. 4096x4096,4096x16384")
     ap.add_argument("--ragged-count", type=int, default=8192,
                     help="ragged workload: number of matrices (a smaller count keeps profiler "
@@ -805,12 +942,22 @@ def main():
             args.workload](args, peaks, peak_src)
         return
 
-    if world > 1:
+    if world > 1 or args.dp:
         import torch
         import torch.distributed as dist
+        if world == 1:
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            os.environ.setdefault("MASTER_PORT", "29517")
+            os.environ.setdefault("RANK", "0")
+            os.environ.setdefault("WORLD_SIZE", "1")
         dist.init_process_group("nccl", device_id=torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))))
 
     W = gpt2_workload(args.ns_method, args.mode) if args.workload == "gpt2" else llama_workload(args.mode)
+    if world > 1 or args.dp:
+        m = run_dp(args, W, rank, world)
+        if rank == 0:
+            print(json.dumps(dp_line(args, W, m, world)))
+        return
     m = run_gpu(args, W, rank, world)
     fields = contract_fields(args, W, m, peaks, peak_src, world)
     secondary = None
@@ -834,7 +981,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": m["ms"], "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": args.mode + "+fp32",
         "data": "synthetic",
-        "config": {"workload": W.desc, "parallelism": f"replicas{world}" if world > 1 else "single",
+        "config": {"workload": W.desc, "parallelism": "single",
                    "l2": "inputs larger than L2 (each fp32 state buffer "
                          f"{4 * W.lay.storage_size / 1e9:.2f} GB), no flush",
                    "ns_method": W.ns_method, "operand_mode": args.mode,

@@ -254,10 +254,6 @@ int validate_and_build(const muon_param_t* params, int nparams, const muon_parti
       if (o.is_muon) {
         o.ldx = static_cast<int32_t>(round_up(o.n, 8));
         o.ldm = static_cast<int32_t>(round_up(o.m, 8));
-        o.x_off = L.x_elems;
-        o.sq_off = L.sq_elems;
-        L.x_elems += round_up(int64_t(o.m) * o.ldx, 64);
-        L.sq_elems += round_up(int64_t(o.m) * o.ldm, 64);
         L.muon_elems += o.numel;
         ++L.n_muon_owners;
       } else {
@@ -266,6 +262,51 @@ int validate_and_build(const muon_param_t* params, int nparams, const muon_parti
       L.owners.push_back(o);
     }
   }
+
+  // Newton-Schulz problems stack runs of consecutive Muon blocks of one
+  // shape (ns_blocks).  A table that interleaves shapes (many small matrices
+  // of mixed sizes) stacks far better with its Muon blocks ordered by shape,
+  // so that order is taken when it gives fewer problems at the single-SM
+  // stack cap; otherwise (GPT-2's head blocks already run together) the
+  // table order stays.  The order depends on the parameters alone, so it is
+  // the same for every partitioning.
+  {
+    auto problems_at_128 = [](const std::vector<Owner>& v) {
+      int64_t n = 0;
+      int run_m = 0, run_n = 0, run_rows = 0;
+      bool prev_muon = false;
+      for (const Owner& o : v) {
+        if (!o.is_muon) { prev_muon = false; continue; }
+        const bool join = prev_muon && o.m % 32 == 0 && 2 * o.m <= 128 && o.m == run_m &&
+                          o.n == run_n && run_rows + o.m <= 128;
+        if (join) {
+          run_rows += o.m;
+        } else {
+          ++n;
+          run_m = o.m;
+          run_n = o.n;
+          run_rows = o.m;
+        }
+        prev_muon = true;
+      }
+      return n;
+    };
+    std::vector<Owner> by_shape = L.owners;
+    std::stable_sort(by_shape.begin(), by_shape.end(), [](const Owner& x, const Owner& y) {
+      if (x.is_muon != y.is_muon) return x.is_muon > y.is_muon;
+      if (!x.is_muon) return false;
+      if (x.m != y.m) return x.m < y.m;
+      return x.n < y.n;
+    });
+    if (problems_at_128(by_shape) < problems_at_128(L.owners)) L.owners.swap(by_shape);
+  }
+  for (Owner& o : L.owners)
+    if (o.is_muon) {
+      o.x_off = L.x_elems;
+      o.sq_off = L.sq_elems;
+      L.x_elems += round_up(int64_t(o.m) * o.ldx, 64);
+      L.sq_elems += round_up(int64_t(o.m) * o.ldm, 64);
+    }
 
   // A tile qualifies for the kernels' 16-byte path when it lies in one
   // segment with 16-byte aligned storage (see ETile).
@@ -1190,6 +1231,11 @@ void set_last_error(const char* msg) {
 }
 
 std::mutex& library_mutex() { return g_mu; }
+
+void count_launches(int n) {
+  g_cnt.launches_last = n;
+  g_cnt.launches_total += n;
+}
 
 int validate_tables(const muon_param_t* params, int nparams, const muon_partition_t* parts,
                     int nparts) {

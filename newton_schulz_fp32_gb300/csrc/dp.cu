@@ -414,6 +414,7 @@ extern "C" int muon_dp_pack(muon_dp_plan_t* plan, int direction, float* buf, con
   k_dp_gather<<<static_cast<unsigned>(chunks.size()), kDpThreads, 0,
                 static_cast<cudaStream_t>(stream)>>>(d, buf, a, b);
   if (cudaGetLastError() != cudaSuccess) return dpfail(MUON_ERR_CUDA, "kernel launch failed");
+  count_launches(1);
   return MUON_OK;
 }
 
@@ -435,6 +436,7 @@ extern "C" int muon_dp_unpack(muon_dp_plan_t* plan, int direction, const float* 
   k_dp_scatter<<<static_cast<unsigned>(chunks.size()), kDpThreads, 0,
                  static_cast<cudaStream_t>(stream)>>>(d, buf, a, b);
   if (cudaGetLastError() != cudaSuccess) return dpfail(MUON_ERR_CUDA, "kernel launch failed");
+  count_launches(1);
   return MUON_OK;
 }
 
@@ -459,5 +461,6 @@ extern "C" int muon_dp_finish(muon_dp_plan_t* plan, const float* buf, float* acc
   }
   k_dp_result<<<1, 1, 0, s>>>(stats, clip, d_result);
   if (cudaGetLastError() != cudaSuccess) return dpfail(MUON_ERR_CUDA, "kernel launch failed");
+  count_launches(plan->send_chunks.empty() ? 1 : 2);
   return MUON_OK;
 }

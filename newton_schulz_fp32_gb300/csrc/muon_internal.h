@@ -233,6 +233,9 @@ constexpr int kX3BM = 128, kX3BN = 128;
 void set_last_error(const char* msg);
 // The lock every entry point holds for the whole call.
 std::mutex& library_mutex();
+// Adds n kernel launches to muon_get_stats' counters (the caller holds the
+// library lock).
+void count_launches(int n);
 // The table checks of muon_step (host only): MUON_OK or the error it would
 // report, with muon_last_error() set.
 int validate_tables(const muon_param_t* params, int nparams, const muon_partition_t* parts,

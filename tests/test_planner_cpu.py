@@ -95,6 +95,18 @@ def test_ragged_blocks_use_single_sms(lib):
     assert d["ns_problems"] <= 512
 
 
+def test_ragged_blocks_stack_by_shape(lib):
+    """Randomly ordered small matrices stack as if grouped by shape: per
+    canonical shape (m, n), blocks of 32 or 64 rows fill 128-row stacks."""
+    from collections import Counter
+    lay = wl.ragged_layout(2048, seed=1003)
+    shapes = Counter((min(s.rows, s.cols), max(s.rows, s.cols)) for s in lay.specs)
+    want = sum(-(-c // (128 // m)) if m % 32 == 0 and 2 * m <= 128 else c
+               for (m, n), c in shapes.items())
+    d = nsg.describe_tables(lay.params, lay.parts, "gram", "bf16")
+    assert d["ns_problems"] == want < 2048
+
+
 def test_describe_rejects_what_the_step_rejects(lib):
     bad = np.zeros(1, dtype=nsg.PARAM_DTYPE)
     bad[0] = (0, 10, 8, 3, 1)                        # 10 rows in 3 heads

@@ -1,7 +1,7 @@
-"""The multi-GPU run is N independent replicas (the partition table emulates
-the ranks on one GPU; there is no data-path collective): the only
-cross-rank step is the bench's barrier and the maximum of the per-rank
-times.  Checked here with two gloo processes on the CPU."""
+"""The bench's multi-GPU line takes the slowest rank's time for the whole
+job (the maximum of the per-rank times over the process group).  Checked
+here with two gloo processes on the CPU; the data-parallel step's own
+exchange is tested in test_dp_cpu.py."""
 import os
 import socket
 
