@@ -124,14 +124,19 @@ void record_event(cudaEvent_t e, cudaStream_t s) {
     cudaEventRecord(e, s);
 }
 
-// Brackets one launch group with events (when profiling) and counts kernels.
+const char* const kPhaseNames[MUON_PHASE_COUNT] = {
+    "muon:accumulate", "muon:reduce", "muon:gather", "muon:ns_gemm", "muon:norm", "muon:scatter"};
+
+// Brackets one launch group with events (when profiling), an NVTX range
+// and counts kernels.
 struct PhaseScope {
   int phase, kernels;
   double bytes, flops;
   cudaStream_t s;
+  NvtxRange range_;
   cudaEvent_t a = nullptr, b = nullptr;
   PhaseScope(int ph, cudaStream_t st, int nkern, double by, double fl)
-      : phase(ph), kernels(nkern), bytes(by), flops(fl), s(st) {
+      : phase(ph), kernels(nkern), bytes(by), flops(fl), s(st), range_(kPhaseNames[ph]) {
     if ((g_profile >> ph & 1u) && nkern > 0) {
       a = get_event();
       b = get_event();
@@ -1252,6 +1257,7 @@ using namespace muon;
 extern "C" int muon_accumulate(float* accum, const uint16_t* grad, int64_t n, float scale,
                                int overwrite, const muon_param_t* params, int nparams,
                                const muon_partition_t* parts, int nparts, void* stream) {
+  NvtxRange nvtx_("muon_accumulate");
   std::lock_guard<std::mutex> lk(g_mu);
   g_err.clear();
   g_cnt.launches_last = 0;
@@ -1533,6 +1539,7 @@ extern "C" int muon_step(float* accum, float* momentum, float* master, const muo
                          int nparams, const muon_partition_t* parts, int nparts, float beta,
                          float lr, int ns_method, int ns_steps, float clip, int operand_mode,
                          muon_result_t* d_result, void* stream) {
+  NvtxRange nvtx_("muon_step");
   std::lock_guard<std::mutex> lk(g_mu);
   return step_impl(accum, momentum, master, params, nparams, parts, nparts, beta, lr, ns_method,
                    ns_steps, clip, operand_mode, nullptr, d_result, stream);
@@ -1544,6 +1551,7 @@ extern "C" int muon_step_ex(float* accum, float* momentum, float* master,
                             int ns_method, int ns_steps, float clip, int operand_mode,
                             const muon_step_options_t* opts, muon_result_t* d_result,
                             void* stream) {
+  NvtxRange nvtx_("muon_step_ex");
   std::lock_guard<std::mutex> lk(g_mu);
   return step_impl(accum, momentum, master, params, nparams, parts, nparts, beta, lr, ns_method,
                    ns_steps, clip, operand_mode, opts, d_result, stream);
@@ -1551,6 +1559,7 @@ extern "C" int muon_step_ex(float* accum, float* momentum, float* master,
 
 extern "C" int muon_newton_schulz(const void* X, void* Y, int rows, int cols, int io_dtype,
                                   int ns_method, int ns_steps, int operand_mode, void* stream) {
+  NvtxRange nvtx_("muon_newton_schulz");
   std::lock_guard<std::mutex> lk(g_mu);
   g_err.clear();
   g_cnt.launches_last = 0;

@@ -399,6 +399,7 @@ extern "C" int muon_dp_plan_tables(const muon_dp_plan_t* plan, int32_t* owner,
 extern "C" int muon_dp_pack(muon_dp_plan_t* plan, int direction, float* buf, const float* a,
                             const float* b, void* stream) {
   std::lock_guard<std::mutex> lk(library_mutex());
+  NvtxRange nvtx_("muon_dp_pack");
   set_last_error(nullptr);
   if (!plan) return dpfail(MUON_ERR_INVALID, "plan is NULL");
   if (direction != MUON_DP_SEND && direction != MUON_DP_RECV)
@@ -421,6 +422,7 @@ extern "C" int muon_dp_pack(muon_dp_plan_t* plan, int direction, float* buf, con
 extern "C" int muon_dp_unpack(muon_dp_plan_t* plan, int direction, const float* buf, float* a,
                               float* b, void* stream) {
   std::lock_guard<std::mutex> lk(library_mutex());
+  NvtxRange nvtx_("muon_dp_unpack");
   set_last_error(nullptr);
   if (!plan) return dpfail(MUON_ERR_INVALID, "plan is NULL");
   if (direction != MUON_DP_SEND && direction != MUON_DP_RECV)
@@ -444,6 +446,7 @@ extern "C" int muon_dp_finish(muon_dp_plan_t* plan, const float* buf, float* acc
                               float* momentum, float* master, const double* stats, float lr,
                               float clip, muon_result_t* d_result, void* stream) {
   std::lock_guard<std::mutex> lk(library_mutex());
+  NvtxRange nvtx_("muon_dp_finish");
   set_last_error(nullptr);
   if (!plan) return dpfail(MUON_ERR_INVALID, "plan is NULL");
   if (!stats || !d_result) return dpfail(MUON_ERR_INVALID, "stats or d_result is NULL");

@@ -11,6 +11,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/muon.h"
 
@@ -231,6 +232,16 @@ constexpr int kX3BM = 128, kX3BN = 128;
 
 // Sets (msg != nullptr) or clears the text muon_last_error() returns.
 void set_last_error(const char* msg);
+// An NVTX range over a scope (host side): each entry point and each launch
+// group of a step is named in timeline tools (Nsight Systems, ncu's NVTX
+// filters).  Without a tool attached the calls cost a branch.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 // The lock every entry point holds for the whole call.
 std::mutex& library_mutex();
 // Adds n kernel launches to muon_get_stats' counters (the caller holds the

@@ -121,6 +121,7 @@ extern "C" int muon_newton_schulz_noalloc(const void* X, void* Y, int rows, int 
                                           int ns_method, int ns_steps, int operand_mode,
                                           void* stream) {
   std::lock_guard<std::mutex> lk(library_mutex());
+  NvtxRange nvtx_("muon_newton_schulz_noalloc");
   set_last_error(nullptr);
   if (!X || !Y || X == Y) return nofail(MUON_ERR_INVALID, "X, Y must be distinct device arrays");
   if (rows < 1 || cols < 1) return nofail(MUON_ERR_INVALID, "rows and cols must be >= 1");

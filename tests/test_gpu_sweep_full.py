@@ -111,8 +111,11 @@ CASES = [
     (4096, 16384, "standard", "bf16"),
     (4096, 16384, "gram", "bf16"),
     (4096, 16384, "gram", "fp32"),
+    (4096, 16384, "standard", "fp32"),
     (16384, 4096, "standard", "bf16"),
     (16384, 4096, "standard", "fp32"),
+    (16384, 4096, "gram", "bf16"),
+    (16384, 4096, "gram", "fp32"),
 ]
 
 
