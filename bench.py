@@ -412,7 +412,8 @@ def run_gpu(args, W, rank, world):
     torch.cuda.synchronize()
     if nsg.read_result(res)["applied"] != 1:
         raise RuntimeError("graph replay: step not applied")
-    nsg.profile_read(reset=True)
+    # the event nodes are read once, after the timed replay: they then hold
+    # that replay's times
 
     # ---- device-resident timed region: one replay = exactly K steps
     clocks = ClockSampler(dev)

@@ -441,13 +441,16 @@ MUON_API int muon_describe_tables(const muon_param_t* params, int nparams,
  *                         0 one launch per product
  *   MUON_TEST_FLOW_LAG    0 default (half the problems); k >= 1
  *   MUON_TEST_FLOW_WAVES  1 default; k >= 1 groups of problems
+ *   MUON_TEST_RASTER      0 default (large products with an MN-major B run
+ *                         their tiles in column groups); 1 row-major order
  * Errors: MUON_ERR_INVALID for an unknown knob or value. */
 typedef enum {
   MUON_TEST_GEMM = 0,
   MUON_TEST_STACK = 1,
   MUON_TEST_FLOW = 2,
   MUON_TEST_FLOW_LAG = 3,
-  MUON_TEST_FLOW_WAVES = 4
+  MUON_TEST_FLOW_WAVES = 4,
+  MUON_TEST_RASTER = 5
 } muon_test_knob_t;
 MUON_API int muon_testing_set(int knob, int value);
 

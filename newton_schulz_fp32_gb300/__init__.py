@@ -313,7 +313,7 @@ def profile_read(reset: bool = False) -> dict:
 
 # muon_testing_set knobs and their product-path defaults
 TEST_KNOBS = {"gemm": (0, 0), "stack": (1, 1), "flow": (2, 1), "flow_lag": (3, 0),
-              "flow_waves": (4, 1)}
+              "flow_waves": (4, 1), "raster": (5, 0)}
 TEST_GEMM = {"default": 0, "simt": 1, "tc1": 2}
 
 
@@ -321,7 +321,7 @@ class testing:
     """Cross-check context for tests: plans built inside it route the
     Newton-Schulz products as the knobs say (gemm="simt" CUDA-core GEMM,
     gemm="tc1" single-SM tensor-core kernel, stack=0, flow=0, flow_lag=k,
-    flow_waves=k).  Plans are dropped on entry and exit, and every knob
+    flow_waves=k, raster=1 row-major tile order).  Plans are dropped on entry and exit, and every knob
     returns to its product-path default on exit."""
 
     def __init__(self, **knobs):

@@ -89,6 +89,7 @@ struct TestKnobs {
   int flow = 1;         // 0: one pair launch per product
   int flow_lag = 0;     // pair task wavefront lag (0: half the problems)
   int flow_waves = 1;   // pair task order by groups of problems
+  int raster = 0;       // 0: column-grouped tiles for large MN-major products; 1: row-major
 };
 TestKnobs g_knobs;
 
@@ -536,6 +537,9 @@ int finish_phase(GemmPhase& ph) {
 // (wave, phase), so a wave's operands tend to stay in L2 from one product
 // to the next while the other waves fill the gaps.
 
+constexpr int kRasterCols = 4;        // column tiles per raster group (1024 columns)
+constexpr int kRasterMinTiles = 128;  // products with fewer tiles keep row-major order
+
 int build_pair_program(std::vector<std::unique_ptr<GemmPhase>>& phases, int a, int b,
                        int waves, PairProgram& G) {
   G.first_phase = a;
@@ -551,6 +555,25 @@ int build_pair_program(std::vector<std::unique_ptr<GemmPhase>>& phases, int a, i
     for (const GemmProblem& q : phases[k]->probs) G.probs.push_back(q);
     G.flops += phases[k]->flops;
   }
+  // Products with an MN-major B (X' = B X + a X, Y = Q X0) and many tiles
+  // run their tiles in groups of kRasterCols column tiles, every row of a
+  // group before the next group: the concurrent tiles then share the m x m
+  // operand (small enough to stay in L2) and one column panel of X, so X is
+  // read from DRAM about once.  In row-major order every row of tiles
+  // streams the whole of X again (for a 4096 x 14336 X, 117 MB, next to a
+  // 129 MB L2).
+  if (g_knobs.raster == 0)
+    for (int k = 0; k < b - a; ++k)
+      for (int j = 0; j < np; ++j) {
+        std::vector<GemmTile>& v = tl[k][j];
+        if (phases[a + k]->probs[j].b_kmajor != 0 || static_cast<int>(v.size()) < kRasterMinTiles)
+          continue;
+        std::stable_sort(v.begin(), v.end(), [](const GemmTile& x, const GemmTile& y) {
+          if (x.tn / kRasterCols != y.tn / kRasterCols) return x.tn / kRasterCols < y.tn / kRasterCols;
+          if (x.tm != y.tm) return x.tm < y.tm;
+          return x.tn < y.tn;
+        });
+      }
   auto counter = [&](int k, int j) { return 1 + k * np + j; };
   G.ncounters = 1 + (b - a) * np;
   waves = std::max(1, std::min(waves, np));
@@ -1688,6 +1711,10 @@ extern "C" int muon_testing_set(int knob, int value) {
     case MUON_TEST_FLOW_WAVES:
       if (value < 1) return fail(MUON_ERR_INVALID, "MUON_TEST_FLOW_WAVES takes a value >= 1");
       g_knobs.flow_waves = value;
+      return MUON_OK;
+    case MUON_TEST_RASTER:
+      if (value != 0 && value != 1) return fail(MUON_ERR_INVALID, "MUON_TEST_RASTER takes 0 or 1");
+      g_knobs.raster = value;
       return MUON_OK;
     default:
       return fail(MUON_ERR_INVALID, "unknown testing knob");

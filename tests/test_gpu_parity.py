@@ -397,7 +397,7 @@ def test_stacked_head_blocks_match_separate_blocks(torch, method, mode):
 
 
 @pytest.mark.parametrize("knobs", [{"flow": 0}, {"flow_lag": 1}, {"flow_lag": 1000},
-                                   {"flow_waves": 3, "flow_lag": 1000}])
+                                   {"flow_waves": 3, "flow_lag": 1000}, {"raster": 1}])
 def test_pair_dataflow_schedule_is_bitwise_neutral(torch, knobs):
     """The SM-pair kernel's task order and dependency counters change only
     when tiles run, never what they compute: one launch per product, the
@@ -417,6 +417,21 @@ def test_pair_dataflow_schedule_is_bitwise_neutral(torch, knobs):
             outs.append(st.numpy())
     for a, b in zip(*outs):
         assert np.array_equal(bits(a), bits(b))
+    assert nsg.device_error() == 0
+
+
+def test_pair_tile_raster_is_bitwise_neutral(torch):
+    """Column-grouped tile order (the default for products with an MN-major
+    B and 128+ tiles: here 8 x 32 tiles of X' = B X) against row-major order:
+    the same tiles, the same bits."""
+    G = wl.to_bf16_values(wl.rng_for(58).standard_normal((2048, 8192)).astype(np.float32))
+    X = to_dev(G, torch, torch.bfloat16)
+    outs = []
+    for raster in (0, 1):
+        with nsg.testing(raster=raster):
+            outs.append(nsg.newton_schulz(X, ns_method="standard", operand_mode="bf16")
+                        .float().cpu().numpy())
+    assert np.array_equal(bits(outs[0]), bits(outs[1]))
     assert nsg.device_error() == 0
 
 
