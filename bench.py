@@ -37,14 +37,21 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 
 # DRAM bytes per launch of the BF16 pair GEMM (one launch runs all NS
 # products of a step), from ncu (dram__bytes_read.sum +
-# dram__bytes_write.sum), valid only for the kernel sources they were taken
-# on (hash below).  GPT-2: the full step, averaged over two launches.
-# Llama-3-8B: the full step does not fit a capture, so one layer (the same
-# seven shapes) was captured and scaled by the 32 layers.
-GEMM_SOURCES = ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
-                "newton_schulz_fp32_gb300/csrc/tc_common.cuh"]
-GEMM_TRAFFIC = {"gpt2": {"bytes_per_launch": 3.8489e9, "sources_sha256_16": "3ef1b59e79164675"},
-                "llama": None}
+# dram__bytes_write.sum, averaged over two launches), valid only for the
+# sources they were taken on (hash below: the kernel, and for Llama-3-8B
+# also the planner whose task order sets the L2 reuse).  GPT-2: the full
+# step.  Llama-3-8B: the full step is too large to capture, so one layer
+# (the same seven shapes) was captured, 13.079 GB per launch, and scaled by
+# the 32 layers.
+GEMM_TRAFFIC = {
+    "gpt2": {"bytes_per_launch": 3.8489e9, "sources_sha256_16": "3ef1b59e79164675",
+             "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
+                       "newton_schulz_fp32_gb300/csrc/tc_common.cuh"]},
+    "llama": {"bytes_per_launch": 32 * 13.0788e9, "sources_sha256_16": "82d0a142b8cd3d37",
+              "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
+                        "newton_schulz_fp32_gb300/csrc/tc_common.cuh",
+                        "newton_schulz_fp32_gb300/csrc/api.cu"]},
+}
 
 
 def gemm_traffic(workload):
@@ -53,11 +60,11 @@ def gemm_traffic(workload):
     if rec is None:
         return None
     h = hashlib.sha256()
-    for f in GEMM_SOURCES:
+    for f in rec["files"]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     if h.hexdigest()[:16] != rec["sources_sha256_16"]:
-        return None   # the kernel changed since the counters were taken
+        return None   # the kernel or its task order changed since the counters were taken
     return rec["bytes_per_launch"]
 
 
@@ -875,6 +882,7 @@ def dp_line(args, W, m, world):
     the same parameter set over more GPUs)."""
     lay = m["layout"]
     desc = W.desc.replace("P=64", f"P={world}").replace("P=8", f"P={world}")
+    desc = desc.split("; the ")[0] + "; every micro-batch accumulated by muon_accumulate"
     return {
         "metric": METRIC, "value": m["ms"], "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": m["ms"], "higher_is_better": False,
@@ -955,9 +963,11 @@ def main():
 
     W = gpt2_workload(args.ns_method, args.mode) if args.workload == "gpt2" else llama_workload(args.mode)
     if world > 1 or args.dp:
+        import torch.distributed as dist
         m = run_dp(args, W, rank, world)
         if rank == 0:
             print(json.dumps(dp_line(args, W, m, world)))
+        dist.destroy_process_group()
         return
     m = run_gpu(args, W, rank, world)
     fields = contract_fields(args, W, m, peaks, peak_src, world)
