@@ -442,7 +442,8 @@ MUON_API int muon_describe_tables(const muon_param_t* params, int nparams,
  *   MUON_TEST_FLOW_LAG    0 default (half the problems); k >= 1
  *   MUON_TEST_FLOW_WAVES  1 default; k >= 1 groups of problems
  *   MUON_TEST_RASTER      0 default (large products with an MN-major B run
- *                         their tiles in column groups); 1 row-major order
+ *                         their tiles in groups of 4 column tiles); 1
+ *                         row-major order; k in [2, 64]: groups of k
  * Errors: MUON_ERR_INVALID for an unknown knob or value. */
 typedef enum {
   MUON_TEST_GEMM = 0,

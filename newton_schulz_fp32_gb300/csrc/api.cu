@@ -89,7 +89,7 @@ struct TestKnobs {
   int flow = 1;         // 0: one pair launch per product
   int flow_lag = 0;     // pair task wavefront lag (0: half the problems)
   int flow_waves = 1;   // pair task order by groups of problems
-  int raster = 0;       // 0: column-grouped tiles for large MN-major products; 1: row-major
+  int raster = 0;       // 0: default column groups; 1: row-major; k >= 2: groups of k column tiles
 };
 TestKnobs g_knobs;
 
@@ -562,14 +562,15 @@ int build_pair_program(std::vector<std::unique_ptr<GemmPhase>>& phases, int a, i
   // read from DRAM about once.  In row-major order every row of tiles
   // streams the whole of X again (for a 4096 x 14336 X, 117 MB, next to a
   // 129 MB L2).
-  if (g_knobs.raster == 0)
+  const int group = g_knobs.raster == 0 ? kRasterCols : g_knobs.raster;   // 1: row-major
+  if (group > 1)
     for (int k = 0; k < b - a; ++k)
       for (int j = 0; j < np; ++j) {
         std::vector<GemmTile>& v = tl[k][j];
         if (phases[a + k]->probs[j].b_kmajor != 0 || static_cast<int>(v.size()) < kRasterMinTiles)
           continue;
-        std::stable_sort(v.begin(), v.end(), [](const GemmTile& x, const GemmTile& y) {
-          if (x.tn / kRasterCols != y.tn / kRasterCols) return x.tn / kRasterCols < y.tn / kRasterCols;
+        std::stable_sort(v.begin(), v.end(), [group](const GemmTile& x, const GemmTile& y) {
+          if (x.tn / group != y.tn / group) return x.tn / group < y.tn / group;
           if (x.tm != y.tm) return x.tm < y.tm;
           return x.tn < y.tn;
         });
@@ -1713,7 +1714,7 @@ extern "C" int muon_testing_set(int knob, int value) {
       g_knobs.flow_waves = value;
       return MUON_OK;
     case MUON_TEST_RASTER:
-      if (value != 0 && value != 1) return fail(MUON_ERR_INVALID, "MUON_TEST_RASTER takes 0 or 1");
+      if (value < 0 || value > 64) return fail(MUON_ERR_INVALID, "MUON_TEST_RASTER takes 0 to 64");
       g_knobs.raster = value;
       return MUON_OK;
     default:
