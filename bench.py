@@ -5,9 +5,9 @@ Default workload (the benchmark line): the Llama-3-8B-shaped parameter set
 4096x14336; 6.98G elements, 64 partitions, 128 alignment; even-indexed
 matrices rank 8 plus 1e-3 noise, odd-indexed N(0,1)), two BF16 micro-batches
 accumulated in FP32, then one Muon step (5 standard Newton-Schulz steps,
-BF16 operands).  One timed step = muon_accumulate of the first micro-batch
-+ muon_step_ex that accumulates the second in its first pass, all kernels
-of the library, every input resident in HBM (accum, momentum and master
+BF16 operands).  One timed step = one muon_step_ex that accumulates both
+micro-batches in its first read pass (options prev_grad and last_grad), all
+kernels of the library, every input resident in HBM (accum, momentum and master
 are 27.9 GB each, far larger than the 129 MB L2, so no flush is needed);
 the K timed steps are recorded into one CUDA graph and timed as one replay.
 ``--workload gpt2`` runs the same contract line on the GPT-2-small
@@ -99,8 +99,8 @@ def gpt2_workload(ns_method, mode):
     lay = wl.gpt2_small_layout()
     desc = (f"gpt2-small muon step: 12 layers (q,k 12-head, v, o 768x768; up 3072x768; "
             f"down 768x3072), 84.9M params, P=8, align 128, gas=4 bf16 grads, "
-            f"{ns_method} NS x5, {mode} operands, clip 0.05; the 4th micro-batch is "
-            f"accumulated inside the step's first pass")
+            f"{ns_method} NS x5, {mode} operands, clip 0.05; the 3rd and 4th micro-batches "
+            f"are accumulated inside the step's first pass")
     return Workload("gpt2", lay, 4, ns_method, 0.05, desc)
 
 
@@ -109,7 +109,7 @@ def llama_workload(mode, layers=32):
     desc = (f"llama3-8b muon step: {layers} layers (q,o 4096x4096; k,v 1024x4096; gate,up "
             f"14336x4096; down 4096x14336), {lay.n_param_elements / 1e9:.2f}G params, P=64, "
             f"align 128, gas=2 bf16 grads (even-indexed matrices rank 8 + 1e-3 noise), "
-            f"standard NS x5, {mode} operands; the 2nd micro-batch is accumulated inside "
+            f"standard NS x5, {mode} operands; both micro-batches are accumulated inside "
             f"the step's first pass")
     return Workload("llama", lay, 2, "standard", 0.0, desc)
 
@@ -376,14 +376,20 @@ def run_gpu(args, W, rank, world):
         res_host = torch.zeros(4, dtype=torch.int32).pin_memory()
     torch.cuda.synchronize()
     P, Q = lay.params, lay.parts
-    # the last micro-batch is accumulated by the step itself, in its first
-    # read of accum (muon_step_ex last_grad: the same arithmetic, one read
-    # and one write of accum fewer)
-    fold = nsg.step_options(last_grad=g_dev[gas - 1], last_grad_scale=1.0 / gas,
-                            last_grad_overwrite=(gas == 1))
+    # the last two micro-batches are accumulated by the step itself, in its
+    # first read of accum (muon_step_ex prev_grad and last_grad: the same
+    # arithmetic as muon_accumulate, with accum read once and written once)
+    nfold = min(2, gas)
+    nacc = gas - nfold
+
+    def fold_options(prev, last):
+        return nsg.step_options(last_grad=last, last_grad_scale=1.0 / gas,
+                                last_grad_overwrite=(gas == 1), prev_grad=prev,
+                                prev_grad_scale=1.0 / gas, prev_grad_overwrite=(nacc == 0))
+    fold = fold_options(g_dev[gas - 2] if nfold == 2 else None, g_dev[gas - 1])
 
     def step(grad_list):
-        for mb in range(gas - 1):
+        for mb in range(nacc):
             nsg.accumulate(acc, grad_list[mb], 1.0 / gas, overwrite=(mb == 0), params=P, parts=Q,
                            stream=stream)
         nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, W.ns_method, 5, W.clip, args.mode, result=res,
@@ -450,21 +456,20 @@ def run_gpu(args, W, rank, world):
 
     # ---- end to end: host grads -> device, the step, result -> host.
     # Every step copies its micro-batches from pinned host memory on a copy
-    # stream (micro-batch i waits until the step before has accumulated its
-    # buffer) and reads its result back; the compute stream accumulates
-    # micro-batch i once it has arrived, so the next step's copies overlap
-    # this step's Newton-Schulz.  The host reads each step's result.
+    # stream and reads its result back.  A micro-batch that muon_accumulate
+    # takes is free again once accumulated, so the next step's copy into it
+    # overlaps this step's Newton-Schulz; the folded ones are read until the
+    # step's first pass ends, so each alternates between two device buffers.
+    # The host reads each step's result.
     h2d = sum(g.numel() * 2 for g in g_host)
     copy_stream = torch.cuda.Stream()
     copied = [torch.cuda.Event() for _ in range(gas)]
     consumed = [torch.cuda.Event() for _ in range(gas)]
-    # the folded last micro-batch is read until the step's first pass ends,
-    # so it alternates between two device buffers: the next step's copy of
-    # it need not wait for this step's Newton-Schulz
-    g_last = [g_dev[gas - 1], torch.empty_like(g_dev[gas - 1])]
-    folds = [fold, nsg.step_options(last_grad=g_last[1], last_grad_scale=1.0 / gas,
-                                    last_grad_overwrite=(gas == 1))]
-    consumed_last = [torch.cuda.Event() for _ in range(2)]
+    spare = [torch.empty_like(g_dev[i]) for i in range(nacc, gas)]
+    buf = [[g_dev[i], spare[i - nacc]] if i >= nacc else [g_dev[i], g_dev[i]]
+           for i in range(gas)]
+    folds = [fold] + [fold_options(buf[gas - 2][1] if nfold == 2 else None, buf[gas - 1][1])]
+    consumed_fold = [torch.cuda.Event() for _ in range(2)]
     res_ready = [torch.cuda.Event() for _ in range(2)]
     res_hosts = [res_host, torch.zeros(4, dtype=torch.int32).pin_memory()]
     e2 = torch.cuda.Event(enable_timing=True)
@@ -476,23 +481,24 @@ def run_gpu(args, W, rank, world):
     for k in range(args.steps):
         b = k & 1
         for i in range(gas):
-            last = i == gas - 1
-            if last and k > 1:
-                copy_stream.wait_event(consumed_last[b])
-            elif not last and k > 0:
+            folded = i >= nacc
+            if folded and k > 1:
+                copy_stream.wait_event(consumed_fold[b])
+            elif not folded and k > 0:
                 copy_stream.wait_event(consumed[i])
             with torch.cuda.stream(copy_stream):
-                (g_last[b] if last else g_dev[i]).copy_(g_host[i], non_blocking=True)
+                buf[i][b if folded else 0].copy_(g_host[i], non_blocking=True)
             copied[i].record(copy_stream)
-        for mb in range(gas - 1):
+        for mb in range(nacc):
             stream.wait_event(copied[mb])
             nsg.accumulate(acc, g_dev[mb], 1.0 / gas, overwrite=(mb == 0), params=P, parts=Q,
                            stream=stream)
             consumed[mb].record(stream)
-        stream.wait_event(copied[gas - 1])
+        for mb in range(nacc, gas):
+            stream.wait_event(copied[mb])
         nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, W.ns_method, 5, W.clip, args.mode, result=res,
                  stream=stream, options=folds[b])
-        consumed_last[b].record(stream)
+        consumed_fold[b].record(stream)
         with torch.cuda.stream(stream):
             res_hosts[k & 1].copy_(res, non_blocking=True)
         res_ready[k & 1].record(stream)
@@ -506,7 +512,7 @@ def run_gpu(args, W, rank, world):
     if nsg.read_result(res_hosts[(args.steps - 1) & 1])["applied"] != 1:
         raise RuntimeError("end-to-end step not applied")
     ws = nsg.get_stats()["workspace_bytes"]
-    del acc, mom, mst, g_dev, g_host, g_last
+    del acc, mom, mst, g_dev, g_host, spare, buf
     nsg.release_workspace()
     torch.cuda.empty_cache()
     return {"ms": ms, "e2e_ms": e2e_ms, "h2d": h2d, "phases": phases, "clocks": clk,
@@ -814,13 +820,13 @@ def run_llama_layers(args, peaks, peak_src):
     P, Q = lay.params, lay.parts
 
     def step():
-        nsg.accumulate(acc, grads[0], 0.5, overwrite=True, params=P, parts=Q, stream=stream)
         nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, "standard", 5, 0.0, args.mode, result=res,
                  stream=stream, options=opts)
-    # the second micro-batch is folded into the step's first pass;
+    # both micro-batches are folded into the step's first pass;
     # --workspace-budget: the NS blocks run in waves whose workspace fits it
     opts = nsg.step_options(workspace_budget=args.workspace_budget, last_grad=grads[1],
-                            last_grad_scale=0.5)
+                            last_grad_scale=0.5, prev_grad=grads[0], prev_grad_scale=0.5,
+                            prev_grad_overwrite=True)
     ms, ph = timed(torch, nsg, step, args.steps, args.warmup, stream)
     flops = ns_formula_flops(lay, "standard")
     g = ph["ns_gemm"]
@@ -996,7 +1002,7 @@ def main():
                    "l2": "inputs larger than L2 (each fp32 state buffer "
                          f"{4 * W.lay.storage_size / 1e9:.2f} GB), no flush",
                    "ns_method": W.ns_method, "operand_mode": args.mode,
-                   "launch": "timed: one replay of a CUDA graph of the K steps (accumulations + "
+                   "launch": "timed: one replay of a CUDA graph of the K steps (any accumulations + "
                              "muon_step_ex), event nodes around the NS launch only (roofline); "
                              "other phases split in an eager pass of the same K steps; e2e: "
                              "issued eagerly, with the host copies"},

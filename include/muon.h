@@ -198,6 +198,13 @@ MUON_API int muon_step(float* accum, float* momentum, float* master,
  *              by the step (bit-identical accum, momentum, master and
  *              result, a skipped step included), one read and one write of
  *              accum fewer.  last_grad must be 8-byte aligned.
+ *   prev_grad  non-NULL (with last_grad): one more micro-batch folded in
+ *              before last_grad: accum[s] = (prev_grad_overwrite ? 0 :
+ *              accum[s]) + prev_grad_scale * float(prev_grad[s]), then
+ *              last_grad as above -- the arithmetic of two muon_accumulate
+ *              calls (prev, then last) followed by the step, bit for bit,
+ *              with accum read at most once and written once.  8-byte
+ *              aligned.
  *   stats_out  non-NULL: device double[4], written at the end of the step:
  *              [0] the sum of squares the clip norm was taken over (the
  *              Muon updates and the auxiliary gradients), [1] 1 if the step
@@ -226,6 +233,9 @@ typedef struct muon_step_options {
   int32_t last_grad_overwrite;
   /* -- absent when struct_size <= MUON_STEP_OPTIONS_V2_SIZE -- */
   double* stats_out;            /* device double[4], or NULL */
+  const uint16_t* prev_grad;    /* device bf16, accum's layout, or NULL */
+  float prev_grad_scale;
+  int32_t prev_grad_overwrite;
 } muon_step_options_t;
 #define MUON_STEP_OPTIONS_V1_SIZE 64   /* struct_size of the layout without last_grad */
 #define MUON_STEP_OPTIONS_V2_SIZE 80   /* struct_size of the layout without stats_out */

@@ -63,7 +63,9 @@ class StepOptions(ctypes.Structure):
                 ("adam_step", ctypes.c_int64), ("exp_avg", ctypes.c_void_p),
                 ("exp_avg_sq", ctypes.c_void_p), ("workspace_budget", ctypes.c_uint64),
                 ("last_grad", ctypes.c_void_p), ("last_grad_scale", ctypes.c_float),
-                ("last_grad_overwrite", ctypes.c_int32), ("stats_out", ctypes.c_void_p)]
+                ("last_grad_overwrite", ctypes.c_int32), ("stats_out", ctypes.c_void_p),
+                ("prev_grad", ctypes.c_void_p), ("prev_grad_scale", ctypes.c_float),
+                ("prev_grad_overwrite", ctypes.c_int32)]
 
 
 STEP_OPTIONS_V1_SIZE = 64   # struct_size of the layout that ends at workspace_budget
@@ -171,14 +173,17 @@ def accumulate(accum, grad, scale: float, overwrite: bool = False, params=None, 
 
 def step_options(clip_mode="update", grad_scale: float = 1.0, adam: dict | None = None,
                  workspace_budget: int = 0, last_grad=None, last_grad_scale: float = 1.0,
-                 last_grad_overwrite: bool = False, stats_out=None) -> StepOptions:
+                 last_grad_overwrite: bool = False, stats_out=None, prev_grad=None,
+                 prev_grad_scale: float = 1.0, prev_grad_overwrite: bool = False) -> StepOptions:
     """A muon_step_options_t.  adam: dict(lr, beta1, beta2, eps, step,
     exp_avg, exp_avg_sq) with device float buffers in accum's layout.
     last_grad: the last micro-batch's bf16 gradients (accum's layout), which
     the step accumulates itself, as accumulate(accum, last_grad,
     last_grad_scale, last_grad_overwrite) would.  stats_out: a device
     float64[4] the step fills with (sum of squares of the clip norm, skipped,
-    NS problems, 0)."""
+    NS problems, 0).  prev_grad: one more micro-batch folded in before
+    last_grad (as accumulate(accum, prev_grad, prev_grad_scale,
+    prev_grad_overwrite) would)."""
     o = StepOptions()
     o.struct_size = ctypes.sizeof(StepOptions)
     o.clip_mode = CLIP_MODES[clip_mode] if isinstance(clip_mode, str) else int(clip_mode)
@@ -186,6 +191,10 @@ def step_options(clip_mode="update", grad_scale: float = 1.0, adam: dict | None 
     o.workspace_budget = int(workspace_budget)
     if stats_out is not None:
         o.stats_out = _ptr(stats_out)
+    if prev_grad is not None:
+        o.prev_grad = _ptr(prev_grad)
+        o.prev_grad_scale = prev_grad_scale
+        o.prev_grad_overwrite = int(prev_grad_overwrite)
     if last_grad is not None:
         o.last_grad = _ptr(last_grad)
         o.last_grad_scale = last_grad_scale
@@ -226,12 +235,14 @@ def step_ex(accum, momentum, master, params, parts, beta: float, lr: float, ns_m
             ns_steps: int = 5, clip: float = 0.0, operand_mode="bf16", clip_mode="update",
             grad_scale: float = 1.0, adam: dict | None = None, workspace_budget: int = 0,
             last_grad=None, last_grad_scale: float = 1.0, last_grad_overwrite: bool = False,
-            result=None, stream=None):
+            prev_grad=None, prev_grad_scale: float = 1.0, prev_grad_overwrite: bool = False,
+            stats_out=None, result=None, stream=None):
     """muon_step_ex with its options as keyword arguments."""
     return step(accum, momentum, master, params, parts, beta, lr, ns_method, ns_steps, clip,
                 operand_mode, result, stream,
                 step_options(clip_mode, grad_scale, adam, workspace_budget, last_grad,
-                             last_grad_scale, last_grad_overwrite))
+                             last_grad_scale, last_grad_overwrite, stats_out, prev_grad,
+                             prev_grad_scale, prev_grad_overwrite))
 
 
 def describe_tables(params, parts, ns_method="gram", operand_mode="bf16") -> dict:

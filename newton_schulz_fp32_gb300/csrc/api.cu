@@ -1337,6 +1337,9 @@ int apply_options(const muon_step_options_t* opts, StreamLaunchArgs& a) {
   a.last_scale = 1.f;
   a.last_overwrite = 0;
   a.stats_out = nullptr;
+  a.prev_grad = nullptr;
+  a.prev_scale = 1.f;
+  a.prev_overwrite = 0;
   if (!opts) return MUON_OK;
   const bool v3 = opts->struct_size == static_cast<int32_t>(sizeof(muon_step_options_t));
   const bool v2 = v3 || opts->struct_size == MUON_STEP_OPTIONS_V2_SIZE;
@@ -1359,6 +1362,18 @@ int apply_options(const muon_step_options_t* opts, StreamLaunchArgs& a) {
     a.last_grad = opts->last_grad;
     a.last_scale = opts->last_grad_scale;
     a.last_overwrite = opts->last_grad_overwrite;
+  }
+  if (v3 && opts->prev_grad) {
+    if (!a.last_grad) return fail(MUON_ERR_INVALID, "prev_grad needs last_grad");
+    if (reinterpret_cast<uintptr_t>(opts->prev_grad) % 8)
+      return fail(MUON_ERR_INVALID, "prev_grad must be 8-byte aligned");
+    if (!std::isfinite(opts->prev_grad_scale))
+      return fail(MUON_ERR_INVALID, "prev_grad_scale must be finite");
+    if (opts->prev_grad_overwrite != 0 && opts->prev_grad_overwrite != 1)
+      return fail(MUON_ERR_INVALID, "prev_grad_overwrite must be 0 or 1");
+    a.prev_grad = opts->prev_grad;
+    a.prev_scale = opts->prev_grad_scale;
+    a.prev_overwrite = opts->prev_grad_overwrite;
   }
   if (opts->clip_mode != MUON_CLIP_UPDATE && opts->clip_mode != MUON_CLIP_GRAD)
     return fail(MUON_ERR_INVALID, "unknown clip_mode");
@@ -1454,13 +1469,19 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
   const double me = double(L.muon_elems), ae = double(L.aux_elems);
   MUON_CUDA_TRY(cudaMemsetAsync(a.state, 0, sizeof(StepState), s));
   // a folded last micro-batch adds a bf16 read and an accum write; when it
-  // overwrites, accum's old value is not read
-  const double lg = a.last_grad ? (me + ae) * (a.last_overwrite ? 2 : 6) : 0.0;
+  // overwrites, accum's old value is not read.  A folded previous one adds
+  // its bf16 read (and takes over the read of accum, or drops it when it
+  // overwrites)
+  const bool lg_reads_accum = a.last_grad && !a.last_overwrite &&
+                              !(a.prev_grad && a.prev_overwrite);
+  const double lg = a.last_grad ? (me + ae) * ((lg_reads_accum ? 0 : -4) + 6 +
+                                               (a.prev_grad && !a.last_overwrite ? 2 : 0)) : 0.0;
   if (!pre) {
     PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 1 : 0) + 1, me * 8 + ae * 4 + lg, 0.0);
     a.reduce_mode = 0;
     launch_reduce(a, s);
     a.last_grad = nullptr;   // accum now holds the full gradient
+    a.prev_grad = nullptr;
     launch_owner_norm(a, s);
   } else {
     // gradient norm over every parameter, clip coefficient, then the
@@ -1469,6 +1490,7 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
     a.reduce_mode = 1;
     launch_reduce(a, s);
     a.last_grad = nullptr;
+    a.prev_grad = nullptr;
     launch_finalize_pre(a, s);
     a.reduce_mode = 2;
     launch_reduce(a, s);

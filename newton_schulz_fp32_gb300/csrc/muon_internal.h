@@ -193,6 +193,10 @@ struct StreamLaunchArgs {
   const uint16_t* last_grad;
   float last_scale;
   int last_overwrite;
+  // non-null (with last_grad): a micro-batch accumulated before last_grad
+  const uint16_t* prev_grad;
+  float prev_scale;
+  int prev_overwrite;
   // non-null: k_finalize writes {sum of squares, skipped, NS problems, 0}
   double* stats_out;
 };

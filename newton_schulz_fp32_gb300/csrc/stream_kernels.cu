@@ -225,14 +225,19 @@ k_reduce(StreamLaunchArgs a) {
   float acc = 0.f;
   bool bad = false;
   // a folded last micro-batch: accum = (overwrite ? 0 : accum) + scale * g,
-  // written back before the element is used (muon_accumulate's arithmetic)
+  // written back before the element is used (muon_accumulate's arithmetic);
+  // a folded previous micro-batch is added the same way before it
   const uint16_t* LG = a.last_grad;
   const float ls = a.last_scale;
   const int lo = a.last_overwrite;
+  const uint16_t* LP = lo ? nullptr : a.prev_grad;   // an overwriting last one replaces it
+  const float ps = a.prev_scale;
+  const int po = a.prev_overwrite;
   if (t.fast) {
     float* G = a.accum + t.sdelta + tb;
     const float* M = a.momentum + t.sdelta + tb;
     const uint16_t* GL = LG ? LG + t.sdelta + tb : nullptr;
+    const uint16_t* GP = LP ? LP + t.sdelta + tb : nullptr;
     constexpr int U = 4;
     for (int g0 = threadIdx.x; g0 < ngroups; g0 += NT * U) {
       float4 gv[U], mv[U];
@@ -242,7 +247,15 @@ k_reduce(StreamLaunchArgs a) {
         if (g < ngroups) {
           if (GL) {
             const uint2 b = *reinterpret_cast<const uint2*>(GL + 4 * g);
-            const float4 old = lo ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(G + 4 * g);
+            float4 old = (lo || (GP && po)) ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                            : *reinterpret_cast<const float4*>(G + 4 * g);
+            if (GP) {
+              const uint2 p = *reinterpret_cast<const uint2*>(GP + 4 * g);
+              old.x = acc_one(old.x, __uint_as_float(p.x << 16), ps, po);
+              old.y = acc_one(old.y, __uint_as_float(p.x & 0xffff0000u), ps, po);
+              old.z = acc_one(old.z, __uint_as_float(p.y << 16), ps, po);
+              old.w = acc_one(old.w, __uint_as_float(p.y & 0xffff0000u), ps, po);
+            }
             gv[u].x = acc_one(old.x, __uint_as_float(b.x << 16), ls, lo);
             gv[u].y = acc_one(old.y, __uint_as_float(b.x & 0xffff0000u), ls, lo);
             gv[u].z = acc_one(old.z, __uint_as_float(b.y << 16), ls, lo);
@@ -276,6 +289,7 @@ k_reduce(StreamLaunchArgs a) {
         const int64_t st = segs[si].storage_begin + (rel - segs[si].rel_begin);
         float gr = a.accum[st];
         if (LG) {
+          if (LP) gr = acc_one(gr, bf16_bits_to_float(LP[st]), ps, po);
           gr = acc_one(gr, bf16_bits_to_float(LG[st]), ls, lo);
           a.accum[st] = gr;
         }

@@ -1,6 +1,6 @@
-"""The step's folded last micro-batch (muon_step_ex's last_grad): the step
-accumulates the last bf16 micro-batch itself, in its first read of accum,
-with muon_accumulate's arithmetic.  accum, momentum, master and the device
+"""The step's folded micro-batches (muon_step_ex's last_grad, and prev_grad
+before it): the step accumulates the last one or two bf16 micro-batches
+itself, in its first read of accum, with muon_accumulate's arithmetic.  accum, momentum, master and the device
 result must therefore equal, bit for bit, muon_accumulate on that
 micro-batch followed by the step; that sequence is itself checked against
 the oracle by the parity tests.  Padding holds NaN sentinels and must come
@@ -37,8 +37,10 @@ def mixed_layout(nparts, storage):
 
 
 def run(torch, lay, grads, gas, fold, method, mode, nan_last=False, **opts):
-    """accumulate the micro-batches (all, or all but the last when fold),
-    then one step; returns the three storage buffers and the result."""
+    """accumulate the micro-batches (all, or all but the last `fold` of
+    them, which the step folds in: 1 = last_grad, 2 = prev_grad and
+    last_grad), then one step; returns the three storage buffers and the
+    result."""
     m = [np.float32(0.01) * x for x in wl.gaussian_grads(lay, 11, 1, None, bf16=False)]
     w = wl.gaussian_grads(lay, 11, 2, None, bf16=False)
     z = [np.zeros((s.rows, s.cols), np.float32) for s in lay.specs]
@@ -49,11 +51,14 @@ def run(torch, lay, grads, gas, fold, method, mode, nan_last=False, **opts):
         g[-1][0] = g[-1][0].copy()
         g[-1][0].flat[3] = np.nan
     gb = [bf16_tensor(wl.bf16_storage_grad(lay, x), torch) for x in g]
-    for mb in range(gas - (1 if fold else 0)):
+    fold = min(int(fold), gas)
+    for mb in range(gas - fold):
         nsg.accumulate(st.accum, gb[mb], 1.0 / gas, overwrite=(mb == 0), params=lay.params,
                        parts=lay.parts)
     if fold:
         opts.update(last_grad=gb[-1], last_grad_scale=1.0 / gas, last_grad_overwrite=(gas == 1))
+    if fold == 2:
+        opts.update(prev_grad=gb[-2], prev_grad_scale=1.0 / gas, prev_grad_overwrite=(gas == 2))
     res = nsg.step_ex(st.accum, st.momentum, st.master, lay.params, lay.parts, BETA, LR, method, 5,
                       CLIP, mode, **opts)
     return st.numpy(), nsg.read_result(res)
@@ -69,12 +74,14 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("fold", [1, 2])
 @pytest.mark.parametrize("nparts,storage,gas,method,mode,opts", CASES)
-def test_folded_last_micro_batch_is_bit_identical(torch, nparts, storage, gas, method, mode, opts):
+def test_folded_last_micro_batch_is_bit_identical(torch, nparts, storage, gas, method, mode, opts,
+                                                  fold):
     lay = mixed_layout(nparts, storage)
     grads = micro_batch_grads(lay, 5, 0, gas, wl.loguniform_sigmas(lay, 5, 1e-3, 1e-1))
-    (a0, m0, w0), r0 = run(torch, lay, grads, gas, False, method, mode, **opts)
-    (a1, m1, w1), r1 = run(torch, lay, grads, gas, True, method, mode, **opts)
+    (a0, m0, w0), r0 = run(torch, lay, grads, gas, 0, method, mode, **opts)
+    (a1, m1, w1), r1 = run(torch, lay, grads, gas, fold, method, mode, **opts)
     assert r0["applied"] == 1 and r1 == r0
     for x, y in ((a0, a1), (m0, m1), (w0, w1)):
         np.testing.assert_array_equal(bits(x), bits(y))
@@ -82,25 +89,27 @@ def test_folded_last_micro_batch_is_bit_identical(torch, nparts, storage, gas, m
     assert (bits(a1)[pad] == wl.NAN_SENTINEL_BITS).all()
 
 
-def test_folded_non_finite_micro_batch_skips_identically(torch):
+@pytest.mark.parametrize("fold", [1, 2])
+def test_folded_non_finite_micro_batch_skips_identically(torch, fold):
     lay = mixed_layout(3, "shuffled")
     grads = micro_batch_grads(lay, 6, 0, 3)
-    (a0, m0, w0), r0 = run(torch, lay, grads, 3, False, "standard", "bf16", nan_last=True)
-    (a1, m1, w1), r1 = run(torch, lay, grads, 3, True, "standard", "bf16", nan_last=True)
+    (a0, m0, w0), r0 = run(torch, lay, grads, 3, 0, "standard", "bf16", nan_last=True)
+    (a1, m1, w1), r1 = run(torch, lay, grads, 3, fold, "standard", "bf16", nan_last=True)
     assert r0["applied"] == 0 and r1 == r0
     for x, y in ((a0, a1), (m0, m1), (w0, w1)):
         np.testing.assert_array_equal(bits(x), bits(y))
 
 
-def test_folded_large_layout_matches(torch):
+@pytest.mark.parametrize("fold", [1, 2])
+def test_folded_large_layout_matches(torch, fold):
     """GPT-2-small-shaped blocks (one layer, P = 8): the fast 16-byte path
     of the first pass over large tiles."""
     lay = wl.build_layout([[wl.ParamSpec("q", 768, 768, 12), wl.ParamSpec("k", 768, 768, 12),
                             wl.ParamSpec("v", 768, 768), wl.ParamSpec("up", 3072, 768),
                             wl.ParamSpec("down", 768, 3072)]], 128, 8)
     grads = micro_batch_grads(lay, 8, 0, 4, wl.loguniform_sigmas(lay, 8, 1e-4, 1e-1))
-    (a0, m0, w0), r0 = run(torch, lay, grads, 4, False, "standard", "bf16")
-    (a1, m1, w1), r1 = run(torch, lay, grads, 4, True, "standard", "bf16")
+    (a0, m0, w0), r0 = run(torch, lay, grads, 4, 0, "standard", "bf16")
+    (a1, m1, w1), r1 = run(torch, lay, grads, 4, fold, "standard", "bf16")
     assert r0["applied"] == 1 and r1 == r0
     for x, y in ((a0, a1), (m0, m1), (w0, w1)):
         np.testing.assert_array_equal(bits(x), bits(y))

@@ -234,12 +234,15 @@ def test_tensor_core_path_matches_cuda_core_path(torch, method, mode):
         assert_close_update(o, want, mode, f"{method} {mode} vs oracle")
 
 
-def test_gpt2_small_config(torch):
+@pytest.mark.parametrize("method,mode", [("standard", "bf16"), ("gram", "bf16"),
+                                         ("standard", "fp32"), ("gram", "fp32")])
+def test_gpt2_small_config(torch, method, mode):
     """GPT-2-small shapes: 12 layers of Q, K (12 heads), V, O 768x768,
     up 3072x768, down 768x3072; P=8, 128 alignment; gas=4, bf16 grads with
-    per-matrix sigma log-uniform in [1e-4, 1e-1]; one standard-method step.
-    Accumulation and momentum bit-exact everywhere; sampled matrices against
-    the oracle; every block's update in the quintic's band."""
+    per-matrix sigma log-uniform in [1e-4, 1e-1]; one step in each method
+    and operand mode.  Accumulation and momentum bit-exact everywhere; every
+    one of the 72 matrices against the oracle by the mode's rule; every
+    block's update in the quintic's band."""
     lay = wl.gpt2_small_layout()
     seed = wl.CONFIG_SEED["gpt2"]
     sig = wl.loguniform_sigmas(lay, seed, 1e-4, 1e-1)
@@ -252,7 +255,7 @@ def test_gpt2_small_config(torch):
     before = st.numpy()
     assert np.array_equal(bits(before[0]), bits(oracle_accumulate(wl.pack(lay, z), lay, grads, 4)))
     gres = nsg.read_result(nsg.step(st.accum, st.momentum, st.master, lay.params, lay.parts,
-                                    BETA, LR, "standard", 5, CLIP, "bf16"))
+                                    BETA, LR, method, 5, CLIP, mode))
     assert gres["applied"] == 1 and gres["ns_calls"] == 12 * 28
     ga, gm, gw = st.numpy()
     g_un, m_un, u_un = wl.unpack(lay, before[0]), wl.unpack(lay, before[1]), wl.unpack(lay, ga)
@@ -269,10 +272,10 @@ def test_gpt2_small_config(torch):
             mm = min(blk.shape)
             sq = float(np.sum(blk * blk))
             assert mm * BAND_LO ** 2 * 0.98 <= sq <= mm * BAND_HI ** 2 * 1.02, (spec.name, b, sq / mm)
-    for k in [0, 1, 2, 3, 4, 5, 64, 65]:        # layer 0 all, layer 10 up/down
-        spec = lay.specs[k]
-        _, u_or = om.muon_update(g_un[k], m_un[k], BETA, "standard", 5, spec.num_heads, "bf16")
-        assert_close_update(u_un[k] / gres["clip_coef"], u_or, "bf16", spec.name)
+    for k, spec in enumerate(lay.specs):         # all 72 matrices
+        _, u_or = om.muon_update(g_un[k], m_un[k], BETA, method, 5, spec.num_heads,
+                                 ORACLE_MODE[mode])
+        assert_close_update(u_un[k] / gres["clip_coef"], u_or, mode, f"{spec.name} {method} {mode}")
 
 
 @pytest.mark.parametrize("nparts", [1, 8])

@@ -110,12 +110,15 @@ def _step_ex(lib, opts, ptrs=(FAKE, FAKE, FAKE)):
 def test_step_options_struct_layout():
     # muon.h: the original layout ends at workspace_budget (64 bytes); the
     # folded last micro-batch follows it (80), then the statistics pointer
-    assert ctypes.sizeof(nsg.StepOptions) == 88
+    assert ctypes.sizeof(nsg.StepOptions) == 104
     assert nsg.StepOptions.adam_step.offset == 32 and nsg.StepOptions.workspace_budget.offset == 56
     assert nsg.StepOptions.last_grad.offset == nsg.STEP_OPTIONS_V1_SIZE == 64
     assert nsg.StepOptions.last_grad_scale.offset == 72
     assert nsg.StepOptions.last_grad_overwrite.offset == 76
     assert nsg.StepOptions.stats_out.offset == nsg.STEP_OPTIONS_V2_SIZE == 80
+    assert nsg.StepOptions.prev_grad.offset == 88
+    assert nsg.StepOptions.prev_grad_scale.offset == 96
+    assert nsg.StepOptions.prev_grad_overwrite.offset == 100
 
 
 def test_step_options_rejected_on_host(lib):
@@ -138,6 +141,12 @@ def test_step_options_rejected_on_host(lib):
     o = nsg.step_options(); o.struct_size = 72
     cases.append((o, "struct_size"))
     cases.append((nsg.step_options(stats_out=FAKE + 4), "stats_out"))
+    cases.append((nsg.step_options(prev_grad=FAKE), "needs last_grad"))
+    cases.append((nsg.step_options(last_grad=FAKE, prev_grad=FAKE + 2), "8-byte"))
+    cases.append((nsg.step_options(last_grad=FAKE, prev_grad=FAKE, prev_grad_scale=float("inf")),
+                  "prev_grad_scale"))
+    o = nsg.step_options(last_grad=FAKE, prev_grad=FAKE); o.prev_grad_overwrite = 3
+    cases.append((o, "prev_grad_overwrite"))
     for opts, word in cases:
         rc = _step_ex(lib, opts)
         assert rc == nsg.MUON_ERR_INVALID, (word, rc)
