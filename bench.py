@@ -478,17 +478,23 @@ def run_gpu(args, W, rank, world):
     t_wall = time.perf_counter()
     e2.record(stream)
     copy_stream.wait_event(e2)
+    copy_marks, step_marks = [], []
     for k in range(args.steps):
         b = k & 1
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for i in range(gas):
             folded = i >= nacc
             if folded and k > 1:
                 copy_stream.wait_event(consumed_fold[b])
             elif not folded and k > 0:
                 copy_stream.wait_event(consumed[i])
+            if i == 0:
+                c0.record(copy_stream)
             with torch.cuda.stream(copy_stream):
                 buf[i][b if folded else 0].copy_(g_host[i], non_blocking=True)
             copied[i].record(copy_stream)
+        c1.record(copy_stream)
+        copy_marks.append((c0, c1))
         for mb in range(nacc):
             stream.wait_event(copied[mb])
             nsg.accumulate(acc, g_dev[mb], 1.0 / gas, overwrite=(mb == 0), params=P, parts=Q,
@@ -496,8 +502,12 @@ def run_gpu(args, W, rank, world):
             consumed[mb].record(stream)
         for mb in range(nacc, gas):
             stream.wait_event(copied[mb])
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
         nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, W.ns_method, 5, W.clip, args.mode, result=res,
                  stream=stream, options=folds[b])
+        s1.record(stream)
+        step_marks.append((s0, s1))
         consumed_fold[b].record(stream)
         with torch.cuda.stream(stream):
             res_hosts[k & 1].copy_(res, non_blocking=True)
@@ -511,12 +521,19 @@ def run_gpu(args, W, rank, world):
     e2e_ms = max(e2.elapsed_time(e3) / args.steps, wall_ms)
     if nsg.read_result(res_hosts[(args.steps - 1) & 1])["applied"] != 1:
         raise RuntimeError("end-to-end step not applied")
+    # the copies' own time per step (first copy start to last copy end; a
+    # copy that waits for its buffer is included from where it was issued)
+    copy_list = [a.elapsed_time(b) for a, b in copy_marks]
+    copy_ms = sum(copy_list) / args.steps
+    step_ms_e2e = sum(a.elapsed_time(b) for a, b in step_marks) / args.steps
     ws = nsg.get_stats()["workspace_bytes"]
     del acc, mom, mst, g_dev, g_host, spare, buf
     nsg.release_workspace()
     torch.cuda.empty_cache()
     return {"ms": ms, "e2e_ms": e2e_ms, "h2d": h2d, "phases": phases, "clocks": clk,
-            "launches": launches, "workspace_bytes": ws}
+            "launches": launches, "workspace_bytes": ws, "copy_ms": copy_ms,
+            "copy_list": [round(x, 1) for x in copy_list],
+            "step_ms_e2e": step_ms_e2e}
 
 
 def run_dp(args, W, rank, world):
@@ -626,6 +643,35 @@ def run_dp(args, W, rank, world):
             "layout": lay, "owned_params": int(plan.sizes["owned_params"]),
             "balance": plan.sizes["owned_cost"] / max(plan.sizes["max_cost"], 1e-30),
             "exchange_elems_per_step": 2 * (plan.send_elems + plan.recv_elems)}
+
+
+def host_numa():
+    """The NUMA node of the GPU, the nodes of the CPUs this process may run
+    on (pinned host buffers are placed near the allocating thread)."""
+    out = {}
+    try:
+        bus = subprocess.run(["nvidia-smi", "-i", os.environ.get("LOCAL_RANK", "0"),
+                              "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=10).stdout.strip().lower()
+        for cand in (bus, bus[4:]):
+            path = f"/sys/bus/pci/devices/{cand}/numa_node"
+            if cand and os.path.exists(path):
+                out["gpu_node"] = int(open(path).read().strip())
+                break
+        cpus = os.sched_getaffinity(0)
+        nodes = set()
+        base = "/sys/devices/system/node"
+        for nd in os.listdir(base):
+            if nd.startswith("node") and nd[4:].isdigit():
+                for part in open(f"{base}/{nd}/cpulist").read().strip().split(","):
+                    if part:
+                        a, _, b = part.partition("-")
+                        if cpus & set(range(int(a), int(b or a) + 1)):
+                            nodes.add(int(nd[4:]))
+        out["cpu_nodes"] = sorted(nodes)
+    except (OSError, ValueError, subprocess.SubprocessError):
+        pass
+    return out
 
 
 def contract_fields(args, W, m, peaks, peak_src, world):
@@ -1010,7 +1056,10 @@ def main():
         "workspace_bytes": m["workspace_bytes"],
         "cpu_baseline": cpu,
         "e2e": {"value": m["e2e_ms"], "unit": "ms", "h2d_bytes_per_step": m["h2d"],
-                "d2h_bytes_per_step": 16},
+                "d2h_bytes_per_step": 16, "copy_stream_ms_per_step": m["copy_ms"],
+                "step_call_ms_in_e2e": m["step_ms_e2e"],
+                "copy_stream_ms_each_step": m["copy_list"],
+                "host_numa": host_numa()},
         "gpu_launches": m["launches"],
         "clocks": m["clocks"],
     }
