@@ -454,6 +454,10 @@ MUON_API int muon_describe_tables(const muon_param_t* params, int nparams,
  *   MUON_TEST_RASTER      0 default (large products with an MN-major B run
  *                         their tiles in groups of 4 column tiles); 1
  *                         row-major order; k in [2, 64]: groups of k
+ *   MUON_TEST_EXTENT_SHRINK  0 default; k > 0: a library built with
+ *                         MUON_DEBUG checks its streaming kernels' tiles
+ *                         against a storage extent k elements smaller than
+ *                         the partitions describe (to see the check report)
  * Errors: MUON_ERR_INVALID for an unknown knob or value. */
 typedef enum {
   MUON_TEST_GEMM = 0,
@@ -461,7 +465,8 @@ typedef enum {
   MUON_TEST_FLOW = 2,
   MUON_TEST_FLOW_LAG = 3,
   MUON_TEST_FLOW_WAVES = 4,
-  MUON_TEST_RASTER = 5
+  MUON_TEST_RASTER = 5,
+  MUON_TEST_EXTENT_SHRINK = 6
 } muon_test_knob_t;
 MUON_API int muon_testing_set(int knob, int value);
 
@@ -474,7 +479,10 @@ MUON_API void muon_release_workspace(void);
 /* Synchronises the device and returns the first error code a kernel
  * recorded since the last query (0 = none), clearing it.  The tensor-core
  * kernels bound every wait; a wait that runs out records a positive code
- * here instead of hanging (1 = TMA producer, 2 = MMA issuer, 3 = epilogue).
+ * here instead of hanging (1 = TMA producer, 2 = MMA issuer, 3 = epilogue,
+ * 4 = a dependency of the SM-pair kernel).  A library built with MUON_DEBUG
+ * also checks every streaming-kernel tile against the extents its tables
+ * describe and records 16 for a tile that would leave them (and skips it).
  * A step whose products hit such an error also reports applied = -1. */
 MUON_API int muon_device_error(void);
 

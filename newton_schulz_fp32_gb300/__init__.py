@@ -19,6 +19,7 @@ import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmuon.so")
+DEBUG_LIB_PATH = os.path.join(HERE, "libmuon_debug.so")
 
 PARAM_DTYPE = np.dtype([("offset", "<i8"), ("rows", "<i4"), ("cols", "<i4"),
                         ("num_heads", "<i4"), ("use_muon", "<i4")])
@@ -89,9 +90,18 @@ class PhaseTime(ctypes.Structure):
 _lib = None
 
 
-def build(force: bool = False, verbose: bool = False):
+def build(force: bool = False, verbose: bool = False, debug: bool = False):
     from . import builder as _b
-    return _b.build(force=force, verbose=verbose)
+    return _b.build(force=force, verbose=verbose, debug=debug)
+
+
+def use_library(path: str):
+    """Load `path` (e.g. DEBUG_LIB_PATH, the bounds-checking build) instead
+    of libmuon.so; only before the library's first use in this process."""
+    global LIB_PATH
+    if _lib is not None:
+        raise MuonError(MUON_ERR_INVALID, "the library is already loaded in this process")
+    LIB_PATH = path
 
 
 def lib():
@@ -324,7 +334,7 @@ def profile_read(reset: bool = False) -> dict:
 
 # muon_testing_set knobs and their product-path defaults
 TEST_KNOBS = {"gemm": (0, 0), "stack": (1, 1), "flow": (2, 1), "flow_lag": (3, 0),
-              "flow_waves": (4, 1), "raster": (5, 0)}
+              "flow_waves": (4, 1), "raster": (5, 0), "extent_shrink": (6, 0)}
 TEST_GEMM = {"default": 0, "simt": 1, "tc1": 2}
 
 

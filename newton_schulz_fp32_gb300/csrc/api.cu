@@ -90,6 +90,7 @@ struct TestKnobs {
   int flow_lag = 0;     // pair task wavefront lag (0: half the problems)
   int flow_waves = 1;   // pair task order by groups of problems
   int raster = 0;       // 0: default column groups; 1: row-major; k >= 2: groups of k column tiles
+  int extent_shrink = 0; // debug builds: the storage extent the checks use, made this much smaller
 };
 TestKnobs g_knobs;
 
@@ -169,6 +170,7 @@ struct Layout {
   int n_muon_owners = 0;
   int64_t muon_elems = 0, aux_elems = 0;
   int64_t x_elems = 0, sq_elems = 0;   // per workspace region
+  int64_t storage_extent = 0;          // storage elements the partitions describe
 };
 
 int validate_and_build(const muon_param_t* params, int nparams, const muon_partition_t* parts,
@@ -197,6 +199,9 @@ int validate_and_build(const muon_param_t* params, int nparams, const muon_parti
       if (st[i - 1].second > st[i].first)
         return fail(MUON_ERR_INVALID, "partitions overlap in storage");
   }
+  for (int i = 0; i < nparts; ++i)
+    L.storage_extent = std::max(L.storage_extent,
+                                parts[i].storage_offset + parts[i].flat_end - parts[i].flat_begin);
   std::vector<std::pair<int64_t, int64_t>> pr;
   for (int i = 0; i < nparams; ++i) {
     const muon_param_t& p = params[i];
@@ -452,6 +457,7 @@ struct WaveRange {
 struct NsPlan {
   int esize = 2;       // X0 / Y element format: 2 bf16, 4 fp32, 6 split-3
   int64_t x_ps = 0;    // split-3: elements between the planes of an X region
+  int64_t x_elems = 0; // elements of one X region
   bool use_tc = false;
   int method = 0, steps = 5;
   DevBuf ws;
@@ -814,6 +820,7 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
   for (int i = 0; i < nsq; ++i) S[i] = sq_base + i * bytes_of(se) * size_t(sq_elems);
   char* Qbf = sq_base + nsq * bytes_of(se) * size_t(sq_elems);
   P.x0 = X[0];
+  P.x_elems = x_elems;
   const float a = kNsA, b = kNsB, c = kNsC;
 
   auto xm = [&](char* r, const Owner& o) {
@@ -1145,6 +1152,7 @@ int build_wave_plan(const Layout& L, int method, int mode, int steps, uint64_t b
   }
   P.esize = F.xe;
   P.x_ps = F.xe == 6 ? mx : 0;
+  P.x_elems = mx;
   P.use_tc = F.tc;
   P.method = method;
   P.steps = steps;
@@ -1307,7 +1315,8 @@ extern "C" int muon_accumulate(float* accum, const uint16_t* grad, int64_t n, fl
     }
     const int nruns = static_cast<int>((n + 32767) / 32768);
     PhaseScope sc(MUON_PHASE_ACCUMULATE, s, 1, double(n) * (overwrite ? 6 : 10), 0.0);
-    launch_accumulate(accum, grad, it->second->as<Run>(), nruns, scale, overwrite, s);
+    launch_accumulate(accum, grad, it->second->as<Run>(), nruns, scale, overwrite,
+                      n - g_knobs.extent_shrink, nullptr, s);
   } else {
     TablePlan* tp = nullptr;
     int rc = get_table_plan(params, nparams, parts, nparts, &tp);
@@ -1315,7 +1324,7 @@ extern "C" int muon_accumulate(float* accum, const uint16_t* grad, int64_t n, fl
     const double el = double(tp->L.muon_elems + tp->L.aux_elems);
     PhaseScope sc(MUON_PHASE_ACCUMULATE, s, tp->L.runs.empty() ? 0 : 1, el * (overwrite ? 6 : 10), 0.0);
     launch_accumulate(accum, grad, tp->d_runs.as<Run>(), static_cast<int>(tp->L.runs.size()), scale,
-                      overwrite, s);
+                      overwrite, tp->L.storage_extent - g_knobs.extent_shrink, tp->d_err.as<int>(), s);
   }
   MUON_CUDA_TRY(cudaGetLastError());
   return MUON_OK;
@@ -1462,6 +1471,9 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
   a.clip = clip;
   a.state = tp->d_state.as<StepState>();
   a.err_flag = tp->d_err.as<int>();
+  a.dbg_flag = tp->d_err.as<int>();
+  a.dbg_storage_extent = L.storage_extent - g_knobs.extent_shrink;
+  a.dbg_x_extent = P->x_elems;
   a.result = d_result;
   a.ns_calls = L.n_muon_owners;
   const bool pre = a.clip_mode == MUON_CLIP_GRAD;
@@ -1734,6 +1746,10 @@ extern "C" int muon_testing_set(int knob, int value) {
     case MUON_TEST_FLOW_WAVES:
       if (value < 1) return fail(MUON_ERR_INVALID, "MUON_TEST_FLOW_WAVES takes a value >= 1");
       g_knobs.flow_waves = value;
+      return MUON_OK;
+    case MUON_TEST_EXTENT_SHRINK:
+      if (value < 0) return fail(MUON_ERR_INVALID, "MUON_TEST_EXTENT_SHRINK takes a value >= 0");
+      g_knobs.extent_shrink = value;
       return MUON_OK;
     case MUON_TEST_RASTER:
       if (value < 0 || value > 64) return fail(MUON_ERR_INVALID, "MUON_TEST_RASTER takes 0 to 64");

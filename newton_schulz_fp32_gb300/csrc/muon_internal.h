@@ -199,10 +199,21 @@ struct StreamLaunchArgs {
   int prev_overwrite;
   // non-null: k_finalize writes {sum of squares, skipped, NS problems, 0}
   double* stats_out;
+  // Debug builds (MUON_DEBUG): the extents the tables describe -- storage
+  // elements of accum / momentum / master / grads, elements of one X region
+  // of the workspace -- and the flag a tile that would leave them records
+  // kErrBounds in (the tile is then skipped).  Unused in release builds.
+  int64_t dbg_storage_extent;
+  int64_t dbg_x_extent;
+  int* dbg_flag;
 };
 
+// Error code of a debug build's bounds check (muon_device_error).
+constexpr int kErrBounds = 16;
+
 void launch_accumulate(float* accum, const uint16_t* grad, const Run* runs, int nruns,
-                       float scale, int overwrite, cudaStream_t s);
+                       float scale, int overwrite, int64_t dbg_extent, int* dbg_flag,
+                       cudaStream_t s);
 void launch_reduce(const StreamLaunchArgs& a, cudaStream_t s);
 void launch_owner_norm(const StreamLaunchArgs& a, cudaStream_t s);
 void launch_gather(const StreamLaunchArgs& a, cudaStream_t s);
