@@ -724,7 +724,17 @@ struct NsBlocks {
   bool pairs = false;                       // BF16 products on SM pairs
 };
 
-NsBlocks ns_blocks(const std::vector<Owner>& owners, bool tc, bool bf16, int force_cap) {
+// The gram form stacks no further than the single-SM tile (128 rows), and
+// takes SM pairs only for blocks of 192+ rows unstacked: its m x m
+// recurrence runs on the split-3 kernel over each problem's whole stacked
+// square, so a 256-row stack of four 64-row heads costs 16 times the
+// recurrence flops and 4 times its bytes of the heads alone (GPT-2-small,
+// gram, BF16: NS 3.11 ms with 256-row stacks on pairs, 2.91 ms unstacked),
+// while the ragged set's stacks of 32- and 64-row blocks into 128 gain 3%.
+// force_cap >= 0 (the waves of a bounded plan) repeats the unbounded plan's
+// choice, force_pairs included.
+NsBlocks ns_blocks(const std::vector<Owner>& owners, bool tc, bool bf16, bool gram, int force_cap,
+                   bool force_pairs) {
   const bool allow_pairs = tc && bf16 && g_knobs.gemm != 2;
   const bool stack = g_knobs.stack != 0;
   auto group = [&](int cap) {
@@ -765,11 +775,11 @@ NsBlocks ns_blocks(const std::vector<Owner>& owners, bool tc, bool bf16, int for
   if (!tc) return group(0);
   if (force_cap >= 0) {
     NsBlocks B = group(force_cap);
-    B.pairs = allow_pairs && force_cap == kTcPairBM;
+    B.pairs = allow_pairs && force_pairs;
     return B;
   }
   if (allow_pairs) {
-    NsBlocks B = group(kTcPairBM);
+    NsBlocks B = group(gram ? 0 : kTcPairBM);
     bool ok = true;
     for (const Owner& q : B.probs) ok = ok && q.m >= 192;   // a 256-row tile at least 3/4 used
     if (ok) {
@@ -784,10 +794,11 @@ NsBlocks ns_blocks(const std::vector<Owner>& owners, bool tc, bool bf16, int for
 // x_elems elements; the m x m regions are laid out per NS problem).  The
 // workspace is allocated unless `ext` is given, in which case the m x m
 // regions hold ext_sq elements (at least the problems' need) and the
-// problems are stacked with rows cap `force_cap`.
+// problems are stacked with rows cap `force_cap` on the engine `force_pairs`
+// names.
 int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method, int mode,
                   int steps, NsPlan& P, char* ext = nullptr, int64_t ext_sq = 0,
-                  int force_cap = -1, double* ext_ssq = nullptr) {
+                  int force_cap = -1, double* ext_ssq = nullptr, bool force_pairs = false) {
   const bool bf16 = mode == MUON_OPERANDS_BF16;
   NsFormats F;
   int rc0 = ns_formats(method, mode, F);
@@ -798,7 +809,7 @@ int build_ns_plan(const std::vector<Owner>& owners, int64_t x_elems, int method,
   const bool need_qbf = F.need_qbf;
   auto bytes_of = NsFormats::bytes_of;
   auto eb = [](int es) { return int64_t(es == 6 ? 2 : es); };
-  const NsBlocks NB = ns_blocks(owners, tc, bf16, force_cap);
+  const NsBlocks NB = ns_blocks(owners, tc, bf16, method == MUON_NS_GRAM, force_cap, force_pairs);
   const std::vector<Owner>& probs = NB.probs;
   int64_t sq_elems = NB.sq_elems;
   if (ext) {
@@ -1102,7 +1113,8 @@ int build_wave_plan(const Layout& L, int method, int mode, int steps, uint64_t b
   NsFormats F;
   int rc = ns_formats(method, mode, F);
   if (rc != MUON_OK) return rc;
-  const NsBlocks NB = ns_blocks(L.owners, F.tc, mode == MUON_OPERANDS_BF16, -1);
+  const NsBlocks NB = ns_blocks(L.owners, F.tc, mode == MUON_OPERANDS_BF16, method == MUON_NS_GRAM,
+                                -1, false);
   // The shared workspace holds the largest wave's m x n regions and the
   // largest wave's m x m regions, which may come from different waves, so
   // a problem joins the current wave only while those running maxima still
@@ -1170,7 +1182,7 @@ int build_wave_plan(const Layout& L, int method, int mode, int steps, uint64_t b
     for (int i : waves[w]) wo.push_back(owners[i]);
     std::unique_ptr<NsPlan> sub(new NsPlan());
     rc = build_ns_plan(wo, mx, method, mode, steps, *sub, P.ws.as<char>(), msq, NB.cap,
-                       P.ssq_ptr ? P.ssq_ptr + ssq_off[wave_prob0[w]] : nullptr);
+                       P.ssq_ptr ? P.ssq_ptr + ssq_off[wave_prob0[w]] : nullptr, NB.pairs);
     if (rc != MUON_OK) return rc;
     P.flops += sub->flops;
     P.x0 = sub->x0;
@@ -1803,7 +1815,8 @@ extern "C" int muon_describe_tables(const muon_param_t* params, int nparams,
   rc = validate_and_build(params, nparams, parts, nparts, L);
   if (rc != MUON_OK) return rc;
   const bool bf16 = operand_mode == MUON_OPERANDS_BF16;
-  const NsBlocks NB = ns_blocks(L.owners, true, bf16, -1);   // as on a GB300
+  const NsBlocks NB = ns_blocks(L.owners, true, bf16, ns_method == MUON_NS_GRAM, -1,
+                                false);   // as on a GB300
   NsFormats F;
   ns_formats_for(true, ns_method, operand_mode, F);
   std::memset(out, 0, sizeof(*out));

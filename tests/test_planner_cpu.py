@@ -58,11 +58,12 @@ def test_gpt2_small_plan(lib, method, operand, x_bytes, sq_planes, sq_bytes):
     assert d["muon_params"] == 72 and d["muon_blocks"] == 12 * (12 + 12 + 4)
     # Q and K heads (64-row blocks, a multiple of 32, adjacent and equal)
     # stack into problems of the engine's row tile: four into 256 rows on SM
-    # pairs (BF16 operands, every problem then at least 192 rows), two into
-    # 128 rows on single SMs (split-3 FP32); plus V, O, up, down
-    per = 4 if operand == "bf16" else 2
+    # pairs (standard form, BF16 operands: every problem then at least 192
+    # rows), two into 128 rows on single SMs (split-3 FP32, and the gram
+    # form, whose m x m recurrence grows with the stack); plus V, O, up, down
+    per = 4 if (operand == "bf16" and method == "standard") else 2
     assert d["ns_problems"] == 12 * (2 * 12 // per + 4)
-    assert d["pair_engine"] == (1 if operand == "bf16" else 0)
+    assert d["pair_engine"] == (1 if per == 4 else 0)
     assert d["stack_rows"] == 64 * per
     assert d["muon_elements"] == 12 * (4 * 768 * 768 + 2 * 3072 * 768) and d["aux_elements"] == 0
     assert d["padding_elements"] == 0          # 84,934,656 is a multiple of 128 x 8
