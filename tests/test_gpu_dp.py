@@ -54,7 +54,8 @@ def local_view(lay, parts_local, pr, rank, glob, size):
     return out
 
 
-def emulated_dp_step(torch, lay, world, acc, mom, mst, method, mode, clip=CLIP, assign="balanced"):
+def emulated_dp_step(torch, lay, world, acc, mom, mst, method, mode, clip=CLIP, assign="balanced",
+                     grad_scale=1.0, budget=0):
     """Runs the data-parallel step of `world` ranks in this process; acc,
     mom, mst are whole-model storage buffers (numpy); returns each rank's
     buffers after the step and each rank's result."""
@@ -65,7 +66,7 @@ def emulated_dp_step(torch, lay, world, acc, mom, mst, method, mode, clip=CLIP, 
         plan = dp.DPPlan(lay.params, parts_local, pr, world, r, method, assign)
         bufs = [torch.from_numpy(local_view(lay, parts_local, pr, r, g, sizes[r])).cuda()
                 for g in (acc, mom, mst)]
-        ranks.append((plan, dp.DataParallelMuon(plan), bufs,
+        ranks.append((plan, dp.DataParallelMuon(plan, workspace_budget=budget), bufs,
                       torch.zeros(4, dtype=torch.int32, device="cuda")))
     off = lambda counts: np.concatenate([[0], np.cumsum(counts)])
     # 1. pack, all-to-all
@@ -80,7 +81,7 @@ def emulated_dp_step(torch, lay, world, acc, mom, mst, method, mode, clip=CLIP, 
             dt.recv[ro[s]:ro[s] + n].copy_(ds.send[so[t]:so[t] + n])
     # 2. owners' step, all-reduce of the statistics
     for plan, d, _, _ in ranks:
-        d.local_step(BETA, method, 5, mode)
+        d.local_step(BETA, method, 5, mode, grad_scale)
     torch.cuda.synchronize()
     total = sum(d.stats.clone() for _, d, _, _ in ranks)
     for _, d, _, _ in ranks:
@@ -105,9 +106,10 @@ def emulated_dp_step(torch, lay, world, acc, mom, mst, method, mode, clip=CLIP, 
     return out, parts_local, sizes, pr
 
 
-def whole_step(torch, lay, acc, mom, mst, method, mode, clip=CLIP):
+def whole_step(torch, lay, acc, mom, mst, method, mode, clip=CLIP, grad_scale=1.0):
     bufs = [torch.from_numpy(x.copy()).cuda() for x in (acc, mom, mst)]
-    res = nsg.read_result(nsg.step(*bufs, lay.params, lay.parts, BETA, LR, method, 5, clip, mode))
+    res = nsg.read_result(nsg.step_ex(*bufs, lay.params, lay.parts, BETA, LR, method, 5, clip, mode,
+                                      grad_scale=grad_scale))
     return [b.cpu().numpy() for b in bufs] + [res]
 
 
@@ -121,21 +123,26 @@ def make_state(lay, seed, nan=False):
             wl.storage_with_sentinels(lay, w0))
 
 
-CASES = [("tiny", 2, "gram", "bf16"), ("tiny", 3, "standard", "fp32"),
-         ("gpt2_layer", 2, "standard", "bf16"), ("gpt2_layer", 4, "gram", "fp32"),
-         ("gpt2_layer", 3, "gram", "bf16")]
+CASES = [("tiny", 2, "gram", "bf16", {}), ("tiny", 3, "standard", "fp32", {}),
+         ("gpt2_layer", 2, "standard", "bf16", {}), ("gpt2_layer", 4, "gram", "fp32", {}),
+         ("gpt2_layer", 3, "gram", "bf16", {}),
+         # a loss scale undone (2^-3) and the owners' NS in waves of one block
+         ("gpt2_layer", 3, "standard", "bf16", {"grad_scale": 0.125, "budget": 1}),
+         ("tiny", 2, "gram", "fp32", {"grad_scale": 0.5, "budget": 1})]
 LAYOUTS = {"tiny": lambda w: wl.tiny_layout(nparts=w),
            "gpt2_layer": lambda w: wl.gpt2_small_layout(layers=1, nparts=w)}
 
 
-@pytest.mark.parametrize("name,world,method,mode", CASES)
-def test_emulated_ranks_match_whole_step_and_oracle(torch, name, world, method, mode):
+@pytest.mark.parametrize("name,world,method,mode,opts", CASES)
+def test_emulated_ranks_match_whole_step_and_oracle(torch, name, world, method, mode, opts):
     lay = LAYOUTS[name](world)
     acc, mom, mst = make_state(lay, 900 + world)
-    ranks, parts_local, sizes, pr = emulated_dp_step(torch, lay, world, acc, mom, mst, method, mode)
-    ref = whole_step(torch, lay, acc, mom, mst, method, mode)
+    gs = opts.get("grad_scale", 1.0)
+    ranks, parts_local, sizes, pr = emulated_dp_step(torch, lay, world, acc, mom, mst, method, mode,
+                                                     grad_scale=gs, budget=opts.get("budget", 0))
+    ref = whole_step(torch, lay, acc, mom, mst, method, mode, grad_scale=gs)
     ores = om.muon_step_flat(acc, mom, mst, lay.params, lay.parts, BETA, LR, method, 5, CLIP,
-                             ORACLE_MODE[mode])
+                             ORACLE_MODE[mode], grad_scale=gs)
     r0 = ranks[0][3]
     assert all(r[3]["applied"] == 1 for r in ranks)
     assert all(r[3] == r0 for r in ranks)          # every rank reports the same step
