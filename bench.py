@@ -54,6 +54,26 @@ GEMM_TRAFFIC = {
 }
 
 
+# DRAM bytes of the ragged gram step's 16 GEMM launches (R0, the 14 launches
+# of the split-3 m x m recurrence, Y), summed from one ncu capture of the
+# full 8192-matrix step (dram__bytes_read.sum + dram__bytes_write.sum,
+# one pass), valid for the sources hashed.
+RAGGED_NS_TRAFFIC = {"bytes_per_step": 46.476e9, "sources_sha256_16": "d0a0151e96145d4c",
+                     "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc3.cu",
+                               "newton_schulz_fp32_gb300/csrc/gemm_tc.cu",
+                               "newton_schulz_fp32_gb300/csrc/tc_common.cuh",
+                               "newton_schulz_fp32_gb300/csrc/api.cu"]}
+
+
+def _traffic_if_current(rec, key):
+    import hashlib
+    h = hashlib.sha256()
+    for f in rec["files"]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return rec[key] if h.hexdigest()[:16] == rec["sources_sha256_16"] else None
+
+
 def gemm_traffic(workload):
     import hashlib
     rec = GEMM_TRAFFIC.get(workload)
@@ -840,11 +860,22 @@ def run_ragged(args, peaks, peak_src):
                  result=res, stream=stream)
     ms, ph = timed(torch, nsg, step, args.steps, args.warmup, stream, prepare=refill)
     flops = ns_formula_flops(lay, "gram")
+    ns_ms = ph["ns_gemm"]["ms"] / args.steps
+    # the recurrence moves split-3 operands: its roofline is HBM (bytes from
+    # one ncu capture of this workload, BF16 mode, 8192 matrices)
+    traffic = _traffic_if_current(RAGGED_NS_TRAFFIC, "bytes_per_step") \
+        if args.mode == "bf16" and args.ragged_count == 8192 else None
+    hbm = peak_value(peaks, "hbm_gbs")
     print(json.dumps({"metric": "Muon step time", "value": ms, "unit": "ms",
                       "config": {"workload": f"ragged {args.ragged_count} matrices, gram NS x5",
                                  "operand_mode": args.mode,
                                  "elements": lay.n_muon_elements},
-                      "ns_tflops_gram_flops": flops / (ph["ns_gemm"]["ms"] / args.steps * 1e-3) / 1e12,
+                      "ns_tflops_gram_flops": flops / (ns_ms * 1e-3) / 1e12,
+                      "ns_roofline": None if traffic is None else {
+                          "bound": "hbm", "achieved": traffic / (ns_ms * 1e-3) / 1e9,
+                          "peak": hbm, "unit": "GB/s", "frac": traffic / (ns_ms * 1e-3) / 1e9 / hbm,
+                          "traffic": traffic, "traffic_note": "DRAM bytes of the step's 16 GEMM "
+                          "launches, ncu"},
                       "phases_ms_per_step": {k: ph[k]["ms"] / args.steps for k in ph}}))
 
 
