@@ -25,8 +25,12 @@ constexpr double kNormEps = 1e-7;   // X0 = m / (||m||_F + kNormEps)
 constexpr double kClipEps = 1e-6;   // coef = min(1, clip / (norm + kClipEps))
 
 // Work granularity of the streaming kernels.
-constexpr int kReduceTile = 16384;  // elements per pass-1 tile (sum order fixed by it)
-constexpr int kRowTile = 16384;     // target elements per row-aligned 1-D tile
+// Elements per pass-1 tile (the sum order is fixed by it).  Fewer, longer
+// tiles spend less on each block's closing reduction: on Llama-3-8B layers
+// the first pass took 4.36 / 4.06 / 3.92 ms with 16384 / 32768 / 65536.
+constexpr int kReduceTile = 65536;
+constexpr int kRowTile = 16384;     // target elements per row-aligned 1-D tile (32768 and
+                                    // 65536 measured the same on Llama-3-8B layers)
 constexpr int kTT = 64;             // 2-D transpose tile edge
 constexpr int kStreamThreads = 256;
 
