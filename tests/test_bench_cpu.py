@@ -32,3 +32,16 @@ def test_reference_arm_prints_one_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["cpu"]
     assert d["e2e"] == {"value": d["value"], "unit": "ms", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_roofline_traffic_records_match_the_sources():
+    """The DRAM traffic the bench reports beside its roofline comes from ncu
+    captures of particular sources; a record whose kernel or task order has
+    changed since reads as null in the bench line.  The records for the
+    headline (Llama-3-8B), GPT-2-small and ragged workloads must match the
+    sources as committed."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.gemm_traffic("llama") is not None
+    assert bench.gemm_traffic("gpt2") is not None
+    assert bench._traffic_if_current(bench.RAGGED_NS_TRAFFIC, "bytes_per_step") is not None
