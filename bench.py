@@ -494,7 +494,15 @@ def run_gpu(args, W, rank, world):
     res_hosts = [res_host, torch.zeros(4, dtype=torch.int32).pin_memory()]
     e2 = torch.cuda.Event(enable_timing=True)
     e3 = torch.cuda.Event(enable_timing=True)
+    # this host's plain host-to-device rate: one micro-batch copied alone
     barrier()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(copy_stream)
+    with torch.cuda.stream(copy_stream):
+        buf[0][1 if nacc == 0 else 0].copy_(g_host[0], non_blocking=True)
+    a1.record(copy_stream)
+    barrier()
+    h2d_alone_gbs = g_host[0].numel() * 2 / (a0.elapsed_time(a1) * 1e-3) / 1e9
     t_wall = time.perf_counter()
     e2.record(stream)
     copy_stream.wait_event(e2)
@@ -552,6 +560,7 @@ def run_gpu(args, W, rank, world):
     torch.cuda.empty_cache()
     return {"ms": ms, "e2e_ms": e2e_ms, "h2d": h2d, "phases": phases, "clocks": clk,
             "launches": launches, "workspace_bytes": ws, "copy_ms": copy_ms,
+            "h2d_alone_gbs": h2d_alone_gbs,
             "copy_list": [round(x, 1) for x in copy_list],
             "step_ms_e2e": step_ms_e2e}
 
@@ -1089,6 +1098,7 @@ def main():
         "e2e": {"value": m["e2e_ms"], "unit": "ms", "h2d_bytes_per_step": m["h2d"],
                 "d2h_bytes_per_step": 16, "copy_stream_ms_per_step": m["copy_ms"],
                 "step_call_ms_in_e2e": m["step_ms_e2e"],
+                "h2d_gbs_one_copy_alone": m["h2d_alone_gbs"],
                 "copy_stream_ms_each_step": m["copy_list"],
                 "host_numa": host_numa()},
         "gpu_launches": m["launches"],
