@@ -309,3 +309,24 @@ def test_gloo_exchange_matches_single_process_oracle_bitwise(world):
         res = dict(out)
     for r in range(world):
         assert res[r] == [True] * len(CASES), (r, res[r])
+
+
+def test_plan_of_degenerate_tables():
+    """An empty table, and a table of auxiliary parameters only: every rank's
+    plan is consistent and owns what it should."""
+    empty = wl.build_layout([[]], 128, 2)
+    pr = part_ranks(empty) if len(empty.parts) else np.zeros(0, np.int32)
+    parts, _ = dp.local_partition_table(empty.parts, pr, 2)
+    for r in range(2):
+        p = dp.DPPlan(empty.params, parts, pr, 2, r)
+        assert p.owned_elems == 0 and p.send_elems == 0 and p.recv_elems == 0
+        p.close()
+    aux = wl.build_layout([[wl.ParamSpec("ln", 1, 768, use_muon=False),
+                            wl.ParamSpec("emb", 40, 96, use_muon=False)]], 128, 3)
+    pr = part_ranks(aux)
+    parts, _ = dp.local_partition_table(aux.parts, pr, 3)
+    plans = [dp.DPPlan(aux.params, parts, pr, 3, r) for r in range(3)]
+    assert sum(p.sizes["owned_params"] for p in plans) == 2
+    for p in plans:
+        assert not p.send_segs["is_muon"].any() and not p.recv_segs["is_muon"].any()
+        p.close()
