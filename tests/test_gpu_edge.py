@@ -88,3 +88,49 @@ def test_empty_table(torch):
     assert r["applied"] == 1 and r["ns_calls"] == 0
     assert r["global_norm"] == 0.0 and r["clip_coef"] == 1.0
     assert not acc.any() and not mom.any() and not mst.any()
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+@pytest.mark.parametrize("mode", ["bf16", "fp32"])
+def test_tall_head_blocks(torch, method, mode):
+    """Per-head splits whose blocks are taller than wide, so every head block
+    is transposed into its canonical orientation on its own (1536 x 64 in 4
+    heads of 384 x 64; 96 x 32 in 2 heads of 48 x 32), beside a wide
+    head-split matrix; partitions cut through the blocks."""
+    lay = wl.build_layout(
+        [[wl.ParamSpec("tall4", 1536, 64, 4), wl.ParamSpec("tall2", 96, 32, 2),
+          wl.ParamSpec("wide3", 96, 320, 3)]], 32, 3)
+    before, after, ores, gres = run(torch, lay, method, mode)
+    assert gres["ns_calls"] == 4 + 2 + 3
+    check_step(lay, before, after, ores, gres, mode, wl.padding_mask(lay))
+
+
+@pytest.mark.parametrize("steps", [1, 2, 7])
+@pytest.mark.parametrize("method", ["standard", "gram"])
+@pytest.mark.parametrize("mode", ["bf16", "fp32"])
+def test_other_step_counts(torch, steps, method, mode):
+    """ns_steps other than 5, through the step and the NS entry, against the
+    oracle with the same count."""
+    from oracle import newton_schulz as ons
+    from harness import assert_close_update, to_dev
+    lay = wl.tiny_layout()
+    seed = 43
+    grads = micro_batch_grads(lay, seed, 0, 1)
+    z = [np.zeros((s.rows, s.cols), np.float32) for s in lay.specs]
+    st = GpuState(torch, wl.storage_with_sentinels(lay, z), wl.storage_with_sentinels(lay, z),
+                  wl.storage_with_sentinels(lay, z))
+    gpu_accumulate(st, lay, grads, 1, torch)
+    before = st.numpy()
+    gres = nsg.read_result(nsg.step(st.accum, st.momentum, st.master, lay.params, lay.parts, BETA,
+                                    LR, method, steps, CLIP, mode))
+    ores = om.muon_step_flat(*before, lay.params, lay.parts, BETA, LR, method, steps, CLIP,
+                             ORACLE_MODE[mode])
+    check_step(lay, before, st.numpy(), ores, gres, mode, wl.padding_mask(lay))
+    G = wl.rng_for(seed, 300, 77).standard_normal((300, 77)).astype(np.float32)
+    if mode == "bf16":
+        G = wl.to_bf16_values(G)
+    X = to_dev(G, torch, torch.bfloat16 if mode == "bf16" else None)
+    Y = nsg.newton_schulz(X, ns_method=method, ns_steps=steps, operand_mode=mode)
+    assert_close_update(Y.float().cpu().numpy(), ons.newton_schulz(G, method, steps, ORACLE_MODE[mode]),
+                        mode, f"NS entry {method} {mode} steps={steps}")
+    assert nsg.device_error() == 0
