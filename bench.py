@@ -494,15 +494,7 @@ def run_gpu(args, W, rank, world):
     res_hosts = [res_host, torch.zeros(4, dtype=torch.int32).pin_memory()]
     e2 = torch.cuda.Event(enable_timing=True)
     e3 = torch.cuda.Event(enable_timing=True)
-    # this host's plain host-to-device rate: one micro-batch copied alone
     barrier()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(copy_stream)
-    with torch.cuda.stream(copy_stream):
-        buf[0][1 if nacc == 0 else 0].copy_(g_host[0], non_blocking=True)
-    a1.record(copy_stream)
-    barrier()
-    h2d_alone_gbs = g_host[0].numel() * 2 / (a0.elapsed_time(a1) * 1e-3) / 1e9
     t_wall = time.perf_counter()
     e2.record(stream)
     copy_stream.wait_event(e2)
@@ -554,6 +546,16 @@ def run_gpu(args, W, rank, world):
     copy_list = [a.elapsed_time(b) for a, b in copy_marks]
     copy_ms = sum(copy_list) / args.steps
     step_ms_e2e = sum(a.elapsed_time(b) for a, b in step_marks) / args.steps
+    # this host's plain host-to-device rate: one micro-batch copied alone,
+    # after the timed loop (the first copy from a pinned buffer pays a
+    # one-time cost that the steady copies do not)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(copy_stream)
+    with torch.cuda.stream(copy_stream):
+        buf[0][0].copy_(g_host[0], non_blocking=True)
+    a1.record(copy_stream)
+    a1.synchronize()
+    h2d_alone_gbs = g_host[0].numel() * 2 / (a0.elapsed_time(a1) * 1e-3) / 1e9
     ws = nsg.get_stats()["workspace_bytes"]
     del acc, mom, mst, g_dev, g_host, spare, buf
     nsg.release_workspace()
