@@ -47,7 +47,7 @@ GEMM_TRAFFIC = {
     "gpt2": {"bytes_per_launch": 3.8489e9, "sources_sha256_16": "3ef1b59e79164675",
              "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
                        "newton_schulz_fp32_gb300/csrc/tc_common.cuh"]},
-    "llama": {"bytes_per_launch": 32 * 13.1782e9, "sources_sha256_16": "b0a210eac2b2ccb3",
+    "llama": {"bytes_per_launch": 32 * 13.1782e9, "sources_sha256_16": "eedb20031d541eef",
               "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
                         "newton_schulz_fp32_gb300/csrc/tc_common.cuh",
                         "newton_schulz_fp32_gb300/csrc/api.cu"]},
@@ -58,7 +58,7 @@ GEMM_TRAFFIC = {
 # of the split-3 m x m recurrence, Y), summed from one ncu capture of the
 # full 8192-matrix step (dram__bytes_read.sum + dram__bytes_write.sum,
 # one pass), valid for the sources hashed.
-RAGGED_NS_TRAFFIC = {"bytes_per_step": 46.476e9, "sources_sha256_16": "d0a0151e96145d4c",
+RAGGED_NS_TRAFFIC = {"bytes_per_step": 46.476e9, "sources_sha256_16": "842d9ac616de7980",
                      "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc3.cu",
                                "newton_schulz_fp32_gb300/csrc/gemm_tc.cu",
                                "newton_schulz_fp32_gb300/csrc/tc_common.cuh",

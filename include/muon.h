@@ -189,22 +189,29 @@ MUON_API int muon_step(float* accum, float* momentum, float* master,
  *              coefficient (with MUON_CLIP_GRAD the coefficient is known
  *              before the waves and updates are written directly).  Results
  *              are bit-identical to the unbounded step.
- *   last_grad  non-NULL: the last micro-batch's gradients, accumulated by
- *              the step itself in its first read of accum, before the
- *              overflow check: accum[s] = (last_grad_overwrite ? 0 :
- *              accum[s]) + last_grad_scale * float(last_grad[s]) on every
- *              element some parameter covers, then the step.  The same
- *              arithmetic as muon_accumulate with those arguments followed
- *              by the step (bit-identical accum, momentum, master and
- *              result, a skipped step included), one read and one write of
- *              accum fewer.  last_grad must be 8-byte aligned.
- *   prev_grad  non-NULL (with last_grad): one more micro-batch folded in
- *              before last_grad: accum[s] = (prev_grad_overwrite ? 0 :
- *              accum[s]) + prev_grad_scale * float(prev_grad[s]), then
- *              last_grad as above -- the arithmetic of two muon_accumulate
- *              calls (prev, then last) followed by the step, bit for bit,
- *              with accum read at most once and written once.  8-byte
+ *   last_grad  non-NULL: the last micro-batch's gradients, folded into the
+ *              step: on every element some parameter covers, the step's
+ *              gradient is g[s] = (last_grad_overwrite ? 0 : accum[s]) +
+ *              last_grad_scale * float(last_grad[s]), the arithmetic of
+ *              muon_accumulate with those arguments.  accum, momentum,
+ *              master and the result are bit-identical to that call
+ *              followed by the step (a skipped step leaves g in accum).
+ *              When a folded micro-batch overwrites accum's old value
+ *              (last_grad_overwrite, or prev_grad_overwrite below), the
+ *              step's kernels form g wherever they read it, so accum is
+ *              written once per element (by the write-back) instead of
+ *              twice; otherwise the step's first pass writes g into accum
+ *              and the rest read it there.  Either way last_grad may be
+ *              read by any of the step's kernels: it must stay unchanged
+ *              until the step's work on `stream` has completed.  8-byte
  *              aligned.
+ *   prev_grad  non-NULL (with last_grad): one more micro-batch folded in
+ *              before last_grad: g[s] = (prev_grad_overwrite ? 0 :
+ *              accum[s]) + prev_grad_scale * float(prev_grad[s]), then
+ *              last_grad added as above -- the arithmetic of two
+ *              muon_accumulate calls (prev, then last) followed by the
+ *              step, bit for bit; accum is read only when neither
+ *              overwrites it.  Same lifetime as last_grad; 8-byte aligned.
  *   stats_out  non-NULL: device double[4], written at the end of the step:
  *              [0] the sum of squares the clip norm was taken over (the
  *              Muon updates and the auxiliary gradients), [1] 1 if the step

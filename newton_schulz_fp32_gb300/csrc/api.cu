@@ -328,11 +328,11 @@ int validate_and_build(const muon_param_t* params, int nparams, const muon_parti
       a = int64_t(t.r0) * o.cols;
       b = int64_t(t.r0 + t.nr) * o.cols;
       shape_ok = o.cols % 4 == 0 && o.ldx == o.cols;
-    } else if (t.kind == 1) {
-      const int re = std::min(t.r0 + kTT, o.rows);
+    } else if (t.kind == 1 || t.kind == 3) {
+      const int re = std::min(t.r0 + kTT, o.rows), w = t.kind == 3 ? 2 * kTT : kTT;
       a = int64_t(t.r0) * o.cols + t.c0;
-      b = int64_t(re - 1) * o.cols + t.c0 + kTT;
-      shape_ok = o.cols % 4 == 0 && t.c0 + kTT <= o.cols;
+      b = int64_t(re - 1) * o.cols + t.c0 + w;
+      shape_ok = o.cols % 4 == 0 && t.c0 + w <= o.cols;
     } else {
       a = t.rel_begin;
       b = t.rel_begin + t.len;
@@ -390,8 +390,25 @@ int validate_and_build(const muon_param_t* params, int nparams, const muon_parti
             ETile t{};
             t.owner = oi; t.kind = 1; t.r0 = r; t.c0 = c;
             mark_fast(t, o);
-            L.gtiles.push_back(t);
             L.stiles.push_back(t);
+          }
+        // the gather reads 128-column row pieces where it can (each folded
+        // bf16 micro-batch then arrives in 256-byte runs)
+        for (int r = 0; r < o.rows; r += kTT)
+          for (int c = 0; c < o.cols;) {
+            ETile t{};
+            t.owner = oi; t.kind = 3; t.r0 = r; t.c0 = c;
+            mark_fast(t, o);
+            if (t.fast) {
+              L.gtiles.push_back(t);
+              c += 2 * kTT;
+              continue;
+            }
+            t = ETile{};
+            t.owner = oi; t.kind = 1; t.r0 = r; t.c0 = c;
+            mark_fast(t, o);
+            L.gtiles.push_back(t);
+            c += kTT;
           }
       }
       o.ytile_begin = static_cast<int32_t>(L.ytiles.size());
@@ -1361,6 +1378,7 @@ int apply_options(const muon_step_options_t* opts, StreamLaunchArgs& a) {
   a.prev_grad = nullptr;
   a.prev_scale = 1.f;
   a.prev_overwrite = 0;
+  a.fold_vec16 = 0;
   if (!opts) return MUON_OK;
   const bool v3 = opts->struct_size == static_cast<int32_t>(sizeof(muon_step_options_t));
   const bool v2 = v3 || opts->struct_size == MUON_STEP_OPTIONS_V2_SIZE;
@@ -1396,6 +1414,8 @@ int apply_options(const muon_step_options_t* opts, StreamLaunchArgs& a) {
     a.prev_scale = opts->prev_grad_scale;
     a.prev_overwrite = opts->prev_grad_overwrite;
   }
+  a.fold_vec16 = a.last_grad && reinterpret_cast<uintptr_t>(a.last_grad) % 16 == 0 &&
+                 reinterpret_cast<uintptr_t>(a.prev_grad) % 16 == 0;
   if (opts->clip_mode != MUON_CLIP_UPDATE && opts->clip_mode != MUON_CLIP_GRAD)
     return fail(MUON_ERR_INVALID, "unknown clip_mode");
   if (!std::isfinite(opts->grad_scale) || opts->grad_scale < 0.f)
@@ -1492,29 +1512,38 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
 
   const double me = double(L.muon_elems), ae = double(L.aux_elems);
   MUON_CUDA_TRY(cudaMemsetAsync(a.state, 0, sizeof(StepState), s));
-  // a folded last micro-batch adds a bf16 read and an accum write; when it
-  // overwrites, accum's old value is not read.  A folded previous one adds
-  // its bf16 read (and takes over the read of accum, or drops it when it
-  // overwrites)
-  const bool lg_reads_accum = a.last_grad && !a.last_overwrite &&
-                              !(a.prev_grad && a.prev_overwrite);
-  const double lg = a.last_grad ? (me + ae) * ((lg_reads_accum ? 0 : -4) + 6 +
-                                               (a.prev_grad && !a.last_overwrite ? 2 : 0)) : 0.0;
-  if (!pre) {
-    PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 1 : 0) + 1, me * 8 + ae * 4 + lg, 0.0);
-    a.reduce_mode = 0;
+  // Folded micro-batches: the first pass reads 2 bytes per folded
+  // micro-batch per element, and accum's 4 when they add to its old value;
+  // it then writes the gradient into accum (4 bytes), and the later passes
+  // read accum.  When a folded micro-batch overwrites accum, every pass forms
+  // the gradient from the bf16 micro-batches instead, and a skipped step
+  // writes it into accum at the end.
+  const bool fold_old = fold_reads_accum(a);
+  const double g_first = (a.last_grad && !fold_old ? 0.0 : 4.0) + (a.last_grad ? 2.0 : 0.0) +
+                         (a.prev_grad && !a.last_overwrite ? 2.0 : 0.0);
+  const double g_write = fold_old ? 4.0 : 0.0;
+  const double g_bytes = fold_old ? 4.0 : g_first;   // per element, each later pass
+  const bool fold_commit = a.last_grad != nullptr && !fold_old && a.n_rtiles > 0;
+  auto first_pass = [&]() {
     launch_reduce(a, s);
-    a.last_grad = nullptr;   // accum now holds the full gradient
-    a.prev_grad = nullptr;
+    if (fold_old) {
+      a.last_grad = nullptr;   // accum now holds the full gradient
+      a.prev_grad = nullptr;
+    }
+  };
+  if (!pre) {
+    PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 1 : 0) + 1,
+                  (me + ae) * (g_first + g_write) + me * 4, 0.0);
+    a.reduce_mode = 0;
+    first_pass();
     launch_owner_norm(a, s);
   } else {
     // gradient norm over every parameter, clip coefficient, then the
     // per-block momentum norms of the clipped gradients
-    PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 2 : 0) + 2, me * 12 + ae * 4 + lg, 0.0);
+    PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 2 : 0) + 2,
+                  (me + ae) * (g_first + g_write) + me * (g_bytes + 4), 0.0);
     a.reduce_mode = 1;
-    launch_reduce(a, s);
-    a.last_grad = nullptr;
-    a.prev_grad = nullptr;
+    first_pass();
     launch_finalize_pre(a, s);
     a.reduce_mode = 2;
     launch_reduce(a, s);
@@ -1524,7 +1553,7 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
     {
       a.etiles = tp->d_gtiles.as<ETile>();
       a.n_etiles = static_cast<int>(L.gtiles.size());
-      PhaseScope sc(MUON_PHASE_GATHER, s, a.n_etiles ? 1 : 0, me * (12 + P->esize), 0.0);
+      PhaseScope sc(MUON_PHASE_GATHER, s, a.n_etiles ? 1 : 0, me * (g_bytes + 8 + P->esize), 0.0);
       launch_gather(a, s);
     }
     rc = enqueue_gemms(*P, a.state, tp->d_err.as<int>(), s);
@@ -1544,9 +1573,10 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
     {
       a.etiles = tp->d_stiles.as<ETile>();
       a.n_etiles = static_cast<int>(L.stiles.size());
-      PhaseScope sc(MUON_PHASE_SCATTER, s, a.n_etiles ? 1 : 0,
-                    me * (12 + P->esize) + ae * (a.adam ? 32 : 8), 0.0);
+      PhaseScope sc(MUON_PHASE_SCATTER, s, (a.n_etiles ? 1 : 0) + (fold_commit ? 1 : 0),
+                    me * (12 + P->esize) + ae * (g_bytes + (a.adam ? 28 : 4)), 0.0);
       launch_scatter(a, s);
+      if (fold_commit) launch_fold_commit(a, s);
     }
   } else {
     // bounded workspace: per wave gather, NS, update sums and the Muon
@@ -1558,7 +1588,8 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
       {
         b.etiles = tp->d_gtiles.as<ETile>() + R.g0;
         b.n_etiles = R.g1 - R.g0;
-        PhaseScope sc(MUON_PHASE_GATHER, s, b.n_etiles ? 1 : 0, R.elems * (12 + P->esize), 0.0);
+        PhaseScope sc(MUON_PHASE_GATHER, s, b.n_etiles ? 1 : 0, R.elems * (g_bytes + 8 + P->esize),
+                      0.0);
         launch_gather(b, s);
       }
       rc = enqueue_gemms(*P->waves[w], a.state, tp->d_err.as<int>(), s);
@@ -1591,9 +1622,10 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
       a.park = 2;
       a.etiles = tp->d_stiles.as<ETile>();
       a.n_etiles = static_cast<int>(L.stiles.size());
-      PhaseScope sc(MUON_PHASE_SCATTER, s, a.n_etiles ? 1 : 0,
-                    (pre ? 0.0 : me * 16) + ae * (a.adam ? 32 : 8), 0.0);
+      PhaseScope sc(MUON_PHASE_SCATTER, s, (a.n_etiles ? 1 : 0) + (fold_commit ? 1 : 0),
+                    (pre ? 0.0 : me * 16) + ae * (g_bytes + (a.adam ? 28 : 4)), 0.0);
       launch_scatter(a, s);
+      if (fold_commit) launch_fold_commit(a, s);
     }
   }
   MUON_CUDA_TRY(cudaGetLastError());

@@ -33,6 +33,7 @@ constexpr int kRowTile = 16384;     // target elements per row-aligned 1-D tile 
                                     // 65536 measured the same on Llama-3-8B layers)
 constexpr int kTT = 64;             // 2-D transpose tile edge
 constexpr int kStreamThreads = 256;
+constexpr int kFoldCommitCtas = 152 * 8;   // k_fold_commit: 8 CTAs per SM, tiles strided
 
 // A contiguous run shared by flat space and storage: the intersection of one
 // owner (head block or auxiliary parameter) with one partition.
@@ -79,6 +80,8 @@ struct RTile {
 //   kind 0: rows [r0, r0 + nr) of a non-transposed Muon owner
 //   kind 1: 64 x 64 tile at (r0, c0) of a transposed Muon owner
 //   kind 2: elements [rel_begin, rel_begin + len) of an auxiliary owner
+//   kind 3: gather only, 64 x 128 tile at (r0, c0) of a transposed Muon
+//           owner, always fast (where it would not be, two kind-1 tiles)
 // fast = 1 when the whole tile lies in one segment, its storage is 16-byte
 // aligned and its rows are whole multiples of 4 elements: then storage index
 // = sdelta + owner-relative index and the kernels use 16-byte accesses.
@@ -193,7 +196,9 @@ struct StreamLaunchArgs {
   float* exp_avg;
   float* exp_avg_sq;
   int park;              // bounded workspace: scatter writes the unclipped update to accum only
-  // non-null: the first k_reduce pass accumulates this micro-batch into accum first
+  // non-null: a micro-batch folded into the step's gradient (see Fold in
+  // stream_kernels.cu: formed by every pass that reads the gradient, or by
+  // the first pass alone, which then writes it into accum)
   const uint16_t* last_grad;
   float last_scale;
   int last_overwrite;
@@ -201,6 +206,7 @@ struct StreamLaunchArgs {
   const uint16_t* prev_grad;
   float prev_scale;
   int prev_overwrite;
+  int fold_vec16;        // the folded micro-batches are 16-byte aligned (16-byte loads)
   // non-null: k_finalize writes {sum of squares, skipped, NS problems, 0}
   double* stats_out;
   // Debug builds (MUON_DEBUG): the extents the tables describe -- storage
@@ -219,6 +225,9 @@ void launch_accumulate(float* accum, const uint16_t* grad, const Run* runs, int 
                        float scale, int overwrite, int64_t dbg_extent, int* dbg_flag,
                        cudaStream_t s);
 void launch_reduce(const StreamLaunchArgs& a, cudaStream_t s);
+void launch_fold_commit(const StreamLaunchArgs& a, cudaStream_t s);
+// folded micro-batches that add to accum's old value (the first pass then writes the gradient)
+bool fold_reads_accum(const StreamLaunchArgs& a);
 void launch_owner_norm(const StreamLaunchArgs& a, cudaStream_t s);
 void launch_gather(const StreamLaunchArgs& a, cudaStream_t s);
 void launch_update_sumsq(const StreamLaunchArgs& a, cudaStream_t s);

@@ -141,6 +141,74 @@ __device__ __forceinline__ float acc_one(float a, float g, float scale, int over
   return overwrite ? sg : __fadd_rn(a, sg);
 }
 
+__device__ __forceinline__ float4 acc_four(float4 a, uint2 b, float scale, int overwrite) {
+  return make_float4(acc_one(a.x, __uint_as_float(b.x << 16), scale, overwrite),
+                     acc_one(a.y, __uint_as_float(b.x & 0xffff0000u), scale, overwrite),
+                     acc_one(a.z, __uint_as_float(b.y << 16), scale, overwrite),
+                     acc_one(a.w, __uint_as_float(b.y & 0xffff0000u), scale, overwrite));
+}
+
+// Where the step's gradient comes from, fixed per launch (the launchers pick
+// the instantiation, so the loads of the 16-byte paths carry no branch):
+// kind 0 reads accum; kind 1 folds last_grad in; kind 2 folds prev_grad and
+// then last_grad in.  old: accum's old value is read (false when a folded
+// micro-batch overwrites it).
+//
+// When a folded micro-batch overwrites accum's old value, forming the
+// gradient reads as many bytes as reading accum would, so the first pass does
+// not write it: every pass that reads the gradient forms it again with
+// muon_accumulate's arithmetic (all of them see the same bits), and accum is
+// written once, by the write-back (or by k_fold_commit when the step is
+// skipped).  Otherwise (old) the first pass writes the formed gradient into
+// accum and the later passes read accum (the host launches them with kind 0):
+// forming it again there would add bytes and read streams to the gather,
+// which measured slower.  (Writing it in the first pass for the transposed
+// blocks alone measured slower on the Llama-3-8B step too: 2 ms less in the
+// gather, 3 ms more in the first pass.)
+template <int K, bool OLD>
+struct Fold {
+  static constexpr int kind = K;
+  static constexpr bool old = OLD;
+};
+
+template <class F>
+__device__ __forceinline__ float grad_at(const StreamLaunchArgs& a, int64_t st) {
+  float g = F::old ? a.accum[st] : 0.f;
+  if (F::kind == 2) g = acc_one(g, bf16_bits_to_float(a.prev_grad[st]), a.prev_scale, a.prev_overwrite);
+  if (F::kind >= 1) g = acc_one(g, bf16_bits_to_float(a.last_grad[st]), a.last_scale, a.last_overwrite);
+  return g;
+}
+
+// grad_at of the four elements st .. st+3 (st a multiple of 4): one 16-byte
+// accum load and one 8-byte load per folded micro-batch
+template <class F>
+__device__ __forceinline__ float4 grad_at4(const StreamLaunchArgs& a, int64_t st) {
+  float4 g = F::old ? *reinterpret_cast<const float4*>(a.accum + st) : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (F::kind == 2)
+    g = acc_four(g, *reinterpret_cast<const uint2*>(a.prev_grad + st), a.prev_scale, a.prev_overwrite);
+  if (F::kind >= 1)
+    g = acc_four(g, *reinterpret_cast<const uint2*>(a.last_grad + st), a.last_scale, a.last_overwrite);
+  return g;
+}
+
+// grad_at of the eight elements st .. st+7 (st a multiple of 8, the folded
+// micro-batches 16-byte aligned): 16-byte loads of each bf16 micro-batch
+template <class F>
+__device__ __forceinline__ void grad_at8(const StreamLaunchArgs& a, int64_t st, float4& lo, float4& hi) {
+  lo = F::old ? *reinterpret_cast<const float4*>(a.accum + st) : make_float4(0.f, 0.f, 0.f, 0.f);
+  hi = F::old ? *reinterpret_cast<const float4*>(a.accum + st + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (F::kind == 2) {
+    const uint4 p = *reinterpret_cast<const uint4*>(a.prev_grad + st);
+    lo = acc_four(lo, make_uint2(p.x, p.y), a.prev_scale, a.prev_overwrite);
+    hi = acc_four(hi, make_uint2(p.z, p.w), a.prev_scale, a.prev_overwrite);
+  }
+  if (F::kind >= 1) {
+    const uint4 l = *reinterpret_cast<const uint4*>(a.last_grad + st);
+    lo = acc_four(lo, make_uint2(l.x, l.y), a.last_scale, a.last_overwrite);
+    hi = acc_four(hi, make_uint2(l.z, l.w), a.last_scale, a.last_overwrite);
+  }
+}
+
 // ------------------------------------------------------------------ debug bounds checks
 // Debug builds (MUON_DEBUG) check, before a block touches memory, that its
 // tile stays inside the extents the tables describe: the storage range of
@@ -171,8 +239,8 @@ __device__ __forceinline__ void dbg_etile_range(const ETile& t, const Owner& o, 
   if (t.kind == 0) {
     lo = int64_t(t.r0) * o.cols;
     hi = int64_t(t.r0 + t.nr) * o.cols;
-  } else if (t.kind == 1) {
-    const int re = min(t.r0 + kTT, o.rows), ce = min(t.c0 + kTT, o.cols);
+  } else if (t.kind == 1 || t.kind == 3) {
+    const int re = min(t.r0 + kTT, o.rows), ce = min(t.c0 + (t.kind == 3 ? 2 * kTT : kTT), o.cols);
     lo = int64_t(t.r0) * o.cols + t.c0;
     hi = int64_t(re - 1) * o.cols + ce;
   } else {
@@ -244,10 +312,6 @@ k_accumulate(float* __restrict__ accum, const uint16_t* __restrict__ grad,
 
 // ------------------------------------------------------------------ S2 pass 1
 
-// Thread t of the tile sums the 4-element groups t, t + NT, t + 2 NT, ...
-// (elements in order within a group), whatever segments they fall in: the
-// sum order depends only on the owner-relative index.  Tiles inside one
-// aligned segment read float4s; others resolve each element's segment.
 // One element of pass 1: the sum of squares of what the mode needs and the
 // overflow check on the gradient the step uses.
 __device__ __forceinline__ void reduce_one(const StreamLaunchArgs& a, float graw, float m, bool use_m,
@@ -259,41 +323,17 @@ __device__ __forceinline__ void reduce_one(const StreamLaunchArgs& a, float graw
   acc = __fmaf_rn(v, v, acc);
 }
 
-// Thread t of the tile sums the 4-element groups t, t + NT, t + 2 NT, ...
-// (elements in order within a group), whatever segments they fall in: the
-// sum order depends only on the owner-relative index.  Tiles inside one
-// aligned segment read float4s; others resolve each element's segment.
-// reduce_mode 0: Muon tiles sum (beta m + g)^2, auxiliary tiles g^2;
-//             1: every tile sums g^2 (the gradient norm, clip-before-Muon);
-//             2: Muon tiles sum (beta m + coef g)^2 after the gradient clip.
-__global__ void __launch_bounds__(kStreamThreads)
-k_reduce(StreamLaunchArgs a) {
+// One pass-1 tile, the gradient read through F (and written into accum when
+// F reads accum's old value).
+template <class F>
+__device__ __forceinline__ void reduce_tile(const StreamLaunchArgs& a, const RTile& t, const Owner& o,
+                                            bool use_m, float c, float& acc, bool& bad) {
   constexpr int NT = kStreamThreads;
-  const RTile t = a.rtiles[blockIdx.x];
-  const Owner o = a.owners[t.owner];
-  if (a.reduce_mode == 2 && (!o.is_muon || a.state->overflow)) return;
-  MUON_DBG_CHECK(dbg_tile_ok(a, o, t.fast, t.sdelta, t.rel_begin, t.rel_begin + t.len, false),
-                 a.dbg_flag);
-  const bool use_m = a.reduce_mode == 1 ? false : (o.is_muon != 0);
-  const float c = a.reduce_mode == 2 ? a.state->coef : 1.f;
   const int64_t tb = t.rel_begin, te = t.rel_begin + t.len;
   const int ngroups = (t.len + 3) / 4;
-  float acc = 0.f;
-  bool bad = false;
-  // a folded last micro-batch: accum = (overwrite ? 0 : accum) + scale * g,
-  // written back before the element is used (muon_accumulate's arithmetic);
-  // a folded previous micro-batch is added the same way before it
-  const uint16_t* LG = a.last_grad;
-  const float ls = a.last_scale;
-  const int lo = a.last_overwrite;
-  const uint16_t* LP = lo ? nullptr : a.prev_grad;   // an overwriting last one replaces it
-  const float ps = a.prev_scale;
-  const int po = a.prev_overwrite;
   if (t.fast) {
-    float* G = a.accum + t.sdelta + tb;
-    const float* M = a.momentum + t.sdelta + tb;
-    const uint16_t* GL = LG ? LG + t.sdelta + tb : nullptr;
-    const uint16_t* GP = LP ? LP + t.sdelta + tb : nullptr;
+    const int64_t base = t.sdelta + tb;
+    const float* M = a.momentum + base;
     constexpr int U = 4;   // 8 or 16 groups in flight per thread measured 1.8x / 3.4x slower
     for (int g0 = threadIdx.x; g0 < ngroups; g0 += NT * U) {
       float4 gv[U], mv[U];
@@ -301,25 +341,8 @@ k_reduce(StreamLaunchArgs a) {
       for (int u = 0; u < U; ++u) {
         const int g = g0 + u * NT;
         if (g < ngroups) {
-          if (GL) {
-            const uint2 b = *reinterpret_cast<const uint2*>(GL + 4 * g);
-            float4 old = (lo || (GP && po)) ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                            : *reinterpret_cast<const float4*>(G + 4 * g);
-            if (GP) {
-              const uint2 p = *reinterpret_cast<const uint2*>(GP + 4 * g);
-              old.x = acc_one(old.x, __uint_as_float(p.x << 16), ps, po);
-              old.y = acc_one(old.y, __uint_as_float(p.x & 0xffff0000u), ps, po);
-              old.z = acc_one(old.z, __uint_as_float(p.y << 16), ps, po);
-              old.w = acc_one(old.w, __uint_as_float(p.y & 0xffff0000u), ps, po);
-            }
-            gv[u].x = acc_one(old.x, __uint_as_float(b.x << 16), ls, lo);
-            gv[u].y = acc_one(old.y, __uint_as_float(b.x & 0xffff0000u), ls, lo);
-            gv[u].z = acc_one(old.z, __uint_as_float(b.y << 16), ls, lo);
-            gv[u].w = acc_one(old.w, __uint_as_float(b.y & 0xffff0000u), ls, lo);
-            *reinterpret_cast<float4*>(G + 4 * g) = gv[u];
-          } else {
-            gv[u] = *reinterpret_cast<const float4*>(G + 4 * g);
-          }
+          gv[u] = grad_at4<F>(a, base + 4 * g);
+          if (F::kind > 0 && F::old) *reinterpret_cast<float4*>(a.accum + base + 4 * g) = gv[u];
           mv[u] = use_m ? *reinterpret_cast<const float4*>(M + 4 * g) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
@@ -343,19 +366,71 @@ k_reduce(StreamLaunchArgs a) {
         if (si < 0) si = find_seg(segs, o.seg_count, rel);
         while (rel >= segs[si].rel_begin + segs[si].len) ++si;
         const int64_t st = segs[si].storage_begin + (rel - segs[si].rel_begin);
-        float gr = a.accum[st];
-        if (LG) {
-          if (LP) gr = acc_one(gr, bf16_bits_to_float(LP[st]), ps, po);
-          gr = acc_one(gr, bf16_bits_to_float(LG[st]), ls, lo);
-          a.accum[st] = gr;
-        }
+        const float gr = grad_at<F>(a, st);
+        if (F::kind > 0 && F::old) a.accum[st] = gr;
         reduce_one(a, gr, use_m ? a.momentum[st] : 0.f, use_m, c, acc, bad);
       }
     }
   }
+}
+
+// Thread t of the tile sums the 4-element groups t, t + NT, t + 2 NT, ...
+// (elements in order within a group), whatever segments they fall in: the
+// sum order depends only on the owner-relative index.  Tiles inside one
+// aligned segment read float4s; others resolve each element's segment.
+// reduce_mode 0: Muon tiles sum (beta m + g)^2, auxiliary tiles g^2;
+//             1: every tile sums g^2 (the gradient norm, clip-before-Muon);
+//             2: Muon tiles sum (beta m + coef g)^2 after the gradient clip.
+template <class F>
+__global__ void __launch_bounds__(kStreamThreads)
+k_reduce(StreamLaunchArgs a) {
+  constexpr int NT = kStreamThreads;
+  const RTile t = a.rtiles[blockIdx.x];
+  const Owner o = a.owners[t.owner];
+  if (a.reduce_mode == 2 && (!o.is_muon || a.state->overflow)) return;
+  MUON_DBG_CHECK(dbg_tile_ok(a, o, t.fast, t.sdelta, t.rel_begin, t.rel_begin + t.len, false),
+                 a.dbg_flag);
+  const bool use_m = a.reduce_mode == 1 ? false : (o.is_muon != 0);
+  const float c = a.reduce_mode == 2 ? a.state->coef : 1.f;
+  float acc = 0.f;
+  bool bad = false;
+  reduce_tile<F>(a, t, o, use_m, c, acc, bad);
   if (__syncthreads_or(bad) && threadIdx.x == 0 && a.reduce_mode != 2) atomicOr(&a.state->overflow, 1);
   const double s = block_sum<NT>(static_cast<double>(acc));
   if (threadIdx.x == 0) a.rtile_sum[blockIdx.x] = s;
+}
+
+// A skipped step with folded micro-batches: accum takes the gradient the
+// step formed (grad_at), the state muon_accumulate on those micro-batches
+// would have left; padding stays untouched.  The tiles of k_reduce, strided
+// over a grid of a few CTAs per SM, so an applied step costs one flag read
+// per CTA.
+template <class F>
+__global__ void __launch_bounds__(kStreamThreads)
+k_fold_commit(StreamLaunchArgs a) {
+  if (!a.state->overflow) return;
+  for (int k = blockIdx.x; k < a.n_rtiles; k += gridDim.x) {
+    const RTile t = a.rtiles[k];
+    const Owner o = a.owners[t.owner];
+    MUON_DBG_CHECK(dbg_tile_ok(a, o, t.fast, t.sdelta, t.rel_begin, t.rel_begin + t.len, false),
+                   a.dbg_flag);
+    const int64_t tb = t.rel_begin, te = t.rel_begin + t.len;
+    if (t.fast) {
+      const int64_t base = t.sdelta + tb;
+      for (int g = threadIdx.x; g < t.len / 4; g += kStreamThreads)
+        *reinterpret_cast<float4*>(a.accum + base + 4 * g) = grad_at4<F>(a, base + 4 * g);
+      continue;
+    }
+    const Segment* segs = a.segs + o.seg_begin;
+    for (int si = find_seg(segs, o.seg_count, tb); si < o.seg_count && segs[si].rel_begin < te; ++si) {
+      const Segment sg = segs[si];
+      const int64_t lo = sg.rel_begin > tb ? sg.rel_begin : tb;
+      const int64_t hi = (sg.rel_begin + sg.len) < te ? (sg.rel_begin + sg.len) : te;
+      const int64_t base = sg.storage_begin - sg.rel_begin;
+      for (int64_t rel = lo + threadIdx.x; rel < hi; rel += kStreamThreads)
+        a.accum[base + rel] = grad_at<F>(a, base + rel);
+    }
+  }
 }
 
 __global__ void k_owner_norm(StreamLaunchArgs a) {
@@ -434,11 +509,11 @@ __device__ __forceinline__ float4 load4_ws(const void* base, int esize, int64_t 
 }
 
 // rows of a non-transposed block: owner elements [e0, e1), X0 index = rel
+template <class F>
 __device__ __forceinline__ void gather_fast_rows(const StreamLaunchArgs& a, const ETile& t,
                                                  const Owner& o, float d, float cpre, char* x0) {
   constexpr int U = 4;
   const int64_t e0 = int64_t(t.r0) * o.cols, e1 = int64_t(t.r0 + t.nr) * o.cols;
-  const float* __restrict__ G = a.accum + t.sdelta;
   float* __restrict__ M = a.momentum + t.sdelta;
   const int64_t stride = int64_t(4) * kStreamThreads;
   for (int64_t i0 = e0 + 4 * threadIdx.x; i0 < e1; i0 += stride * U) {
@@ -447,7 +522,7 @@ __device__ __forceinline__ void gather_fast_rows(const StreamLaunchArgs& a, cons
     for (int u = 0; u < U; ++u) {
       const int64_t i = i0 + u * stride;
       if (i < e1) {
-        g[u] = *reinterpret_cast<const float4*>(G + i);
+        g[u] = grad_at4<F>(a, t.sdelta + i);
         m[u] = *reinterpret_cast<const float4*>(M + i);
       }
     }
@@ -470,7 +545,54 @@ __device__ __forceinline__ void gather_fast_rows(const StreamLaunchArgs& a, cons
   }
 }
 
+// gather_fast_rows with eight elements per thread and step: used when the
+// gradient is formed from bf16 micro-batches (16-byte loads of each instead
+// of 8-byte ones; measured faster), the tile's storage 8-element aligned and
+// its length a multiple of 8
+__device__ __forceinline__ void gather_math4(const StreamLaunchArgs& a, float d, float cpre, float4 g,
+                                             float4 m, float* M, char* x0, int64_t xi) {
+  float4 mv;
+  mv.x = momentum_of(a.beta, m.x, grad_m(a, cpre, g.x));
+  mv.y = momentum_of(a.beta, m.y, grad_m(a, cpre, g.y));
+  mv.z = momentum_of(a.beta, m.z, grad_m(a, cpre, g.z));
+  mv.w = momentum_of(a.beta, m.w, grad_m(a, cpre, g.w));
+  *reinterpret_cast<float4*>(M) = mv;
+  store4_ws(x0, a.esize, xi,
+            make_float4(__fdiv_rn(mv.x, d), __fdiv_rn(mv.y, d), __fdiv_rn(mv.z, d), __fdiv_rn(mv.w, d)),
+            a.x_ps);
+}
+
+template <class F>
+__device__ __forceinline__ void gather_fast_rows8(const StreamLaunchArgs& a, const ETile& t,
+                                                  const Owner& o, float d, float cpre, char* x0) {
+  constexpr int U = 2;
+  const int64_t e0 = int64_t(t.r0) * o.cols, e1 = int64_t(t.r0 + t.nr) * o.cols;
+  float* __restrict__ M = a.momentum + t.sdelta;
+  const int64_t stride = int64_t(8) * kStreamThreads;
+  for (int64_t i0 = e0 + 8 * threadIdx.x; i0 < e1; i0 += stride * U) {
+    float4 g[U][2], m[U][2];
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < e1) {
+        grad_at8<F>(a, t.sdelta + i, g[u][0], g[u][1]);
+        m[u][0] = *reinterpret_cast<const float4*>(M + i);
+        m[u][1] = *reinterpret_cast<const float4*>(M + i + 4);
+      }
+    }
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < e1) {
+        gather_math4(a, d, cpre, g[u][0], m[u][0], M + i, x0, i);
+        gather_math4(a, d, cpre, g[u][1], m[u][1], M + i + 4, x0, i + 4);
+      }
+    }
+  }
+}
+
 // 64 x 64 tile of a transposed block: read rows, write X0 = tile^T
+template <class F>
 __device__ __forceinline__ void gather_fast_tr(const StreamLaunchArgs& a, const ETile& t,
                                                const Owner& o, float d, float cpre, char* x0,
                                                float (*tile)[kTT + 1]) {
@@ -482,7 +604,7 @@ __device__ __forceinline__ void gather_fast_tr(const StreamLaunchArgs& a, const 
     const int r = t.r0 + rq + 16 * k;
     if (r < r_end) {
       const int64_t i = t.sdelta + int64_t(r) * o.cols + t.c0 + cq;
-      g[k] = *reinterpret_cast<const float4*>(a.accum + i);
+      g[k] = grad_at4<F>(a, i);
       m[k] = *reinterpret_cast<const float4*>(a.momentum + i);
     }
   }
@@ -509,6 +631,128 @@ __device__ __forceinline__ void gather_fast_tr(const StreamLaunchArgs& a, const 
   const int xr = threadIdx.x >> 3, rs = (threadIdx.x & 7) * 8;
   #pragma unroll
   for (int pass = 0; pass < 2; ++pass) {
+    const int cc = xr + 32 * pass;
+    const int64_t xi = int64_t(t.c0 + cc) * o.ldx + t.r0 + rs;
+    if (t.r0 + rs + 8 <= r_end) {
+      float v[8];
+      #pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = tile[rs + k][cc];
+      store4_ws(x0, a.esize, xi, make_float4(v[0], v[1], v[2], v[3]), a.x_ps);
+      store4_ws(x0, a.esize, xi + 4, make_float4(v[4], v[5], v[6], v[7]), a.x_ps);
+    } else {
+      for (int k = 0; k < 8 && t.r0 + rs + k < r_end; ++k)
+        store_ws(x0, a.esize, xi + k, tile[rs + k][cc], a.x_ps);
+    }
+  }
+}
+
+// 64 x 128 tile of a transposed block (kind 3): 128-column row pieces, eight
+// rows of 32 float4 per pass in two halves of four passes; X0 = tile^T
+template <class F>
+__device__ __forceinline__ void gather_fast_tr2(const StreamLaunchArgs& a, const ETile& t,
+                                                const Owner& o, float d, float cpre, char* x0,
+                                                float (*tile)[2 * kTT + 1]) {
+  const int r_end = min(t.r0 + kTT, o.rows);
+  const int rq = threadIdx.x >> 5, cq = (threadIdx.x & 31) * 4;
+  #pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float4 g[4], m[4];
+    #pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = t.r0 + rq + 8 * (4 * h + k);
+      if (r < r_end) {
+        const int64_t i = t.sdelta + int64_t(r) * o.cols + t.c0 + cq;
+        g[k] = grad_at4<F>(a, i);
+        m[k] = *reinterpret_cast<const float4*>(a.momentum + i);
+      }
+    }
+    #pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int rr = rq + 8 * (4 * h + k);
+      if (t.r0 + rr < r_end) {
+        const int64_t i = t.sdelta + int64_t(t.r0 + rr) * o.cols + t.c0 + cq;
+        float4 mv;
+        mv.x = momentum_of(a.beta, m[k].x, grad_m(a, cpre, g[k].x));
+        mv.y = momentum_of(a.beta, m[k].y, grad_m(a, cpre, g[k].y));
+        mv.z = momentum_of(a.beta, m[k].z, grad_m(a, cpre, g[k].z));
+        mv.w = momentum_of(a.beta, m[k].w, grad_m(a, cpre, g[k].w));
+        *reinterpret_cast<float4*>(a.momentum + i) = mv;
+        float* tr = tile[rr];
+        tr[cq] = __fdiv_rn(mv.x, d);
+        tr[cq + 1] = __fdiv_rn(mv.y, d);
+        tr[cq + 2] = __fdiv_rn(mv.z, d);
+        tr[cq + 3] = __fdiv_rn(mv.w, d);
+      }
+    }
+  }
+  __syncthreads();
+  // X0 rows c0..c0+127 (block columns), 8 elements per thread, 32 rows per pass
+  const int xr = threadIdx.x >> 3, rs = (threadIdx.x & 7) * 8;
+  #pragma unroll
+  for (int pass = 0; pass < 4; ++pass) {
+    const int cc = xr + 32 * pass;
+    const int64_t xi = int64_t(t.c0 + cc) * o.ldx + t.r0 + rs;
+    if (t.r0 + rs + 8 <= r_end) {
+      float v[8];
+      #pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = tile[rs + k][cc];
+      store4_ws(x0, a.esize, xi, make_float4(v[0], v[1], v[2], v[3]), a.x_ps);
+      store4_ws(x0, a.esize, xi + 4, make_float4(v[4], v[5], v[6], v[7]), a.x_ps);
+    } else {
+      for (int k = 0; k < 8 && t.r0 + rs + k < r_end; ++k)
+        store_ws(x0, a.esize, xi + k, tile[rs + k][cc], a.x_ps);
+    }
+  }
+}
+
+// gather_fast_tr2 with eight columns per thread (16 rows of 16 threads per
+// pass, two halves of two passes), for gradients formed from 16-byte aligned
+// bf16 micro-batches; the tile's storage rows 8-element aligned
+template <class F>
+__device__ __forceinline__ void gather_fast_tr2x8(const StreamLaunchArgs& a, const ETile& t,
+                                                  const Owner& o, float d, float cpre, char* x0,
+                                                  float (*tile)[2 * kTT + 1]) {
+  const int r_end = min(t.r0 + kTT, o.rows);
+  const int rq = threadIdx.x >> 4, cq = (threadIdx.x & 15) * 8;
+  #pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float4 g[2][2], m[2][2];
+    #pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int r = t.r0 + rq + 16 * (2 * h + k);
+      if (r < r_end) {
+        const int64_t i = t.sdelta + int64_t(r) * o.cols + t.c0 + cq;
+        grad_at8<F>(a, i, g[k][0], g[k][1]);
+        m[k][0] = *reinterpret_cast<const float4*>(a.momentum + i);
+        m[k][1] = *reinterpret_cast<const float4*>(a.momentum + i + 4);
+      }
+    }
+    #pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int rr = rq + 16 * (2 * h + k);
+      if (t.r0 + rr < r_end) {
+        const int64_t i = t.sdelta + int64_t(t.r0 + rr) * o.cols + t.c0 + cq;
+        float* tr = tile[rr];
+        #pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          float4 mv;
+          mv.x = momentum_of(a.beta, m[k][q].x, grad_m(a, cpre, g[k][q].x));
+          mv.y = momentum_of(a.beta, m[k][q].y, grad_m(a, cpre, g[k][q].y));
+          mv.z = momentum_of(a.beta, m[k][q].z, grad_m(a, cpre, g[k][q].z));
+          mv.w = momentum_of(a.beta, m[k][q].w, grad_m(a, cpre, g[k][q].w));
+          *reinterpret_cast<float4*>(a.momentum + i + 4 * q) = mv;
+          tr[cq + 4 * q] = __fdiv_rn(mv.x, d);
+          tr[cq + 4 * q + 1] = __fdiv_rn(mv.y, d);
+          tr[cq + 4 * q + 2] = __fdiv_rn(mv.z, d);
+          tr[cq + 4 * q + 3] = __fdiv_rn(mv.w, d);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int xr = threadIdx.x >> 3, rs = (threadIdx.x & 7) * 8;
+  #pragma unroll
+  for (int pass = 0; pass < 4; ++pass) {
     const int cc = xr + 32 * pass;
     const int64_t xi = int64_t(t.c0 + cc) * o.ldx + t.r0 + rs;
     if (t.r0 + rs + 8 <= r_end) {
@@ -614,6 +858,7 @@ __device__ __forceinline__ void scatter_fast_tr(const StreamLaunchArgs& a, const
 
 // auxiliary elements [rel_begin, rel_begin + len): accum = coef * g, plus
 // Adam on the master when enabled
+template <class F>
 __device__ __forceinline__ void scatter_fast_aux(const StreamLaunchArgs& a, const ETile& t, float coef) {
   constexpr int U = 4;
   float* __restrict__ A = a.accum + t.sdelta;
@@ -623,7 +868,7 @@ __device__ __forceinline__ void scatter_fast_aux(const StreamLaunchArgs& a, cons
     float4 g[U];
     #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (i0 + u * stride < e1) g[u] = *reinterpret_cast<const float4*>(A + i0 + u * stride);
+      if (i0 + u * stride < e1) g[u] = grad_at4<F>(a, t.sdelta + i0 + u * stride);
     #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t i = i0 + u * stride;
@@ -683,10 +928,12 @@ __device__ __forceinline__ void apply_parked(const StreamLaunchArgs& a, const ET
   }
 }
 
+template <class F>
 __global__ void __launch_bounds__(kStreamThreads)
 k_gather(StreamLaunchArgs a) {
   if (a.state->overflow) return;
-  __shared__ float tile[kTT][kTT + 1];
+  __shared__ float tile2[kTT][2 * kTT + 1];   // kind 3; kind 1 uses it as kTT x (kTT + 1)
+  float (*tile)[kTT + 1] = reinterpret_cast<float (*)[kTT + 1]>(&tile2[0][0]);
   const ETile t = a.etiles[blockIdx.x];
   const Owner o = a.owners[t.owner];
 #ifdef MUON_DEBUG
@@ -703,15 +950,26 @@ k_gather(StreamLaunchArgs a) {
   char* x0 = static_cast<char*>(a.x0) + o.x_off * ebytes(a.esize);
   const float cpre = a.clip_mode == 1 ? a.state->coef : 1.f;
   if (t.fast) {
-    if (t.kind == 0) gather_fast_rows(a, t, o, d, cpre, x0);
-    else gather_fast_tr(a, t, o, d, cpre, x0, tile);
+    // gradients formed from bf16 micro-batches: 16-byte loads where aligned
+    const bool v8 = F::kind > 0 && !F::old && a.fold_vec16;
+    if (t.kind == 0) {
+      const int64_t e0 = int64_t(t.r0) * o.cols, n = int64_t(t.nr) * o.cols;
+      if (v8 && ((t.sdelta + e0) & 7) == 0 && (n & 7) == 0) gather_fast_rows8<F>(a, t, o, d, cpre, x0);
+      else gather_fast_rows<F>(a, t, o, d, cpre, x0);
+    } else if (t.kind == 1) {
+      gather_fast_tr<F>(a, t, o, d, cpre, x0, tile);
+    } else if (v8 && ((t.sdelta + int64_t(t.r0) * o.cols + t.c0) & 7) == 0 && (o.cols & 7) == 0) {
+      gather_fast_tr2x8<F>(a, t, o, d, cpre, x0, tile2);
+    } else {
+      gather_fast_tr2<F>(a, t, o, d, cpre, x0, tile2);
+    }
     return;
   }
   if (t.kind == 0) {
     for (int r = t.r0 + warp; r < t.r0 + t.nr; r += nw) {
       const int64_t rb = int64_t(r) * o.cols;
       for_row(segs, o.seg_count, rb, rb + o.cols, lane, [&](int64_t rel, int64_t st) {
-        const float mv = momentum_of(a.beta, a.momentum[st], grad_m(a, cpre, a.accum[st]));
+        const float mv = momentum_of(a.beta, a.momentum[st], grad_m(a, cpre, grad_at<F>(a, st)));
         a.momentum[st] = mv;
         store_ws(x0, a.esize, int64_t(r) * o.ldx + (rel - rb), __fdiv_rn(mv, d), a.x_ps);
       });
@@ -724,7 +982,7 @@ k_gather(StreamLaunchArgs a) {
       if (r >= r_end) break;
       const int64_t rb = int64_t(r) * o.cols;
       for_row(segs, o.seg_count, rb + t.c0, rb + c_end, lane, [&](int64_t rel, int64_t st) {
-        const float mv = momentum_of(a.beta, a.momentum[st], grad_m(a, cpre, a.accum[st]));
+        const float mv = momentum_of(a.beta, a.momentum[st], grad_m(a, cpre, grad_at<F>(a, st)));
         a.momentum[st] = mv;
         tile[rr][rel - rb - t.c0] = __fdiv_rn(mv, d);
       });
@@ -856,6 +1114,7 @@ k_finalize(StreamLaunchArgs a) {
 
 // ------------------------------------------------------------------ S4b
 
+template <class F>
 __global__ void __launch_bounds__(kStreamThreads)
 k_scatter(StreamLaunchArgs a) {
   if (a.state->overflow) return;
@@ -890,7 +1149,7 @@ k_scatter(StreamLaunchArgs a) {
     const char* yb = static_cast<const char*>(a.y) + o.x_off * ebytes(a.esize);
     if (t.kind == 0) scatter_fast_rows(a, t, o, post, wm, yb);
     else if (t.kind == 1) scatter_fast_tr(a, t, o, post, wm, yb, tile);
-    else scatter_fast_aux(a, t, coef);
+    else scatter_fast_aux<F>(a, t, coef);
     return;
   }
   if (t.kind == 2) {
@@ -903,7 +1162,7 @@ k_scatter(StreamLaunchArgs a) {
       const int64_t hi = (sg.rel_begin + sg.len) < te ? (sg.rel_begin + sg.len) : te;
       const int64_t base = sg.storage_begin - sg.rel_begin;
       for (int64_t rel = lo + threadIdx.x; rel < hi; rel += blockDim.x) {
-        const float v = __fmul_rn(coef, grad_in(a, a.accum[base + rel]));
+        const float v = __fmul_rn(coef, grad_in(a, grad_at<F>(a, base + rel)));
         a.accum[base + rel] = v;
         if (a.adam) adam_one(a, base + rel, v);
       }
@@ -1041,14 +1300,34 @@ void launch_accumulate(float* accum, const uint16_t* grad, const Run* runs, int 
     k_accumulate<<<nruns, kStreamThreads, 0, s>>>(accum, grad, runs, scale, overwrite, dbg_extent,
                                                   dbg_flag);
 }
+// The instantiation for the launch's gradient source (Fold above).
+#define MUON_FOLD_LAUNCH(kernel, grid, a, s)                                                  \
+  do {                                                                                       \
+    const bool lg = (a).last_grad != nullptr;                                                \
+    const bool two = lg && (a).prev_grad != nullptr && !(a).last_overwrite;                  \
+    const bool old = !lg || !((a).last_overwrite || (two && (a).prev_overwrite));            \
+    if (!lg) kernel<Fold<0, true>><<<(grid), kStreamThreads, 0, (s)>>>(a);                   \
+    else if (!two && old) kernel<Fold<1, true>><<<(grid), kStreamThreads, 0, (s)>>>(a);      \
+    else if (!two) kernel<Fold<1, false>><<<(grid), kStreamThreads, 0, (s)>>>(a);            \
+    else if (old) kernel<Fold<2, true>><<<(grid), kStreamThreads, 0, (s)>>>(a);              \
+    else kernel<Fold<2, false>><<<(grid), kStreamThreads, 0, (s)>>>(a);                      \
+  } while (0)
+
 void launch_reduce(const StreamLaunchArgs& a, cudaStream_t s) {
-  if (a.n_rtiles > 0) k_reduce<<<a.n_rtiles, kStreamThreads, 0, s>>>(a);
+  if (a.n_rtiles > 0) MUON_FOLD_LAUNCH(k_reduce, a.n_rtiles, a, s);
+}
+void launch_fold_commit(const StreamLaunchArgs& a, cudaStream_t s) {
+  if (a.n_rtiles > 0 && a.last_grad)
+    MUON_FOLD_LAUNCH(k_fold_commit, std::min(a.n_rtiles, kFoldCommitCtas), a, s);
+}
+bool fold_reads_accum(const StreamLaunchArgs& a) {
+  return a.last_grad && !(a.last_overwrite || (a.prev_grad && a.prev_overwrite));
 }
 void launch_owner_norm(const StreamLaunchArgs& a, cudaStream_t s) {
   if (a.n_owners > 0) k_owner_norm<<<(a.n_owners + 127) / 128, 128, 0, s>>>(a);
 }
 void launch_gather(const StreamLaunchArgs& a, cudaStream_t s) {
-  if (a.n_etiles > 0) k_gather<<<a.n_etiles, kStreamThreads, 0, s>>>(a);
+  if (a.n_etiles > 0) MUON_FOLD_LAUNCH(k_gather, a.n_etiles, a, s);
 }
 void launch_update_sumsq(const StreamLaunchArgs& a, cudaStream_t s) {
   if (a.n_ytiles > 0) k_update_sumsq<<<a.n_ytiles, kStreamThreads, 0, s>>>(a);
@@ -1060,7 +1339,7 @@ void launch_finalize_pre(const StreamLaunchArgs& a, cudaStream_t s) {
   k_finalize_pre<<<1, kFinThreads, 0, s>>>(a);
 }
 void launch_scatter(const StreamLaunchArgs& a, cudaStream_t s) {
-  if (a.n_etiles > 0) k_scatter<<<a.n_etiles, kStreamThreads, 0, s>>>(a);
+  if (a.n_etiles > 0) MUON_FOLD_LAUNCH(k_scatter, a.n_etiles, a, s);
 }
 
 void launch_ns_sumsq(const void* X, int io_esize, int64_t numel, double* tile_sum, int ntiles,

@@ -36,7 +36,16 @@ def mixed_layout(nparts, storage):
         storage, 7)
 
 
-def run(torch, lay, grads, gas, fold, method, mode, nan_last=False, **opts):
+def misaligned(t, torch):
+    """The same bf16 values at an address that is 8- but not 16-byte
+    aligned (the step's 8-byte loads of folded micro-batches)."""
+    buf = torch.empty(t.numel() + 4, dtype=t.dtype, device=t.device)[4:]
+    buf.copy_(t)
+    assert buf.data_ptr() % 16 == 8
+    return buf
+
+
+def run(torch, lay, grads, gas, fold, method, mode, nan_last=False, misalign=False, **opts):
     """accumulate the micro-batches (all, or all but the last `fold` of
     them, which the step folds in: 1 = last_grad, 2 = prev_grad and
     last_grad), then one step; returns the three storage buffers and the
@@ -51,6 +60,8 @@ def run(torch, lay, grads, gas, fold, method, mode, nan_last=False, **opts):
         g[-1][0] = g[-1][0].copy()
         g[-1][0].flat[3] = np.nan
     gb = [bf16_tensor(wl.bf16_storage_grad(lay, x), torch) for x in g]
+    if misalign:
+        gb = [misaligned(x, torch) for x in gb]
     fold = min(int(fold), gas)
     for mb in range(gas - fold):
         nsg.accumulate(st.accum, gb[mb], 1.0 / gas, overwrite=(mb == 0), params=lay.params,
@@ -89,27 +100,34 @@ def test_folded_last_micro_batch_is_bit_identical(torch, nparts, storage, gas, m
     assert (bits(a1)[pad] == wl.NAN_SENTINEL_BITS).all()
 
 
-@pytest.mark.parametrize("fold", [1, 2])
-def test_folded_non_finite_micro_batch_skips_identically(torch, fold):
+@pytest.mark.parametrize("gas,fold", [(3, 1), (3, 2), (2, 2), (1, 1)])
+def test_folded_non_finite_micro_batch_skips_identically(torch, gas, fold):
+    """A skipped step leaves the accumulated gradient in accum, whether the
+    first pass wrote it (gas 3) or the step writes it only on a skip (the
+    folded micro-batches overwrite accum: gas 2 and 1)."""
     lay = mixed_layout(3, "shuffled")
-    grads = micro_batch_grads(lay, 6, 0, 3)
-    (a0, m0, w0), r0 = run(torch, lay, grads, 3, 0, "standard", "bf16", nan_last=True)
-    (a1, m1, w1), r1 = run(torch, lay, grads, 3, fold, "standard", "bf16", nan_last=True)
+    grads = micro_batch_grads(lay, 6, 0, gas)
+    (a0, m0, w0), r0 = run(torch, lay, grads, gas, 0, "standard", "bf16", nan_last=True)
+    (a1, m1, w1), r1 = run(torch, lay, grads, gas, fold, "standard", "bf16", nan_last=True)
     assert r0["applied"] == 0 and r1 == r0
     for x, y in ((a0, a1), (m0, m1), (w0, w1)):
         np.testing.assert_array_equal(bits(x), bits(y))
 
 
-@pytest.mark.parametrize("fold", [1, 2])
-def test_folded_large_layout_matches(torch, fold):
-    """GPT-2-small-shaped blocks (one layer, P = 8): the fast 16-byte path
-    of the first pass over large tiles."""
+@pytest.mark.parametrize("gas,fold,misalign", [(4, 1, False), (4, 2, False), (2, 2, False),
+                                               (2, 2, True), (1, 1, False)])
+def test_folded_large_layout_matches(torch, gas, fold, misalign):
+    """GPT-2-small-shaped blocks (one layer, P = 8): the fast paths over
+    large tiles.  gas 4: the folded micro-batches add to accum (the first
+    pass writes the gradient); gas 2 and 1: they overwrite it (every pass
+    forms the gradient, 16-byte loads of 16-byte aligned micro-batches,
+    8-byte loads of misaligned ones)."""
     lay = wl.build_layout([[wl.ParamSpec("q", 768, 768, 12), wl.ParamSpec("k", 768, 768, 12),
                             wl.ParamSpec("v", 768, 768), wl.ParamSpec("up", 3072, 768),
                             wl.ParamSpec("down", 768, 3072)]], 128, 8)
-    grads = micro_batch_grads(lay, 8, 0, 4, wl.loguniform_sigmas(lay, 8, 1e-4, 1e-1))
-    (a0, m0, w0), r0 = run(torch, lay, grads, 4, 0, "standard", "bf16")
-    (a1, m1, w1), r1 = run(torch, lay, grads, 4, fold, "standard", "bf16")
+    grads = micro_batch_grads(lay, 8, 0, gas, wl.loguniform_sigmas(lay, 8, 1e-4, 1e-1))
+    (a0, m0, w0), r0 = run(torch, lay, grads, gas, 0, "standard", "bf16")
+    (a1, m1, w1), r1 = run(torch, lay, grads, gas, fold, "standard", "bf16", misalign=misalign)
     assert r0["applied"] == 1 and r1 == r0
     for x, y in ((a0, a1), (m0, m1), (w0, w1)):
         np.testing.assert_array_equal(bits(x), bits(y))
