@@ -6,7 +6,8 @@ Default workload (the benchmark line): the Llama-3-8B-shaped parameter set
 matrices rank 8 plus 1e-3 noise, odd-indexed N(0,1)), two BF16 micro-batches
 accumulated in FP32, then one Muon step (5 standard Newton-Schulz steps,
 BF16 operands).  One timed step = one muon_step_ex that accumulates both
-micro-batches in its first read pass (options prev_grad and last_grad), all
+micro-batches itself (options prev_grad and last_grad: they overwrite accum,
+so the step forms the gradient from them wherever it reads it), all
 kernels of the library, every input resident in HBM (accum, momentum and master
 are 27.9 GB each, far larger than the 129 MB L2, so no flush is needed);
 the K timed steps are recorded into one CUDA graph and timed as one replay.
@@ -120,7 +121,7 @@ def gpt2_workload(ns_method, mode):
     desc = (f"gpt2-small muon step: 12 layers (q,k 12-head, v, o 768x768; up 3072x768; "
             f"down 768x3072), 84.9M params, P=8, align 128, gas=4 bf16 grads, "
             f"{ns_method} NS x5, {mode} operands, clip 0.05; the 3rd and 4th micro-batches "
-            f"are accumulated inside the step's first pass")
+            f"are accumulated inside the step")
     return Workload("gpt2", lay, 4, ns_method, 0.05, desc)
 
 
@@ -130,7 +131,7 @@ def llama_workload(mode, layers=32):
             f"14336x4096; down 4096x14336), {lay.n_param_elements / 1e9:.2f}G params, P=64, "
             f"align 128, gas=2 bf16 grads (even-indexed matrices rank 8 + 1e-3 noise), "
             f"standard NS x5, {mode} operands; both micro-batches are accumulated inside "
-            f"the step's first pass")
+            f"the step")
     return Workload("llama", lay, 2, "standard", 0.0, desc)
 
 
@@ -396,9 +397,9 @@ def run_gpu(args, W, rank, world):
         res_host = torch.zeros(4, dtype=torch.int32).pin_memory()
     torch.cuda.synchronize()
     P, Q = lay.params, lay.parts
-    # the last two micro-batches are accumulated by the step itself, in its
-    # first read of accum (muon_step_ex prev_grad and last_grad: the same
-    # arithmetic as muon_accumulate, with accum read once and written once)
+    # the last two micro-batches are accumulated by the step itself
+    # (muon_step_ex prev_grad and last_grad: the same arithmetic as
+    # muon_accumulate; when they overwrite accum it is written only once)
     nfold = min(2, gas)
     nacc = gas - nfold
 
@@ -478,8 +479,8 @@ def run_gpu(args, W, rank, world):
     # Every step copies its micro-batches from pinned host memory on a copy
     # stream and reads its result back.  A micro-batch that muon_accumulate
     # takes is free again once accumulated, so the next step's copy into it
-    # overlaps this step's Newton-Schulz; the folded ones are read until the
-    # step's first pass ends, so each alternates between two device buffers.
+    # overlaps this step's Newton-Schulz; the folded ones may be read until
+    # the step ends, so each alternates between two device buffers.
     # The host reads each step's result.
     h2d = sum(g.numel() * 2 for g in g_host)
     copy_stream = torch.cuda.Stream()
@@ -909,7 +910,7 @@ def run_llama_layers(args, peaks, peak_src):
 
     def step():
         nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, "standard", 5, 0.0, args.mode, result=res,
-                 stream=stream, options=opts)
+    # both micro-batches are folded into the step;
     # both micro-batches are folded into the step's first pass;
     # --workspace-budget: the NS blocks run in waves whose workspace fits it
     opts = nsg.step_options(workspace_budget=args.workspace_budget, last_grad=grads[1],

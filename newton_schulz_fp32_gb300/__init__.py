@@ -189,7 +189,8 @@ def step_options(clip_mode="update", grad_scale: float = 1.0, adam: dict | None 
     exp_avg, exp_avg_sq) with device float buffers in accum's layout.
     last_grad: the last micro-batch's bf16 gradients (accum's layout), which
     the step accumulates itself, as accumulate(accum, last_grad,
-    last_grad_scale, last_grad_overwrite) would.  stats_out: a device
+    last_grad_scale, last_grad_overwrite) would (read by any of the step's
+    kernels: keep it unchanged until the step is done).  stats_out: a device
     float64[4] the step fills with (sum of squares of the clip norm, skipped,
     NS problems, 0).  prev_grad: one more micro-batch folded in before
     last_grad (as accumulate(accum, prev_grad, prev_grad_scale,

@@ -100,15 +100,18 @@ def test_folded_last_micro_batch_is_bit_identical(torch, nparts, storage, gas, m
     assert (bits(a1)[pad] == wl.NAN_SENTINEL_BITS).all()
 
 
-@pytest.mark.parametrize("gas,fold", [(3, 1), (3, 2), (2, 2), (1, 1)])
-def test_folded_non_finite_micro_batch_skips_identically(torch, gas, fold):
+@pytest.mark.parametrize("gas,fold,opts", [(3, 1, {}), (3, 2, {}), (2, 2, {}), (1, 1, {}),
+                                           (2, 2, {"workspace_budget": 1}),
+                                           (2, 2, {"clip_mode": "grad"})])
+def test_folded_non_finite_micro_batch_skips_identically(torch, gas, fold, opts):
     """A skipped step leaves the accumulated gradient in accum, whether the
     first pass wrote it (gas 3) or the step writes it only on a skip (the
-    folded micro-batches overwrite accum: gas 2 and 1)."""
+    folded micro-batches overwrite accum: gas 2 and 1; also in waves and
+    with the gradient clipped before Muon)."""
     lay = mixed_layout(3, "shuffled")
     grads = micro_batch_grads(lay, 6, 0, gas)
-    (a0, m0, w0), r0 = run(torch, lay, grads, gas, 0, "standard", "bf16", nan_last=True)
-    (a1, m1, w1), r1 = run(torch, lay, grads, gas, fold, "standard", "bf16", nan_last=True)
+    (a0, m0, w0), r0 = run(torch, lay, grads, gas, 0, "standard", "bf16", nan_last=True, **opts)
+    (a1, m1, w1), r1 = run(torch, lay, grads, gas, fold, "standard", "bf16", nan_last=True, **opts)
     assert r0["applied"] == 0 and r1 == r0
     for x, y in ((a0, a1), (m0, m1), (w0, w1)):
         np.testing.assert_array_equal(bits(x), bits(y))
