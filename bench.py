@@ -910,8 +910,8 @@ def run_llama_layers(args, peaks, peak_src):
 
     def step():
         nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, "standard", 5, 0.0, args.mode, result=res,
+                 stream=stream, options=opts)
     # both micro-batches are folded into the step;
-    # both micro-batches are folded into the step's first pass;
     # --workspace-budget: the NS blocks run in waves whose workspace fits it
     opts = nsg.step_options(workspace_budget=args.workspace_budget, last_grad=grads[1],
                             last_grad_scale=0.5, prev_grad=grads[0], prev_grad_scale=0.5,
