@@ -376,6 +376,79 @@ def cpu_baseline(workload, ns_method, mode, budget_s):
                       f"(x{total / flops:.0f})"}
 
 
+SWEEP_CPU_FULL_MAX = 4096   # sweep shapes up to this size are timed in full on the host
+
+
+def sweep_cpu_baseline(r, c, ns_method, mode, cache):
+    """The oracle's Newton-Schulz of one r x c matrix (N(0,1), bf16-valued in
+    BF16 mode) on the host cores: timed in full up to 4096 on each side,
+    else the 4096 x 4096 time scaled by formula flops (cached per method and
+    mode)."""
+    import oracle.newton_schulz as ons
+    import oracle.bf16 as obf
+    cores, model = cpu_info()
+
+    def flops(rr, cc):
+        m, n = min(rr, cc), max(rr, cc)
+        return 5 * (4.0 * m * m * n + 2.0 * m ** 3) if ns_method == "standard" \
+            else 4.0 * m * m * n + 34.0 * m ** 3
+
+    def run(rr, cc):
+        rng = wl.rng_for(wl.CONFIG_SEED["sweep"], rr, cc)
+        X = rng.standard_normal((rr, cc), dtype=np.float32)
+        if mode == "bf16":
+            X = obf.round_bf16(X)
+        t0 = time.perf_counter()
+        ons.newton_schulz(X, ns_method, 5, _oracle_mode(mode))
+        return time.perf_counter() - t0
+
+    base = {"unit": "ms", "cores": cores, "cpu": model, "kind": "oracle"}
+    if max(r, c) <= SWEEP_CPU_FULL_MAX:
+        sec = run(r, c)
+        return dict(base, value=1000.0 * sec, sampled=False,
+                    sample=f"oracle ({_oracle_mode(mode)} mode, numpy fp64 BLAS) on the whole "
+                           f"{r}x{c} Newton-Schulz, one rep")
+    key = (ns_method, mode)
+    if key not in cache:
+        cache[key] = run(SWEEP_CPU_FULL_MAX, SWEEP_CPU_FULL_MAX)
+    sec = cache[key]
+    scale = flops(r, c) / flops(SWEEP_CPU_FULL_MAX, SWEEP_CPU_FULL_MAX)
+    return dict(base, value=1000.0 * sec * scale, sampled=True, sample_seconds=sec,
+                sample=f"oracle ({_oracle_mode(mode)} mode) on a {SWEEP_CPU_FULL_MAX}x"
+                       f"{SWEEP_CPU_FULL_MAX} matrix in {sec:.1f} s, scaled to {r}x{c} by "
+                       f"formula flops (x{scale:.1f})")
+
+
+def ragged_cpu_baseline(lay, mats, mode, budget_s):
+    """The oracle's whole gram Muon step on the first matrices of the ragged
+    set (momentum, norm, Newton-Schulz, write-back), as many as about
+    budget_s of host time allows, extrapolated to all of them by gram
+    formula flops."""
+    import oracle.muon as om
+    cores, model = cpu_info()
+    total = ns_formula_flops(lay, "gram")
+    k, sec, done = 128, 0.0, 0
+    while True:
+        sub = wl.build_layout([lay.specs[:k]], 128, 1)
+        g = wl.pack(sub, mats[:k])
+        z = np.zeros_like(g)
+        t0 = time.perf_counter()
+        om.muon_step_flat(g, z, z.copy(), sub.params, sub.parts, 0.95, 0.02, "gram", 5, 0.0,
+                          _oracle_mode(mode))
+        sec, done = time.perf_counter() - t0, k
+        if k >= len(lay.specs) or sec * 4 > budget_s:
+            break
+        k = min(4 * k, len(lay.specs))
+    part = ns_formula_flops(wl.build_layout([lay.specs[:done]], 128, 1), "gram")
+    full = done >= len(lay.specs)
+    return {"value": 1000.0 * sec * total / part, "unit": "ms", "cores": cores, "cpu": model,
+            "kind": "oracle", "sampled": not full, "sample_seconds": sec,
+            "sample": f"oracle ({_oracle_mode(mode)} mode, numpy fp64 BLAS) on the whole gram "
+                      f"step of the first {done} of {len(lay.specs)} matrices in {sec:.1f} s"
+                      + ("" if full else f", extrapolated by gram formula flops "
+                                         f"(x{total / part:.1f})")}
+
+
 # ------------------------------------------------------------------ GPU run
 
 def run_gpu(args, W, rank, world):
@@ -816,6 +889,7 @@ def run_sweep(args, peaks, peak_src):
     shapes = [tuple(int(v) for v in s.split("x")) for s in args.shapes.split(",")] if args.shapes \
         else wl.SWEEP_SHAPES
     gen = torch.Generator(device="cuda").manual_seed(wl.CONFIG_SEED["sweep"])
+    cpu_cache = {}
     for (r, c) in shapes:
         with torch.cuda.stream(stream):
             X = torch.randn((r, c), generator=gen, device="cuda", dtype=torch.float32)
@@ -837,7 +911,9 @@ def run_sweep(args, peaks, peak_src):
                           "ns_tflops": tf, "frac_of_peak": (tf / peak) if peak else None,
                           "peak_source": peak_src,
                           "gemm_ms": g["ms"] / args.steps, "gemm_launches": g["launches"] / args.steps,
-                          "gemm_tflops_on_gemm_time": g["flops"] / max(g["ms"] * 1e-3, 1e-12) / 1e12}))
+                          "gemm_tflops_on_gemm_time": g["flops"] / max(g["ms"] * 1e-3, 1e-12) / 1e12,
+                          "cpu_baseline": None if args.no_cpu_baseline else
+                          sweep_cpu_baseline(r, c, args.ns_method, args.mode, cpu_cache)}))
         del X, Y
         nsg.release_workspace()
         torch.cuda.empty_cache()
@@ -888,7 +964,9 @@ def run_ragged(args, peaks, peak_src):
                           "peak": hbm, "unit": "GB/s", "frac": traffic / (ns_ms * 1e-3) / 1e9 / hbm,
                           "traffic": traffic, "traffic_note": "DRAM bytes of the step's 16 GEMM "
                           "launches, ncu"},
-                      "phases_ms_per_step": {k: ph[k]["ms"] / args.steps for k in ph}}))
+                      "phases_ms_per_step": {k: ph[k]["ms"] / args.steps for k in ph},
+                      "cpu_baseline": None if args.no_cpu_baseline else
+                      ragged_cpu_baseline(lay, mats, args.mode, args.cpu_budget)}))
 
 
 def run_llama_layers(args, peaks, peak_src):

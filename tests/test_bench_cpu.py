@@ -45,3 +45,30 @@ def test_roofline_traffic_records_match_the_sources():
     assert bench.gemm_traffic("llama") is not None
     assert bench.gemm_traffic("gpt2") is not None
     assert bench._traffic_if_current(bench.RAGGED_NS_TRAFFIC, "bytes_per_step") is not None
+
+
+def test_sweep_and_ragged_cpu_baselines_say_what_was_timed(monkeypatch):
+    """The oracle baselines of the sweep and ragged lines: a shape within
+    the full-timing bound is timed whole; a larger one is the bound's square
+    scaled by formula flops; the ragged step is timed on a prefix of the
+    matrices and scaled by gram flops, or whole when the budget allows."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    import workloads as wl
+    monkeypatch.setattr(bench, "SWEEP_CPU_FULL_MAX", 32)
+    cache = {}
+    whole = bench.sweep_cpu_baseline(32, 24, "standard", "bf16", cache)
+    assert whole["sampled"] is False and whole["value"] > 0 and whole["kind"] == "oracle"
+    big = bench.sweep_cpu_baseline(64, 128, "gram", "fp32", cache)
+    ratio = (4.0 * 64 * 64 * 128 + 34.0 * 64 ** 3) / (4.0 * 32 ** 3 + 34.0 * 32 ** 3)
+    assert big["sampled"] is True and ("gram", "fp32") in cache
+    assert abs(big["value"] - 1000.0 * cache[("gram", "fp32")] * ratio) <= 1e-9 * big["value"]
+    lay = wl.ragged_layout(160, seed=7)
+    mats = [wl.rng_for(7, 2, i).standard_normal((s.rows, s.cols), dtype=np.float32)
+            for i, s in enumerate(lay.specs)]
+    part = bench.ragged_cpu_baseline(lay, mats, "bf16", 0.0)
+    assert part["sampled"] is True and "first 128 of 160" in part["sample"]
+    full = bench.ragged_cpu_baseline(lay, mats, "bf16", 1e9)
+    assert full["sampled"] is False and "first 160 of 160" in full["sample"]
+    assert abs(full["value"] - 1000.0 * full["sample_seconds"]) <= 1e-9 * full["value"]
