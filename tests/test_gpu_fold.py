@@ -134,3 +134,58 @@ def test_folded_large_layout_matches(torch, gas, fold, misalign):
     assert r0["applied"] == 1 and r1 == r0
     for x, y in ((a0, a1), (m0, m1), (w0, w1)):
         np.testing.assert_array_equal(bits(x), bits(y))
+
+
+def test_folded_llama3_8b_step_matches_accumulate_then_step(torch):
+    """The benchmark's configuration at full size (Llama-3-8B, 6.98G
+    elements, P = 64, both bf16 micro-batches folded with overwrite, so
+    every pass forms the gradient from them): accum, momentum and master
+    after the step equal those of muon_accumulate twice followed by the
+    step -- fingerprinted in 64M-element chunks (exact integer sums of the
+    bit patterns) and bit for bit on six sampled matrices of both
+    orientations."""
+    lay = wl.llama3_8b_layout()
+    seed = wl.CONFIG_SEED["llama"]
+    n = lay.storage_size
+    P, Q = lay.params, lay.parts
+    g = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    for mb in range(2):
+        wl.llama_grad_into(lay, seed, mb, g[mb])
+    state = [torch.zeros(n, dtype=torch.float32, device="cuda") for _ in range(3)]
+    sample = [1, 3, 5, 7 * 31 + 1, 7 * 31 + 4, 7 * 31 + 6]
+    chunk = 1 << 26
+
+    def run(fold):
+        acc, mom, mst = state
+        acc.zero_()
+        mom.copy_(g[1]).mul_(0.1)
+        mst.copy_(g[0])
+        opts = None
+        if fold:
+            opts = nsg.step_options(prev_grad=g[0], prev_grad_scale=0.5, prev_grad_overwrite=True,
+                                    last_grad=g[1], last_grad_scale=0.5)
+        else:
+            for mb in range(2):
+                nsg.accumulate(acc, g[mb], 0.5, overwrite=(mb == 0), params=P, parts=Q)
+        res = nsg.read_result(nsg.step(acc, mom, mst, P, Q, BETA, LR, "standard", 5, 0.0, "bf16",
+                                       options=opts))
+        prints = [torch.stack([t.view(torch.int32)[i:i + chunk].sum(dtype=torch.int64)
+                               for i in range(0, n, chunk)]).cpu().numpy() for t in state]
+        mats = []
+        for k in sample:
+            off, s = int(P["offset"][k]), lay.specs[k]
+            mats.append([t[off:off + s.numel].cpu().numpy() for t in state])
+        return res, prints, mats
+
+    r0, p0, m0 = run(False)
+    r1, p1, m1 = run(True)
+    assert r0["applied"] == 1 and r1 == r0
+    for a, b in zip(p0, p1):
+        np.testing.assert_array_equal(a, b)
+    for x, y in zip(m0, m1):
+        for a, b in zip(x, y):
+            np.testing.assert_array_equal(bits(a), bits(b))
+    del g, state
+    nsg.release_workspace()
+    torch.cuda.empty_cache()
+    assert nsg.device_error() == 0
