@@ -240,7 +240,7 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
         if (t.ti < 0) break;
         // the operands were written by other SMs (generic release / acquire
         // above); order the TMA reads after that
-        asm volatile("fence.proxy.async;" ::: "memory");
+        asm volatile("fence.proxy.async.global;" ::: "memory");
         const TcMaps* mp = maps + t.problem;
         if (t.problem != last_problem) {
           asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mp->a)));
@@ -352,8 +352,9 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
       t.tm = __shfl_sync(0xffffffffu, t.tm, 0);
       t.tn = __shfl_sync(0xffffffffu, t.tn, 0);
       t.done = __shfl_sync(0xffffffffu, t.done, 0);
-      asm volatile("fence.proxy.async;" ::: "memory");   // addends come from other SMs
       const GemmProblem& p = probs[t.problem];
+      if (p.E != nullptr && lane == 0)   // addends come from other SMs
+        asm volatile("fence.proxy.async.global;" ::: "memory");
       const TcMaps* mp = maps + t.problem;
       const int gm0 = t.tm * BM + static_cast<int>(rank) * BMC + q * 32;
       uint32_t todo = 0;
@@ -477,7 +478,7 @@ k_gemm_tc2(const GemmProblem* __restrict__ probs, const TcMaps* __restrict__ map
         __syncwarp();
         asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(32 * EPI_WARPS) : "memory");
         if (ew == 0 && lane == 0) {
-          asm volatile("fence.proxy.async;" ::: "memory");
+          asm volatile("fence.proxy.async.global;" ::: "memory");
           asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(counters + t.done) : "memory");
         }
       }
