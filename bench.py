@@ -48,7 +48,7 @@ GEMM_TRAFFIC = {
     "gpt2": {"bytes_per_launch": 3.8480e9, "sources_sha256_16": "7179c2b5092211c5",
              "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
                        "newton_schulz_fp32_gb300/csrc/tc_common.cuh"]},
-    "llama": {"bytes_per_launch": 32 * 13.1362e9, "sources_sha256_16": "fb358a32501ba72e",
+    "llama": {"bytes_per_launch": 32 * 13.1362e9, "sources_sha256_16": "42a6c1fe87eda04d",
               "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
                         "newton_schulz_fp32_gb300/csrc/tc_common.cuh",
                         "newton_schulz_fp32_gb300/csrc/api.cu"]},
@@ -59,7 +59,7 @@ GEMM_TRAFFIC = {
 # of the split-3 m x m recurrence, Y), summed from one ncu capture of the
 # full 8192-matrix step (dram__bytes_read.sum + dram__bytes_write.sum,
 # one pass), valid for the sources hashed.
-RAGGED_NS_TRAFFIC = {"bytes_per_step": 46.476e9, "sources_sha256_16": "842d9ac616de7980",
+RAGGED_NS_TRAFFIC = {"bytes_per_step": 46.476e9, "sources_sha256_16": "015f97f277704382",
                      "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc3.cu",
                                "newton_schulz_fp32_gb300/csrc/gemm_tc.cu",
                                "newton_schulz_fp32_gb300/csrc/tc_common.cuh",
@@ -120,8 +120,9 @@ def gpt2_workload(ns_method, mode):
     lay = wl.gpt2_small_layout()
     desc = (f"gpt2-small muon step: 12 layers (q,k 12-head, v, o 768x768; up 3072x768; "
             f"down 768x3072), 84.9M params, P=8, align 128, gas=4 bf16 grads, "
-            f"{ns_method} NS x5, {mode} operands, clip 0.05; the 3rd and 4th micro-batches "
-            f"are accumulated inside the step")
+            f"{ns_method} NS x5, {mode} operands, clip 0.05; the 1st and 2nd micro-batches "
+            f"are accumulated in one pass (muon_accumulate_n), the 3rd and 4th inside "
+            f"the step")
     return Workload("gpt2", lay, 4, ns_method, 0.05, desc)
 
 
@@ -483,9 +484,9 @@ def run_gpu(args, W, rank, world):
     fold = fold_options(g_dev[gas - 2] if nfold == 2 else None, g_dev[gas - 1])
 
     def step(grad_list):
-        for mb in range(nacc):
-            nsg.accumulate(acc, grad_list[mb], 1.0 / gas, overwrite=(mb == 0), params=P, parts=Q,
-                           stream=stream)
+        if nacc:   # the micro-batches before the folded ones, in one pass
+            nsg.accumulate_n(acc, grad_list[:nacc], 1.0 / gas, overwrite=True, params=P, parts=Q,
+                             stream=stream)
         nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, W.ns_method, 5, W.clip, args.mode, result=res,
                  stream=stream, options=fold)
 
@@ -550,7 +551,7 @@ def run_gpu(args, W, rank, world):
 
     # ---- end to end: host grads -> device, the step, result -> host.
     # Every step copies its micro-batches from pinned host memory on a copy
-    # stream and reads its result back.  A micro-batch that muon_accumulate
+    # stream and reads its result back.  A micro-batch that muon_accumulate_n
     # takes is free again once accumulated, so the next step's copy into it
     # overlaps this step's Newton-Schulz; the folded ones may be read until
     # the step ends, so each alternates between two device buffers.
@@ -591,8 +592,10 @@ def run_gpu(args, W, rank, world):
         copy_marks.append((c0, c1))
         for mb in range(nacc):
             stream.wait_event(copied[mb])
-            nsg.accumulate(acc, g_dev[mb], 1.0 / gas, overwrite=(mb == 0), params=P, parts=Q,
-                           stream=stream)
+        if nacc:
+            nsg.accumulate_n(acc, g_dev[:nacc], 1.0 / gas, overwrite=True, params=P, parts=Q,
+                             stream=stream)
+        for mb in range(nacc):
             consumed[mb].record(stream)
         for mb in range(nacc, gas):
             stream.wait_event(copied[mb])
@@ -690,8 +693,7 @@ def run_dp(args, W, rank, world):
     D = dp.DataParallelMuon(plan)
 
     def step():
-        for mb in range(gas):
-            nsg.accumulate(acc, g_dev[mb], 1.0 / gas, overwrite=(mb == 0), n=n, stream=stream)
+        nsg.accumulate_n(acc, g_dev, 1.0 / gas, overwrite=True, n=n, stream=stream)
         D.step(acc, mom, mst, 0.95, 0.02, W.ns_method, 5, W.clip, args.mode, result=res,
                stream=stream)
 

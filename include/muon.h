@@ -136,6 +136,28 @@ MUON_API int muon_accumulate(float* accum, const uint16_t* grad, int64_t n, floa
                     int overwrite, const muon_param_t* params, int nparams,
                     const muon_partition_t* parts, int nparts, void* stream);
 
+/* S1 for several micro-batches in one pass over accum: bit for bit the
+ * result of muon_accumulate called on grads[0], ..., grads[count - 1] in
+ * that order, the first call with `overwrite` and the others adding:
+ *     a = overwrite ? 0 : accum[s];
+ *     for j in 0 .. count-1:  a = a + scales[j] * float(grads[j][s])
+ *     accum[s] = a
+ * (each product rounded to FP32 before its sum), reading accum at most once
+ * and writing it once instead of once per micro-batch.
+ *   grads  : host array of `count` device pointers, each bf16 bit patterns
+ *            with accum's layout, 8-byte aligned; read during the call's
+ *            work on `stream`
+ *   scales : host array of `count` floats
+ *   count  : 1 .. MUON_ACCUMULATE_MAX
+ *   the other arguments as muon_accumulate.
+ * Errors: as muon_accumulate; MUON_ERR_INVALID for count out of range or a
+ * NULL or misaligned grads[j]. */
+#define MUON_ACCUMULATE_MAX 8
+MUON_API int muon_accumulate_n(float* accum, const uint16_t* const* grads, const float* scales,
+                               int count, int64_t n, int overwrite, const muon_param_t* params,
+                               int nparams, const muon_partition_t* parts, int nparts,
+                               void* stream);
+
 /* S2-S4, the optimizer step, once per accumulation boundary ([ONCE], "The
  * change"; [BF16], PR description):
  *   1. overflow check: any non-finite accum element of any parameter

@@ -33,7 +33,7 @@ DTYPES = {"bf16": 0, "fp32": 1}
 PHASES = ["accumulate", "reduce", "gather", "ns_gemm", "norm", "scatter"]
 
 # Every symbol include/muon.h declares.
-EXPORTED = ["muon_accumulate", "muon_step", "muon_newton_schulz", "muon_get_stats",
+EXPORTED = ["muon_accumulate", "muon_accumulate_n", "muon_step", "muon_newton_schulz", "muon_get_stats",
             "muon_last_error", "muon_release_workspace", "muon_device_error",
             "muon_profile_enable", "muon_profile_read", "muon_newton_schulz_noalloc",
             "muon_step_ex", "muon_profile_enable_phases", "muon_describe_tables",
@@ -114,6 +114,7 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
         L.muon_accumulate.argtypes = [P, P, I64, F, I, P, I, P, I, P]
+        L.muon_accumulate_n.argtypes = [P, P, P, I, I64, I, P, I, P, I, P]
         L.muon_step.argtypes = [P, P, P, P, I, P, I, F, F, I, I, F, I, P, P]
         L.muon_step_ex.argtypes = [P, P, P, P, I, P, I, F, F, I, I, F, I,
                                    ctypes.POINTER(StepOptions), P, P]
@@ -127,8 +128,8 @@ def lib():
         L.muon_describe_tables.argtypes = [P, I, P, I, I, I, ctypes.POINTER(TableInfo)]
         L.muon_profile_read.argtypes = [ctypes.POINTER(PhaseTime), I, I]
         L.muon_testing_set.argtypes = [I, I]
-        for name in ("muon_accumulate", "muon_step", "muon_step_ex", "muon_newton_schulz",
-                     "muon_newton_schulz_noalloc", "muon_get_stats",
+        for name in ("muon_accumulate", "muon_accumulate_n", "muon_step", "muon_step_ex",
+                     "muon_newton_schulz", "muon_newton_schulz_noalloc", "muon_get_stats",
                      "muon_device_error", "muon_profile_enable", "muon_profile_read",
                      "muon_profile_enable_phases", "muon_describe_tables",
                      "muon_testing_set"):
@@ -179,6 +180,31 @@ def accumulate(accum, grad, scale: float, overwrite: bool = False, params=None, 
     _check(lib().muon_accumulate(_ptr(accum), _ptr(grad), n, scale, int(overwrite),
                                  p.ctypes.data if p is not None else None, np_,
                                  q.ctypes.data if q is not None else None, nq, _stream(stream)))
+
+
+ACCUMULATE_MAX = 8
+
+
+def accumulate_n(accum, grads, scales, overwrite: bool = False, params=None, parts=None,
+                 n: int | None = None, stream=None):
+    """accumulate() over several micro-batches in one pass: the same bits as
+    accumulate(accum, grads[j], scales[j], overwrite and j == 0) for j in
+    order.  scales: one float for all, or one per micro-batch."""
+    grads = list(grads)
+    if not isinstance(scales, (list, tuple)):
+        scales = [float(scales)] * len(grads)
+    if len(scales) != len(grads):
+        raise ValueError("one scale per micro-batch")
+    p, np_ = _table(params, PARAM_DTYPE)
+    q, nq = _table(parts, PART_DTYPE)
+    if n is None:
+        n = accum.numel() if hasattr(accum, "numel") else -1
+    gp = (ctypes.c_void_p * max(len(grads), 1))(*[_ptr(g) for g in grads])
+    sc = (ctypes.c_float * max(len(scales), 1))(*[float(x) for x in scales])
+    _check(lib().muon_accumulate_n(_ptr(accum), ctypes.cast(gp, ctypes.c_void_p),
+                                   ctypes.cast(sc, ctypes.c_void_p), len(grads), n, int(overwrite),
+                                   p.ctypes.data if p is not None else None, np_,
+                                   q.ctypes.data if q is not None else None, nq, _stream(stream)))
 
 
 def step_options(clip_mode="update", grad_scale: float = 1.0, adam: dict | None = None,

@@ -1315,21 +1315,23 @@ int validate_tables(const muon_param_t* params, int nparams, const muon_partitio
 
 using namespace muon;
 
-extern "C" int muon_accumulate(float* accum, const uint16_t* grad, int64_t n, float scale,
-                               int overwrite, const muon_param_t* params, int nparams,
-                               const muon_partition_t* parts, int nparts, void* stream) {
-  NvtxRange nvtx_("muon_accumulate");
-  std::lock_guard<std::mutex> lk(g_mu);
-  g_err.clear();
-  g_cnt.launches_last = 0;
-  if (!accum || !grad) return fail(MUON_ERR_INVALID, "accum or grad is NULL");
-  if (reinterpret_cast<uintptr_t>(accum) % 16 || reinterpret_cast<uintptr_t>(grad) % 8)
-    return fail(MUON_ERR_INVALID, "accum must be 16-byte and grad 8-byte aligned");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+namespace {
+
+// The runs an accumulation covers: every element (params == NULL, a cached
+// list of 32768-element runs over n) or the elements some parameter covers.
+struct AccRuns {
+  const Run* runs = nullptr;
+  int nruns = 0;
+  double elems = 0.0;
+  int64_t extent = 0;
+  int* dbg_flag = nullptr;
+};
+
+int accumulate_runs(int64_t n, const muon_param_t* params, int nparams,
+                    const muon_partition_t* parts, int nparts, AccRuns* out) {
   if (params == nullptr) {
     if (n < 0) return fail(MUON_ERR_INVALID, "n < 0");
     if (n == 0) return MUON_OK;
-    // dense: cached run list per n
     static std::map<std::pair<int, int64_t>, std::unique_ptr<DevBuf>> dense;
     int dev = 0;
     MUON_CUDA_TRY(cudaGetDevice(&dev));
@@ -1342,19 +1344,72 @@ extern "C" int muon_accumulate(float* accum, const uint16_t* grad, int64_t n, fl
       MUON_CUDA_TRY(upload(*b, runs));
       it = dense.emplace(key, std::move(b)).first;
     }
-    const int nruns = static_cast<int>((n + 32767) / 32768);
-    PhaseScope sc(MUON_PHASE_ACCUMULATE, s, 1, double(n) * (overwrite ? 6 : 10), 0.0);
-    launch_accumulate(accum, grad, it->second->as<Run>(), nruns, scale, overwrite,
-                      n - g_knobs.extent_shrink, nullptr, s);
-  } else {
-    TablePlan* tp = nullptr;
-    int rc = get_table_plan(params, nparams, parts, nparts, &tp);
-    if (rc != MUON_OK) return rc;
-    const double el = double(tp->L.muon_elems + tp->L.aux_elems);
-    PhaseScope sc(MUON_PHASE_ACCUMULATE, s, tp->L.runs.empty() ? 0 : 1, el * (overwrite ? 6 : 10), 0.0);
-    launch_accumulate(accum, grad, tp->d_runs.as<Run>(), static_cast<int>(tp->L.runs.size()), scale,
-                      overwrite, tp->L.storage_extent - g_knobs.extent_shrink, tp->d_err.as<int>(), s);
+    out->runs = it->second->as<Run>();
+    out->nruns = static_cast<int>((n + 32767) / 32768);
+    out->elems = double(n);
+    out->extent = n - g_knobs.extent_shrink;
+    return MUON_OK;
   }
+  TablePlan* tp = nullptr;
+  int rc = get_table_plan(params, nparams, parts, nparts, &tp);
+  if (rc != MUON_OK) return rc;
+  out->runs = tp->d_runs.as<Run>();
+  out->nruns = static_cast<int>(tp->L.runs.size());
+  out->elems = double(tp->L.muon_elems + tp->L.aux_elems);
+  out->extent = tp->L.storage_extent - g_knobs.extent_shrink;
+  out->dbg_flag = tp->d_err.as<int>();
+  return MUON_OK;
+}
+
+}  // namespace
+
+extern "C" int muon_accumulate(float* accum, const uint16_t* grad, int64_t n, float scale,
+                               int overwrite, const muon_param_t* params, int nparams,
+                               const muon_partition_t* parts, int nparts, void* stream) {
+  NvtxRange nvtx_("muon_accumulate");
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_err.clear();
+  g_cnt.launches_last = 0;
+  if (!accum || !grad) return fail(MUON_ERR_INVALID, "accum or grad is NULL");
+  if (reinterpret_cast<uintptr_t>(accum) % 16 || reinterpret_cast<uintptr_t>(grad) % 8)
+    return fail(MUON_ERR_INVALID, "accum must be 16-byte and grad 8-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  AccRuns r;
+  int rc = accumulate_runs(n, params, nparams, parts, nparts, &r);
+  if (rc != MUON_OK || r.nruns == 0) return rc;
+  PhaseScope sc(MUON_PHASE_ACCUMULATE, s, 1, r.elems * (overwrite ? 6 : 10), 0.0);
+  launch_accumulate(accum, grad, r.runs, r.nruns, scale, overwrite, r.extent, r.dbg_flag, s);
+  MUON_CUDA_TRY(cudaGetLastError());
+  return MUON_OK;
+}
+
+extern "C" int muon_accumulate_n(float* accum, const uint16_t* const* grads, const float* scales,
+                                 int count, int64_t n, int overwrite, const muon_param_t* params,
+                                 int nparams, const muon_partition_t* parts, int nparts,
+                                 void* stream) {
+  NvtxRange nvtx_("muon_accumulate_n");
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_err.clear();
+  g_cnt.launches_last = 0;
+  if (!accum || !grads || !scales) return fail(MUON_ERR_INVALID, "accum, grads or scales is NULL");
+  if (count < 1 || count > MUON_ACCUMULATE_MAX)
+    return fail(MUON_ERR_INVALID, "count must be 1 .. MUON_ACCUMULATE_MAX");
+  if (reinterpret_cast<uintptr_t>(accum) % 16)
+    return fail(MUON_ERR_INVALID, "accum must be 16-byte aligned");
+  GradSet gs{};
+  gs.count = count;
+  for (int j = 0; j < count; ++j) {
+    if (!grads[j] || reinterpret_cast<uintptr_t>(grads[j]) % 8)
+      return fail(MUON_ERR_INVALID, "every grads[j] must be non-NULL and 8-byte aligned");
+    gs.grad[j] = grads[j];
+    gs.scale[j] = scales[j];
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  AccRuns r;
+  int rc = accumulate_runs(n, params, nparams, parts, nparts, &r);
+  if (rc != MUON_OK || r.nruns == 0) return rc;
+  PhaseScope sc(MUON_PHASE_ACCUMULATE, s, 1, r.elems * ((overwrite ? 4 : 8) + 2.0 * count), 0.0);
+  launch_accumulate_n(accum, gs, r.runs, r.nruns, overwrite, r.extent, r.dbg_flag, s);
   MUON_CUDA_TRY(cudaGetLastError());
   return MUON_OK;
 }

@@ -224,6 +224,14 @@ constexpr int kErrBounds = 16;
 void launch_accumulate(float* accum, const uint16_t* grad, const Run* runs, int nruns,
                        float scale, int overwrite, int64_t dbg_extent, int* dbg_flag,
                        cudaStream_t s);
+// Several micro-batches in one pass (muon_accumulate_n).
+struct GradSet {
+  const uint16_t* grad[MUON_ACCUMULATE_MAX];
+  float scale[MUON_ACCUMULATE_MAX];
+  int count;
+};
+void launch_accumulate_n(float* accum, const GradSet& gs, const Run* runs, int nruns, int overwrite,
+                         int64_t dbg_extent, int* dbg_flag, cudaStream_t s);
 void launch_reduce(const StreamLaunchArgs& a, cudaStream_t s);
 void launch_fold_commit(const StreamLaunchArgs& a, cudaStream_t s);
 // folded micro-batches that add to accum's old value (the first pass then writes the gradient)

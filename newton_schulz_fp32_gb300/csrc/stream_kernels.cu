@@ -310,6 +310,61 @@ k_accumulate(float* __restrict__ accum, const uint16_t* __restrict__ grad,
     accum[j] = acc_one(accum[j], bf16_bits_to_float(grad[j]), scale, overwrite);
 }
 
+// C micro-batches in one pass: element by element the arithmetic of C
+// k_accumulate launches in order (the first with `overwrite`), accum read at
+// most once and written once.  Same runs and vector layout as k_accumulate.
+template <int C>
+__device__ __forceinline__ float acc_set(const GradSet& gs, float a, int64_t i, int overwrite) {
+  #pragma unroll
+  for (int j = 0; j < C; ++j)
+    a = acc_one(a, bf16_bits_to_float(gs.grad[j][i]), gs.scale[j], j == 0 ? overwrite : 0);
+  return a;
+}
+
+template <int C>
+__global__ void __launch_bounds__(kStreamThreads)
+k_accumulate_n(float* __restrict__ accum, const GradSet gs, const Run* __restrict__ runs,
+               int overwrite, int64_t dbg_extent, int* dbg_flag) {
+  const Run r = runs[blockIdx.x];
+  MUON_DBG_CHECK(dbg_in(r.begin, r.begin + r.len, dbg_extent), dbg_flag);
+  const int64_t b = r.begin, e = r.begin + r.len;
+  int64_t vb = (b + 3) & ~int64_t(3);
+  if (vb > e) vb = e;
+  const int64_t ve = vb + ((e - vb) & ~int64_t(3));
+  for (int64_t i = b + threadIdx.x; i < vb; i += blockDim.x)
+    accum[i] = acc_set<C>(gs, overwrite ? 0.f : accum[i], i, overwrite);
+  constexpr int U = C <= 2 ? 4 : 2;
+  const int64_t step = int64_t(4) * blockDim.x;
+  int64_t i = vb + int64_t(4) * threadIdx.x;
+  for (; i + (U - 1) * step < ve; i += U * step) {
+    float4 a[U];
+    uint2 g[U][C];
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+      #pragma unroll
+      for (int j = 0; j < C; ++j) g[u][j] = *reinterpret_cast<const uint2*>(gs.grad[j] + i + u * step);
+      a[u] = overwrite ? make_float4(0.f, 0.f, 0.f, 0.f)
+                       : *reinterpret_cast<const float4*>(accum + i + u * step);
+    }
+    #pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float4 o = a[u];
+      #pragma unroll
+      for (int j = 0; j < C; ++j) o = acc_four(o, g[u][j], gs.scale[j], j == 0 ? overwrite : 0);
+      *reinterpret_cast<float4*>(accum + i + u * step) = o;
+    }
+  }
+  for (; i < ve; i += step) {
+    float4 o = overwrite ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(accum + i);
+    #pragma unroll
+    for (int j = 0; j < C; ++j)
+      o = acc_four(o, *reinterpret_cast<const uint2*>(gs.grad[j] + i), gs.scale[j], j == 0 ? overwrite : 0);
+    *reinterpret_cast<float4*>(accum + i) = o;
+  }
+  for (int64_t j = ve + threadIdx.x; j < e; j += blockDim.x)
+    accum[j] = acc_set<C>(gs, overwrite ? 0.f : accum[j], j, overwrite);
+}
+
 // ------------------------------------------------------------------ S2 pass 1
 
 // One element of pass 1: the sum of squares of what the mode needs and the
@@ -1313,6 +1368,22 @@ void launch_accumulate(float* accum, const uint16_t* grad, const Run* runs, int 
     else kernel<Fold<2, false>><<<(grid), kStreamThreads, 0, (s)>>>(a);                      \
   } while (0)
 
+void launch_accumulate_n(float* accum, const GradSet& gs, const Run* runs, int nruns, int overwrite,
+                         int64_t dbg_extent, int* dbg_flag, cudaStream_t s) {
+  if (nruns <= 0) return;
+  switch (gs.count) {
+#define MUON_ACC_CASE(C)                                                                         \
+  case C:                                                                                        \
+    k_accumulate_n<C><<<nruns, kStreamThreads, 0, s>>>(accum, gs, runs, overwrite, dbg_extent,  \
+                                                       dbg_flag);                                \
+    break;
+    MUON_ACC_CASE(1) MUON_ACC_CASE(2) MUON_ACC_CASE(3) MUON_ACC_CASE(4)
+    MUON_ACC_CASE(5) MUON_ACC_CASE(6) MUON_ACC_CASE(7) MUON_ACC_CASE(8)
+#undef MUON_ACC_CASE
+    default:
+      break;
+  }
+}
 void launch_reduce(const StreamLaunchArgs& a, cudaStream_t s) {
   if (a.n_rtiles > 0) MUON_FOLD_LAUNCH(k_reduce, a.n_rtiles, a, s);
 }

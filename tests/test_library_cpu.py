@@ -172,3 +172,22 @@ def test_valid_options_without_gpu_fail_cleanly(lib):
                  nsg.step_options(last_grad=FAKE, last_grad_scale=0.25), v1, v2,
                  nsg.step_options(stats_out=FAKE)):
         assert _step_ex(lib, opts) == nsg.MUON_ERR_CUDA
+
+
+def test_accumulate_n_arguments_rejected_on_host(lib):
+    """muon_accumulate_n checks its micro-batch list before any CUDA call."""
+    def call(ptrs, count, accum=FAKE):
+        grads = (ctypes.c_void_p * max(len(ptrs), 1))(*ptrs)
+        scales = (ctypes.c_float * max(len(ptrs), 1))(*([0.5] * len(ptrs)))
+        return lib.muon_accumulate_n(accum, ctypes.cast(grads, ctypes.c_void_p),
+                                     ctypes.cast(scales, ctypes.c_void_p), count, 1024, 1,
+                                     None, 0, None, 0, None)
+    assert nsg.ACCUMULATE_MAX == 8
+    for ptrs, count, word in [([FAKE], 0, "count"), ([FAKE] * 9, 9, "count"),
+                              ([FAKE, None], 2, "grads"), ([FAKE, FAKE + 4], 2, "grads")]:
+        assert call(ptrs, count) == nsg.MUON_ERR_INVALID, word
+        assert word in lib.muon_last_error().decode(), lib.muon_last_error()
+    assert call([FAKE], 1, accum=FAKE + 8) == nsg.MUON_ERR_INVALID
+    assert "aligned" in lib.muon_last_error().decode()
+    with pytest.raises(ValueError):
+        nsg.accumulate_n(FAKE, [FAKE, FAKE], [0.5], n=16)
