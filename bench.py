@@ -48,7 +48,7 @@ GEMM_TRAFFIC = {
     "gpt2": {"bytes_per_launch": 3.8480e9, "sources_sha256_16": "7179c2b5092211c5",
              "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
                        "newton_schulz_fp32_gb300/csrc/tc_common.cuh"]},
-    "llama": {"bytes_per_launch": 32 * 13.1362e9, "sources_sha256_16": "42a6c1fe87eda04d",
+    "llama": {"bytes_per_launch": 32 * 13.1362e9, "sources_sha256_16": "932fe30ce6969503",
               "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc2.cu",
                         "newton_schulz_fp32_gb300/csrc/tc_common.cuh",
                         "newton_schulz_fp32_gb300/csrc/api.cu"]},
@@ -59,7 +59,7 @@ GEMM_TRAFFIC = {
 # of the split-3 m x m recurrence, Y), summed from one ncu capture of the
 # full 8192-matrix step (dram__bytes_read.sum + dram__bytes_write.sum,
 # one pass), valid for the sources hashed.
-RAGGED_NS_TRAFFIC = {"bytes_per_step": 46.476e9, "sources_sha256_16": "015f97f277704382",
+RAGGED_NS_TRAFFIC = {"bytes_per_step": 46.476e9, "sources_sha256_16": "5bd3eca0ff84a1f3",
                      "files": ["newton_schulz_fp32_gb300/csrc/gemm_tc3.cu",
                                "newton_schulz_fp32_gb300/csrc/gemm_tc.cu",
                                "newton_schulz_fp32_gb300/csrc/tc_common.cuh",

@@ -1053,7 +1053,7 @@ struct TablePlan {
   std::vector<uint8_t> key;
   Layout L;
   DevBuf d_owners, d_segs, d_rtiles, d_gtiles, d_stiles, d_ytiles, d_runs;
-  DevBuf d_rsum, d_ysum, d_div, d_state, d_err;
+  DevBuf d_rsum, d_ysum, d_fin, d_div, d_state, d_err;
   std::map<std::tuple<int, int, int, uint64_t>, std::unique_ptr<NsPlan>> ns;
 };
 
@@ -1114,6 +1114,7 @@ int get_table_plan(const muon_param_t* params, int nparams, const muon_partition
   MUON_CUDA_TRY(upload(tp->d_runs, L.runs));
   MUON_CUDA_TRY(tp->d_rsum.alloc(sizeof(double) * (L.rtiles.size() + 1)));
   MUON_CUDA_TRY(tp->d_ysum.alloc(sizeof(double) * (L.ytiles.size() + 1)));
+  MUON_CUDA_TRY(tp->d_fin.alloc(sizeof(double) * kFinParts));
   MUON_CUDA_TRY(tp->d_div.alloc(sizeof(float) * (L.owners.size() + 1)));
   MUON_CUDA_TRY(tp->d_state.alloc(sizeof(StepState)));
   MUON_CUDA_TRY(tp->d_err.alloc(sizeof(int)));
@@ -1548,6 +1549,7 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
   a.master = master;
   a.rtile_sum = tp->d_rsum.as<double>();
   a.ytile_sum = tp->d_ysum.as<double>();
+  a.fin_part = tp->d_fin.as<double>();
   a.owner_div = tp->d_div.as<float>();
   a.x0 = P->x0;
   a.y = P->y;
@@ -1595,7 +1597,7 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
   } else {
     // gradient norm over every parameter, clip coefficient, then the
     // per-block momentum norms of the clipped gradients
-    PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 2 : 0) + 2,
+    PhaseScope sc(MUON_PHASE_REDUCE, s, (a.n_rtiles ? 2 : 0) + 3,
                   (me + ae) * (g_first + g_write) + me * (g_bytes + 4), 0.0);
     a.reduce_mode = 1;
     first_pass();
@@ -1615,7 +1617,7 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
     if (rc != MUON_OK) return rc;
     {
       const bool fused = P->ssq_ptr != nullptr;   // the last product summed the squares
-      PhaseScope sc(MUON_PHASE_NORM, s, (a.n_ytiles && !pre && !fused ? 1 : 0) + 1,
+      PhaseScope sc(MUON_PHASE_NORM, s, (a.n_ytiles && !pre && !fused ? 1 : 0) + (pre ? 1 : 2),
                     pre || fused ? 0.0 : me * P->esize, 0.0);
       if (fused) {
         a.ytile_sum = P->ssq_ptr;
@@ -1670,7 +1672,7 @@ int step_impl(float* accum, float* momentum, float* master, const muon_param_t* 
         a.ytile_sum = P->ssq_ptr;
         a.n_ytiles = static_cast<int>(P->n_ssq);
       }
-      PhaseScope sc(MUON_PHASE_NORM, s, 1, 0.0, 0.0);
+      PhaseScope sc(MUON_PHASE_NORM, s, pre ? 1 : 2, 0.0, 0.0);
       launch_finalize(a, s);
     }
     {

@@ -34,6 +34,7 @@ constexpr int kRowTile = 16384;     // target elements per row-aligned 1-D tile 
 constexpr int kTT = 64;             // 2-D transpose tile edge
 constexpr int kStreamThreads = 256;
 constexpr int kFoldCommitCtas = 152 * 8;   // k_fold_commit: 8 CTAs per SM, tiles strided
+constexpr int kFinParts = 256;             // blocks of the global sum's first level
 
 // A contiguous run shared by flat space and storage: the intersection of one
 // owner (head block or auxiliary parameter) with one partition.
@@ -177,6 +178,7 @@ struct StreamLaunchArgs {
   float* master;
   double* rtile_sum;
   double* ytile_sum;
+  double* fin_part;      // kFinParts partial sums of the global sum of squares
   float* owner_div;
   void* x0;          // X0 region (m x n per owner)
   const void* y;     // final NS result region

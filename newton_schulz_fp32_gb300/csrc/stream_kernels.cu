@@ -1117,14 +1117,44 @@ __device__ __forceinline__ void set_clip(const StreamLaunchArgs& a, double tot) 
   a.state->sumsq = tot;
 }
 
+// First level of the global sum of squares: block b of kFinParts adds a
+// fixed contiguous range of the tile sums, each thread a fixed strided part
+// of it, so the order depends on the tile counts alone.  all_rtiles = 0: the
+// update tile sums, then the auxiliary owners' first-pass tile sums (the
+// norm over the updates and the auxiliary gradients); 1: every first-pass
+// tile sum (clip before Muon: the gradient norm).
+__global__ void __launch_bounds__(kStreamThreads)
+k_finalize_parts(StreamLaunchArgs a, int all_rtiles) {
+  if (a.state->overflow) return;
+  const int64_t ny = all_rtiles ? 0 : a.n_ytiles;
+  const int64_t total = ny + a.n_rtiles;
+  const int64_t per = (total + kFinParts - 1) / kFinParts;
+  const int64_t b0 = int64_t(blockIdx.x) * per, b1 = min(total, b0 + per);
+  double s = 0.0;
+  for (int64_t i = b0 + threadIdx.x; i < b1; i += kStreamThreads) {
+    if (i < ny) {
+      s += a.ytile_sum[i];
+    } else {
+      const int64_t j = i - ny;
+      if (all_rtiles || !a.owners[a.rtiles[j].owner].is_muon) s += a.rtile_sum[j];
+    }
+  }
+  const double tot = block_sum<kStreamThreads>(s);
+  if (threadIdx.x == 0) a.fin_part[blockIdx.x] = tot;
+}
+
+__device__ __forceinline__ double fin_total(const StreamLaunchArgs& a) {
+  double s = 0.0;
+  for (int i = threadIdx.x; i < kFinParts; i += kFinThreads) s += a.fin_part[i];
+  return block_sum<kFinThreads>(s);
+}
+
 // Clip before Muon: the global norm over every parameter's gradient, from
 // the tile sums of reduce mode 1, in a fixed order.
 __global__ void __launch_bounds__(kFinThreads)
 k_finalize_pre(StreamLaunchArgs a) {
   if (a.state->overflow) return;
-  double s = 0.0;
-  for (int i = threadIdx.x; i < a.n_rtiles; i += kFinThreads) s += a.rtile_sum[i];
-  const double tot = block_sum<kFinThreads>(s);
+  const double tot = fin_total(a);
   if (threadIdx.x == 0) set_clip(a, tot);
 }
 
@@ -1147,11 +1177,7 @@ k_finalize(StreamLaunchArgs a) {
   }
   const int applied = (a.err_flag != nullptr && *a.err_flag != 0) ? -1 : 1;
   if (a.clip_mode == 0) {
-    double s = 0.0;
-    for (int i = threadIdx.x; i < a.n_ytiles; i += kFinThreads) s += a.ytile_sum[i];
-    for (int i = threadIdx.x; i < a.n_rtiles; i += kFinThreads)
-      if (!a.owners[a.rtiles[i].owner].is_muon) s += a.rtile_sum[i];
-    const double tot = block_sum<kFinThreads>(s);
+    const double tot = fin_total(a);
     if (threadIdx.x == 0) set_clip(a, tot);
   }
   if (threadIdx.x == 0) {
@@ -1404,9 +1430,11 @@ void launch_update_sumsq(const StreamLaunchArgs& a, cudaStream_t s) {
   if (a.n_ytiles > 0) k_update_sumsq<<<a.n_ytiles, kStreamThreads, 0, s>>>(a);
 }
 void launch_finalize(const StreamLaunchArgs& a, cudaStream_t s) {
+  if (a.clip_mode == 0) k_finalize_parts<<<kFinParts, kStreamThreads, 0, s>>>(a, 0);
   k_finalize<<<1, kFinThreads, 0, s>>>(a);
 }
 void launch_finalize_pre(const StreamLaunchArgs& a, cudaStream_t s) {
+  k_finalize_parts<<<kFinParts, kStreamThreads, 0, s>>>(a, 1);
   k_finalize_pre<<<1, kFinThreads, 0, s>>>(a);
 }
 void launch_scatter(const StreamLaunchArgs& a, cudaStream_t s) {
