@@ -120,9 +120,8 @@ def gpt2_workload(ns_method, mode):
     lay = wl.gpt2_small_layout()
     desc = (f"gpt2-small muon step: 12 layers (q,k 12-head, v, o 768x768; up 3072x768; "
             f"down 768x3072), 84.9M params, P=8, align 128, gas=4 bf16 grads, "
-            f"{ns_method} NS x5, {mode} operands, clip 0.05; the 1st and 2nd micro-batches "
-            f"are accumulated in one pass (muon_accumulate_n), the 3rd and 4th inside "
-            f"the step")
+            f"{ns_method} NS x5, {mode} operands, clip 0.05; the four micro-batches are "
+            f"accumulated in one pass (muon_accumulate_n)")
     return Workload("gpt2", lay, 4, ns_method, 0.05, desc)
 
 
@@ -471,20 +470,25 @@ def run_gpu(args, W, rank, world):
         res_host = torch.zeros(4, dtype=torch.int32).pin_memory()
     torch.cuda.synchronize()
     P, Q = lay.params, lay.parts
-    # the last two micro-batches are accumulated by the step itself
-    # (muon_step_ex prev_grad and last_grad: the same arithmetic as
-    # muon_accumulate; when they overwrite accum it is written only once)
-    nfold = min(2, gas)
+    # Up to two micro-batches: the step accumulates them itself (muon_step_ex
+    # prev_grad and last_grad, the same arithmetic as muon_accumulate); they
+    # overwrite accum, which the step then writes only once.  More: all of
+    # them in one muon_accumulate_n pass, then the plain step -- fewer bytes
+    # than folding the last two into a step that must also read and write
+    # accum (four micro-batches: 12 + 8 B/elem against 8 + 16).
+    nfold = gas if gas <= 2 else 0
     nacc = gas - nfold
 
     def fold_options(prev, last):
+        if nfold == 0:
+            return None
         return nsg.step_options(last_grad=last, last_grad_scale=1.0 / gas,
                                 last_grad_overwrite=(gas == 1), prev_grad=prev,
                                 prev_grad_scale=1.0 / gas, prev_grad_overwrite=(nacc == 0))
     fold = fold_options(g_dev[gas - 2] if nfold == 2 else None, g_dev[gas - 1])
 
     def step(grad_list):
-        if nacc:   # the micro-batches before the folded ones, in one pass
+        if nacc:   # all micro-batches (none folded), in one pass
             nsg.accumulate_n(acc, grad_list[:nacc], 1.0 / gas, overwrite=True, params=P, parts=Q,
                              stream=stream)
         nsg.step(acc, mom, mst, P, Q, 0.95, 0.02, W.ns_method, 5, W.clip, args.mode, result=res,
