@@ -1,5 +1,7 @@
 """A whole optimizer step -- the micro-batch accumulations and muon_step_ex
-with the folded last micro-batch -- recorded into a CUDA graph once its
+(with the folded last micro-batch; or all micro-batches in one
+muon_accumulate_n pass and the plain step; or two micro-batches folded
+with overwrite, the gradient formed by every pass) -- recorded into a CUDA graph once its
 plans exist, then replayed: the library issues only stream-ordered work on
 the caller's stream in steady state (no allocation, no synchronisation,
 no host reads), so the replays must leave accum, momentum, master and the
@@ -23,12 +25,15 @@ def torch():
     return t
 
 
-@pytest.mark.parametrize("method,mode", [("standard", "bf16"), ("gram", "fp32")])
-def test_step_replays_from_a_cuda_graph(torch, method, mode):
+@pytest.mark.parametrize("method,mode,flow", [("standard", "bf16", "fold_last"),
+                                              ("gram", "fp32", "fold_last"),
+                                              ("standard", "bf16", "accumulate_n"),
+                                              ("gram", "bf16", "fold_both")])
+def test_step_replays_from_a_cuda_graph(torch, method, mode, flow):
     lay = wl.build_layout([[wl.ParamSpec("q", 256, 256, 4), wl.ParamSpec("up", 512, 256),
                             wl.ParamSpec("down", 256, 512)],
                            [wl.ParamSpec("ln", 1, 256, use_muon=False)]], 128, 4)
-    gas = 3
+    gas = 2 if flow == "fold_both" else 3
     grads = micro_batch_grads(lay, 21, 0, gas, wl.loguniform_sigmas(lay, 21, 1e-3, 1e-1))
     gb = [bf16_tensor(wl.bf16_storage_grad(lay, g), torch) for g in grads]
     m0 = wl.storage_with_sentinels(lay, [np.float32(0.01) * x for x in
@@ -41,11 +46,20 @@ def test_step_replays_from_a_cuda_graph(torch, method, mode):
             torch.zeros(4, dtype=torch.int32, device="cuda")
 
     def one_step(acc, mom, mst, res, stream):
-        for mb in range(gas - 1):
-            nsg.accumulate(acc, gb[mb], 1.0 / gas, overwrite=(mb == 0), params=lay.params,
-                           parts=lay.parts, stream=stream)
+        if flow == "fold_last":
+            for mb in range(gas - 1):
+                nsg.accumulate(acc, gb[mb], 1.0 / gas, overwrite=(mb == 0), params=lay.params,
+                               parts=lay.parts, stream=stream)
+            opts = dict(last_grad=gb[-1], last_grad_scale=1.0 / gas)
+        elif flow == "accumulate_n":
+            nsg.accumulate_n(acc, gb, 1.0 / gas, overwrite=True, params=lay.params,
+                             parts=lay.parts, stream=stream)
+            opts = {}
+        else:
+            opts = dict(prev_grad=gb[0], prev_grad_scale=0.5, prev_grad_overwrite=True,
+                        last_grad=gb[1], last_grad_scale=0.5)
         nsg.step_ex(acc, mom, mst, lay.params, lay.parts, 0.95, 0.02, method, 5, 0.05, mode,
-                    last_grad=gb[-1], last_grad_scale=1.0 / gas, result=res, stream=stream)
+                    result=res, stream=stream, **opts)
 
     # eager: two steps (the first also builds the plans)
     e = fresh()
