@@ -45,11 +45,16 @@ def misaligned(t, torch):
     return buf
 
 
-def run(torch, lay, grads, gas, fold, method, mode, nan_last=False, misalign=False, **opts):
+ADAM = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, step=3)
+
+
+def run(torch, lay, grads, gas, fold, method, mode, nan_last=False, misalign=False, adam=False,
+        **opts):
     """accumulate the micro-batches (all, or all but the last `fold` of
     them, which the step folds in: 1 = last_grad, 2 = prev_grad and
     last_grad), then one step; returns the three storage buffers and the
-    result."""
+    result (with `adam`: the auxiliary Adam step on fresh moments, which are
+    returned after the master)."""
     m = [np.float32(0.01) * x for x in wl.gaussian_grads(lay, 11, 1, None, bf16=False)]
     w = wl.gaussian_grads(lay, 11, 2, None, bf16=False)
     z = [np.zeros((s.rows, s.cols), np.float32) for s in lay.specs]
@@ -70,9 +75,17 @@ def run(torch, lay, grads, gas, fold, method, mode, nan_last=False, misalign=Fal
         opts.update(last_grad=gb[-1], last_grad_scale=1.0 / gas, last_grad_overwrite=(gas == 1))
     if fold == 2:
         opts.update(prev_grad=gb[-2], prev_grad_scale=1.0 / gas, prev_grad_overwrite=(gas == 2))
+    moments = []
+    if adam:
+        zero = [np.zeros((s.rows, s.cols), np.float32) for s in lay.specs]
+        moments = [torch.from_numpy(wl.storage_with_sentinels(lay, zero)).cuda() for _ in range(2)]
+        opts["adam"] = dict(ADAM, exp_avg=moments[0], exp_avg_sq=moments[1])
     res = nsg.step_ex(st.accum, st.momentum, st.master, lay.params, lay.parts, BETA, LR, method, 5,
                       CLIP, mode, **opts)
-    return st.numpy(), nsg.read_result(res)
+    bufs = st.numpy()
+    if adam:
+        return tuple(bufs) + tuple(x.cpu().numpy() for x in moments), nsg.read_result(res)
+    return bufs, nsg.read_result(res)
 
 
 CASES = [
@@ -82,6 +95,8 @@ CASES = [
     (3, "identity", 2, "standard", "bf16", {"clip_mode": "grad"}),
     (2, "shuffled", 2, "gram", "bf16", {"workspace_budget": 1}),
     (3, "identity", 4, "standard", "fp32", {"grad_scale": 0.5}),
+    (2, "shuffled", 2, "standard", "bf16", {"adam": True}),
+    (3, "rank_major", 2, "gram", "bf16", {"adam": True, "clip_mode": "grad"}),
 ]
 
 
@@ -91,13 +106,13 @@ def test_folded_last_micro_batch_is_bit_identical(torch, nparts, storage, gas, m
                                                   fold):
     lay = mixed_layout(nparts, storage)
     grads = micro_batch_grads(lay, 5, 0, gas, wl.loguniform_sigmas(lay, 5, 1e-3, 1e-1))
-    (a0, m0, w0), r0 = run(torch, lay, grads, gas, 0, method, mode, **opts)
-    (a1, m1, w1), r1 = run(torch, lay, grads, gas, fold, method, mode, **opts)
+    b0, r0 = run(torch, lay, grads, gas, 0, method, mode, **dict(opts))
+    b1, r1 = run(torch, lay, grads, gas, fold, method, mode, **dict(opts))
     assert r0["applied"] == 1 and r1 == r0
-    for x, y in ((a0, a1), (m0, m1), (w0, w1)):
+    for x, y in zip(b0, b1):   # accum, momentum, master (and the Adam moments)
         np.testing.assert_array_equal(bits(x), bits(y))
     pad = wl.padding_mask(lay)
-    assert (bits(a1)[pad] == wl.NAN_SENTINEL_BITS).all()
+    assert (bits(b1[0])[pad] == wl.NAN_SENTINEL_BITS).all()
 
 
 @pytest.mark.parametrize("gas,fold,opts", [(3, 1, {}), (3, 2, {}), (2, 2, {}), (1, 1, {}),
